@@ -1,0 +1,494 @@
+"""Benchmark of the multi-LoRA path (metadata + shrink + expand) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+    python bench.py --impl reference ...     # the fp64 CPU oracle, timed
+
+One step = one pass of the whole path over one batch: lora_meta_prepare,
+lora_shrink and lora_expand (through the C ABI), on inputs already resident
+in HBM.  Input sets (ids, x, A, B, bias, y, buffer) are replicated until
+they total at least 4x the L2 cache, and consecutive steps rotate through
+them, so every step reads from HBM.  Steps are captured in CUDA graphs (one
+graph per rotation), warm-up steps run first, and exactly K steps are timed
+with CUDA events between a barrier + synchronize on both sides.  Rank 0
+prints one JSON line.  N > 1 (torchrun) runs independent replicas, one per
+GPU, and reports the aggregate over ranks with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "LoRA shrink+expand tokens/s and effective HBM GB/s (% of roofline), 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# the committed ncu summaries, keyed by kernel and the sha256 of the kernel
+# source they were taken on; a stale hash reports traffic as null.
+NCU_TRAFFIC = {}
+
+
+def _src_hash(name: str) -> str:
+    p = os.path.join(ROOT, "expand_gemm_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--workload", default="decode", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--kernel-seconds", type=float, default=0.5,
+                    help="minimum timed seconds per kernel in the per-kernel loops")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured hbm_gbs (burst copy, MEASURED_PEAKS.json)"
+    return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the GPU is under load."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.uuid = gpu_uuid
+        self.rows = []
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            cmd = ["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        for line in self.file:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+        self.file.close()
+        self.proc = None
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------ GPU arm
+
+class DeviceSet:
+    """One resident copy of a workload's inputs and outputs."""
+
+    def __init__(self, inp: W.Inputs, dev, eg):
+        import torch
+        w = inp.workload
+
+        def bf16(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+                torch.bfloat16).to(dev)
+        self.ids = torch.from_numpy(inp.ids).to(dev)
+        self.x = bf16(inp.x)
+        self.A = [bf16(a) for a in inp.lora_a]
+        self.B = [bf16(b) for b in inp.lora_b]
+        self.bias = None if inp.lora_bias is None else [bf16(b) for b in inp.lora_bias]
+        self.y = bf16(inp.y)
+        self.buf = torch.zeros(inp.buf.shape, dtype=torch.float32, device=dev)
+        self.meta = eg.LoRAKernelMeta.make(w.max_loras, w.num_tokens, dev)
+        self.nbytes = sum(t.numel() * t.element_size() for t in
+                          [self.ids, self.x, self.y, self.buf] + self.A + self.B
+                          + (self.bias or []))
+
+    def clone(self, eg):
+        import torch
+        c = object.__new__(DeviceSet)
+        c.ids = self.ids.clone()
+        c.x = self.x.clone()
+        c.A = [a.clone() for a in self.A]
+        c.B = [b.clone() for b in self.B]
+        c.bias = None if self.bias is None else [b.clone() for b in self.bias]
+        c.y = self.y.clone()
+        c.buf = torch.zeros_like(self.buf)
+        c.meta = eg.LoRAKernelMeta.make(self.meta.max_loras, self.meta.max_num_tokens,
+                                        self.meta.device)
+        c.nbytes = self.nbytes
+        return c
+
+
+def run_ours(args, rank, world):
+    import torch
+    import expand_gemm_gb300 as eg
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    eg.library()                                        # fail loudly if not built
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = W.WORKLOADS[args.workload]
+    inp = W.generate(w)
+    ub = W.unique_bytes(w, inp.ids)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+
+    base = DeviceSet(inp, dev, eg)
+    n_sets = max(2, -(-4 * l2 // base.nbytes))
+    sets = [base] + [base.clone(eg) for _ in range(n_sets - 1)]
+
+    def step(s: DeviceSet):
+        s.meta.prepare_tensors(s.ids)
+        eg.lora_shrink(s.x, s.A, s.buf, s.meta, w.scale)
+        eg.lora_expand(s.buf, s.B, s.y, s.meta, w.offset_start, w.add_inputs, s.bias)
+
+    stream = torch.cuda.Stream(dev)
+    # eager pass first: configures kernels (smem attributes, occupancy) before capture
+    with torch.cuda.stream(stream):
+        for s in sets:
+            step(s)
+    torch.cuda.synchronize(dev)
+
+    def capture(fn_list):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for fn in fn_list:
+                fn()
+        return g
+
+    def graphs_for(n_steps, make):
+        """Graphs covering exactly n_steps steps: full rotations + a tail."""
+        rot = capture([make(s) for s in sets])
+        tail_n = n_steps % n_sets
+        tail = capture([make(s) for s in sets[:tail_n]]) if tail_n else None
+        return [rot] * (n_steps // n_sets) + ([tail] if tail else [])
+
+    def mk_step(s):
+        return lambda: step(s)
+
+    warm = graphs_for(args.warmup, mk_step)
+    timed = graphs_for(args.steps, mk_step)
+    gpu_uuid = getattr(props, "uuid", None)
+    gpu_uuid = ("GPU-" + str(gpu_uuid)) if gpu_uuid is not None else None
+    clocks = ClockSampler(gpu_uuid)
+
+    with torch.cuda.stream(stream):
+        for g in warm:
+            g.replay()
+    torch.cuda.synchronize(dev)
+
+    clocks.start()
+    time.sleep(0.3)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for g in timed:
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # ---- per-kernel timing: graphs of one kernel over the rotation
+    def time_kernel(make, min_s):
+        g = capture([make(s) for s in sets])
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        reps = 1
+        while True:
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = a.elapsed_time(b)
+            if ms >= min_s * 1e3 or reps >= 1 << 16:
+                return ms / (reps * n_sets)
+            reps *= 2 if ms <= 0 else max(2, min(16, int(min_s * 1e3 / ms) + 1))
+
+    k_meta = time_kernel(lambda s: (lambda: s.meta.prepare_tensors(s.ids)), args.kernel_seconds)
+    k_shrink = time_kernel(lambda s: (lambda: eg.lora_shrink(s.x, s.A, s.buf, s.meta, w.scale)),
+                           args.kernel_seconds)
+    k_expand = time_kernel(lambda s: (lambda: eg.lora_expand(
+        s.buf, s.B, s.y, s.meta, w.offset_start, w.add_inputs, s.bias)), args.kernel_seconds)
+    clocks.stop()
+
+    # ---- end to end through the public API, host buffers, copies timed
+    e2e = run_e2e(args, inp, w, dev, eg, stream)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return None
+
+    T = w.num_tokens
+    ms_per_step = elapsed_ms / args.steps
+    value = world * T * args.steps / (elapsed_ms / 1e3)
+    hbm, peak_src = peaks()
+    kern = {"meta": k_meta, "shrink": k_shrink, "expand": k_expand}
+    shrink_gbs = ub["shrink"] / (k_shrink * 1e-3) / 1e9
+    expand_gbs = ub["expand"] / (k_expand * 1e-3) / 1e9
+    dominant = "expand" if k_expand >= k_shrink else "shrink"
+    dom_bytes = ub[dominant]
+    dom_ms = kern[dominant]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    src = {"shrink": "lora_shrink.cu", "expand": "lora_expand.cu"}[dominant]
+    tr = NCU_TRAFFIC.get((dominant, args.workload))
+    traffic = tr[1] if (tr and tr[0] == _src_hash(src)) else None
+    step_bytes = ub["shrink"] + ub["expand"]
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64; no dataset or weights)",
+        "config": {
+            "workload": "%s: %s" % (w.name, w.description),
+            "num_tokens": T, "active_tokens": ub["t_active"], "distinct_loras": ub["distinct"],
+            "hidden": w.hidden, "rank": w.rank, "max_loras": w.max_loras,
+            "slices": list(w.slices), "bias": w.bias, "scale": w.scale,
+            "l2": "inputs larger than L2: %d resident input sets of %.1f MB rotated "
+                  "(%.0f MB total, L2 %.0f MB)" % (n_sets, base.nbytes / 1e6,
+                                                   n_sets * base.nbytes / 1e6, l2 / 1e6),
+            "timing": "CUDA graphs of one rotation of steps, CUDA events on the launch stream",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "effective_gbps": step_bytes / (ms_per_step * 1e-3) / 1e9,
+        "step_unique_bytes": step_bytes,
+        "kernels_us": {k: v * 1e3 for k, v in kern.items()},
+        "kernels_gbps": {"shrink": shrink_gbs, "expand": expand_gbs},
+        "roofline": {
+            "bound": "hbm", "kernel": "lora_" + dominant,
+            "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": dom_bytes,
+            "launch_us": dom_ms * 1e3,
+            "peak_source": peak_src + " (of measured)" if "measured" in peak_src else peak_src,
+        },
+        "hbm_frac_step": (step_bytes / (ms_per_step * 1e-3) / 1e9) / hbm,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "wall_s_timed": wall,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(w, inp, target_s=10.0)
+    elif world > 1:
+        out["cpu_baseline"] = cpu_baseline(w, inp, target_s=10.0) if rank == 0 else None
+    if dist:
+        dist.destroy_process_group()
+    return out
+
+
+def run_e2e(args, inp, w, dev, eg, stream):
+    """Same step through the public API from pinned host buffers: H2D of the
+    step's ids, x and y, the three calls, D2H of y; all inside the timing."""
+    import torch
+    ids_h = torch.from_numpy(inp.ids).pin_memory()
+    x_h = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).pin_memory()
+    y_h = torch.from_numpy(np.ascontiguousarray(inp.y).view(np.int16)).pin_memory()
+    out_h = torch.empty_like(y_h).pin_memory()
+    s = DeviceSet(inp, dev, eg)
+    x_d = s.x.view(torch.int16)
+    y_d = s.y.view(torch.int16)
+
+    def one():
+        s.ids.copy_(ids_h, non_blocking=True)
+        x_d.copy_(x_h, non_blocking=True)
+        y_d.copy_(y_h, non_blocking=True)
+        s.meta.prepare_tensors(s.ids)
+        eg.lora_shrink(s.x, s.A, s.buf, s.meta, w.scale)
+        eg.lora_expand(s.buf, s.B, s.y, s.meta, w.offset_start, w.add_inputs, s.bias)
+        out_h.copy_(y_d, non_blocking=True)
+
+    n = max(3, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            one()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / n
+    h2d = ids_h.numel() * 4 + x_h.numel() * 2 + y_h.numel() * 2
+    return {"value": w.num_tokens / (ms * 1e-3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_h.numel() * 2,
+            "ms_per_step": ms, "steps": n}
+
+
+# ------------------------------------------------------ oracle (CPU) arm
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_step(oracle, w, inp, sel):
+    """One oracle pass: metadata on the whole map, shrink + expand on tokens sel."""
+    oracle.meta_prepare(inp.ids, w.max_loras)
+    ids = inp.ids[sel]
+    buf = np.zeros((w.num_slices, sel.size, w.rank), np.float32)
+    b = oracle.shrink(inp.x[sel], inp.lora_a, ids, w.scale, buf)
+    oracle.expand(b.astype(np.float32), inp.lora_b, ids, inp.y[sel], w.slices,
+                  w.offset_start, w.add_inputs, inp.lora_bias)
+
+
+def cpu_baseline(w, inp, target_s=10.0):
+    import oracle
+    oracle.build()
+    T = w.num_tokens
+    n = min(T, 64)
+    sel = np.arange(n)
+    t0 = time.perf_counter()
+    _oracle_step(oracle, w, inp, sel)
+    per_tok = (time.perf_counter() - t0) / n
+    n = int(min(T, max(1, target_s / max(per_tok, 1e-9))))
+    rng = np.random.default_rng(0)
+    sel = np.sort(rng.choice(T, size=n, replace=False)) if n < T else np.arange(T)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(oracle, w, inp, sel)
+        done += sel.size
+        el = time.perf_counter() - t0
+        if el >= target_s * 0.5 or done >= 64 * T:
+            break
+    return {"value": done / el, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+            "sample": "%d of %d tokens of the %s batch per pass (metadata on the full map), "
+                      "%d tokens in %.1f s" % (sel.size, T, w.name, done, el)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    w = W.WORKLOADS[args.workload]
+    inp = W.generate(w)
+    T = w.num_tokens
+    sel = np.arange(min(T, 16))
+    t0 = time.perf_counter()
+    _oracle_step(oracle, w, inp, sel)
+    per_tok = (time.perf_counter() - t0) / sel.size
+    budget = 90.0 / max(1, args.steps + args.warmup)      # seconds per step
+    n = int(min(T, max(1, budget / max(per_tok, 1e-9))))
+    sel = np.sort(np.random.default_rng(0).choice(T, size=n, replace=False))
+    for _ in range(args.warmup):
+        _oracle_step(oracle, w, inp, sel)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(oracle, w, inp, sel)
+    el = time.perf_counter() - t0
+    value = args.steps * n / el
+    sample = ("%d of %d tokens of the %s batch per step (metadata on the full map)"
+              % (n, T, w.name))
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy PCG64)",
+        "config": {"workload": "%s: %s" % (w.name, w.description), "num_tokens": T,
+                   "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    out = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,225 @@
+"""GB300 (sm_103a) multi-LoRA shrink/expand: thin PyTorch binding.
+
+Every step runs in the CUDA kernels of ``liblora_punica.so`` (C ABI in
+``include/lora_punica.h``); this module only checks tensor dtypes and
+layouts, collects device pointers and the current CUDA stream, and calls the
+library.  PyTorch provides device memory and streams, nothing else.  There
+is no CPU fallback: without the built library every call raises.
+
+Names follow vLLM's API pages:
+
+* :class:`LoRAKernelMeta` -- page ``vllm.lora.ops.triton_ops.lora_kernel_metadata``
+  (``make``, ``prepare_tensors``, ``meta_args``).
+* :func:`lora_shrink`, :func:`lora_expand`, :func:`add_lora_linear` -- page
+  ``vllm.lora.punica_wrapper.punica_gpu`` (``PunicaWrapperGPU.add_shrink``,
+  ``add_expand``, ``add_lora_linear``).
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import LoraError, LORA_MAX_LORAS, LORA_MAX_RANK, LORA_MAX_SLICES  # noqa: F401
+
+__all__ = ["LoRAKernelMeta", "lora_meta_prepare", "lora_shrink", "lora_expand",
+           "add_lora_linear", "LoraError", "library", "build"]
+
+
+def library():
+    """The loaded ctypes library (raises if it is not built)."""
+    return _lib.load()
+
+
+def build(force: bool = False) -> str:
+    from .build import build as _build
+    return _build(force=force)
+
+
+def _stream_handle(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (no CPU path exists)" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def _ptr_array(tensors) -> ctypes.Array:
+    arr = (ctypes.c_void_p * len(tensors))()
+    for i, t in enumerate(tensors):
+        arr[i] = None if t is None else t.data_ptr()
+    return arr
+
+
+class LoRAKernelMeta:
+    """Per-forward metadata buffers (LoRAKernelMeta of the metadata page).
+
+    Buffers are int32 device tensors allocated once by :meth:`make`; the
+    no-LoRA flag lives on the device (the kernels read it there, so no host
+    sync is needed); ``error_word`` counts ids outside ``[-1, max_loras)``
+    seen by the last :meth:`prepare_tensors`.
+    """
+
+    def __init__(self, max_loras: int, max_num_tokens: int, device):
+        if not 1 <= max_loras <= LORA_MAX_LORAS:
+            raise ValueError("max_loras must be in [1, %d]" % LORA_MAX_LORAS)
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.max_loras = int(max_loras)
+        self.max_num_tokens = int(max_num_tokens)
+        self.token_lora_mapping = torch.empty(max(max_num_tokens, 1), **i32)
+        self.token_indices_sorted_by_lora_ids = torch.empty(max(max_num_tokens, 1), **i32)
+        self.active_lora_ids = torch.full((max_loras + 1,), -1, **i32)
+        self.num_tokens_per_lora = torch.zeros(max_loras + 1, **i32)
+        self.lora_token_start_loc = torch.zeros(max_loras + 2, **i32)
+        self.no_lora_flag = torch.ones(1, **i32)
+        self.error_word = torch.zeros(1, **i32)
+        self.c = _lib.LoraMetaC(
+            self.token_lora_mapping.data_ptr(),
+            self.token_indices_sorted_by_lora_ids.data_ptr(),
+            self.num_tokens_per_lora.data_ptr(),
+            self.lora_token_start_loc.data_ptr(),
+            self.active_lora_ids.data_ptr(),
+            self.no_lora_flag.data_ptr(),
+            self.error_word.data_ptr(),
+            self.max_loras, self.max_num_tokens)
+        self.device = dev
+
+    @staticmethod
+    def make(max_loras: int, max_num_tokens: int, device) -> "LoRAKernelMeta":
+        return LoRAKernelMeta(max_loras, max_num_tokens, device)
+
+    def prepare_tensors(self, token_lora_mapping: torch.Tensor) -> None:
+        lora_meta_prepare(token_lora_mapping, self)
+
+    def meta_args(self, token_nums: int):
+        """The six metadata tensors in the order the kernels take them."""
+        return (self.token_lora_mapping[:token_nums],
+                self.token_indices_sorted_by_lora_ids[:token_nums],
+                self.num_tokens_per_lora, self.lora_token_start_loc,
+                self.active_lora_ids, self.no_lora_flag)
+
+    def no_lora(self) -> bool:
+        """Host read of the flag (synchronises; the kernels never need it)."""
+        return bool(self.no_lora_flag.item())
+
+
+def lora_meta_prepare(token_lora_mapping: torch.Tensor, meta: LoRAKernelMeta) -> None:
+    m = token_lora_mapping
+    _need(m, "token_lora_mapping", torch.int32)
+    if m.dim() != 1 or not m.is_contiguous():
+        raise ValueError("token_lora_mapping must be a contiguous 1-D tensor")
+    st = _lib.load().lora_meta_prepare(m.data_ptr() if m.numel() else None, m.numel(),
+                                      ctypes.byref(meta.c), _stream_handle(meta.device))
+    _lib.check("lora_meta_prepare", st)
+
+
+def _weights(ws: Sequence[torch.Tensor], name: str):
+    if isinstance(ws, torch.Tensor):
+        ws = (ws,)
+    out = []
+    for i, w in enumerate(ws):
+        _need(w, "%s[%d]" % (name, i), torch.bfloat16)
+        if not w.is_contiguous():
+            raise ValueError("%s[%d] must be contiguous" % (name, i))
+        if w.dim() == 4 and w.size(1) == 1:          # [L, 1, rows, cols] layer dim
+            w = w.view(w.size(0), w.size(2), w.size(3))
+        if w.dim() != 3:
+            raise ValueError("%s[%d] must be [max_loras, rows, cols]" % (name, i))
+        out.append(w)
+    return out
+
+
+def lora_shrink(x: torch.Tensor, lora_a_stacked, y: torch.Tensor,
+                meta: LoRAKernelMeta, scale: float) -> None:
+    """y[s] += scale * x @ lora_a_stacked[s][id]^T for tokens with a LoRA."""
+    _need(x, "x", torch.bfloat16)
+    _need(y, "y", torch.float32)
+    x2 = x.view(-1, x.shape[-1]) if x.dim() != 2 else x
+    if x2.stride(1) != 1:
+        raise ValueError("x rows must be contiguous")
+    A = _weights(lora_a_stacked, "lora_a_stacked")
+    T, H = x2.shape
+    L, r, Ha = A[0].shape
+    if Ha != H or any(a.shape != A[0].shape for a in A):
+        raise ValueError("lora_a_stacked shapes must all be [L, r, %d]" % H)
+    if L < meta.max_loras:
+        raise ValueError("lora_a_stacked has %d LoRAs, metadata expects %d" % (L, meta.max_loras))
+    if tuple(y.shape) != (len(A), T, r) or not y.is_contiguous():
+        raise ValueError("y must be a contiguous fp32 [%d, %d, %d] tensor" % (len(A), T, r))
+    st = _lib.load().lora_shrink(x2.data_ptr(), T, H, x2.stride(0), _ptr_array(A), len(A), r,
+                                 y.data_ptr(), ctypes.byref(meta.c), float(scale),
+                                 _stream_handle(x.device))
+    _lib.check("lora_shrink", st)
+
+
+def lora_expand(x: torch.Tensor, lora_b_stacked, y: torch.Tensor,
+                meta: LoRAKernelMeta, offset_start: int = 0, add_inputs: bool = True,
+                lora_bias_stacked: Optional[Sequence[Optional[torch.Tensor]]] = None) -> None:
+    """y[:, off_s:off_s+n_s] (+)= x[s] @ lora_b_stacked[s][id]^T (+ bias)."""
+    _need(x, "x", torch.float32)
+    _need(y, "y", torch.bfloat16)
+    B = _weights(lora_b_stacked, "lora_b_stacked")
+    if x.dim() != 3 or not x.is_contiguous() or x.size(0) != len(B):
+        raise ValueError("x must be a contiguous fp32 [num_slices, T, r] tensor")
+    S, T, r = x.shape
+    L = B[0].size(0)
+    if L < meta.max_loras:
+        raise ValueError("lora_b_stacked has %d LoRAs, metadata expects %d" % (L, meta.max_loras))
+    for i, b in enumerate(B):
+        if b.size(0) != L or b.size(2) != r:
+            raise ValueError("lora_b_stacked[%d] must be [%d, n, %d]" % (i, L, r))
+    sizes = [b.size(1) for b in B]
+    y2 = y.view(-1, y.shape[-1]) if y.dim() != 2 else y
+    if y2.stride(1) != 1 or y2.size(0) != T:
+        raise ValueError("y must be [T, width] with contiguous rows")
+    bias_arr = None
+    if lora_bias_stacked is not None:
+        if len(lora_bias_stacked) != S:
+            raise ValueError("lora_bias_stacked needs one entry per slice")
+        bl = []
+        for i, (bb, n) in enumerate(zip(lora_bias_stacked, sizes)):
+            if bb is None:
+                bl.append(None)
+                continue
+            _need(bb, "lora_bias_stacked[%d]" % i, torch.bfloat16)
+            if not bb.is_contiguous() or bb.numel() != L * n:
+                raise ValueError("lora_bias_stacked[%d] must be [%d, %d]" % (i, L, n))
+            bl.append(bb)
+        bias_arr = _ptr_array(bl)
+    size_arr = (ctypes.c_int32 * S)(*sizes)
+    st = _lib.load().lora_expand(x.data_ptr(), _ptr_array(B), bias_arr, size_arr, S, r,
+                                 y2.data_ptr(), y2.stride(0), T, int(offset_start),
+                                 1 if add_inputs else 0, ctypes.byref(meta.c),
+                                 _stream_handle(x.device))
+    _lib.check("lora_expand", st)
+
+
+def add_lora_linear(y: torch.Tensor, x: torch.Tensor, lora_a_stacked, lora_b_stacked,
+                    lora_bias_stacked, scale: float, output_slices, meta: LoRAKernelMeta,
+                    *, buffer: Optional[torch.Tensor] = None) -> None:
+    """PunicaWrapperGPU.add_lora_linear: shrink into an fp32 buffer, then
+    expand into y with the bias fused into the expand kernel."""
+    A = _weights(lora_a_stacked, "lora_a_stacked")
+    B = _weights(lora_b_stacked, "lora_b_stacked")
+    if not len(A) == len(B) == len(output_slices):
+        raise ValueError("lora_a_stacked, lora_b_stacked and output_slices differ in length")
+    if lora_bias_stacked is not None and len(lora_bias_stacked) != len(output_slices):
+        raise ValueError("lora_bias_stacked needs one entry per slice")
+    for b, n in zip(B, output_slices):
+        if b.size(1) != n:
+            raise ValueError("lora_b_stacked widths must match output_slices")
+    x2 = x.view(-1, x.shape[-1])
+    r = B[0].size(-1)
+    if buffer is None:
+        buffer = torch.zeros((len(output_slices), x2.size(0), r), dtype=torch.float32,
+                             device=x.device)
+    lora_shrink(x2, A, buffer, meta, scale)
+    lora_expand(buffer, B, y, meta, 0, True, lora_bias_stacked)

@@ -1,0 +1,40 @@
+// lora_api.cu -- library-wide C entry points (status names, version) and
+// the host helpers the launchers share.
+#include "lora_common.cuh"
+
+namespace lora {
+
+int device_sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 1;
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+}  // namespace lora
+
+LORA_API const char *lora_status_string(int status)
+{
+    switch (status) {
+    case LORA_OK: return "ok";
+    case LORA_ERR_NULL: return "a required pointer is NULL";
+    case LORA_ERR_SIZE: return "a size is negative or out of range";
+    case LORA_ERR_ALIGN: return "a pointer or stride breaks the 16-byte alignment rule";
+    case LORA_ERR_RANK: return "rank must be a multiple of 8 in [8, 128]";
+    case LORA_ERR_SLICES: return "num_slices must be in [1, 8]";
+    case LORA_ERR_TOKENS: return "num_tokens exceeds meta->max_num_tokens";
+    case LORA_ERR_WIDTH: return "offset_start + sum(slice_sizes) exceeds y_ld";
+    case LORA_ERR_DEVICE: return "no usable CUDA device";
+    default: break;
+    }
+    if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));
+    return "unknown status";
+}
+
+LORA_API int lora_version(void) { return LORA_PUNICA_VERSION; }

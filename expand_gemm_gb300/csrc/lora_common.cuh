@@ -1,0 +1,148 @@
+// lora_common.cuh -- device helpers shared by the metadata, shrink and
+// expand kernels: inline-PTX wrappers (cp.async, ldmatrix, mma.sync), the
+// shared-memory swizzle, and the segment -> tile schedule that both GEMM
+// kernels walk.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lora_punica.h"
+
+#define LORA_API extern "C" __attribute__((visibility("default")))
+
+namespace lora {
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global -> shared copy, cached in L2 only.  When `valid` is false
+// nothing is read and the 16 destination bytes are zero-filled; `src` must
+// still be a mapped address, so callers pass a known-good base pointer.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
+{
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n"
+                 :: "r"(dst), "l"(src), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;\n" :: "n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                            uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+// D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two fp32 -> packed bf16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t v) { return __uint_as_float(uint32_t(v) << 16); }
+
+// ------------------------------------------------------------ swizzle
+//
+// A K-contiguous bf16 tile is stored as rows of CPR 16-byte chunks.  ldmatrix
+// reads one 16-byte chunk from each of 8 consecutive rows; the XOR below
+// spreads those 8 chunks over all 32 banks for every CPR used here (2, 4, 8,
+// 16), which makes both the cp.async writes and the ldmatrix reads
+// conflict-free.
+template <int CPR>
+__device__ __forceinline__ uint32_t swz(int row, int chunk)
+{
+    static_assert(CPR == 2 || CPR == 4 || CPR >= 8, "chunks per row");
+    int phys;
+    if constexpr (CPR >= 8) {
+        phys = (chunk & ~7) | ((chunk ^ row) & 7);
+    } else {
+        constexpr int SHIFT = (CPR == 4) ? 1 : 2;      // rows that share a bank line
+        phys = chunk ^ ((row >> SHIFT) & (CPR - 1));
+    }
+    return static_cast<uint32_t>(row * CPR * 16 + phys * 16);
+}
+
+// ----------------------------------------------------------- schedule
+//
+// The metadata step leaves, for k < nbins, active_lora_ids[k] and
+// num_tokens_per_lora[k] (segment k of the sorted token order starts at
+// lora_token_start_loc[k]).  A GEMM kernel cuts every segment with a valid
+// id into tiles of `tile_rows` tokens.  build_tile_table() writes
+// s_tile[k] = number of tiles in segments before k (s_tile[nbins] = total)
+// and returns the total; every thread of the block gets it.
+__device__ __forceinline__ int build_tile_table(const int32_t *active, const int32_t *counts,
+                                                int nbins, int tile_rows, int *s_tile)
+{
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int carry = 0;
+        for (int b0 = 0; b0 < nbins; b0 += 32) {
+            const int k = b0 + lane;
+            int n = 0;
+            if (k < nbins) {
+                const int id = active[k];
+                const int c = counts[k];
+                n = (id >= 0 && c > 0) ? (c + tile_rows - 1) / tile_rows : 0;
+            }
+            int v = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (k < nbins) s_tile[k] = carry + v - n;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) s_tile[nbins] = carry;
+    }
+    __syncthreads();
+    return s_tile[nbins];
+}
+
+// Segment that holds global tile `tile`: the last k with s_tile[k] <= tile.
+__device__ __forceinline__ int find_segment(const int *s_tile, int nbins, int tile)
+{
+    int lo = 0, hi = nbins;          // answer in [lo, hi)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_tile[mid] <= tile) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+}  // namespace lora
+
+// Host-side launch helpers (lora_api.cu).
+namespace lora {
+int device_sm_count();
+}

@@ -1,0 +1,191 @@
+/*
+ * lora_punica.h -- C ABI of the GB300 (sm_103a) multi-LoRA shrink/expand
+ * library (liblora_punica.so).
+ *
+ * The three entry points are the three steps of the Punica-style batched
+ * LoRA apply described by vLLM's API pages:
+ *
+ *   lora_meta_prepare  page "vllm.lora.ops.triton_ops.lora_kernel_metadata",
+ *                      class LoRAKernelMeta, methods make / _reset /
+ *                      prepare_tensors / meta_args.
+ *   lora_shrink        page "vllm.lora.punica_wrapper.punica_gpu", method
+ *                      PunicaWrapperGPU.add_shrink and its lora_shrink call
+ *                      (argument order x, lora_a_stacked, y, meta, scale).
+ *   lora_expand        same page, method PunicaWrapperGPU.add_expand and its
+ *                      lora_expand call (x, lora_b_stacked, y, meta,
+ *                      offset_start, add_inputs); the bias step of
+ *                      PunicaWrapperTPU._apply_bias (page
+ *                      "vllm.lora.punica_wrapper.punica_tpu") is fused into
+ *                      it.
+ *
+ * Conventions shared by every call:
+ *   - Every data pointer is a DEVICE pointer owned by the caller; the
+ *     library allocates nothing and keeps no pointer after a call returns.
+ *     Arrays of per-slice pointers (lora_a, lora_b, lora_bias) and
+ *     slice_sizes are HOST arrays, read during the call only.
+ *   - bf16 tensors are passed as pointers to their raw 16-bit patterns
+ *     (lora_bf16_t).  All tensors are row-major and dense unless a leading
+ *     dimension argument says otherwise.
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t passed
+ *     as void*; NULL is the legacy default stream).  Nothing is
+ *     synchronised and nothing is read back to the host.
+ *   - Return value: 0 on success; a negative LORA_ERR_* code when an
+ *     argument is rejected on the host (nothing is launched); a positive
+ *     cudaError_t when a launch fails.  lora_status_string() names both.
+ *   - Invalid LoRA ids (outside [-1, max_loras)) are not host errors: the
+ *     metadata kernel counts them into meta->error_word and treats those
+ *     tokens as having no LoRA, so shrink/expand skip them.
+ *   - The no-LoRA early exit is taken on the device: shrink and expand read
+ *     *meta->no_lora_flag and return at once when it is set, so a whole
+ *     forward pass stays capturable in a CUDA graph with no host sync.
+ */
+#ifndef LORA_PUNICA_H
+#define LORA_PUNICA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Raw bit pattern of one bfloat16 value. */
+typedef uint16_t lora_bf16_t;
+
+#define LORA_PUNICA_VERSION 1
+#define LORA_MAX_SLICES 8      /* slices per shrink/expand call          */
+#define LORA_MAX_LORAS 1024    /* max_loras accepted by the metadata step */
+#define LORA_MAX_RANK 128      /* rank r: a multiple of 8, 8 <= r <= 128 */
+
+enum lora_status {
+    LORA_OK = 0,
+    LORA_ERR_NULL = -1,        /* a required pointer is NULL               */
+    LORA_ERR_SIZE = -2,        /* a size is negative or out of range       */
+    LORA_ERR_ALIGN = -3,       /* a pointer / stride breaks an alignment rule */
+    LORA_ERR_RANK = -4,        /* rank not a multiple of 8 in [8, 128]      */
+    LORA_ERR_SLICES = -5,      /* num_slices not in [1, LORA_MAX_SLICES]    */
+    LORA_ERR_TOKENS = -6,      /* num_tokens > meta->max_num_tokens         */
+    LORA_ERR_WIDTH = -7,       /* offset_start + sum(slice_sizes) > y_ld    */
+    LORA_ERR_DEVICE = -8       /* no usable CUDA device / wrong architecture */
+};
+
+/*
+ * Per-forward metadata, the device-side counterpart of LoRAKernelMeta
+ * (page "vllm.lora.ops.triton_ops.lora_kernel_metadata", LoRAKernelMeta.make
+ * gives the buffer sizes).  The caller allocates every buffer once (int32,
+ * device memory) and may reuse them for every forward pass:
+ *   token_lora_mapping                [max_num_tokens]  copy of the id map
+ *   token_indices_sorted_by_lora_ids  [max_num_tokens]  stable argsort
+ *   num_tokens_per_lora               [max_loras + 1]   tokens per active id
+ *   lora_token_start_loc              [max_loras + 2]   0, running sums
+ *   active_lora_ids                   [max_loras + 1]   ascending, pad -1
+ *   no_lora_flag                      [1]               1 = every id is -1
+ *   error_word                        [1]               invalid ids counted
+ * The same struct (by pointer) is then handed to lora_shrink/lora_expand;
+ * they read it on the device.  The struct itself is host memory and is only
+ * read during each call.
+ */
+typedef struct lora_meta {
+    int32_t *token_lora_mapping;
+    int32_t *token_indices_sorted_by_lora_ids;
+    int32_t *num_tokens_per_lora;
+    int32_t *lora_token_start_loc;
+    int32_t *active_lora_ids;
+    int32_t *no_lora_flag;
+    int32_t *error_word;
+    int32_t max_loras;
+    int32_t max_num_tokens;
+} lora_meta_t;
+
+/*
+ * lora_meta_prepare -- LoRAKernelMeta.prepare_tensors on the device.
+ *
+ *   token_lora_mapping  device int32 [num_tokens], LoRA id per token, -1 =
+ *                       no LoRA.
+ *   num_tokens          0 <= num_tokens <= meta->max_num_tokens.
+ *   meta                buffers as described above; 1 <= max_loras <=
+ *                       LORA_MAX_LORAS.
+ *
+ * Writes, in one kernel: the reset values (active ids -1, counts 0,
+ * start_loc 0); no_lora_flag = all(ids == -1) (true for num_tokens == 0);
+ * and, only when the flag is false: the mapping copy, the stable permutation
+ * of tokens sorted by id (ties keep token order, so id -1 tokens come
+ * first), the distinct ids in ascending order with their counts, and
+ * start_loc[k + 1] = counts[0] + ... + counts[k].  error_word receives the
+ * number of ids outside [-1, max_loras); those tokens are sorted as -1.
+ * Result: bit-exact, deterministic.
+ */
+int lora_meta_prepare(const int32_t *token_lora_mapping, int32_t num_tokens,
+                      const lora_meta_t *meta, void *stream);
+
+/*
+ * lora_shrink -- y[s][t, :] += scale * x[t, :] @ lora_a[s][id(t)]^T for
+ * every slice s and every token t whose id is not -1 (page
+ * "vllm.lora.punica_wrapper.punica_gpu", PunicaWrapperGPU.add_shrink,
+ * "Semantics").  Rows of tokens without a LoRA are not touched.
+ *
+ *   x           device bf16 [num_tokens, x_ld]; the first `hidden` values of
+ *               each row are used.  16-byte aligned, x_ld % 8 == 0.
+ *   num_tokens  rows of x, <= meta->max_num_tokens; the metadata must have
+ *               been prepared for exactly these tokens.
+ *   hidden      H, a multiple of 8.
+ *   lora_a      host array of num_slices device pointers, each bf16
+ *               [max_loras, rank, hidden] (a leading singleton layer
+ *               dimension is the same layout), 16-byte aligned.
+ *   rank        r, a multiple of 8 in [8, LORA_MAX_RANK].
+ *   y           device fp32 [num_slices, num_tokens, rank], 16-byte
+ *               aligned; accumulated into (the caller zeroes it first to
+ *               get a plain product).
+ *   scale       multiplies the product before it is added.
+ *
+ * Accumulation is fp32 on the tensor cores; when the hidden dimension is
+ * split across CTAs the partial sums are added with fp32 atomics, so the
+ * rounding order is not fixed from run to run.
+ */
+int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidden,
+                int64_t x_ld, const lora_bf16_t *const *lora_a,
+                int32_t num_slices, int32_t rank, float *y,
+                const lora_meta_t *meta, float scale, void *stream);
+
+/*
+ * lora_expand -- for every slice s and token t whose id is not -1:
+ *   v = x[s][t, :] @ lora_b[s][id(t)]^T + (bias ? lora_bias[s][id(t)] : 0)
+ *   y[t, off_s : off_s + n_s] = (add_inputs ? y[t, off_s : off_s + n_s] : 0) + v
+ * with off_s = offset_start + n_0 + ... + n_{s-1} (page
+ * "vllm.lora.punica_wrapper.punica_gpu", PunicaWrapperGPU.add_expand,
+ * "Semantics"; bias as PunicaWrapperTPU._apply_bias).  Rows of tokens
+ * without a LoRA, and columns outside the slices, are not touched.
+ *
+ *   x            device fp32 [num_slices, num_tokens, rank], 16-byte aligned
+ *                (the shrink output).
+ *   lora_b       host array of num_slices device pointers, each bf16
+ *                [max_loras, n_s, rank], 16-byte aligned.
+ *   lora_bias    NULL, or a host array of num_slices entries, each NULL or
+ *                a device pointer to bf16 [max_loras, n_s].
+ *   slice_sizes  host int32 [num_slices], n_s >= 1.
+ *   y            device bf16 [num_tokens, y_ld],
+ *                offset_start + sum(n_s) <= y_ld.
+ *   add_inputs   nonzero: add to y; zero: overwrite the slice columns.
+ *
+ * x is rounded to bf16 for the tensor cores (as the Triton kernel does when
+ * it casts its input to the weight type); products accumulate in fp32; y,
+ * the bias and the product are summed in fp32 and rounded to bf16 once
+ * (round to nearest even).  Output: deterministic.
+ */
+int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
+                const lora_bf16_t *const *lora_bias,
+                const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
+                lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
+                int32_t offset_start, int32_t add_inputs,
+                const lora_meta_t *meta, void *stream);
+
+/* Human-readable name of a status (negative LORA_ERR_* or cudaError_t). */
+const char *lora_status_string(int status);
+
+/* LORA_PUNICA_VERSION of the loaded library. */
+int lora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_PUNICA_H */

@@ -1,0 +1,115 @@
+"""GPU parity of lora_meta_prepare against the oracle: bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from gpu_helpers import dev_i32
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 0x5A5A5A5A
+
+
+def _gpu_meta(ids: np.ndarray, L: int, max_tokens: int | None = None):
+    import expand_gemm_gb300 as eg
+    T = ids.shape[0]
+    meta = eg.LoRAKernelMeta.make(L, max_tokens or max(T, 1), "cuda")
+    for t in (meta.token_lora_mapping, meta.token_indices_sorted_by_lora_ids,
+              meta.active_lora_ids, meta.num_tokens_per_lora, meta.lora_token_start_loc,
+              meta.no_lora_flag, meta.error_word):
+        t.fill_(SENTINEL)
+    meta.prepare_tensors(dev_i32(ids))
+    torch.cuda.synchronize()
+    return meta
+
+
+def _check(ids: np.ndarray, L: int, oracle_mod, max_tokens=None):
+    T = ids.shape[0]
+    g = _gpu_meta(ids, L, max_tokens)
+    o = oracle_mod.meta_prepare(ids, L, oracle_mod.Meta(L, max(T, 1), fill=SENTINEL))
+    flag = int(g.no_lora_flag.item())
+    assert flag == int(o.no_lora_flag[0])
+    np.testing.assert_array_equal(g.active_lora_ids.cpu().numpy(), o.active_lora_ids)
+    np.testing.assert_array_equal(g.num_tokens_per_lora.cpu().numpy(), o.num_tokens_per_lora)
+    np.testing.assert_array_equal(g.lora_token_start_loc.cpu().numpy(), o.lora_token_start_loc)
+    assert int(g.error_word.item()) == o.invalid_ids
+    if flag:
+        # early exit: neither side writes the copy or the permutation
+        assert (g.token_lora_mapping.cpu().numpy() == SENTINEL).all()
+        assert (g.token_indices_sorted_by_lora_ids.cpu().numpy() == SENTINEL).all()
+    else:
+        np.testing.assert_array_equal(g.token_indices_sorted_by_lora_ids[:T].cpu().numpy(),
+                                      o.token_indices_sorted_by_lora_ids[:T])
+        np.testing.assert_array_equal(g.token_lora_mapping[:T].cpu().numpy(),
+                                      o.token_lora_mapping[:T])
+    return g
+
+
+@pytest.mark.parametrize("seed,T,L,p_none", [
+    (0, 1, 1, 0.0), (1, 31, 3, 0.2), (2, 32, 4, 0.0), (3, 33, 4, 0.5),
+    (4, 1000, 7, 0.1), (5, 1023, 16, 0.0), (6, 1025, 64, 0.3), (7, 4097, 2, 0.9),
+    (8, 16384, 64, 0.2), (9, 65536, 1024, 0.05), (10, 70001, 300, 0.0),
+    (11, 5, 1024, 0.0)])
+def test_meta_random_maps(oracle_mod, seed, T, L, p_none):
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(0, L, size=T).astype(np.int32)
+    ids[rng.random(T) < p_none] = -1
+    _check(ids, L, oracle_mod)
+
+
+def test_meta_sorted_runs_and_single_id(oracle_mod):
+    ids = np.repeat(np.array([3, -1, 0, 3, 2], np.int32), [100, 7, 300, 1, 64])
+    _check(ids, 4, oracle_mod)
+    _check(np.full(777, 2, np.int32), 3, oracle_mod)
+
+
+def test_meta_worked_example_maps(oracle_mod):
+    rng = np.random.default_rng(0)
+    for ids_, counts in (([-1, 0, 1, 2], [3, 10, 5, 2]), ([-1, 0, 2, 1], [3, 10, 5, 2])):
+        m = np.repeat(np.array(ids_, np.int32), counts)
+        rng.shuffle(m)
+        g = _check(m, 3, oracle_mod)
+        if ids_[2] == 1:
+            assert g.lora_token_start_loc.cpu().tolist() == [0, 3, 13, 18, 20]
+
+
+def test_meta_no_lora_and_empty(oracle_mod):
+    g = _check(np.full(4096, -1, np.int32), 8, oracle_mod)
+    assert g.no_lora()
+    g = _check(np.zeros(0, np.int32), 8, oracle_mod, max_tokens=16)
+    assert g.no_lora()
+
+
+def test_meta_invalid_ids_counted(oracle_mod):
+    ids = np.array([0, 9, -1, 2, -7, 0, 3, 3, 1 << 30], np.int32)
+    g = _check(ids, 3, oracle_mod)
+    assert int(g.error_word.item()) == 4
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "mlp", "large", "none"])
+def test_meta_workload_maps(oracle_mod, name):
+    w = W.WORKLOADS[name]
+    rng = np.random.default_rng(w.seed)
+    ids = W.token_ids(w, rng)
+    _check(ids, w.max_loras, oracle_mod)
+
+
+def test_meta_reuse_across_batches(oracle_mod):
+    """Buffers reused for a smaller batch after a larger one (stale tail)."""
+    import expand_gemm_gb300 as eg
+    L = 8
+    meta = eg.LoRAKernelMeta.make(L, 5000, "cuda")
+    rng = np.random.default_rng(5)
+    for T in (5000, 300, 0, 4999, 1):
+        ids = rng.integers(-1, L, size=T).astype(np.int32)
+        meta.prepare_tensors(dev_i32(ids))
+        torch.cuda.synchronize()
+        o = oracle_mod.meta_prepare(ids, L)
+        assert int(meta.no_lora_flag.item()) == int(o.no_lora_flag[0])
+        np.testing.assert_array_equal(meta.active_lora_ids.cpu().numpy(), o.active_lora_ids)
+        np.testing.assert_array_equal(meta.num_tokens_per_lora.cpu().numpy(), o.num_tokens_per_lora)
+        np.testing.assert_array_equal(meta.lora_token_start_loc.cpu().numpy(), o.lora_token_start_loc)
+        if not o.no_lora_flag[0]:
+            np.testing.assert_array_equal(meta.token_indices_sorted_by_lora_ids[:T].cpu().numpy(),
+                                          o.token_indices_sorted_by_lora_ids[:T])

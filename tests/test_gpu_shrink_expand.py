@@ -1,0 +1,226 @@
+"""GPU parity of lora_shrink / lora_expand against the fp64 oracle.
+
+Sizes are ones the oracle finishes in seconds but that still span several
+token tiles, hidden chunks and column chunks, with ragged tails; the edge
+cases cover empty and all-no-LoRA batches, a single token, padded ranks,
+ragged hidden sizes, strided x, eight slices, unaligned outputs (scalar
+epilogue), overwrite mode and offsets.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from gpu_helpers import (EXPAND_ATOL, EXPAND_RTOL, SHRINK_ATOL, SHRINK_RTOL, assert_close,
+                         bits_to_f64, dev_bf16, dev_f32, dev_i32, host_bits)
+
+pytestmark = pytest.mark.gpu
+
+
+def _eg():
+    import expand_gemm_gb300 as eg
+    return eg
+
+
+def _meta(ids, L):
+    eg = _eg()
+    meta = eg.LoRAKernelMeta.make(L, max(ids.shape[0], 1), "cuda")
+    meta.prepare_tensors(dev_i32(ids))
+    return meta
+
+
+def _run_shrink(inp, ids, scale, buf0=None, x_pad=0):
+    eg = _eg()
+    T, H = inp.x.shape
+    if x_pad:
+        xw = torch.zeros((T, H + x_pad), dtype=torch.bfloat16, device="cuda")
+        xw[:, :H] = dev_bf16(inp.x)
+        x = xw[:, :H]
+    else:
+        x = dev_bf16(inp.x)
+    A = [dev_bf16(a) for a in inp.lora_a]
+    buf = dev_f32(inp.buf if buf0 is None else buf0)
+    meta = _meta(ids, inp.lora_a[0].shape[0])
+    eg.lora_shrink(x, A, buf, meta, scale)
+    torch.cuda.synchronize()
+    return buf.cpu().numpy()
+
+
+def _shrink_case(oracle_mod, inp, ids=None, scale=None, buf0=None, x_pad=0):
+    ids = inp.ids if ids is None else ids
+    scale = inp.workload.scale if scale is None else scale
+    b0 = inp.buf if buf0 is None else buf0
+    got = _run_shrink(inp, ids, scale, b0, x_pad)
+    ref = oracle_mod.shrink(inp.x, inp.lora_a, ids, scale, b0)
+    assert_close(got, ref, SHRINK_ATOL, SHRINK_RTOL, "shrink")
+    none = (ids < 0) | (ids >= inp.lora_a[0].shape[0])
+    np.testing.assert_array_equal(got[:, none], b0[:, none])     # bit-untouched
+    return got
+
+
+def _custom(T, H, r, L, slices, seed, ids="uniform", p_none=0.0, bias=False, scale=1.0):
+    w = W.Workload("custom", seed, T, H, r, L, tuple(slices), ids, p_none=p_none,
+                   seq_len=(3, 40), bias=bias, scale=scale)
+    return W.generate(w)
+
+
+# ------------------------------------------------------------------ shrink
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("prefill", 1536),
+                                    ("mlp", 512), ("large", 384)])
+def test_shrink_workloads_reduced(oracle_mod, name, T):
+    inp = W.generate(name, num_tokens=T)
+    _shrink_case(oracle_mod, inp)
+
+
+@pytest.mark.parametrize("T,H,r,L,S", [
+    (1, 64, 16, 1, 1),          # single token
+    (7, 200, 8, 3, 2),          # ragged hidden (not a multiple of 64), rank 8
+    (130, 512, 24, 5, 3),       # padded rank 24 -> 32, ragged token tile
+    (257, 1024, 128, 4, 1),     # rank 128
+    (96, 136, 40, 6, 8),        # eight slices, rank 40 -> 64
+    (3000, 256, 16, 2, 1),      # many tiles, no split
+])
+def test_shrink_shapes(oracle_mod, T, H, r, L, S):
+    inp = _custom(T, H, r, L, [16] * S, seed=T + H + r)
+    _shrink_case(oracle_mod, inp, scale=0.37)
+
+
+def test_shrink_accumulates_and_scales(oracle_mod):
+    inp = _custom(300, 512, 32, 4, [8, 8], seed=9)
+    rng = np.random.default_rng(0)
+    b0 = rng.standard_normal(inp.buf.shape).astype(np.float32)
+    _shrink_case(oracle_mod, inp, scale=-1.5, buf0=b0)
+    got = _run_shrink(inp, inp.ids, 0.0, b0)
+    np.testing.assert_array_equal(got, b0)
+
+
+def test_shrink_strided_x(oracle_mod):
+    inp = _custom(200, 264, 16, 3, [8], seed=11)
+    _shrink_case(oracle_mod, inp, x_pad=24)
+
+
+def test_shrink_zipf_segments_and_no_lora(oracle_mod):
+    inp = _custom(2000, 256, 16, 9, [8, 8, 8], seed=12, ids="zipf_seq", p_none=0.3)
+    _shrink_case(oracle_mod, inp)
+    none = np.full(2000, -1, np.int32)
+    b0 = np.random.default_rng(1).standard_normal(inp.buf.shape).astype(np.float32)
+    got = _run_shrink(inp, none, 1.0, b0)
+    np.testing.assert_array_equal(got, b0)
+
+
+def test_shrink_invalid_ids_skipped(oracle_mod):
+    inp = _custom(100, 128, 16, 3, [8], seed=13)
+    ids = inp.ids.copy()
+    ids[::7] = 5
+    ids[::11] = -4
+    _shrink_case(oracle_mod, inp, ids=ids)
+
+
+# ------------------------------------------------------------------ expand
+
+def _run_expand(inp, ids, xin, y_bits, slices, offset, add_inputs, bias, y_col_pad=0):
+    eg = _eg()
+    B = [dev_bf16(b) for b in inp.lora_b]
+    bias_d = None if bias is None else [None if b is None else dev_bf16(b) for b in bias]
+    if y_col_pad:
+        T, ld = y_bits.shape
+        yw = torch.zeros((T, ld + y_col_pad), dtype=torch.bfloat16, device="cuda")
+        yw[:, :ld] = dev_bf16(y_bits)
+        y = yw[:, :ld]
+    else:
+        y = dev_bf16(y_bits)
+    meta = _meta(ids, inp.lora_b[0].shape[0])
+    eg.lora_expand(dev_f32(xin), B, y, meta, offset, add_inputs, bias_d)
+    torch.cuda.synchronize()
+    return host_bits(y)
+
+
+def _expand_case(oracle_mod, inp, ids=None, xin=None, offset=0, add_inputs=True,
+                 bias="workload", y_extra=0, y_col_pad=0):
+    ids = inp.ids if ids is None else ids
+    S, T, r = inp.buf.shape
+    if xin is None:
+        xin = np.random.default_rng(7).standard_normal((S, T, r)).astype(np.float32)
+    bias = inp.lora_bias if bias == "workload" else bias
+    slices = list(inp.workload.slices)
+    width = offset + sum(slices) + y_extra
+    y0 = W.normal_bf16(np.random.default_rng(8), (T, width), 1.0)
+    got = _run_expand(inp, ids, xin, y0, slices, offset, add_inputs, bias, y_col_pad)
+    ref = oracle_mod.expand(xin, inp.lora_b, ids, y0, slices, offset, add_inputs, bias)
+    assert_close(bits_to_f64(got), ref, EXPAND_ATOL, EXPAND_RTOL, "expand")
+    none = (ids < 0) | (ids >= inp.lora_b[0].shape[0])
+    np.testing.assert_array_equal(got[none], y0[none])                   # rows untouched
+    np.testing.assert_array_equal(got[:, :offset], y0[:, :offset])       # columns untouched
+    np.testing.assert_array_equal(got[:, offset + sum(slices):], y0[:, offset + sum(slices):])
+    return got
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("prefill", 1536),
+                                    ("mlp", 512), ("large", 384)])
+def test_expand_workloads_reduced(oracle_mod, name, T):
+    inp = W.generate(name, num_tokens=T)
+    _expand_case(oracle_mod, inp)
+
+
+@pytest.mark.parametrize("T,r,L,slices,offset,y_extra", [
+    (1, 16, 1, (128,), 0, 0),
+    (70, 8, 3, (200, 56), 0, 8),          # ragged column chunk, rank 8
+    (300, 24, 4, (64, 64, 64), 16, 0),    # padded rank, offset
+    (129, 128, 2, (1024, 136), 8, 24),    # rank 128
+    (50, 32, 5, (16,) * 8, 0, 0),         # eight slices
+])
+def test_expand_shapes(oracle_mod, T, r, L, slices, offset, y_extra):
+    rng_bias = [True, False][T % 2]
+    inp = _custom(T, 64, r, L, slices, seed=T + r, bias=rng_bias)
+    _expand_case(oracle_mod, inp, offset=offset, y_extra=y_extra)
+
+
+@pytest.mark.parametrize("slices,offset", [((100, 7), 0), ((64, 64), 3), ((13,), 5)])
+def test_expand_unaligned_scalar_path(oracle_mod, slices, offset):
+    inp = _custom(90, 64, 16, 3, slices, seed=21, bias=True)
+    _expand_case(oracle_mod, inp, offset=offset, y_extra=1)
+
+
+def test_expand_overwrite_mode(oracle_mod):
+    inp = _custom(333, 64, 32, 4, (256, 128), seed=22, bias=True)
+    _expand_case(oracle_mod, inp, add_inputs=False, offset=8, y_extra=16)
+    _expand_case(oracle_mod, inp, add_inputs=False, offset=3, y_extra=1)   # scalar path
+
+
+def test_expand_partial_bias_and_strided_y(oracle_mod):
+    inp = _custom(150, 64, 16, 3, (128, 64, 64), seed=23, bias=True)
+    bias = [inp.lora_bias[0], None, inp.lora_bias[2]]
+    _expand_case(oracle_mod, inp, bias=bias, y_col_pad=40)
+
+
+def test_expand_no_lora_batch_untouched(oracle_mod):
+    inp = _custom(500, 64, 16, 3, (256,), seed=24, bias=True)
+    _expand_case(oracle_mod, inp, ids=np.full(500, -1, np.int32))
+
+
+def test_expand_invalid_ids_skipped(oracle_mod):
+    inp = _custom(100, 64, 16, 3, (128,), seed=25)
+    ids = inp.ids.copy()
+    ids[::5] = 3
+    _expand_case(oracle_mod, inp, ids=ids)
+
+
+# ------------------------------------------------------------- composition
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("mlp", 256)])
+def test_add_lora_linear_matches_oracle_composition(oracle_mod, name, T):
+    eg = _eg()
+    inp = W.generate(name, num_tokens=T)
+    w = inp.workload
+    x = dev_bf16(inp.x)
+    y = dev_bf16(inp.y)
+    A = [dev_bf16(a) for a in inp.lora_a]
+    B = [dev_bf16(b) for b in inp.lora_b]
+    bias = None if inp.lora_bias is None else [dev_bf16(b) for b in inp.lora_bias]
+    meta = _meta(inp.ids, w.max_loras)
+    eg.add_lora_linear(y, x, A, B, bias, w.scale, w.slices, meta)
+    torch.cuda.synchronize()
+    buf = oracle_mod.shrink(inp.x, inp.lora_a, inp.ids, w.scale, inp.buf).astype(np.float32)
+    ref = oracle_mod.expand(buf, inp.lora_b, inp.ids, inp.y, w.slices, 0, True, inp.lora_bias)
+    assert_close(bits_to_f64(host_bits(y)), ref, EXPAND_ATOL, EXPAND_RTOL, "add_lora_linear")
