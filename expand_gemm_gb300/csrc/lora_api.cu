@@ -1,5 +1,7 @@
 // lora_api.cu -- library-wide C entry points (status names, version) and
 // the host helpers the launchers share.
+#include <stdlib.h>
+
 #include "lora_common.cuh"
 
 namespace lora {
@@ -15,6 +17,18 @@ int device_sm_count()
         n = 1;
     if (dev < 64) cache[dev] = n;
     return n;
+}
+
+// Programmatic dependent launch is on unless LORA_PUNICA_PDL=0 is set in
+// the environment (read once).
+bool pdl_enabled()
+{
+    static int cached = -1;
+    if (cached < 0) {
+        const char *v = getenv("LORA_PUNICA_PDL");
+        cached = (v != nullptr && v[0] == '0') ? 0 : 1;
+    }
+    return cached == 1;
 }
 
 }  // namespace lora

@@ -92,17 +92,63 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk)
     return static_cast<uint32_t>(row * CPR * 16 + phys * 16);
 }
 
+// Programmatic dependent launch.  Every kernel waits for the grids it
+// depends on before its first global read, then lets the next kernel in the
+// stream begin its launch (which overlaps that kernel's launch latency with
+// this kernel's work).  Both are no-ops when the launch carried no
+// programmatic dependency.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // ----------------------------------------------------------- schedule
 //
-// The metadata step leaves, for k < nbins, active_lora_ids[k] and
-// num_tokens_per_lora[k] (segment k of the sorted token order starts at
-// lora_token_start_loc[k]).  A GEMM kernel cuts every segment with a valid
-// id into tiles of `tile_rows` tokens.  build_tile_table() writes
-// s_tile[k] = number of tiles in segments before k (s_tile[nbins] = total)
-// and returns the total; every thread of the block gets it.
-__device__ __forceinline__ int build_tile_table(const int32_t *active, const int32_t *counts,
-                                                int nbins, int tile_rows, int *s_tile)
+// Segment table held in shared memory (4 * nbins + 2 ints):
+//   tile[k]  (k <= nbins)  tiles in segments before k (tile[nbins] = total)
+//   id[k], start[k], count[k]  copies of active_lora_ids, lora_token_start_loc
+//                              and num_tokens_per_lora
+struct SegTab {
+    int *tile, *id, *start, *count;
+};
+
+__device__ __forceinline__ SegTab seg_tab(int *base, int nbins)
 {
+    SegTab t;
+    t.tile = base;
+    t.id = base + nbins + 1;
+    t.start = t.id + nbins;
+    t.count = t.start + nbins;
+    return t;
+}
+
+__host__ __device__ constexpr size_t seg_tab_bytes(int nbins)
+{
+    return size_t(4 * nbins + 2) * sizeof(int);
+}
+
+// Reads the no-LoRA flag and the whole segment table with one round of
+// independent loads, then scans tile counts.  Returns 0 (no work) when the
+// flag is set; otherwise the total number of tiles of `tile_rows` tokens.
+// Every thread of the block gets the result.
+__device__ __forceinline__ int load_segments(const int32_t *no_lora, const int32_t *active,
+                                             const int32_t *counts, const int32_t *start_loc,
+                                             int nbins, int tile_rows, SegTab t)
+{
+    int *s_flag = t.count + nbins;
+    for (int k = threadIdx.x; k < nbins; k += blockDim.x) {
+        t.id[k] = active[k];
+        t.count[k] = counts[k];
+        t.start[k] = start_loc[k];
+    }
+    if (threadIdx.x == 0) *s_flag = *no_lora;
+    __syncthreads();
+    if (*s_flag) return 0;
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         int carry = 0;
@@ -110,9 +156,8 @@ __device__ __forceinline__ int build_tile_table(const int32_t *active, const int
             const int k = b0 + lane;
             int n = 0;
             if (k < nbins) {
-                const int id = active[k];
-                const int c = counts[k];
-                n = (id >= 0 && c > 0) ? (c + tile_rows - 1) / tile_rows : 0;
+                const int c = t.count[k];
+                n = (t.id[k] >= 0 && c > 0) ? (c + tile_rows - 1) / tile_rows : 0;
             }
             int v = n;
 #pragma unroll
@@ -120,16 +165,18 @@ __device__ __forceinline__ int build_tile_table(const int32_t *active, const int
                 const int u = __shfl_up_sync(0xffffffffu, v, o);
                 if (lane >= o) v += u;
             }
-            if (k < nbins) s_tile[k] = carry + v - n;
+            if (k < nbins) t.tile[k] = carry + v - n;
             carry += __shfl_sync(0xffffffffu, v, 31);
         }
-        if (lane == 0) s_tile[nbins] = carry;
+        if (lane == 0) t.tile[nbins] = carry;
     }
     __syncthreads();
-    return s_tile[nbins];
+    return t.tile[nbins];
 }
 
 // Segment that holds global tile `tile`: the last k with s_tile[k] <= tile.
+// Segments with no tiles (id -1, or no tokens) share their successor's
+// prefix value and are skipped by the search.
 __device__ __forceinline__ int find_segment(const int *s_tile, int nbins, int tile)
 {
     int lo = 0, hi = nbins;          // answer in [lo, hi)
@@ -145,4 +192,25 @@ __device__ __forceinline__ int find_segment(const int *s_tile, int nbins, int ti
 // Host-side launch helpers (lora_api.cu).
 namespace lora {
 int device_sm_count();
+bool pdl_enabled();
+
+// Launch with the programmatic-stream-serialization attribute (when
+// enabled), so the kernel may start while its predecessor drains; the
+// kernel itself calls pdl_wait() before touching memory.
+template <typename Kern, typename Arg>
+cudaError_t launch_kernel(Kern kernel, dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, const Arg &arg)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
 }

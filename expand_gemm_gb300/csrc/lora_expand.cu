@@ -3,27 +3,28 @@
 // PunicaWrapperGPU.add_expand; bias step of page
 // "vllm.lora.punica_wrapper.punica_tpu", PunicaWrapperTPU._apply_bias).
 //
-// Work item = (token tile of one LoRA segment, 128-column chunk of one
-// slice).  Items are numbered tile-fastest, so the CTAs resident at one
-// time share the same B chunk (read once from HBM, then from L2) while the
-// y rows, the dominant traffic, stream through exactly once.
+// Work items are (token tile of one LoRA segment, BN-column chunk of one
+// slice), numbered chunk-fastest.  The grid is persistent and every CTA
+// takes one contiguous, balanced range of items, so a CTA walks the column
+// chunks of one token tile in order: the tile's tokens and its x rows (the
+// MMA's A operand, rounded to bf16) are fetched once and held in registers,
+// while the y tile and the B tile of each chunk stream through a 3-stage
+// cp.async ring.  CTAs that start at the same chunk index of different
+// tiles of one segment share that chunk of B in L2; y, the dominant
+// traffic, is read and written exactly once.
 //
-// Per item: the y tile (64 rows x 128 columns, bf16) is fetched with
-// 16-byte cp.async into shared memory at the start, overlapping the B tile
-// and the fp32 x tile; x is rounded to bf16 while it is staged (the rank-r
-// contraction then runs on mma.sync m16n8k16 with fp32 accumulation).  The
-// epilogue adds bias and the old y in fp32, rounds once to bf16 in place in
-// the shared y tile, and the tile leaves with 128-bit coalesced stores.
-// When y, its stride, the offsets or a slice width are not multiples of 8
-// elements, a scalar epilogue reads and writes y element by element.
+// Epilogue: the product (mma.sync m16n8k16, fp32 accumulate), the bias and
+// the old y are summed in fp32, rounded once to bf16 in place in the shared
+// y tile, and the tile leaves with 128-bit coalesced stores.  When y, its
+// stride, the offsets or a slice width are not multiples of 8 elements, y
+// is not prefetched and a scalar epilogue reads and writes it per element.
 #include "lora_common.cuh"
 
 namespace lora {
 
 constexpr int EX_BM = 64;          // tokens per tile
-constexpr int EX_BN = 128;         // output columns per item
-constexpr int EX_THREADS = 256;    // 8 warps: 2 (rows) x 4 (columns), 32x32 each
-constexpr int EX_Y_LD = EX_BN * 2 + 16;   // bytes per shared y row (padded)
+constexpr int EX_THREADS = 256;    // 8 warps
+constexpr int EX_STAGES = 3;
 
 struct ExpandArgs {
     const float *x;
@@ -38,7 +39,7 @@ struct ExpandArgs {
     int64_t y_ld;
     int32_t num_tokens;
     int32_t add_inputs;
-    int32_t vec;                         // 16-byte epilogue allowed
+    int32_t vec;                         // 16-byte y path allowed
     const int32_t *sorted;
     const int32_t *counts;
     const int32_t *start_loc;
@@ -51,12 +52,25 @@ template <int KT>
 struct ExpandTile {
     static constexpr int RP = 16 * KT;                 // padded rank
     static constexpr int CPR = RP / 8;                 // 16-byte chunks per row
-    static constexpr int A_BYTES = EX_BM * RP * 2;     // bf16 x tile
-    static constexpr int B_BYTES = EX_BN * RP * 2;     // bf16 B tile
-    static constexpr int Y_BYTES = EX_BM * EX_Y_LD;
-    static constexpr int BIAS_BYTES = EX_BN * 4;
-    static constexpr int BYTES = A_BYTES + B_BYTES + Y_BYTES + BIAS_BYTES;
+    static constexpr int BN = (KT >= 8) ? 64 : 128;    // columns per chunk
+    static constexpr int WARPS_M = (BN == 128) ? 2 : 4;
+    static constexpr int WARPS_N = 8 / WARPS_M;
+    static constexpr int WM = EX_BM / WARPS_M;         // rows per warp
+    static constexpr int WN = BN / WARPS_N;            // columns per warp (32)
+    static constexpr int MI = WM / 16;
+    static constexpr int NI = WN / 8;
+    static constexpr int YCH = BN / 8;                 // 16-byte chunks per y row
+    static constexpr int Y_LD = BN * 2 + 16;           // padded shared y row (bytes)
+    static constexpr int Y_BYTES = EX_BM * Y_LD;
+    static constexpr int B_BYTES = BN * RP * 2;
+    static constexpr int STAGE_BYTES = Y_BYTES + B_BYTES;
+    static constexpr int A_BYTES = EX_BM * RP * 2;
+    static constexpr int BYTES = EX_STAGES * STAGE_BYTES + A_BYTES;
+    static_assert(WN == 32 && MI >= 1, "warp tile");
 };
+
+template <int KT>
+constexpr int expand_bn() { return ExpandTile<KT>::BN; }
 
 size_t expand_smem_bytes(int kt, int nbins)
 {
@@ -67,176 +81,207 @@ size_t expand_smem_bytes(int kt, int nbins)
     case 4: t = ExpandTile<4>::BYTES; break;
     default: t = ExpandTile<8>::BYTES; break;
     }
-    return t + size_t(nbins + 1) * sizeof(int);
+    return t + seg_tab_bytes(nbins);
 }
 
 template <int KT>
-__global__ void __launch_bounds__(EX_THREADS) expand_kernel(ExpandArgs p)
+__global__ void __launch_bounds__(EX_THREADS, (KT <= 2) ? 3 : 2) expand_kernel(ExpandArgs p)
 {
     using Cfg = ExpandTile<KT>;
-    constexpr int CPR = Cfg::CPR;
+    constexpr int CPR = Cfg::CPR, BN = Cfg::BN, MI = Cfg::MI, NI = Cfg::NI, YCH = Cfg::YCH;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_tok[EX_BM];
 
-    if (*p.no_lora) return;
+    pdl_wait();
+    pdl_launch_dependents();
 
-    uint8_t *sA = smem;
-    uint8_t *sB = sA + Cfg::A_BYTES;
-    uint8_t *sY = sB + Cfg::B_BYTES;
-    float *sBias = reinterpret_cast<float *>(sY + Cfg::Y_BYTES);
-    int *s_tile = reinterpret_cast<int *>(smem + Cfg::BYTES);
-
-    const int total_tiles = build_tile_table(p.active, p.counts, p.nbins, EX_BM, s_tile);
+    uint8_t *sA = smem + EX_STAGES * Cfg::STAGE_BYTES;
+    const SegTab tab = seg_tab(reinterpret_cast<int *>(sA + Cfg::A_BYTES), p.nbins);
+    const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
+                                          p.nbins, EX_BM, tab);
     if (total_tiles == 0) return;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int wm = warp >> 2, wn = warp & 3;
+    const int wm = warp / Cfg::WARPS_N, wn = warp % Cfg::WARPS_N;
     const int S = p.num_slices, R = p.rank, T = p.num_tokens;
-    const int total_items = total_tiles * p.chunk0[S];
-    const uint32_t aA = smem_addr(sA), aB = smem_addr(sB), aY = smem_addr(sY);
+    const int nchunks = p.chunk0[S];
+    const int64_t total = int64_t(total_tiles) * nchunks;
+    int64_t w = int64_t(blockIdx.x) * total / gridDim.x;
+    const int64_t w_end = int64_t(blockIdx.x + 1) * total / gridDim.x;
+    const uint32_t ring = smem_addr(smem), aA = smem_addr(sA);
+    const bool prefetch_y = p.vec && p.add_inputs;
 
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const int tile = item % total_tiles;
-        const int chunk = item / total_tiles;
+    while (w < w_end) {
+        // ---- one row item: token tile `tile`, slice s, chunks [cb, ce)
+        const int tile = int(w / nchunks);
+        const int cb = int(w - int64_t(tile) * nchunks);
         int s = 0;
-        while (s + 1 < S && p.chunk0[s + 1] <= chunk) ++s;
-        const int n_s = p.n[s];
-        const int c0 = (chunk - p.chunk0[s]) * EX_BN;        // first column in the slice
-        const int ncols = min(EX_BN, n_s - c0);
+        while (s + 1 < S && p.chunk0[s + 1] <= cb) ++s;
+        const int ce = int(min(int64_t(p.chunk0[s + 1]), int64_t(cb) + (w_end - w)));
+        w += ce - cb;
 
-        const int seg = find_segment(s_tile, p.nbins, tile);
-        const int id = p.active[seg];
-        const int row0 = p.start_loc[seg] + (tile - s_tile[seg]) * EX_BM;
-        const int nrows = min(EX_BM, p.start_loc[seg] + p.counts[seg] - row0);
+        const int seg = find_segment(tab.tile, p.nbins, tile);
+        const int id = tab.id[seg];
+        const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * EX_BM;
+        const int nrows = min(EX_BM, tab.start[seg] + tab.count[seg] - row0);
+        const int n_s = p.n[s];
+        const uint16_t *bslice = p.b[s] + int64_t(id) * n_s * R;
+        const uint16_t *bias_row = p.bias[s] ? p.bias[s] + int64_t(id) * n_s : nullptr;
+        uint16_t *yslice = p.y + p.col0[s];
+
         if (tid < EX_BM) s_tok[tid] = (tid < nrows) ? p.sorted[row0 + tid] : -1;
-        if (tid < EX_BN) {
-            const uint16_t *bb = p.bias[s];
-            sBias[tid] = (bb != nullptr && tid < ncols)
-                             ? bf16_to_f32(bb[int64_t(id) * n_s + c0 + tid]) : 0.f;
-        }
         __syncthreads();
 
-        uint16_t *ybase = p.y + p.col0[s] + c0;              // + tok * y_ld
+        auto load_chunk = [&](int slot, int c) {
+            const int c0 = (c - p.chunk0[s]) * BN;
+            const int ncols = min(BN, n_s - c0);
+            const uint32_t sy = ring + slot * Cfg::STAGE_BYTES;
+            const uint32_t sb = sy + Cfg::Y_BYTES;
+            if (prefetch_y) {
+                for (int i = tid; i < EX_BM * YCH; i += EX_THREADS) {
+                    const int r = i / YCH, cc = i - r * YCH;
+                    const int tok = s_tok[r];
+                    const bool ok = tok >= 0 && cc * 8 < ncols;
+                    cp_async16(sy + r * Cfg::Y_LD + cc * 16,
+                               ok ? yslice + int64_t(tok) * p.y_ld + c0 + cc * 8 : p.y, ok);
+                }
+            }
+            for (int i = tid; i < BN * CPR; i += EX_THREADS) {
+                const int r = i / CPR, cc = i - r * CPR;
+                const bool ok = r < ncols && cc * 8 < R;
+                cp_async16(sb + swz<CPR>(r, cc),
+                           ok ? bslice + int64_t(c0 + r) * R + cc * 8 : p.b[s], ok);
+            }
+        };
 
-        // (1) y tile -> shared (vector path, add_inputs only).
-        if (p.vec && p.add_inputs) {
-            for (int i = tid; i < EX_BM * (EX_BN / 8); i += EX_THREADS) {
-                const int r = i >> 4, c = i & 15;
-                const int tok = s_tok[r];
-                const bool ok = tok >= 0 && c * 8 < ncols;
-                cp_async16(aY + r * EX_Y_LD + c * 16,
-                           ok ? ybase + int64_t(tok) * p.y_ld + c * 8 : p.y, ok);
-            }
+#pragma unroll
+        for (int st = 0; st < EX_STAGES - 1; ++st) {
+            if (cb + st < ce) load_chunk(st, cb + st);
+            cp_async_commit();
         }
-        // (2) B tile: 128 rows (columns of the slice) x RP, zero past n_s / R.
-        {
-            const uint16_t *bbase = p.b[s] + (int64_t(id) * n_s + c0) * R;
-            for (int i = tid; i < EX_BN * CPR; i += EX_THREADS) {
-                const int r = i / CPR, c = i - r * CPR;
-                const bool ok = r < ncols && c * 8 < R;
-                cp_async16(aB + swz<CPR>(r, c), ok ? bbase + int64_t(r) * R + c * 8 : p.b[s], ok);
-            }
-        }
-        cp_async_commit();
-        // (3) x tile: fp32 rows of the shrink output, rounded to bf16.
+
+        // x rows of this tile and slice -> bf16 A operand (overlaps the ring fill)
         {
             const float *xs = p.x + int64_t(s) * T * R;
             for (int i = tid; i < EX_BM * CPR; i += EX_THREADS) {
-                const int r = i / CPR, c = i - r * CPR;
+                const int r = i / CPR, cc = i - r * CPR;
                 const int tok = s_tok[r];
                 uint4 v = make_uint4(0, 0, 0, 0);
-                if (tok >= 0 && c * 8 < R) {
-                    const float4 *src = reinterpret_cast<const float4 *>(xs + int64_t(tok) * R + c * 8);
-                    const float4 u = src[0], w = src[1];
+                if (tok >= 0 && cc * 8 < R) {
+                    const float4 *src = reinterpret_cast<const float4 *>(xs + int64_t(tok) * R + cc * 8);
+                    const float4 u = src[0], q = src[1];
                     v.x = pack_bf16x2(u.x, u.y);
                     v.y = pack_bf16x2(u.z, u.w);
-                    v.z = pack_bf16x2(w.x, w.y);
-                    v.w = pack_bf16x2(w.z, w.w);
+                    v.z = pack_bf16x2(q.x, q.y);
+                    v.w = pack_bf16x2(q.z, q.w);
                 }
-                *reinterpret_cast<uint4 *>(sA + swz<CPR>(r, c)) = v;
+                *reinterpret_cast<uint4 *>(sA + swz<CPR>(r, cc)) = v;
+            }
+        }
+        __syncthreads();
+        uint32_t af[MI][KT][4];
+#pragma unroll
+        for (int m = 0; m < MI; ++m)
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                const int r = wm * Cfg::WM + m * 16 + (lane & 15);
+                const int c = kk * 2 + (lane >> 4);
+                ldmatrix_x4(aA + swz<CPR>(r, c), af[m][kk][0], af[m][kk][1], af[m][kk][2],
+                            af[m][kk][3]);
+            }
+
+        for (int i = 0; cb + i < ce; ++i) {
+            cp_async_wait<EX_STAGES - 2>();
+            __syncthreads();
+            {
+                const int nxt = i + EX_STAGES - 1;
+                if (cb + nxt < ce) load_chunk(nxt % EX_STAGES, cb + nxt);
+                cp_async_commit();
+            }
+            const int slot = i % EX_STAGES;
+            const int c0 = (cb + i - p.chunk0[s]) * BN;
+            const int ncols = min(BN, n_s - c0);
+            uint8_t *sy = smem + slot * Cfg::STAGE_BYTES;
+            const uint32_t sb = ring + slot * Cfg::STAGE_BYTES + Cfg::Y_BYTES;
+
+            float bv[NI][2];
+#pragma unroll
+            for (int n = 0; n < NI; ++n)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = wn * Cfg::WN + n * 8 + 2 * (lane & 3) + h;
+                    bv[n][h] = (bias_row != nullptr && c < ncols) ? bf16_to_f32(bias_row[c0 + c]) : 0.f;
+                }
+
+            float acc[MI][NI][4];
+#pragma unroll
+            for (int m = 0; m < MI; ++m)
+#pragma unroll
+                for (int n = 0; n < NI; ++n)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[m][n][q] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+                for (int n2 = 0; n2 < NI / 2; ++n2) {
+                    uint32_t b[4];
+                    const int q = lane >> 3;
+                    const int r = wn * Cfg::WN + n2 * 16 + (q >> 1) * 8 + (lane & 7);
+                    const int c = kk * 2 + (q & 1);
+                    ldmatrix_x4(sb + swz<CPR>(r, c), b[0], b[1], b[2], b[3]);
+#pragma unroll
+                    for (int m = 0; m < MI; ++m) {
+                        mma_bf16_16816(acc[m][2 * n2], af[m][kk], b[0], b[1]);
+                        mma_bf16_16816(acc[m][2 * n2 + 1], af[m][kk], b[2], b[3]);
+                    }
+                }
+
+            if (p.vec) {
+#pragma unroll
+                for (int m = 0; m < MI; ++m)
+#pragma unroll
+                    for (int n = 0; n < NI; ++n)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int r = wm * Cfg::WM + m * 16 + (lane >> 2) + 8 * h;
+                            const int c = wn * Cfg::WN + n * 8 + 2 * (lane & 3);
+                            uint32_t *cell = reinterpret_cast<uint32_t *>(sy + r * Cfg::Y_LD + c * 2);
+                            float v0 = acc[m][n][2 * h] + bv[n][0];
+                            float v1 = acc[m][n][2 * h + 1] + bv[n][1];
+                            if (p.add_inputs) {
+                                const uint32_t old = *cell;
+                                v0 += bf16_lo(old);
+                                v1 += bf16_hi(old);
+                            }
+                            *cell = pack_bf16x2(v0, v1);
+                        }
+                __syncthreads();
+                for (int j = tid; j < EX_BM * YCH; j += EX_THREADS) {
+                    const int r = j / YCH, cc = j - r * YCH;
+                    const int tok = s_tok[r];
+                    if (tok < 0 || cc * 8 >= ncols) continue;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sy + r * Cfg::Y_LD + cc * 16);
+                    *reinterpret_cast<uint4 *>(yslice + int64_t(tok) * p.y_ld + c0 + cc * 8) = v;
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < MI; ++m)
+#pragma unroll
+                    for (int n = 0; n < NI; ++n)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int r = wm * Cfg::WM + m * 16 + (lane >> 2) + 8 * (q >> 1);
+                            const int c = wn * Cfg::WN + n * 8 + 2 * (lane & 3) + (q & 1);
+                            const int tok = s_tok[r];
+                            if (tok < 0 || c >= ncols) continue;
+                            uint16_t *dst = yslice + int64_t(tok) * p.y_ld + c0 + c;
+                            float v = acc[m][n][q] + bv[n][q & 1];
+                            if (p.add_inputs) v += bf16_to_f32(*dst);
+                            *dst = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
+                        }
             }
         }
         cp_async_wait<0>();
-        __syncthreads();
-
-        // (4) 64 x 128 x RP on the tensor cores.
-        float acc[2][4][4];
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-            for (int n = 0; n < 4; ++n)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[m][n][q] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < KT; ++kk) {
-            uint32_t af[2][4];
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int r = wm * 32 + m * 16 + (lane & 15);
-                const int c = kk * 2 + (lane >> 4);
-                ldmatrix_x4(aA + swz<CPR>(r, c), af[m][0], af[m][1], af[m][2], af[m][3]);
-            }
-#pragma unroll
-            for (int n2 = 0; n2 < 2; ++n2) {
-                uint32_t b[4];
-                const int q = lane >> 3;
-                const int r = wn * 32 + n2 * 16 + (q >> 1) * 8 + (lane & 7);
-                const int c = kk * 2 + (q & 1);
-                ldmatrix_x4(aB + swz<CPR>(r, c), b[0], b[1], b[2], b[3]);
-#pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    mma_bf16_16816(acc[m][2 * n2], af[m], b[0], b[1]);
-                    mma_bf16_16816(acc[m][2 * n2 + 1], af[m], b[2], b[3]);
-                }
-            }
-        }
-
-        // (5) epilogue.
-        if (p.vec) {
-            // Combine in place in the shared y tile, then 16-byte stores.
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-#pragma unroll
-                for (int n = 0; n < 4; ++n)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int r = wm * 32 + m * 16 + (lane >> 2) + 8 * h;
-                        const int c = wn * 32 + n * 8 + 2 * (lane & 3);
-                        uint32_t *cell = reinterpret_cast<uint32_t *>(sY + r * EX_Y_LD + c * 2);
-                        float v0 = acc[m][n][2 * h] + sBias[c];
-                        float v1 = acc[m][n][2 * h + 1] + sBias[c + 1];
-                        if (p.add_inputs) {
-                            const uint32_t old = *cell;
-                            v0 += bf16_lo(old);
-                            v1 += bf16_hi(old);
-                        }
-                        *cell = pack_bf16x2(v0, v1);
-                    }
-            __syncthreads();
-            for (int i = tid; i < EX_BM * (EX_BN / 8); i += EX_THREADS) {
-                const int r = i >> 4, c = i & 15;
-                const int tok = s_tok[r];
-                if (tok < 0 || c * 8 >= ncols) continue;
-                const uint4 v = *reinterpret_cast<const uint4 *>(sY + r * EX_Y_LD + c * 16);
-                *reinterpret_cast<uint4 *>(ybase + int64_t(tok) * p.y_ld + c * 8) = v;
-            }
-        } else {
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-#pragma unroll
-                for (int n = 0; n < 4; ++n)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int r = wm * 32 + m * 16 + (lane >> 2) + 8 * (q >> 1);
-                        const int c = wn * 32 + n * 8 + 2 * (lane & 3) + (q & 1);
-                        const int tok = s_tok[r];
-                        if (tok < 0 || c >= ncols) continue;
-                        uint16_t *dst = ybase + int64_t(tok) * p.y_ld + c;
-                        float v = acc[m][n][q] + sBias[c];
-                        if (p.add_inputs) v += bf16_to_f32(*dst);
-                        *dst = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
-                    }
-        }
         __syncthreads();
     }
 }
@@ -255,14 +300,22 @@ static int launch_expand_kt(const ExpandArgs &p, cudaStream_t stream)
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return int(e);
         int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, expand_kernel<KT>,
-                                                          EX_THREADS, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, expand_kernel<KT>, EX_THREADS,
+                                                          expand_smem_bytes(KT, 65));
         if (e != cudaSuccess) return int(e);
         grid = device_sm_count() * max(occ, 1);
         if (dev < 64) grid_cache[dev] = grid;
     }
-    expand_kernel<KT><<<grid, EX_THREADS, expand_smem_bytes(KT, p.nbins), stream>>>(p);
-    return int(cudaGetLastError());
+    e = launch_kernel(expand_kernel<KT>, dim3(grid), dim3(EX_THREADS),
+                      expand_smem_bytes(KT, p.nbins), stream, p);
+    return int(e);
+}
+
+static int slice_chunks(int n, int rank)
+{
+    const int bn = (rank <= 16) ? expand_bn<1>() : (rank <= 32) ? expand_bn<2>()
+                 : (rank <= 64) ? expand_bn<4>() : expand_bn<8>();
+    return (n + bn - 1) / bn;
 }
 
 }  // namespace lora
@@ -304,8 +357,9 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
         p.col0[s] = int32_t(col);
         p.chunk0[s] = chunks;
         if (n % 8 != 0) vec = false;
-        chunks += (n + lora::EX_BN - 1) / lora::EX_BN;
+        chunks += lora::slice_chunks(n, rank);
         col += n;
+        if (col > INT32_MAX) return LORA_ERR_SIZE;
     }
     p.chunk0[num_slices] = chunks;
     if (col > y_ld) return LORA_ERR_WIDTH;

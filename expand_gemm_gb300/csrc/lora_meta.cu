@@ -56,6 +56,9 @@ __global__ void __launch_bounds__(META_THREADS, 1) meta_prepare_kernel(MetaArgs 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.num_tokens;
 
+    pdl_wait();
+    pdl_launch_dependents();
+
     for (int i = tid; i < META_WARPS * nb; i += META_THREADS) cnt[i] = 0;
     if (tid == 0) s_invalid = 0;
     __syncthreads();
@@ -180,8 +183,7 @@ int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
         if (e != cudaSuccess) return int(e);
         configured_smem[dev] = want;
     }
-    meta_prepare_kernel<<<1, META_THREADS, smem, stream>>>(a);
-    return int(cudaGetLastError());
+    return int(launch_kernel(meta_prepare_kernel, dim3(1), dim3(META_THREADS), smem, stream, a));
 }
 
 }  // namespace lora

@@ -63,7 +63,7 @@ size_t shrink_smem_bytes(int mt, int nbins)
     case 4: ring = ShrinkTile<4>::RING_BYTES; break;
     default: ring = ShrinkTile<8>::RING_BYTES; break;
     }
-    return ring + size_t(nbins + 1) * sizeof(int);
+    return ring + seg_tab_bytes(nbins);
 }
 
 template <int MT>
@@ -74,10 +74,12 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_tok[SH_BN];
 
-    if (*p.no_lora) return;
+    pdl_wait();
+    pdl_launch_dependents();
 
-    int *s_tile = reinterpret_cast<int *>(smem + Cfg::RING_BYTES);
-    const int total_tiles = build_tile_table(p.active, p.counts, p.nbins, SH_BN, s_tile);
+    const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + Cfg::RING_BYTES), p.nbins);
+    const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
+                                          p.nbins, SH_BN, tab);
     if (total_tiles == 0) return;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -105,10 +107,10 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
         const int tile = rest % total_tiles;
         const int kc = rest / total_tiles;
 
-        const int seg = find_segment(s_tile, p.nbins, tile);
-        const int id = p.active[seg];
-        const int row0 = p.start_loc[seg] + (tile - s_tile[seg]) * SH_BN;
-        const int nrows = min(SH_BN, p.start_loc[seg] + p.counts[seg] - row0);
+        const int seg = find_segment(tab.tile, p.nbins, tile);
+        const int id = tab.id[seg];
+        const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * SH_BN;
+        const int nrows = min(SH_BN, tab.start[seg] + tab.count[seg] - row0);
         if (tid < SH_BN) s_tok[tid] = (tid < nrows) ? p.sorted[row0 + tid] : -1;
         __syncthreads();
 
@@ -243,15 +245,15 @@ static int launch_shrink_mt(const ShrinkArgs &p, cudaStream_t stream)
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return int(e);
         int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, shrink_kernel<MT>,
-                                                          SH_THREADS, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, shrink_kernel<MT>, SH_THREADS,
+                                                          shrink_smem_bytes(MT, 65));
         if (e != cudaSuccess) return int(e);
         grid = device_sm_count() * max(occ, 1);
         if (dev < 64) grid_cache[dev] = grid;
     }
-    const size_t used = shrink_smem_bytes(MT, p.nbins);
-    shrink_kernel<MT><<<grid, SH_THREADS, used, stream>>>(p);
-    return int(cudaGetLastError());
+    e = launch_kernel(shrink_kernel<MT>, dim3(grid), dim3(SH_THREADS),
+                      shrink_smem_bytes(MT, p.nbins), stream, p);
+    return int(e);
 }
 
 }  // namespace lora
