@@ -31,6 +31,15 @@ bool pdl_enabled()
     return cached == 1;
 }
 
+// Integer tuning knob from the environment (read at every call; the
+// callers cache what they need).
+int env_int(const char *name, int fallback)
+{
+    const char *v = getenv(name);
+    if (v == nullptr || *v == 0) return fallback;
+    return atoi(v);
+}
+
 }  // namespace lora
 
 LORA_API const char *lora_status_string(int status)

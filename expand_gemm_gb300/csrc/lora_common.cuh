@@ -136,15 +136,30 @@ __host__ __device__ constexpr size_t seg_tab_bytes(int nbins)
 // independent loads, then scans tile counts.  Returns 0 (no work) when the
 // flag is set; otherwise the total number of tiles of `tile_rows` tokens.
 // Every thread of the block gets the result.
+//   full_tiles_only: each segment contributes only its whole tiles
+//                    (count / tile_rows of them).
+//   skip_rows:       when nonzero, the first (count / skip_rows) * skip_rows
+//                    tokens of every segment are left out (another kernel
+//                    covers them) and only the rest is tiled.
 __device__ __forceinline__ int load_segments(const int32_t *no_lora, const int32_t *active,
                                              const int32_t *counts, const int32_t *start_loc,
-                                             int nbins, int tile_rows, SegTab t)
+                                             int nbins, int tile_rows, SegTab t,
+                                             bool full_tiles_only = false, int skip_rows = 0)
 {
     int *s_flag = t.count + nbins;
     for (int k = threadIdx.x; k < nbins; k += blockDim.x) {
-        t.id[k] = active[k];
-        t.count[k] = counts[k];
-        t.start[k] = start_loc[k];
+        const int id = active[k];
+        int c = counts[k];
+        int st = start_loc[k];
+        if (skip_rows > 0) {
+            const int skip = (c / skip_rows) * skip_rows;
+            st += skip;
+            c -= skip;
+        }
+        if (full_tiles_only) c = (c / tile_rows) * tile_rows;
+        t.id[k] = id;
+        t.count[k] = c;
+        t.start[k] = st;
     }
     if (threadIdx.x == 0) *s_flag = *no_lora;
     __syncthreads();
@@ -193,6 +208,28 @@ __device__ __forceinline__ int find_segment(const int *s_tile, int nbins, int ti
 namespace lora {
 int device_sm_count();
 bool pdl_enabled();
+int env_int(const char *name, int fallback);
+
+// Host-side description of one lora_shrink call, shared by its two paths.
+struct ShrinkLaunch {
+    const uint16_t *x;
+    int64_t x_ld;
+    int32_t hidden;
+    int32_t num_tokens;
+    const uint16_t *a[LORA_MAX_SLICES];
+    int32_t num_slices;
+    int32_t rank;
+    int32_t max_loras;
+    float *y;
+    float scale;
+    const int32_t *sorted;
+    const int32_t *counts;
+    const int32_t *start_loc;
+    const int32_t *active;
+    const int32_t *no_lora;
+    int32_t *error_word;
+};
+int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream);
 
 // Launch with the programmatic-stream-serialization attribute (when
 // enabled), so the kernel may start while its predecessor drains; the

@@ -41,6 +41,7 @@ struct ShrinkArgs {
     const int32_t *active;
     const int32_t *no_lora;
     int32_t nbins;                 // max_loras + 1
+    int32_t skip_rows;             // rows per segment left to the tensor-core path
 };
 
 template <int MT>
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
 
     const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + Cfg::RING_BYTES), p.nbins);
     const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
-                                          p.nbins, SH_BN, tab);
+                                          p.nbins, SH_BN, tab, false, p.skip_rows);
     if (total_tiles == 0) return;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -278,11 +279,12 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
         return LORA_ERR_ALIGN;
 
     lora::ShrinkArgs p;
-    for (int s = 0; s < LORA_MAX_SLICES; ++s) p.a[s] = nullptr;
+    lora::ShrinkLaunch u;
+    for (int s = 0; s < LORA_MAX_SLICES; ++s) p.a[s] = u.a[s] = nullptr;
     for (int s = 0; s < num_slices; ++s) {
         if (lora_a[s] == nullptr) return LORA_ERR_NULL;
         if (reinterpret_cast<uintptr_t>(lora_a[s]) & 15u) return LORA_ERR_ALIGN;
-        p.a[s] = lora_a[s];
+        p.a[s] = u.a[s] = lora_a[s];
     }
     p.x = x;
     p.x_ld = x_ld;
@@ -298,8 +300,36 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
     p.active = meta->active_lora_ids;
     p.no_lora = meta->no_lora_flag;
     p.nbins = meta->max_loras + 1;
+    p.skip_rows = 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // Tensor-core path for the whole 128-token tiles of long segments, when
+    // the batch is large enough to hold such segments (LORA_PUNICA_UMMA=0
+    // disables it; LORA_PUNICA_UMMA_MIN_TOKENS sets the batch threshold).
+    static const int umma_on = lora::env_int("LORA_PUNICA_UMMA", 1);
+    static const int umma_min = lora::env_int("LORA_PUNICA_UMMA_MIN_TOKENS", 1024);
+    if (umma_on && num_tokens >= umma_min && meta->error_word != nullptr) {
+        u.x = x;
+        u.x_ld = x_ld;
+        u.hidden = hidden;
+        u.num_tokens = num_tokens;
+        u.num_slices = num_slices;
+        u.rank = rank;
+        u.max_loras = meta->max_loras;
+        u.y = y;
+        u.scale = scale;
+        u.sorted = p.sorted;
+        u.counts = p.counts;
+        u.start_loc = p.start_loc;
+        u.active = p.active;
+        u.no_lora = p.no_lora;
+        u.error_word = meta->error_word;
+        const int r = lora::launch_shrink_umma(u, st);
+        if (r == 1) p.skip_rows = 128;
+        else if (r != 0) return r;
+    }
+
     if (rank <= 16) return lora::launch_shrink_mt<1>(p, st);
     if (rank <= 32) return lora::launch_shrink_mt<2>(p, st);
     if (rank <= 64) return lora::launch_shrink_mt<4>(p, st);

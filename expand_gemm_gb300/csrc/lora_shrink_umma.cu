@@ -1,0 +1,360 @@
+// lora_shrink_umma.cu -- tensor-core (tcgen05 / TMEM) path of lora_shrink
+// for the full 128-token tiles of long LoRA segments (page
+// "vllm.lora.punica_wrapper.punica_gpu", PunicaWrapperGPU.add_shrink:
+// y[s][t, :] += scale * x[t, :] @ A[s][id(t)]^T).
+//
+// One CTA per SM, persistent over tiles; warp-specialised:
+//   warp 0      producer: per 64-wide hidden block, TMA tile::gather4 loads
+//               the tile's 128 x rows through the sorted permutation (box one
+//               row high, 128-byte swizzle) and 2-D TMA loads the r rows of
+//               A[s][id] for every slice, all completing on one mbarrier.
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (M = 128 tokens,
+//               N = padded rank, K = 16) for every slice into its own TMEM
+//               columns, and commits to free each stage and, at the end of
+//               a tile, to hand the accumulators to the epilogue.
+//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (one token row
+//               per thread), buf[s][t, :] += scale * acc with float4
+//               read-modify-writes (every row has one owner: no atomics).
+// x is read once per tile for all slices; the A block of a LoRA is shared in
+// L2 by the CTAs working on tiles of the same segment.
+//
+// Every mbarrier wait is bounded (about one second); on expiry the kernel
+// sets bit 30 of the metadata error word, stops issuing, waits (bounded)
+// for its copies and MMAs in flight, frees TMEM and returns.
+#include "lora_common.cuh"
+#include "lora_umma.cuh"
+
+namespace lora {
+
+constexpr int UM_BM = 128;            // tokens per tile = UMMA M
+constexpr int UM_BK = 64;             // hidden per stage (one 128-byte swizzle atom)
+constexpr int UM_THREADS = 192;
+constexpr int UM_MAX_STAGES = 8;
+constexpr int UM_SMEM_BUDGET = 200 * 1024;
+constexpr long long UM_TIMEOUT_CYCLES = 2000000000ll;
+constexpr int UM_ERROR_BIT = 1 << 30;
+
+struct UmmaShrinkArgs {
+    CUtensorMap map_x;                         // x: [T, H], box {64, 1}
+    CUtensorMap map_a[LORA_MAX_SLICES];        // A[s]: [L * r, H], box {64, RP}
+    float *y;
+    float scale;
+    int32_t num_tokens;
+    int32_t hidden;
+    int32_t num_slices;
+    int32_t rank;
+    int32_t rp;                                // padded rank (UMMA N), power of 2
+    int32_t stages;
+    int32_t tmem_cols;
+    const int32_t *sorted;
+    const int32_t *counts;
+    const int32_t *start_loc;
+    const int32_t *active;
+    const int32_t *no_lora;
+    int32_t *error_word;
+    int32_t nbins;
+};
+
+struct UmmaLayout {
+    int x_bytes, a_bytes, stage_bytes, ring_bytes, bar_off, misc_off, tab_off, total;
+};
+
+__host__ __device__ inline UmmaLayout umma_layout(int S, int rp, int stages, int nbins)
+{
+    UmmaLayout l;
+    l.x_bytes = UM_BM * UM_BK * 2;                       // 16 KB
+    l.a_bytes = rp * UM_BK * 2;                          // per slice
+    l.stage_bytes = l.x_bytes + S * l.a_bytes;
+    l.ring_bytes = stages * l.stage_bytes;
+    l.bar_off = l.ring_bytes;                            // 2 * stages + 3 mbarriers
+    l.misc_off = l.bar_off + (2 * UM_MAX_STAGES + 3) * 8; // tmem base, abort flag
+    l.tab_off = l.misc_off + 16;
+    l.total = l.tab_off + int(seg_tab_bytes(nbins)) + 1024;  // + alignment slack
+    return l;
+}
+
+__global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid_constant__ UmmaShrinkArgs p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms.
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = p.num_slices, RP = p.rp, STAGES = p.stages;
+    const UmmaLayout L = umma_layout(S, RP, STAGES, p.nbins);
+    const uint32_t base = smem_addr(smem);
+    const uint32_t bar_full = base + L.bar_off;                 // [STAGES]
+    const uint32_t bar_empty = bar_full + 8 * UM_MAX_STAGES;    // [STAGES]
+    const uint32_t bar_acc_full = bar_empty + 8 * UM_MAX_STAGES;
+    const uint32_t bar_acc_empty = bar_acc_full + 8;
+    const uint32_t bar_drain = bar_acc_empty + 8;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L.misc_off);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L.misc_off + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    if (tid == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, 1);
+        }
+        mbar_init(bar_acc_full, 1);
+        mbar_init(bar_acc_empty, 4);
+        mbar_init(bar_drain, 1);
+        mbar_fence_init();
+        *s_abort = 0;
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&p.map_x);
+        for (int s = 0; s < S; ++s) tma_prefetch_map(&p.map_a[s]);
+    }
+    const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + L.tab_off), p.nbins);
+    // Full 128-token tiles only: a segment of c tokens contributes c / 128.
+    const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
+                                          p.nbins, UM_BM, tab, /*full_tiles_only=*/true);
+    if (total_tiles == 0 || int(blockIdx.x) >= total_tiles) return;
+
+    if (warp == 1) tmem_alloc(smem_addr(s_tmem), p.tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    const int H = p.hidden, R = p.rank, T = p.num_tokens;
+    const int nk = (H + UM_BK - 1) / UM_BK;
+    const long long deadline = clock64() + UM_TIMEOUT_CYCLES;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        int stage = 0;
+        uint32_t phase = 0;
+        int filled[UM_MAX_STAGES];
+        uint32_t fill_phase[UM_MAX_STAGES];
+        for (int i = 0; i < UM_MAX_STAGES; ++i) { filled[i] = 0; fill_phase[i] = 0; }
+        const uint32_t tx = uint32_t(L.x_bytes + S * L.a_bytes);
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            const int seg = find_segment(tab.tile, p.nbins, tile);
+            const int id = tab.id[seg];
+            const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * UM_BM;
+            int tok[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tok[i] = p.sorted[row0 + 4 * lane + i];
+            for (int kb = 0; kb < nk; ++kb) {
+                bool got = mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1, s_abort, deadline);
+                got = __all_sync(0xffffffffu, got) != 0;       // keep the warp converged
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sx = base + stage * L.stage_bytes;
+                const uint32_t full = bar_full + 8 * stage;
+                if (lane == 0) mbar_arrive_expect_tx(full, tx);
+                __syncwarp();
+                tma_gather4(sx + lane * 512, &p.map_x, kb * UM_BK, tok[0], tok[1], tok[2], tok[3], full);
+                if (lane == 0) {
+                    for (int s = 0; s < S; ++s)
+                        tma_load_2d(sx + L.x_bytes + s * L.a_bytes, &p.map_a[s], kb * UM_BK, id * R, full);
+                }
+                filled[stage] = 1;
+                fill_phase[stage] = phase;
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+        }
+        // Drain: every issued fill must land before the CTA may exit.
+        if (lane == 0) {
+            const long long drain_deadline = clock64() + UM_TIMEOUT_CYCLES;
+            for (int i = 0; i < STAGES; ++i) {
+                if (!filled[i]) continue;
+                while (!mbar_try_wait(bar_full + 8 * i, fill_phase[i]) &&
+                       clock64() < drain_deadline) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t idesc = umma_idesc_bf16(UM_BM, RP);
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                if (!mbar_wait_bounded(bar_acc_empty, acc_phase ^ 1, s_abort, deadline)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded(bar_full + 8 * stage, phase, s_abort, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sx = base + stage * L.stage_bytes;
+#pragma unroll
+                    for (int kk = 0; kk < UM_BK / 16; ++kk) {
+                        const uint64_t adesc = umma_desc_sw128(sx + kk * 32);
+                        for (int s = 0; s < S; ++s) {
+                            const uint64_t bdesc = umma_desc_sw128(sx + L.x_bytes + s * L.a_bytes + kk * 32);
+                            umma_bf16(tmem + s * RP, adesc, bdesc, idesc, (kb | kk) != 0);
+                        }
+                    }
+                    umma_commit(bar_empty + 8 * stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                umma_commit(bar_acc_full);
+                acc_phase ^= 1;
+            }
+            // After an abort, wait (bounded) until every MMA issued so far
+            // has completed before TMEM is released.
+            if (!ok || *s_abort) {
+                umma_commit(bar_drain);
+                const long long drain_deadline = clock64() + UM_TIMEOUT_CYCLES;
+                while (!mbar_try_wait(bar_drain, 0) && clock64() < drain_deadline) {
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;                 // TMEM lane quarter of this warp
+        const int row = q * 32 + lane;          // token row inside the tile
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            const int seg = find_segment(tab.tile, p.nbins, tile);
+            const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * UM_BM;
+            const int tok = p.sorted[row0 + row];
+            bool got = mbar_wait_bounded(bar_acc_full, acc_phase, s_abort, deadline);
+            if (__all_sync(0xffffffffu, got) == 0) break;       // warp-uniform exit
+            tc_fence_after();
+            for (int s = 0; s < S; ++s) {
+                float *dst = p.y + (int64_t(s) * T + tok) * R;
+                for (int c = 0; c < RP; c += 16) {
+                    float v[16];
+                    tmem_ld16(tmem + (uint32_t(q * 32) << 16) + uint32_t(s * RP + c), v);
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        if (c + j < R) {
+                            float4 *d4 = reinterpret_cast<float4 *>(dst + c + j);
+                            float4 o = *d4;
+                            o.x += p.scale * v[j];
+                            o.y += p.scale * v[j + 1];
+                            o.z += p.scale * v[j + 2];
+                            o.w += p.scale * v[j + 3];
+                            *d4 = o;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acc_empty);
+            acc_phase ^= 1;
+        }
+    }
+
+    if (tid == 0 && *s_abort) atomicOr(p.error_word, UM_ERROR_BIT);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, p.tmem_cols);
+}
+
+// ------------------------------------------------------------------ host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2-D bf16 map over rows x cols (row stride in elements), 128-byte swizzle.
+static bool encode_2d(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols,
+                      uint64_t row_stride, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_stride * 2};
+    const cuuint32_t box[2] = {uint32_t(UM_BK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launches the UMMA path if the shapes allow it; returns 1 if launched, 0
+// if not applicable (caller then covers every row with the mma.sync path),
+// or a negative value / cudaError_t on failure.
+int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream)
+{
+    int rp = 16;
+    while (rp < a.rank) rp <<= 1;
+    const int S = a.num_slices;
+    if (S * rp > 512 || a.hidden < UM_BK || a.num_tokens < UM_BM) return 0;
+    int cols = 32;
+    while (cols < S * rp) cols <<= 1;
+    const int nbins = a.max_loras + 1;
+    int stages = UM_MAX_STAGES;
+    while (stages > 2 && umma_layout(S, rp, stages, nbins).total > UM_SMEM_BUDGET) --stages;
+    const UmmaLayout L = umma_layout(S, rp, stages, nbins);
+    if (L.total > 227 * 1024) return 0;
+
+    static UmmaShrinkArgs p;      // large (>1 KB): keep off the stack
+    if (!encode_2d(&p.map_x, a.x, uint64_t(a.num_tokens), uint64_t(a.hidden), uint64_t(a.x_ld), 1))
+        return 0;
+    for (int s = 0; s < S; ++s)
+        if (!encode_2d(&p.map_a[s], a.a[s], uint64_t(a.max_loras) * a.rank, uint64_t(a.hidden),
+                       uint64_t(a.hidden), uint32_t(rp)))
+            return 0;
+    p.y = a.y;
+    p.scale = a.scale;
+    p.num_tokens = a.num_tokens;
+    p.hidden = a.hidden;
+    p.num_slices = S;
+    p.rank = a.rank;
+    p.rp = rp;
+    p.stages = stages;
+    p.tmem_cols = cols;
+    p.sorted = a.sorted;
+    p.counts = a.counts;
+    p.start_loc = a.start_loc;
+    p.active = a.active;
+    p.no_lora = a.no_lora;
+    p.error_word = a.error_word;
+    p.nbins = nbins;
+
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return int(e);
+    if (dev < 64 && configured[dev] == 0) {
+        e = cudaFuncSetAttribute(shrink_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 227 * 1024);
+        if (e != cudaSuccess) return int(e);
+        configured[dev] = 1;
+    }
+    const int grid = device_sm_count();
+    e = launch_kernel(shrink_umma_kernel, dim3(grid), dim3(UM_THREADS), size_t(L.total), stream, p);
+    if (e != cudaSuccess) return int(e);
+    return 1;
+}
+
+}  // namespace lora

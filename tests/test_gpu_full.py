@@ -55,6 +55,8 @@ def test_full_size_workload(oracle_mod, name):
         np.testing.assert_array_equal(meta.token_indices_sorted_by_lora_ids[:T].cpu().numpy(),
                                       o.token_indices_sorted_by_lora_ids[:T])
 
+    # no pipeline wait of any kernel timed out (bit 30 of the error word)
+    assert int(meta.error_word.item()) & (1 << 30) == 0
     buf_h = buf.cpu().numpy()
     y_h = host_bits(y)
     if name == "none":

@@ -43,6 +43,7 @@ def _run_shrink(inp, ids, scale, buf0=None, x_pad=0):
     meta = _meta(ids, inp.lora_a[0].shape[0])
     eg.lora_shrink(x, A, buf, meta, scale)
     torch.cuda.synchronize()
+    assert int(meta.error_word.item()) & (1 << 30) == 0, "a pipeline wait timed out"
     return buf.cpu().numpy()
 
 
@@ -84,6 +85,24 @@ def test_shrink_workloads_reduced(oracle_mod, name, T):
 def test_shrink_shapes(oracle_mod, T, H, r, L, S):
     inp = _custom(T, H, r, L, [16] * S, seed=T + H + r)
     _shrink_case(oracle_mod, inp, scale=0.37)
+
+
+@pytest.mark.parametrize("T,H,r,L,S", [
+    (1024, 256, 16, 2, 1),      # exactly whole 128-token tiles
+    (1300, 320, 32, 3, 2),      # ragged hidden (5 blocks of 64), remainders
+    (2100, 512, 64, 4, 1),
+    (1500, 192, 128, 3, 3),     # rank 128, three slices: 384 TMEM columns
+    (1100, 128, 24, 2, 2),      # padded rank 24 -> 32
+])
+def test_shrink_long_segments(oracle_mod, T, H, r, L, S):
+    """Long sequences per LoRA: whole 128-token tiles take the tensor-core
+    path, the remainders the mma.sync path."""
+    w = W.Workload("long", T + r, T, H, r, L, tuple([16] * S), "zipf_seq", p_none=0.1,
+                   seq_len=(200, 900), scale=0.75)
+    inp = W.generate(w)
+    rng = np.random.default_rng(3)
+    b0 = rng.standard_normal(inp.buf.shape).astype(np.float32)
+    _shrink_case(oracle_mod, inp, buf0=b0)
 
 
 def test_shrink_accumulates_and_scales(oracle_mod):
