@@ -304,12 +304,17 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    // Tensor-core path for the whole 128-token tiles of long segments, when
-    // the batch is large enough to hold such segments (LORA_PUNICA_UMMA=0
-    // disables it; LORA_PUNICA_UMMA_MIN_TOKENS sets the batch threshold).
-    static const int umma_on = lora::env_int("LORA_PUNICA_UMMA", 1);
-    static const int umma_min = lora::env_int("LORA_PUNICA_UMMA_MIN_TOKENS", 1024);
-    if (umma_on && num_tokens >= umma_min && meta->error_word != nullptr) {
+    // Tensor-core path for the whole 128-token tiles of long segments.  It
+    // pays where the contraction is dense enough to outrun mma.sync: a batch
+    // large enough to hold long segments (LORA_PUNICA_UMMA_MIN_TOKENS,
+    // default 1024) and at least LORA_PUNICA_UMMA_MIN_COLS output columns per
+    // token over all slices (num_slices * rank, default 256).
+    // LORA_PUNICA_UMMA=0 turns it off.  The variables are read at each call.
+    const int umma_on = lora::env_int("LORA_PUNICA_UMMA", 1);
+    const int umma_min_tokens = lora::env_int("LORA_PUNICA_UMMA_MIN_TOKENS", 1024);
+    const int umma_min_cols = lora::env_int("LORA_PUNICA_UMMA_MIN_COLS", 256);
+    if (umma_on && num_tokens >= umma_min_tokens && num_slices * rank >= umma_min_cols &&
+        meta->error_word != nullptr) {
         u.x = x;
         u.x_ld = x_ld;
         u.hidden = hidden;

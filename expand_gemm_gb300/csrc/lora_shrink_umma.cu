@@ -4,15 +4,20 @@
 // y[s][t, :] += scale * x[t, :] @ A[s][id(t)]^T).
 //
 // One CTA per SM, persistent over tiles; warp-specialised:
-//   warp 0      producer: per 64-wide hidden block, TMA tile::gather4 loads
-//               the tile's 128 x rows through the sorted permutation (box one
-//               row high, 128-byte swizzle) and 2-D TMA loads the r rows of
-//               A[s][id] for every slice, all completing on one mbarrier.
-//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (M = 128 tokens,
+//   warps 0..3  producers: per 64-wide hidden block, the tile's 128 x rows
+//               are gathered through the sorted permutation with 16-byte
+//               cp.async into the 128-byte-swizzled K-major layout UMMA
+//               reads, and one thread issues a 2-D TMA load of the r rows of
+//               A[s][id] for every slice; each producer thread signals a
+//               stage (after wait_group + a proxy fence) a few stages behind
+//               its issue point, so several stages stay in flight.
+//               (TMA tile::gather4 with one 128-byte row per request was
+//               measured slower than the LSU gather on these shapes.)
+//   warp 4      allocates TMEM; lane 0 issues tcgen05.mma (M = 128 tokens,
 //               N = padded rank, K = 16) for every slice into its own TMEM
 //               columns, and commits to free each stage and, at the end of
 //               a tile, to hand the accumulators to the epilogue.
-//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (one token row
+//   warps 5..8  epilogue: tcgen05.ld of their 32 TMEM lanes (one token row
 //               per thread), buf[s][t, :] += scale * acc with float4
 //               read-modify-writes (every row has one owner: no atomics).
 // x is read once per tile for all slices; the A block of a LoRA is shared in
@@ -28,14 +33,17 @@ namespace lora {
 
 constexpr int UM_BM = 128;            // tokens per tile = UMMA M
 constexpr int UM_BK = 64;             // hidden per stage (one 128-byte swizzle atom)
-constexpr int UM_THREADS = 192;
+constexpr int UM_PRODUCERS = 128;     // warps 0..3: x gather + A loads
+constexpr int UM_MMA_WARP = 4;        // warp 4: TMEM owner, UMMA issue
+constexpr int UM_THREADS = 288;       // + warps 5..8: epilogue
 constexpr int UM_MAX_STAGES = 8;
 constexpr int UM_SMEM_BUDGET = 200 * 1024;
 constexpr long long UM_TIMEOUT_CYCLES = 2000000000ll;
 constexpr int UM_ERROR_BIT = 1 << 30;
 
 struct UmmaShrinkArgs {
-    CUtensorMap map_x;                         // x: [T, H], box {64, 1}
+    const uint16_t *x;                         // x: [T, x_ld] bf16
+    int64_t x_ld;
     CUtensorMap map_a[LORA_MAX_SLICES];        // A[s]: [L * r, H], box {64, RP}
     float *y;
     float scale;
@@ -73,6 +81,24 @@ __host__ __device__ inline UmmaLayout umma_layout(int S, int rp, int stages, int
     return l;
 }
 
+__device__ __forceinline__ void cp_async_wait_n(int n)
+{
+    switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    default: cp_async_wait<6>(); break;
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
 __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid_constant__ UmmaShrinkArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -97,7 +123,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
 
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(bar_full + 8 * i, 1);
+            // 128 producer threads (x rows) + the expect_tx arrival (A tiles)
+            mbar_init(bar_full + 8 * i, UM_PRODUCERS + 1);
             mbar_init(bar_empty + 8 * i, 1);
         }
         mbar_init(bar_acc_full, 1);
@@ -105,9 +132,6 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
         mbar_init(bar_drain, 1);
         mbar_fence_init();
         *s_abort = 0;
-    }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&p.map_x);
         for (int s = 0; s < S; ++s) tma_prefetch_map(&p.map_a[s]);
     }
     const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + L.tab_off), p.nbins);
@@ -116,7 +140,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
                                           p.nbins, UM_BM, tab, /*full_tiles_only=*/true);
     if (total_tiles == 0 || int(blockIdx.x) >= total_tiles) return;
 
-    if (warp == 1) tmem_alloc(smem_addr(s_tmem), p.tmem_cols);
+    if (warp == UM_MMA_WARP) tmem_alloc(smem_addr(s_tmem), p.tmem_cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -126,54 +150,75 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     const int nk = (H + UM_BK - 1) / UM_BK;
     const long long deadline = clock64() + UM_TIMEOUT_CYCLES;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ producer
-        int stage = 0;
-        uint32_t phase = 0;
-        int filled[UM_MAX_STAGES];
-        uint32_t fill_phase[UM_MAX_STAGES];
-        for (int i = 0; i < UM_MAX_STAGES; ++i) { filled[i] = 0; fill_phase[i] = 0; }
-        const uint32_t tx = uint32_t(L.x_bytes + S * L.a_bytes);
+    if (warp < UM_PRODUCERS / 32) {
+        // ------------------------------------------------------ producers
+        // x rows: 128 rows x 8 16-byte chunks per stage, 8 per thread,
+        // gathered with cp.async into the 128-byte-swizzled K-major layout.
+        // A thread signals a stage only once its own copies have landed
+        // (wait_group + proxy fence), `lag` stages behind its issue point,
+        // so `lag` stages of x stay in flight per thread.
+        const int lag = min(STAGES - 1, 6);
+        const int xc = tid & 7;
+        const uint32_t tx = uint32_t(S * L.a_bytes);
+        int issued = 0, signalled = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
             const int seg = find_segment(tab.tile, p.nbins, tile);
             const int id = tab.id[seg];
             const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * UM_BM;
-            int tok[4];
+            const uint16_t *xrow[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) tok[i] = p.sorted[row0 + 4 * lane + i];
+            for (int j = 0; j < 8; ++j)
+                xrow[j] = p.x + int64_t(p.sorted[row0 + (tid >> 3) + 16 * j]) * p.x_ld;
             for (int kb = 0; kb < nk; ++kb) {
-                bool got = mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1, s_abort, deadline);
-                got = __all_sync(0xffffffffu, got) != 0;       // keep the warp converged
-                if (!got) {
+                const int stage = issued % STAGES;
+                const uint32_t phase = uint32_t(issued / STAGES) & 1u;
+                if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, s_abort, deadline)) {
                     ok = false;
                     break;
                 }
                 const uint32_t sx = base + stage * L.stage_bytes;
                 const uint32_t full = bar_full + 8 * stage;
-                if (lane == 0) mbar_arrive_expect_tx(full, tx);
-                __syncwarp();
-                tma_gather4(sx + lane * 512, &p.map_x, kb * UM_BK, tok[0], tok[1], tok[2], tok[3], full);
-                if (lane == 0) {
-                    for (int s = 0; s < S; ++s)
-                        tma_load_2d(sx + L.x_bytes + s * L.a_bytes, &p.map_a[s], kb * UM_BK, id * R, full);
+                const int k0 = kb * UM_BK + xc * 8;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int r = (tid >> 3) + 16 * j;
+                    cp_async16(sx + swz<8>(r, xc), k0 < H ? xrow[j] + k0 : p.x, k0 < H);
                 }
-                filled[stage] = 1;
-                fill_phase[stage] = phase;
-                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                cp_async_commit();
+                if (tid == 0) {
+                    mbar_arrive_expect_tx(full, tx);
+                    for (int s = 0; s < S; ++s)
+                        tma_load_2d(sx + L.x_bytes + s * L.a_bytes, &p.map_a[s], kb * UM_BK,
+                                    id * R, full);
+                }
+                ++issued;
+                if (issued - signalled > lag) {
+                    cp_async_wait_n(lag);
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar_full + 8 * (signalled % STAGES));
+                    ++signalled;
+                }
             }
         }
-        // Drain: every issued fill must land before the CTA may exit.
-        if (lane == 0) {
+        // Signal what is still open, then make sure every copy has landed
+        // (TMA included) before the CTA may exit.
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        while (signalled < issued) {
+            mbar_arrive(bar_full + 8 * (signalled % STAGES));
+            ++signalled;
+        }
+        if (tid == 0) {
             const long long drain_deadline = clock64() + UM_TIMEOUT_CYCLES;
-            for (int i = 0; i < STAGES; ++i) {
-                if (!filled[i]) continue;
-                while (!mbar_try_wait(bar_full + 8 * i, fill_phase[i]) &&
+            for (int i = max(0, issued - STAGES); i < issued; ++i) {
+                const uint32_t ph = uint32_t(i / STAGES) & 1u;
+                while (!mbar_try_wait(bar_full + 8 * (i % STAGES), ph) &&
                        clock64() < drain_deadline) {
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == UM_MMA_WARP) {
         // ------------------------------------------------------ MMA issue
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_bf16(UM_BM, RP);
@@ -204,6 +249,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
                     umma_commit(bar_empty + 8 * stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
+                if (!ok) break;
                 umma_commit(bar_acc_full);
                 acc_phase ^= 1;
             }
@@ -259,7 +305,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, p.tmem_cols);
+    if (warp == UM_MMA_WARP) tmem_dealloc(tmem, p.tmem_cols);
 }
 
 // ------------------------------------------------------------------ host
@@ -318,8 +364,8 @@ int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream)
     if (L.total > 227 * 1024) return 0;
 
     static UmmaShrinkArgs p;      // large (>1 KB): keep off the stack
-    if (!encode_2d(&p.map_x, a.x, uint64_t(a.num_tokens), uint64_t(a.hidden), uint64_t(a.x_ld), 1))
-        return 0;
+    p.x = a.x;
+    p.x_ld = a.x_ld;
     for (int s = 0; s < S; ++s)
         if (!encode_2d(&p.map_a[s], a.a[s], uint64_t(a.max_loras) * a.rank, uint64_t(a.hidden),
                        uint64_t(a.hidden), uint32_t(rp)))

@@ -94,9 +94,14 @@ def test_shrink_shapes(oracle_mod, T, H, r, L, S):
     (1500, 192, 128, 3, 3),     # rank 128, three slices: 384 TMEM columns
     (1100, 128, 24, 2, 2),      # padded rank 24 -> 32
 ])
-def test_shrink_long_segments(oracle_mod, T, H, r, L, S):
-    """Long sequences per LoRA: whole 128-token tiles take the tensor-core
-    path, the remainders the mma.sync path."""
+@pytest.mark.parametrize("umma", ["0", "1"])
+def test_shrink_long_segments(oracle_mod, monkeypatch, umma, T, H, r, L, S):
+    """Long sequences per LoRA: with the tensor-core path forced on, whole
+    128-token tiles take it and the remainders the mma.sync path; with it
+    off, mma.sync covers everything."""
+    monkeypatch.setenv("LORA_PUNICA_UMMA", umma)
+    monkeypatch.setenv("LORA_PUNICA_UMMA_MIN_COLS", "0")
+    monkeypatch.setenv("LORA_PUNICA_UMMA_MIN_TOKENS", "0")
     w = W.Workload("long", T + r, T, H, r, L, tuple([16] * S), "zipf_seq", p_none=0.1,
                    seq_len=(200, 900), scale=0.75)
     inp = W.generate(w)
