@@ -4,20 +4,20 @@
 // y[s][t, :] += scale * x[t, :] @ A[s][id(t)]^T).
 //
 // One CTA per SM, persistent over tiles; warp-specialised:
-//   warps 0..3  producers: per 64-wide hidden block, the tile's 128 x rows
-//               are gathered through the sorted permutation with 16-byte
-//               cp.async into the 128-byte-swizzled K-major layout UMMA
-//               reads, and one thread issues a 2-D TMA load of the r rows of
-//               A[s][id] for every slice; each producer thread signals a
-//               stage (after wait_group + a proxy fence) a few stages behind
-//               its issue point, so several stages stay in flight.
-//               (TMA tile::gather4 with one 128-byte row per request was
-//               measured slower than the LSU gather on these shapes.)
-//   warp 4      allocates TMEM; lane 0 issues tcgen05.mma (M = 128 tokens,
+//   warp 0      producer: per 64-wide hidden block, the tile's 128 x rows
+//               arrive by 2-D TMA: the tile's tokens (increasing, as the
+//               sort is stable) are cut into runs of consecutive tokens and
+//               each run into power-of-two pieces, one TMA box per piece
+//               (a long prefill sequence makes the tile one 128-row box);
+//               one more 2-D TMA box per slice brings the r rows of
+//               A[s][id].  All complete on the stage's mbarrier.
+//               (Per-row TMA tile::gather4 and an LSU cp.async gather were
+//               both measured slower: they stay near 30 GB/s per SM.)
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (M = 128 tokens,
 //               N = padded rank, K = 16) for every slice into its own TMEM
 //               columns, and commits to free each stage and, at the end of
 //               a tile, to hand the accumulators to the epilogue.
-//   warps 5..8  epilogue: tcgen05.ld of their 32 TMEM lanes (one token row
+//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (one token row
 //               per thread), buf[s][t, :] += scale * acc with float4
 //               read-modify-writes (every row has one owner: no atomics).
 // x is read once per tile for all slices; the A block of a LoRA is shared in
@@ -33,17 +33,16 @@ namespace lora {
 
 constexpr int UM_BM = 128;            // tokens per tile = UMMA M
 constexpr int UM_BK = 64;             // hidden per stage (one 128-byte swizzle atom)
-constexpr int UM_PRODUCERS = 128;     // warps 0..3: x gather + A loads
-constexpr int UM_MMA_WARP = 4;        // warp 4: TMEM owner, UMMA issue
-constexpr int UM_THREADS = 288;       // + warps 5..8: epilogue
+constexpr int UM_MMA_WARP = 1;        // warp 0: TMA producer; warp 1: TMEM owner, UMMA issue
+constexpr int UM_THREADS = 192;       // + warps 2..5: epilogue
+constexpr int UM_XMAPS = 8;           // x box heights 1, 2, 4, ..., 128
 constexpr int UM_MAX_STAGES = 8;
 constexpr int UM_SMEM_BUDGET = 200 * 1024;
 constexpr long long UM_TIMEOUT_CYCLES = 2000000000ll;
 constexpr int UM_ERROR_BIT = 1 << 30;
 
 struct UmmaShrinkArgs {
-    const uint16_t *x;                         // x: [T, x_ld] bf16
-    int64_t x_ld;
+    CUtensorMap map_x[UM_XMAPS];               // x: [T, H], box {64, 2^i rows}
     CUtensorMap map_a[LORA_MAX_SLICES];        // A[s]: [L * r, H], box {64, RP}
     float *y;
     float scale;
@@ -64,7 +63,7 @@ struct UmmaShrinkArgs {
 };
 
 struct UmmaLayout {
-    int x_bytes, a_bytes, stage_bytes, ring_bytes, bar_off, misc_off, tab_off, total;
+    int x_bytes, a_bytes, stage_bytes, ring_bytes, bar_off, misc_off, piece_off, tab_off, total;
 };
 
 __host__ __device__ inline UmmaLayout umma_layout(int S, int rp, int stages, int nbins)
@@ -76,27 +75,10 @@ __host__ __device__ inline UmmaLayout umma_layout(int S, int rp, int stages, int
     l.ring_bytes = stages * l.stage_bytes;
     l.bar_off = l.ring_bytes;                            // 2 * stages + 3 mbarriers
     l.misc_off = l.bar_off + (2 * UM_MAX_STAGES + 3) * 8; // tmem base, abort flag
-    l.tab_off = l.misc_off + 16;
+    l.piece_off = l.misc_off + 16;                      // [UM_BM] (row, token, log2 rows)
+    l.tab_off = l.piece_off + UM_BM * 4;
     l.total = l.tab_off + int(seg_tab_bytes(nbins)) + 1024;  // + alignment slack
     return l;
-}
-
-__device__ __forceinline__ void cp_async_wait_n(int n)
-{
-    switch (n) {
-    case 0: cp_async_wait<0>(); break;
-    case 1: cp_async_wait<1>(); break;
-    case 2: cp_async_wait<2>(); break;
-    case 3: cp_async_wait<3>(); break;
-    case 4: cp_async_wait<4>(); break;
-    case 5: cp_async_wait<5>(); break;
-    default: cp_async_wait<6>(); break;
-    }
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
 __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid_constant__ UmmaShrinkArgs p)
@@ -123,8 +105,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
 
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            // 128 producer threads (x rows) + the expect_tx arrival (A tiles)
-            mbar_init(bar_full + 8 * i, UM_PRODUCERS + 1);
+            mbar_init(bar_full + 8 * i, 1);       // the producer's expect_tx arrival
             mbar_init(bar_empty + 8 * i, 1);
         }
         mbar_init(bar_acc_full, 1);
@@ -133,6 +114,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
         mbar_fence_init();
         *s_abort = 0;
         for (int s = 0; s < S; ++s) tma_prefetch_map(&p.map_a[s]);
+        for (int i = 0; i < UM_XMAPS; ++i) tma_prefetch_map(&p.map_x[i]);
     }
     const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + L.tab_off), p.nbins);
     // Full 128-token tiles only: a segment of c tokens contributes c / 128.
@@ -150,66 +132,66 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     const int nk = (H + UM_BK - 1) / UM_BK;
     const long long deadline = clock64() + UM_TIMEOUT_CYCLES;
 
-    if (warp < UM_PRODUCERS / 32) {
-        // ------------------------------------------------------ producers
-        // x rows: 128 rows x 8 16-byte chunks per stage, 8 per thread,
-        // gathered with cp.async into the 128-byte-swizzled K-major layout.
-        // A thread signals a stage only once its own copies have landed
-        // (wait_group + proxy fence), `lag` stages behind its issue point,
-        // so `lag` stages of x stay in flight per thread.
-        const int lag = min(STAGES - 1, 6);
-        const int xc = tid & 7;
-        const uint32_t tx = uint32_t(S * L.a_bytes);
-        int issued = 0, signalled = 0;
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        // Tokens of a tile are increasing (the sort is stable), so they
+        // split into runs of consecutive tokens.  Lane 0 cuts the tile into
+        // pieces whose heights are powers of two and whose tokens are
+        // consecutive; each piece is one 2-D TMA box of the x map with that
+        // height, written at its row of the 128-byte-swizzled tile.  Long
+        // prefill sequences make most tiles a single 128-row box.
+        uint32_t *pieces = reinterpret_cast<uint32_t *>(smem + L.piece_off);
+        const uint32_t tx = uint32_t(L.x_bytes + S * L.a_bytes);
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
             const int seg = find_segment(tab.tile, p.nbins, tile);
             const int id = tab.id[seg];
             const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * UM_BM;
-            const uint16_t *xrow[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                xrow[j] = p.x + int64_t(p.sorted[row0 + (tid >> 3) + 16 * j]) * p.x_ld;
+            int npieces = 0;
+            if (lane == 0) {
+                const int32_t *tk = p.sorted + row0;
+                int j = 0;
+                while (j < UM_BM) {
+                    int lg = 7;
+                    while ((1 << lg) > UM_BM - j || (j & ((1 << lg) - 1)) != 0 ||
+                           tk[j + (1 << lg) - 1] - tk[j] != (1 << lg) - 1)
+                        --lg;
+                    pieces[npieces++] = uint32_t(j) | (uint32_t(lg) << 8) |
+                                        (uint32_t(tk[j]) << 11);
+                    j += 1 << lg;
+                }
+            }
+            npieces = __shfl_sync(0xffffffffu, npieces, 0);
+            __syncwarp();
             for (int kb = 0; kb < nk; ++kb) {
-                const int stage = issued % STAGES;
-                const uint32_t phase = uint32_t(issued / STAGES) & 1u;
-                if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, s_abort, deadline)) {
+                bool got = mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, s_abort, deadline);
+                if (__all_sync(0xffffffffu, got) == 0) {
                     ok = false;
                     break;
                 }
                 const uint32_t sx = base + stage * L.stage_bytes;
                 const uint32_t full = bar_full + 8 * stage;
-                const int k0 = kb * UM_BK + xc * 8;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int r = (tid >> 3) + 16 * j;
-                    cp_async16(sx + swz<8>(r, xc), k0 < H ? xrow[j] + k0 : p.x, k0 < H);
+                if (lane == 0) mbar_arrive_expect_tx(full, tx);
+                __syncwarp();
+                for (int i = lane; i < npieces; i += 32) {
+                    const uint32_t pc = pieces[i];
+                    const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
+                    tma_load_2d(sx + r * 128, &p.map_x[lg], kb * UM_BK, t0, full);
                 }
-                cp_async_commit();
-                if (tid == 0) {
-                    mbar_arrive_expect_tx(full, tx);
+                if (lane == 0) {
                     for (int s = 0; s < S; ++s)
                         tma_load_2d(sx + L.x_bytes + s * L.a_bytes, &p.map_a[s], kb * UM_BK,
                                     id * R, full);
                 }
                 ++issued;
-                if (issued - signalled > lag) {
-                    cp_async_wait_n(lag);
-                    fence_proxy_async_smem();
-                    mbar_arrive(bar_full + 8 * (signalled % STAGES));
-                    ++signalled;
-                }
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
         }
-        // Signal what is still open, then make sure every copy has landed
-        // (TMA included) before the CTA may exit.
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        while (signalled < issued) {
-            mbar_arrive(bar_full + 8 * (signalled % STAGES));
-            ++signalled;
-        }
-        if (tid == 0) {
+        // Every issued fill must land before the CTA may exit.
+        if (lane == 0) {
             const long long drain_deadline = clock64() + UM_TIMEOUT_CYCLES;
             for (int i = max(0, issued - STAGES); i < issued; ++i) {
                 const uint32_t ph = uint32_t(i / STAGES) & 1u;
@@ -354,7 +336,9 @@ int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream)
     int rp = 16;
     while (rp < a.rank) rp <<= 1;
     const int S = a.num_slices;
-    if (S * rp > 512 || a.hidden < UM_BK || a.num_tokens < UM_BM) return 0;
+    // Token indices travel in 21 bits of a piece descriptor.
+    if (S * rp > 512 || a.hidden < UM_BK || a.num_tokens < UM_BM || a.num_tokens >= (1 << 21))
+        return 0;
     int cols = 32;
     while (cols < S * rp) cols <<= 1;
     const int nbins = a.max_loras + 1;
@@ -364,8 +348,10 @@ int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream)
     if (L.total > 227 * 1024) return 0;
 
     static UmmaShrinkArgs p;      // large (>1 KB): keep off the stack
-    p.x = a.x;
-    p.x_ld = a.x_ld;
+    for (int i = 0; i < UM_XMAPS; ++i)
+        if (!encode_2d(&p.map_x[i], a.x, uint64_t(a.num_tokens), uint64_t(a.hidden),
+                       uint64_t(a.x_ld), 1u << i))
+            return 0;
     for (int s = 0; s < S; ++s)
         if (!encode_2d(&p.map_a[s], a.a[s], uint64_t(a.max_loras) * a.rank, uint64_t(a.hidden),
                        uint64_t(a.hidden), uint32_t(rp)))
