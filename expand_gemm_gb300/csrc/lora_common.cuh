@@ -231,6 +231,31 @@ struct ShrinkLaunch {
 };
 int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream);
 
+// Host-side description of one lora_expand call for its tensor-core path.
+struct ExpandLaunch {
+    const float *x;
+    const uint16_t *b[LORA_MAX_SLICES];
+    const uint16_t *bias[LORA_MAX_SLICES];
+    int32_t n[LORA_MAX_SLICES];
+    int32_t col0[LORA_MAX_SLICES];
+    int32_t num_slices;
+    int32_t rank;
+    int32_t max_loras;
+    uint16_t *y;
+    int64_t y_ld;
+    int32_t num_tokens;
+    int32_t add_inputs;
+    int32_t vec;
+    int32_t bias_vec;
+    const int32_t *sorted;
+    const int32_t *counts;
+    const int32_t *start_loc;
+    const int32_t *active;
+    const int32_t *no_lora;
+    int32_t *error_word;
+};
+int launch_expand_umma(const ExpandLaunch &a, cudaStream_t stream);
+
 // Launch with the programmatic-stream-serialization attribute (when
 // enabled), so the kernel may start while its predecessor drains; the
 // kernel itself calls pdl_wait() before touching memory.

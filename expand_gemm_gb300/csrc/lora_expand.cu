@@ -40,6 +40,7 @@ struct ExpandArgs {
     int32_t num_tokens;
     int32_t add_inputs;
     int32_t vec;                         // 16-byte y path allowed
+    int32_t bias_vec;                    // 16-byte bias loads allowed (every bias)
     const int32_t *sorted;
     const int32_t *counts;
     const int32_t *start_loc;
@@ -63,7 +64,8 @@ struct ExpandTile {
     static constexpr int Y_LD = BN * 2 + 16;           // padded shared y row (bytes)
     static constexpr int Y_BYTES = EX_BM * Y_LD;
     static constexpr int B_BYTES = BN * RP * 2;
-    static constexpr int STAGE_BYTES = Y_BYTES + B_BYTES;
+    static constexpr int BIAS_BYTES = BN * 2;                // bf16 bias chunk
+    static constexpr int STAGE_BYTES = Y_BYTES + B_BYTES + BIAS_BYTES;
     static constexpr int A_BYTES = EX_BM * RP * 2;
     static constexpr int BYTES = EX_STAGES * STAGE_BYTES + A_BYTES;
     static_assert(WN == 32 && MI >= 1, "warp tile");
@@ -152,6 +154,10 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 2) ? 3 : 2) expand_kernel(E
                 cp_async16(sb + swz<CPR>(r, cc),
                            ok ? bslice + int64_t(c0 + r) * R + cc * 8 : p.b[s], ok);
             }
+            if (bias_row != nullptr && p.bias_vec && tid < BN / 8) {
+                const bool ok = tid * 8 < ncols;
+                cp_async16(sb + Cfg::B_BYTES + tid * 16, ok ? bias_row + c0 + tid * 8 : bias_row, ok);
+            }
         };
 
 #pragma unroll
@@ -204,13 +210,19 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 2) ? 3 : 2) expand_kernel(E
             uint8_t *sy = smem + slot * Cfg::STAGE_BYTES;
             const uint32_t sb = ring + slot * Cfg::STAGE_BYTES + Cfg::Y_BYTES;
 
+            // bias of this chunk: staged with the chunk when aligned, else read here
             float bv[NI][2];
+            const uint16_t *sbias = reinterpret_cast<const uint16_t *>(
+                smem + slot * Cfg::STAGE_BYTES + Cfg::Y_BYTES + Cfg::B_BYTES);
 #pragma unroll
             for (int n = 0; n < NI; ++n)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int c = wn * Cfg::WN + n * 8 + 2 * (lane & 3) + h;
-                    bv[n][h] = (bias_row != nullptr && c < ncols) ? bf16_to_f32(bias_row[c0 + c]) : 0.f;
+                    float b = 0.f;
+                    if (bias_row != nullptr && c < ncols)
+                        b = bf16_to_f32(p.bias_vec ? sbias[c] : bias_row[c0 + c]);
+                    bv[n][h] = b;
                 }
 
             float acc[MI][NI][4];
@@ -339,6 +351,7 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
     int chunks = 0;
     bool vec = ((reinterpret_cast<uintptr_t>(y) & 15u) == 0) && (y_ld % 8 == 0) &&
                (offset_start % 8 == 0);
+    bool bias_vec = true;
     for (int s = 0; s < LORA_MAX_SLICES; ++s) {
         p.b[s] = nullptr;
         p.bias[s] = nullptr;
@@ -357,6 +370,7 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
         p.col0[s] = int32_t(col);
         p.chunk0[s] = chunks;
         if (n % 8 != 0) vec = false;
+        if (p.bias[s] != nullptr && (reinterpret_cast<uintptr_t>(p.bias[s]) & 15u)) bias_vec = false;
         chunks += lora::slice_chunks(n, rank);
         col += n;
         if (col > INT32_MAX) return LORA_ERR_SIZE;
@@ -377,6 +391,7 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
     p.num_tokens = num_tokens;
     p.add_inputs = add_inputs ? 1 : 0;
     p.vec = vec ? 1 : 0;
+    p.bias_vec = (vec && bias_vec) ? 1 : 0;
     p.sorted = meta->token_indices_sorted_by_lora_ids;
     p.counts = meta->num_tokens_per_lora;
     p.start_loc = meta->lora_token_start_loc;
@@ -385,6 +400,38 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
     p.nbins = meta->max_loras + 1;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // Tensor-core path (tcgen05, TMEM accumulators) for 16-byte-aligned
+    // outputs; LORA_PUNICA_EXPAND_UMMA=0 keeps every call on mma.sync.
+    if (lora::env_int("LORA_PUNICA_EXPAND_UMMA", 1) && p.vec) {
+        lora::ExpandLaunch u;
+        u.x = x;
+        for (int s = 0; s < LORA_MAX_SLICES; ++s) {
+            u.b[s] = p.b[s];
+            u.bias[s] = p.bias[s];
+            u.n[s] = p.n[s];
+            u.col0[s] = p.col0[s];
+        }
+        u.num_slices = num_slices;
+        u.rank = rank;
+        u.max_loras = meta->max_loras;
+        u.y = y;
+        u.y_ld = y_ld;
+        u.num_tokens = num_tokens;
+        u.add_inputs = p.add_inputs;
+        u.vec = p.vec;
+        u.bias_vec = p.bias_vec;
+        u.sorted = p.sorted;
+        u.counts = p.counts;
+        u.start_loc = p.start_loc;
+        u.active = p.active;
+        u.no_lora = p.no_lora;
+        u.error_word = meta->error_word;
+        const int r = lora::launch_expand_umma(u, st);
+        if (r == 1) return LORA_OK;
+        if (r != 0) return r;
+    }
+
     if (rank <= 16) return lora::launch_expand_kt<1>(p, st);
     if (rank <= 32) return lora::launch_expand_kt<2>(p, st);
     if (rank <= 64) return lora::launch_expand_kt<4>(p, st);

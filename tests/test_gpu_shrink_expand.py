@@ -157,6 +157,7 @@ def _run_expand(inp, ids, xin, y_bits, slices, offset, add_inputs, bias, y_col_p
     meta = _meta(ids, inp.lora_b[0].shape[0])
     eg.lora_expand(dev_f32(xin), B, y, meta, offset, add_inputs, bias_d)
     torch.cuda.synchronize()
+    assert int(meta.error_word.item()) & (1 << 30) == 0, "a pipeline wait timed out"
     return host_bits(y)
 
 
@@ -180,9 +181,14 @@ def _expand_case(oracle_mod, inp, ids=None, xin=None, offset=0, add_inputs=True,
     return got
 
 
+EXPAND_PATHS = [pytest.param("1", id="tcgen05"), pytest.param("0", id="mma_sync")]
+
+
+@pytest.mark.parametrize("path", EXPAND_PATHS)
 @pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("prefill", 1536),
                                     ("mlp", 512), ("large", 384)])
-def test_expand_workloads_reduced(oracle_mod, name, T):
+def test_expand_workloads_reduced(oracle_mod, monkeypatch, path, name, T):
+    monkeypatch.setenv("LORA_PUNICA_EXPAND_UMMA", path)
     inp = W.generate(name, num_tokens=T)
     _expand_case(oracle_mod, inp)
 
@@ -194,7 +200,9 @@ def test_expand_workloads_reduced(oracle_mod, name, T):
     (129, 128, 2, (1024, 136), 8, 24),    # rank 128
     (50, 32, 5, (16,) * 8, 0, 0),         # eight slices
 ])
-def test_expand_shapes(oracle_mod, T, r, L, slices, offset, y_extra):
+@pytest.mark.parametrize("path", EXPAND_PATHS)
+def test_expand_shapes(oracle_mod, monkeypatch, path, T, r, L, slices, offset, y_extra):
+    monkeypatch.setenv("LORA_PUNICA_EXPAND_UMMA", path)
     rng_bias = [True, False][T % 2]
     inp = _custom(T, 64, r, L, slices, seed=T + r, bias=rng_bias)
     _expand_case(oracle_mod, inp, offset=offset, y_extra=y_extra)
@@ -204,6 +212,16 @@ def test_expand_shapes(oracle_mod, T, r, L, slices, offset, y_extra):
 def test_expand_unaligned_scalar_path(oracle_mod, slices, offset):
     inp = _custom(90, 64, 16, 3, slices, seed=21, bias=True)
     _expand_case(oracle_mod, inp, offset=offset, y_extra=1)
+
+
+@pytest.mark.parametrize("path", EXPAND_PATHS)
+def test_expand_long_segments(oracle_mod, monkeypatch, path):
+    """Sequences of hundreds of tokens per LoRA: many full 128-token tiles."""
+    monkeypatch.setenv("LORA_PUNICA_EXPAND_UMMA", path)
+    w = W.Workload("longx", 31, 2500, 64, 64, 5, (384, 136, 8), "zipf_seq", p_none=0.2,
+                   seq_len=(150, 700), bias=True)
+    inp = W.generate(w)
+    _expand_case(oracle_mod, inp, offset=8, y_extra=8)
 
 
 def test_expand_overwrite_mode(oracle_mod):
