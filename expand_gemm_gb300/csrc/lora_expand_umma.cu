@@ -380,46 +380,59 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
                     uint8_t *sy = smem + L.ring_off + stage * L.stage_bytes + L.b_bytes + row * XU_Y_LD;
                     const uint16_t *sbias = reinterpret_cast<const uint16_t *>(
                         smem + L.ring_off + stage * L.stage_bytes + L.bias_off);
-                    for (int j = 0; j < XU_BN / 16; ++j) {
-                        float v[16];
-                        tmem_ld16(tmem + ab * XU_BN + j * 16 + (uint32_t(q * 32) << 16), v);
-                        if (tok < 0 || j * 16 >= ncols) continue;
-                        uint4 *yp = reinterpret_cast<uint4 *>(sy + j * 32);
-                        uint32_t yw[8], bw[8];
-                        if (p.add_inputs) {
-                            const uint4 y0 = yp[0], y1 = yp[1];
-                            yw[0] = y0.x; yw[1] = y0.y; yw[2] = y0.z; yw[3] = y0.w;
-                            yw[4] = y1.x; yw[5] = y1.y; yw[6] = y1.z; yw[7] = y1.w;
-                        } else {
+                    // 64 columns per round: two 32-column TMEM loads in flight, one wait
+                    for (int h = 0; h < XU_BN / 64; ++h) {
+                        uint32_t va[32], vb[32];
+                        const uint32_t ta = tmem + ab * XU_BN + h * 64 + (uint32_t(q * 32) << 16);
+                        tmem_ld32_nowait(ta, va);
+                        tmem_ld32_nowait(ta + 32, vb);
+                        tmem_wait_ld();
+                        if (tok < 0) continue;
 #pragma unroll
-                            for (int k = 0; k < 8; ++k) yw[k] = 0u;
-                        }
-                        if (bias_row != nullptr && p.bias_vec) {
-                            const uint4 b0 = reinterpret_cast<const uint4 *>(sbias + j * 16)[0];
-                            const uint4 b1 = reinterpret_cast<const uint4 *>(sbias + j * 16)[1];
-                            bw[0] = b0.x; bw[1] = b0.y; bw[2] = b0.z; bw[3] = b0.w;
-                            bw[4] = b1.x; bw[5] = b1.y; bw[6] = b1.z; bw[7] = b1.w;
-                        } else if (bias_row != nullptr) {
+                        for (int j4 = 0; j4 < 4; ++j4) {
+                            const int j = h * 4 + j4;
+                            if (j * 16 >= ncols) continue;
+                            float v[16];
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                v[k] = __uint_as_float(j4 < 2 ? va[(j4 & 1) * 16 + k] : vb[(j4 & 1) * 16 + k]);
+                            uint4 *yp = reinterpret_cast<uint4 *>(sy + j * 32);
+                            uint32_t yw[8], bw[8];
+                            if (p.add_inputs) {
+                                const uint4 y0 = yp[0], y1 = yp[1];
+                                yw[0] = y0.x; yw[1] = y0.y; yw[2] = y0.z; yw[3] = y0.w;
+                                yw[4] = y1.x; yw[5] = y1.y; yw[6] = y1.z; yw[7] = y1.w;
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) yw[k] = 0u;
+                            }
+                            if (bias_row != nullptr && p.bias_vec) {
+                                const uint4 b0 = reinterpret_cast<const uint4 *>(sbias + j * 16)[0];
+                                const uint4 b1 = reinterpret_cast<const uint4 *>(sbias + j * 16)[1];
+                                bw[0] = b0.x; bw[1] = b0.y; bw[2] = b0.z; bw[3] = b0.w;
+                                bw[4] = b1.x; bw[5] = b1.y; bw[6] = b1.z; bw[7] = b1.w;
+                            } else if (bias_row != nullptr) {
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) {
+                                    const int cc = j * 16 + 2 * k;
+                                    const uint32_t lo = cc < ncols ? bias_row[c0 + cc] : 0u;
+                                    const uint32_t hi = cc + 1 < ncols ? bias_row[c0 + cc + 1] : 0u;
+                                    bw[k] = lo | (hi << 16);
+                                }
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) bw[k] = 0u;
+                            }
+                            uint32_t o[8];
 #pragma unroll
                             for (int k = 0; k < 8; ++k) {
-                                const int cc = j * 16 + 2 * k;
-                                const uint32_t lo = cc < ncols ? bias_row[c0 + cc] : 0u;
-                                const uint32_t hi = cc + 1 < ncols ? bias_row[c0 + cc + 1] : 0u;
-                                bw[k] = lo | (hi << 16);
+                                const float a0 = v[2 * k] + bf16_lo(bw[k]) + bf16_lo(yw[k]);
+                                const float a1 = v[2 * k + 1] + bf16_hi(bw[k]) + bf16_hi(yw[k]);
+                                o[k] = pack_bf16x2(a0, a1);
                             }
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) bw[k] = 0u;
+                            yp[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                            yp[1] = make_uint4(o[4], o[5], o[6], o[7]);
                         }
-                        uint32_t o[8];
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const float a0 = v[2 * k] + bf16_lo(bw[k]) + bf16_lo(yw[k]);
-                            const float a1 = v[2 * k + 1] + bf16_hi(bw[k]) + bf16_hi(yw[k]);
-                            o[k] = pack_bf16x2(a0, a1);
-                        }
-                        yp[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                        yp[1] = make_uint4(o[4], o[5], o[6], o[7]);
                     }
                     tc_fence_before();
                     __syncwarp();
