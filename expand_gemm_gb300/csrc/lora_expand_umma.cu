@@ -6,25 +6,26 @@
 //
 // Work items are (token tile of 128 tokens of one LoRA segment, 128-column
 // chunk of one slice), numbered chunk-fastest; one persistent CTA per SM
-// takes a contiguous, balanced range of them.  Eight warps, specialised:
-//   warp 0      B producer: one 2-D TMA box per chunk (two for rank 128)
-//               brings B[s][id][c0 : c0 + 128, :] in the swizzled K-major
-//               layout UMMA reads.
+// takes a contiguous, balanced range of them.  Ten warps, specialised:
+//   warp 0      producer, all TMA: per chunk one 2-D box of B[s][id] (two
+//               for rank 128) in the swizzled K-major layout UMMA reads; the
+//               tile's y rows as 2-D boxes over runs of consecutive tokens
+//               (power-of-two heights, two 64-column halves, 128-byte
+//               swizzle); the bias chunk as one 1-D bulk copy.
 //   warp 1      owns TMEM (two 128-column fp32 accumulators); lane 0 issues
 //               tcgen05.mma (M = 128 tokens, N = 128 columns, K = 16 steps
 //               over the rank) and commits.
-//   warps 2, 3  y producers: coalesced 16-byte cp.async of the tile's y rows
-//               (two rows of 256 bytes per warp instruction) and of the bias
-//               chunk into the stage; each thread's copies arrive on the
-//               stage's mbarrier when they land.
-//   warps 4..7  epilogue, one token row per thread (its TMEM lane): at each
-//               new tile, the fp32 x rows are rounded to bf16 into the A
-//               operand tile; per chunk, tcgen05.ld 16 columns at a time,
-//               add bias and old y in fp32, round once to bf16 in place in
-//               the shared y row, then the four warps store the tile back
-//               with coalesced 16-byte stores.
+//   warps 2..9  epilogue, one token row per thread (its TMEM lane), two
+//               warps per lane quarter splitting the columns: at each new
+//               tile the fp32 x rows are rounded to bf16 into the A operand;
+//               per chunk the accumulators are read with tcgen05.ld, bias
+//               and old y added in fp32 and rounded once to bf16 in place in
+//               the swizzled y tile, and one thread sends the tile back with
+//               TMA stores over the same token runs.  A half-chunk that runs
+//               past the end of a slice is stored by its threads directly.
 // The accumulators are double-buffered so the MMA of chunk i + 1 runs while
-// the epilogue drains chunk i; y and B stream through a ring of stages.
+// the epilogue drains chunk i; B, y and bias stream through a ring of stages
+// that is released once the TMA stores of a chunk have read it.
 //
 // Used when y rows, offsets and slice widths are 16-byte aligned (the same
 // condition as the vector path of the mma.sync kernel).  Every mbarrier
@@ -37,15 +38,17 @@ namespace lora {
 
 constexpr int XU_BM = 128;              // tokens per tile (UMMA M, TMEM lanes)
 constexpr int XU_BN = 128;              // columns per chunk (UMMA N)
-constexpr int XU_THREADS = 256;
+constexpr int XU_EPI_WARPS = 8;         // two per TMEM lane quarter (column halves)
+constexpr int XU_THREADS = 64 + 32 * XU_EPI_WARPS;
 constexpr int XU_MAX_STAGES = 4;
 constexpr int XU_SMEM_BUDGET = 200 * 1024;
-constexpr int XU_Y_LD = XU_BN * 2 + 16;  // padded shared y row (bytes)
+constexpr int XU_YMAPS = 8;             // y box heights 1, 2, 4, ..., 128
 constexpr long long XU_TIMEOUT_CYCLES = 2000000000ll;
 constexpr int XU_ERROR_BIT = 1 << 30;
 
 struct ExpandUmmaArgs {
     CUtensorMap map_b[LORA_MAX_SLICES];      // B[s]: [L * n_s rows, r cols], box {min(rp, 64), 128}
+    CUtensorMap map_y[XU_YMAPS];             // y: [T rows, y_ld cols], box {64, 2^i}, 128-byte swizzle
     const float *x;
     uint16_t *y;
     int64_t y_ld;
@@ -70,23 +73,26 @@ struct ExpandUmmaArgs {
 };
 
 struct XuLayout {
-    int a_bytes, y_bytes, b_bytes, bias_off, stage_bytes, ring_off, bar_off, misc_off, tok_off,
-        etok_off, tab_off, total;
+    int a_bytes, b_bytes, y_off, bias_off, stage_bytes, ring_off, bar_off, misc_off, ppc_off,
+        epc_off, etok_off, tab_off, total;
 };
 
+// Stage: B tile | y tile (two 64-column halves of 128 rows x 128 bytes,
+// 128-byte swizzle) | bias chunk.
 __host__ __device__ inline XuLayout xu_layout(int rp, int stages, int nbins)
 {
     XuLayout l;
-    l.a_bytes = XU_BM * rp * 2;                          // x tile, bf16
-    l.y_bytes = XU_BM * XU_Y_LD;
+    l.a_bytes = XU_BM * rp * 2;
     l.b_bytes = XU_BN * rp * 2;
-    l.bias_off = l.b_bytes + l.y_bytes;                  // within the stage
+    l.y_off = l.b_bytes;
+    l.bias_off = l.y_off + 2 * XU_BM * 128;
     l.stage_bytes = ((l.bias_off + XU_BN * 2) + 1023) & ~1023;
-    l.ring_off = l.a_bytes;                              // stage: B tile | y tile | bias
+    l.ring_off = l.a_bytes;
     l.bar_off = l.ring_off + stages * l.stage_bytes;
-    l.misc_off = l.bar_off + (3 * XU_MAX_STAGES + 6) * 8;  // + acc[2] x2, x_ready, drain
-    l.tok_off = l.misc_off + 16;                         // producer-side token rows
-    l.etok_off = l.tok_off + XU_BM * 4;                  // epilogue-side token rows
+    l.misc_off = l.bar_off + (2 * XU_MAX_STAGES + 6) * 8;
+    l.ppc_off = l.misc_off + 16;                         // producer pieces [128]
+    l.epc_off = l.ppc_off + XU_BM * 4;                   // store pieces [128]
+    l.etok_off = l.epc_off + XU_BM * 4;                  // epilogue token rows [128]
     l.tab_off = l.etok_off + XU_BM * 4;
     l.total = l.tab_off + int(seg_tab_bytes(nbins)) + 1024;
     return l;
@@ -124,9 +130,21 @@ __device__ __forceinline__ uint64_t kmajor_desc(int rp, int rows, uint32_t tile,
     return d;
 }
 
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+// Cuts the increasing token list tk[0..n) into pieces of consecutive
+// tokens whose heights are powers of two aligned to their row; each piece
+// is (row | log2 height << 8 | first token << 11).  Returns the count.
+__device__ __forceinline__ int token_pieces(const int32_t *tk, int n, uint32_t *pieces)
 {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" :: "r"(bar) : "memory");
+    int np = 0, j = 0;
+    while (j < n) {
+        int lg = 7;
+        while ((1 << lg) > n - j || (j & ((1 << lg) - 1)) != 0 ||
+               tk[j + (1 << lg) - 1] - tk[j] != (1 << lg) - 1)
+            --lg;
+        pieces[np++] = uint32_t(j) | (uint32_t(lg) << 8) | (uint32_t(tk[j]) << 11);
+        j += 1 << lg;
+    }
+    return np;
 }
 
 __device__ __forceinline__ void named_barrier(int id, int count)
@@ -142,15 +160,16 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
     const int RP = p.rp, STAGES = p.stages, S = p.num_slices, R = p.rank;
     const XuLayout L = xu_layout(RP, STAGES, p.nbins);
     const uint32_t base = smem_addr(smem);
-    const uint32_t bar_full_b = base + L.bar_off;                 // [STAGES] TMA (B)
-    const uint32_t bar_full_y = bar_full_b + 8 * XU_MAX_STAGES;    // [STAGES] 64 y producers
-    const uint32_t bar_empty = bar_full_y + 8 * XU_MAX_STAGES;     // [STAGES] MMA + 4 epilogue warps
-    const uint32_t bar_acc_full = bar_empty + 8 * XU_MAX_STAGES;   // [2]
-    const uint32_t bar_acc_empty = bar_acc_full + 16;              // [2]
+    const uint32_t bar_full = base + L.bar_off;                   // [STAGES] B + y + bias (TMA)
+    const uint32_t bar_empty = bar_full + 8 * XU_MAX_STAGES;      // [STAGES] MMA + stores read
+    const uint32_t bar_acc_full = bar_empty + 8 * XU_MAX_STAGES;  // [2]
+    const uint32_t bar_acc_empty = bar_acc_full + 16;             // [2]
     const uint32_t bar_x_ready = bar_acc_empty + 16;
+    const uint32_t bar_drain = bar_x_ready + 8;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L.misc_off);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L.misc_off + 4);
-    int *s_tok = reinterpret_cast<int *>(smem + L.tok_off);
+    uint32_t *s_ppieces = reinterpret_cast<uint32_t *>(smem + L.ppc_off);
+    uint32_t *s_epieces = reinterpret_cast<uint32_t *>(smem + L.epc_off);
     int *s_etok = reinterpret_cast<int *>(smem + L.etok_off);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -160,18 +179,19 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
 
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(bar_full_b + 8 * i, 1);
-            mbar_init(bar_full_y + 8 * i, 64);
-            mbar_init(bar_empty + 8 * i, 5);
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, 2);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_acc_full + 8 * i, 1);
-            mbar_init(bar_acc_empty + 8 * i, 4);
+            mbar_init(bar_acc_empty + 8 * i, XU_EPI_WARPS);
         }
-        mbar_init(bar_x_ready, 4);
+        mbar_init(bar_x_ready, XU_EPI_WARPS);
+        mbar_init(bar_drain, 1);
         mbar_fence_init();
         *s_abort = 0;
         for (int s = 0; s < S; ++s) tma_prefetch_map(&p.map_b[s]);
+        for (int i = 0; i < XU_YMAPS; ++i) tma_prefetch_map(&p.map_y[i]);
     }
     const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + L.tab_off), p.nbins);
     const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
@@ -191,9 +211,8 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
     const long long deadline = clock64() + XU_TIMEOUT_CYCLES;
     const uint32_t a_tile = base;                                  // x tile at offset 0
     const int b_boxes = (RP > 64) ? 2 : 1;
-    const uint32_t b_tx = uint32_t(L.b_bytes);
 
-    // Row-item decoding shared by all roles.
+    // Row items: token tile `tile`, slice s, chunks [cb, ce) of that slice.
     auto row_item = [&](int64_t w, int &tile, int &s, int &cb, int &ce) {
         tile = int(w / nchunks);
         cb = int(w - int64_t(tile) * nchunks);
@@ -209,40 +228,68 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
     };
 
     if (warp == 0) {
-        // -------------------------------------------------- B producer (TMA)
-        if (lane == 0) {
-            int g = 0;
-            bool ok = true;
-            for (int64_t w = w_begin; ok && w < w_end;) {
-                int tile, s, cb, ce, id, row0, nrows;
-                row_item(w, tile, s, cb, ce);
-                tile_rows(tile, id, row0, nrows);
-                for (int c = cb; c < ce; ++c, ++g) {
-                    const int stage = g % STAGES;
-                    const uint32_t ph = uint32_t(g / STAGES) & 1u;
-                    if (!mbar_wait_bounded(bar_empty + 8 * stage, ph ^ 1u, s_abort, deadline)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t sb = base + L.ring_off + stage * L.stage_bytes;
-                    const uint32_t full = bar_full_b + 8 * stage;
-                    mbar_arrive_expect_tx(full, b_tx);
-                    const int brow = id * p.n[s] + (c - p.chunk0[s]) * XU_BN;
-                    for (int k = 0; k < b_boxes; ++k)
-                        tma_load_2d(sb + k * XU_BN * 128, &p.map_b[s], k * 64, brow, full);
+        // ------------------------------------------ producer: TMA for B, y, bias
+        int g = 0;
+        bool ok = true;
+        for (int64_t w = w_begin; ok && w < w_end;) {
+            int tile, s, cb, ce, id, row0, nrows;
+            row_item(w, tile, s, cb, ce);
+            tile_rows(tile, id, row0, nrows);
+            int np = 0;
+            if (lane == 0) np = token_pieces(p.sorted + row0, nrows, s_ppieces);
+            np = __shfl_sync(0xffffffffu, np, 0);
+            __syncwarp();
+            const int n_s = p.n[s];
+            const uint16_t *bias_row = p.bias[s] ? p.bias[s] + int64_t(id) * n_s : nullptr;
+            for (int c = cb; c < ce; ++c, ++g) {
+                const int stage = g % STAGES;
+                const uint32_t ph = uint32_t(g / STAGES) & 1u;
+                bool got = mbar_wait_bounded(bar_empty + 8 * stage, ph ^ 1u, s_abort, deadline);
+                if (__all_sync(0xffffffffu, got) == 0) {
+                    ok = false;
+                    break;
                 }
-                w += ce - cb;
+                const uint32_t st = base + L.ring_off + stage * L.stage_bytes;
+                const uint32_t full = bar_full + 8 * stage;
+                const int c0 = (c - p.chunk0[s]) * XU_BN;
+                const int ncols = min(XU_BN, n_s - c0);
+                const bool with_bias = bias_row != nullptr && p.bias_vec;
+                if (lane == 0) {
+                    const uint32_t tx = uint32_t(L.b_bytes) +
+                                        (p.add_inputs ? uint32_t(nrows) * 256u : 0u) +
+                                        (with_bias ? uint32_t(ncols) * 2u : 0u);
+                    mbar_arrive_expect_tx(full, tx);
+                }
+                __syncwarp();
+                if (p.add_inputs) {
+                    const int col = p.col0[s] + c0;
+                    for (int i = lane; i < np; i += 32) {
+                        const uint32_t pc = s_ppieces[i];
+                        const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
+                        tma_load_2d(st + L.y_off + r * 128, &p.map_y[lg], col, t0, full);
+                        tma_load_2d(st + L.y_off + XU_BM * 128 + r * 128, &p.map_y[lg], col + 64, t0, full);
+                    }
+                }
+                if (lane == 0) {
+                    const int brow = id * n_s + c0;
+                    for (int k = 0; k < b_boxes; ++k)
+                        tma_load_2d(st + k * XU_BN * 128, &p.map_b[s], k * 64, brow, full);
+                    if (with_bias) bulk_load_1d(st + L.bias_off, bias_row + c0, uint32_t(ncols) * 2u, full);
+                }
             }
-            // every issued box must land before the CTA may exit
+            w += ce - cb;
+        }
+        // every issued fill must land before the CTA may exit
+        if (lane == 0) {
             const long long dd = clock64() + XU_TIMEOUT_CYCLES;
             for (int i = max(0, g - STAGES); i < g; ++i)
-                while (!mbar_try_wait(bar_full_b + 8 * (i % STAGES), uint32_t(i / STAGES) & 1u) &&
+                while (!mbar_try_wait(bar_full + 8 * (i % STAGES), uint32_t(i / STAGES) & 1u) &&
                        clock64() < dd) {
                 }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // -------------------------------------------------- MMA issue
+        // ------------------------------------------ MMA issue
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_bf16(XU_BM, XU_BN);
             int g = 0, items = 0;
@@ -257,7 +304,7 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
                 tc_fence_after();
                 for (int c = cb; c < ce; ++c, ++g) {
                     const int stage = g % STAGES, ab = g & 1;
-                    if (!mbar_wait_bounded(bar_full_b + 8 * stage, uint32_t(g / STAGES) & 1u, s_abort, deadline) ||
+                    if (!mbar_wait_bounded(bar_full + 8 * stage, uint32_t(g / STAGES) & 1u, s_abort, deadline) ||
                         !mbar_wait_bounded(bar_acc_empty + 8 * ab, (uint32_t(g >> 1) & 1u) ^ 1u, s_abort, deadline)) {
                         ok = false;
                         break;
@@ -273,9 +320,6 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
                 w += ce - cb;
             }
             if (!ok || *s_abort) {
-                const uint32_t bar_drain = bar_x_ready + 8;
-                mbar_init(bar_drain, 1);
-                asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
                 umma_commit(bar_drain);
                 const long long dd = clock64() + XU_TIMEOUT_CYCLES;
                 while (!mbar_try_wait(bar_drain, 0) && clock64() < dd) {
@@ -283,70 +327,31 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // -------------------------------------------------- y producers
-        // After an abort the threads keep walking the items (skipping the
-        // work) so that the named barriers stay matched.
-        const int ptid = tid - 64;                       // 0..63
-        const int pw = warp - 2;                         // 0..1
-        int g = 0;
-        bool ok = true;
-        for (int64_t w = w_begin; w < w_end;) {
-            int tile, s, cb, ce, id, row0, nrows;
-            row_item(w, tile, s, cb, ce);
-            tile_rows(tile, id, row0, nrows);
-            named_barrier(1, 64);                        // previous item fully issued
-            for (int r = ptid; r < XU_BM; r += 64) s_tok[r] = (r < nrows) ? p.sorted[row0 + r] : -1;
-            named_barrier(1, 64);
-            const int n_s = p.n[s];
-            const uint16_t *bias_row = p.bias[s] ? p.bias[s] + int64_t(id) * n_s : nullptr;
-            uint16_t *yslice = p.y + p.col0[s];
-            for (int c = cb; c < ce; ++c, ++g) {
-                const int stage = g % STAGES;
-                const uint32_t ph = uint32_t(g / STAGES) & 1u;
-                if (ok) ok = mbar_wait_bounded(bar_empty + 8 * stage, ph ^ 1u, s_abort, deadline);
-                if (!ok) continue;
-                const uint32_t st = base + L.ring_off + stage * L.stage_bytes;
-                const int c0 = (c - p.chunk0[s]) * XU_BN;
-                const int ncols = min(XU_BN, n_s - c0);
-                if (p.add_inputs) {
-                    // warp pw covers row pairs pw, pw + 2, ...: lanes 0..15 one row, 16..31 the next
-                    const int cc = lane & 15;
-                    for (int pr = pw; pr < XU_BM / 2; pr += 2) {
-                        const int r = 2 * pr + (lane >> 4);
-                        const int tok = s_tok[r];
-                        if (tok >= 0 && cc * 8 < ncols)
-                            cp_async16(st + L.b_bytes + r * XU_Y_LD + cc * 16,
-                                       yslice + int64_t(tok) * p.y_ld + c0 + cc * 8, true);
-                    }
-                }
-                if (bias_row != nullptr && p.bias_vec && ptid < XU_BN / 8 && ptid * 8 < ncols)
-                    cp_async16(st + L.bias_off + ptid * 16, bias_row + c0 + ptid * 8, true);
-                cp_async_mbar_arrive_noinc(bar_full_y + 8 * stage);
-            }
-            w += ce - cb;
-        }
-        cp_async_wait<0>();
     } else {
-        // -------------------------------------------------- epilogue
-        // After an abort the warps keep walking the items (skipping the
-        // work) so that the named barriers stay matched.
-        const int q = warp & 3;                          // TMEM lane quarter
+        // ------------------------------------------ epilogue (8 warps)
+        // Warp e = warp - 2: TMEM lane quarter q = warp % 4 (one token row per
+        // thread), column half hf = e / 4.  After an abort the warps keep
+        // walking the items (skipping work) so named barriers stay matched.
+        const int e = warp - 2;
+        const int q = warp & 3;
+        const int hf = e >> 2;
         const int row = q * 32 + lane;
-        const int etid = tid - 128;                      // 0..127
-        int g = 0, items = 0;
+        const int etid = tid - 64;                       // 0..255
+        const bool storer = (etid == 0);
+        int g = 0, items = 0, stores_open = 0, open_stage = 0;
         bool ok = true;
         for (int64_t w = w_begin; w < w_end; ++items) {
             int tile, s, cb, ce, id, row0, nrows;
             row_item(w, tile, s, cb, ce);
             tile_rows(tile, id, row0, nrows);
             const int tok = (row < nrows) ? p.sorted[row0 + row] : -1;
-            named_barrier(2, 128);                       // previous item's stores done
-            s_etok[row] = tok;
-            // x row of this token -> bf16 A operand row (zeros past the rank / rows)
+            named_barrier(2, 32 * XU_EPI_WARPS);         // previous item finished
+            if (hf == 0) s_etok[row] = tok;
+            // x row -> bf16 A operand row; each half converts half of the chunks
             {
                 const float *xr = p.x + (int64_t(s) * p.num_tokens + (tok >= 0 ? tok : 0)) * R;
-                for (int c = 0; c < RP / 8; ++c) {
+                const int nch = RP / 8;
+                for (int c = hf * (nch / 2); c < (hf + 1) * (nch / 2) + (nch & 1) * hf; ++c) {
                     uint4 v = make_uint4(0, 0, 0, 0);
                     if (tok >= 0 && c * 8 < R) {
                         const float4 u = reinterpret_cast<const float4 *>(xr + c * 8)[0];
@@ -358,48 +363,50 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
                     }
                     *reinterpret_cast<uint4 *>(smem + kmajor_off(RP, XU_BM, row, c)) = v;
                 }
-                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_x_ready);
             }
-            named_barrier(2, 128);                       // s_etok visible
+            named_barrier(2, 32 * XU_EPI_WARPS);         // s_etok visible
+            int np = 0;
+            if (storer) np = token_pieces(s_etok, nrows, s_epieces);
             const int n_s = p.n[s];
             const uint16_t *bias_row = p.bias[s] ? p.bias[s] + int64_t(id) * n_s : nullptr;
-            uint16_t *yslice = p.y + p.col0[s];
             for (int c = cb; c < ce; ++c, ++g) {
                 const int stage = g % STAGES, ab = g & 1;
                 if (ok) {
                     bool got = mbar_wait_bounded(bar_acc_full + 8 * ab, uint32_t(g >> 1) & 1u, s_abort, deadline) &&
-                               mbar_wait_bounded(bar_full_y + 8 * stage, uint32_t(g / STAGES) & 1u, s_abort, deadline);
+                               mbar_wait_bounded(bar_full + 8 * stage, uint32_t(g / STAGES) & 1u, s_abort, deadline);
                     ok = __all_sync(0xffffffffu, got) != 0;
                 }
                 const int c0 = (c - p.chunk0[s]) * XU_BN;
                 const int ncols = min(XU_BN, n_s - c0);
+                const int colg = p.col0[s] + c0;         // first column of the chunk in y
+                const bool half_full = (hf + 1) * 64 <= ncols;
                 if (ok) {
                     tc_fence_after();
-                    uint8_t *sy = smem + L.ring_off + stage * L.stage_bytes + L.b_bytes + row * XU_Y_LD;
+                    uint8_t *ysub = smem + L.ring_off + stage * L.stage_bytes + L.y_off + hf * XU_BM * 128;
                     const uint16_t *sbias = reinterpret_cast<const uint16_t *>(
                         smem + L.ring_off + stage * L.stage_bytes + L.bias_off);
-                    // 64 columns per round: two 32-column TMEM loads in flight, one wait
-                    for (int h = 0; h < XU_BN / 64; ++h) {
-                        uint32_t va[32], vb[32];
-                        const uint32_t ta = tmem + ab * XU_BN + h * 64 + (uint32_t(q * 32) << 16);
-                        tmem_ld32_nowait(ta, va);
-                        tmem_ld32_nowait(ta + 32, vb);
-                        tmem_wait_ld();
-                        if (tok < 0) continue;
+                    uint32_t va[32], vb[32];
+                    const uint32_t ta = tmem + ab * XU_BN + hf * 64 + (uint32_t(q * 32) << 16);
+                    tmem_ld32_nowait(ta, va);
+                    tmem_ld32_nowait(ta + 32, vb);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);   // TMEM buffer free
+                    if (tok >= 0) {
 #pragma unroll
                         for (int j4 = 0; j4 < 4; ++j4) {
-                            const int j = h * 4 + j4;
-                            if (j * 16 >= ncols) continue;
-                            float v[16];
-#pragma unroll
-                            for (int k = 0; k < 16; ++k)
-                                v[k] = __uint_as_float(j4 < 2 ? va[(j4 & 1) * 16 + k] : vb[(j4 & 1) * 16 + k]);
-                            uint4 *yp = reinterpret_cast<uint4 *>(sy + j * 32);
+                            const int cl = hf * 64 + j4 * 16;          // chunk column of this group
+                            if (cl >= ncols) continue;
+                            // 16-byte chunks 2*j4, 2*j4+1 of this row's 128-byte half row
+                            uint4 *p0 = reinterpret_cast<uint4 *>(ysub + row * 128 + (((2 * j4) ^ (row & 7)) << 4));
+                            uint4 *p1 = reinterpret_cast<uint4 *>(ysub + row * 128 + (((2 * j4 + 1) ^ (row & 7)) << 4));
                             uint32_t yw[8], bw[8];
                             if (p.add_inputs) {
-                                const uint4 y0 = yp[0], y1 = yp[1];
+                                const uint4 y0 = *p0, y1 = *p1;
                                 yw[0] = y0.x; yw[1] = y0.y; yw[2] = y0.z; yw[3] = y0.w;
                                 yw[4] = y1.x; yw[5] = y1.y; yw[6] = y1.z; yw[7] = y1.w;
                             } else {
@@ -407,14 +414,14 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
                                 for (int k = 0; k < 8; ++k) yw[k] = 0u;
                             }
                             if (bias_row != nullptr && p.bias_vec) {
-                                const uint4 b0 = reinterpret_cast<const uint4 *>(sbias + j * 16)[0];
-                                const uint4 b1 = reinterpret_cast<const uint4 *>(sbias + j * 16)[1];
+                                const uint4 b0 = reinterpret_cast<const uint4 *>(sbias + cl)[0];
+                                const uint4 b1 = reinterpret_cast<const uint4 *>(sbias + cl)[1];
                                 bw[0] = b0.x; bw[1] = b0.y; bw[2] = b0.z; bw[3] = b0.w;
                                 bw[4] = b1.x; bw[5] = b1.y; bw[6] = b1.z; bw[7] = b1.w;
                             } else if (bias_row != nullptr) {
 #pragma unroll
                                 for (int k = 0; k < 8; ++k) {
-                                    const int cc = j * 16 + 2 * k;
+                                    const int cc = cl + 2 * k;
                                     const uint32_t lo = cc < ncols ? bias_row[c0 + cc] : 0u;
                                     const uint32_t hi = cc + 1 < ncols ? bias_row[c0 + cc + 1] : 0u;
                                     bw[k] = lo | (hi << 16);
@@ -426,36 +433,54 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
                             uint32_t o[8];
 #pragma unroll
                             for (int k = 0; k < 8; ++k) {
-                                const float a0 = v[2 * k] + bf16_lo(bw[k]) + bf16_lo(yw[k]);
-                                const float a1 = v[2 * k + 1] + bf16_hi(bw[k]) + bf16_hi(yw[k]);
+                                const uint32_t a = (j4 < 2) ? va[(j4 & 1) * 16 + 2 * k] : vb[(j4 & 1) * 16 + 2 * k];
+                                const uint32_t b = (j4 < 2) ? va[(j4 & 1) * 16 + 2 * k + 1] : vb[(j4 & 1) * 16 + 2 * k + 1];
+                                const float a0 = __uint_as_float(a) + bf16_lo(bw[k]) + bf16_lo(yw[k]);
+                                const float a1 = __uint_as_float(b) + bf16_hi(bw[k]) + bf16_hi(yw[k]);
                                 o[k] = pack_bf16x2(a0, a1);
                             }
-                            yp[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                            yp[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                            const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]);
+                            const uint4 o1 = make_uint4(o[4], o[5], o[6], o[7]);
+                            if (half_full) {
+                                *p0 = o0;                              // leaves by TMA store
+                                *p1 = o1;
+                            } else {
+                                // a half that runs past the slice: store the valid columns here
+                                uint16_t *dst = p.y + int64_t(tok) * p.y_ld + colg + cl;
+                                *reinterpret_cast<uint4 *>(dst) = o0;
+                                if (cl + 8 < ncols) *reinterpret_cast<uint4 *>(dst + 8) = o1;
+                            }
                         }
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
+                    fence_proxy_async_smem();
                 }
-                named_barrier(2, 128);                   // every row of the tile combined
-                if (ok) {
-                    // coalesced store: two rows of 256 bytes per warp instruction
-                    const int cc = lane & 15;
-                    const uint8_t *ys = smem + L.ring_off + stage * L.stage_bytes + L.b_bytes;
-                    for (int pr = etid >> 5; pr < XU_BM / 2; pr += 4) {
-                        const int r = 2 * pr + (lane >> 4);
-                        const int t = s_etok[r];
-                        if (t >= 0 && cc * 8 < ncols) {
-                            const uint4 val = *reinterpret_cast<const uint4 *>(ys + r * XU_Y_LD + cc * 16);
-                            *reinterpret_cast<uint4 *>(yslice + int64_t(t) * p.y_ld + c0 + cc * 8) = val;
+                named_barrier(2, 32 * XU_EPI_WARPS);     // every row of the tile combined
+                if (storer) {
+                    if (ok) {
+                        const uint32_t ys = base + L.ring_off + stage * L.stage_bytes + L.y_off;
+                        for (int i = 0; i < np; ++i) {
+                            const uint32_t pc = s_epieces[i];
+                            const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
+                            for (int h = 0; h < 2; ++h)
+                                if ((h + 1) * 64 <= ncols)
+                                    tma_store_2d(&p.map_y[lg], colg + h * 64, t0, ys + h * XU_BM * 128 + r * 128);
                         }
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
+                    bulk_commit_group();
+                    // the previous chunk's stores have read their tile: free that stage
+                    if (stores_open) {
+                        bulk_wait_group_read<1>();
+                        mbar_arrive(bar_empty + 8 * open_stage);
+                    }
+                    stores_open = 1;
+                    open_stage = stage;
                 }
             }
             w += ce - cb;
+        }
+        if (storer) {
+            bulk_wait_group_all();
+            if (stores_open) mbar_arrive(bar_empty + 8 * open_stage);
         }
     }
 
@@ -489,11 +514,25 @@ static XuEncodeFn xu_encode_fn()
     return fn;
 }
 
+static bool xu_encode(XuEncodeFn fn, CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols,
+                      uint64_t row_stride, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw)
+{
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_stride * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Launches the tensor-core expand if the shapes allow it: returns 1 if
 // launched, 0 if not applicable, or a cudaError_t on a launch failure.
 int launch_expand_umma(const ExpandLaunch &a, cudaStream_t stream)
 {
     if (!a.vec || a.error_word == nullptr) return 0;
+    // Token indices travel in 21 bits of a piece descriptor.
+    if (a.num_tokens >= (1 << 21)) return 0;
     int rp = 16;
     while (rp < a.rank) rp <<= 1;
     if (rp > 128) return 0;
@@ -505,21 +544,20 @@ int launch_expand_umma(const ExpandLaunch &a, cudaStream_t stream)
     const XuLayout L = xu_layout(rp, stages, nbins);
     if (L.total > 227 * 1024) return 0;
 
-    static ExpandUmmaArgs p;      // > 1 KB: keep off the stack
+    static ExpandUmmaArgs p;      // > 2 KB: keep off the stack
     const CUtensorMapSwizzle sw = (rp == 16) ? CU_TENSOR_MAP_SWIZZLE_32B
                                 : (rp == 32) ? CU_TENSOR_MAP_SWIZZLE_64B
                                              : CU_TENSOR_MAP_SWIZZLE_128B;
     for (int s = 0; s < a.num_slices; ++s) {
         if (a.n[s] == 0) continue;
-        const cuuint64_t dims[2] = {cuuint64_t(a.rank), cuuint64_t(a.max_loras) * cuuint64_t(a.n[s])};
-        const cuuint64_t strides[1] = {cuuint64_t(a.rank) * 2};
-        const cuuint32_t box[2] = {cuuint32_t(rp > 64 ? 64 : rp), cuuint32_t(XU_BN)};
-        const cuuint32_t estr[2] = {1, 1};
-        if (fn(&p.map_b[s], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a.b[s]),
-               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        if (!xu_encode(fn, &p.map_b[s], a.b[s], uint64_t(a.max_loras) * uint64_t(a.n[s]),
+                       uint64_t(a.rank), uint64_t(a.rank), uint32_t(rp > 64 ? 64 : rp), XU_BN, sw))
             return 0;
     }
+    for (int i = 0; i < XU_YMAPS; ++i)
+        if (!xu_encode(fn, &p.map_y[i], a.y, uint64_t(a.num_tokens), uint64_t(a.y_ld),
+                       uint64_t(a.y_ld), 64u, 1u << i, CU_TENSOR_MAP_SWIZZLE_128B))
+            return 0;
     p.x = a.x;
     p.y = a.y;
     p.y_ld = a.y_ld;
@@ -528,7 +566,6 @@ int launch_expand_umma(const ExpandLaunch &a, cudaStream_t stream)
         p.n[s] = a.n[s];
         p.col0[s] = a.col0[s];
     }
-    for (int s = 0; s <= a.num_slices; ++s) p.chunk0[s] = 0;
     int chunks = 0;
     for (int s = 0; s < a.num_slices; ++s) {
         p.chunk0[s] = chunks;
