@@ -401,9 +401,12 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    // Tensor-core path (tcgen05, TMEM accumulators) for 16-byte-aligned
-    // outputs; LORA_PUNICA_EXPAND_UMMA=0 keeps every call on mma.sync.
-    if (lora::env_int("LORA_PUNICA_EXPAND_UMMA", 1) && p.vec) {
+    // Tensor-core path (tcgen05, TMEM accumulators, TMA for B and for y over
+    // runs of consecutive tokens) for 16-byte-aligned outputs.  Opt-in with
+    // LORA_PUNICA_EXPAND_UMMA=1: on these workloads it was measured slower
+    // than the mma.sync kernel (a TMA box per scattered token row costs far
+    // more than the cp.async gather), so the default stays on mma.sync.
+    if (lora::env_int("LORA_PUNICA_EXPAND_UMMA", 0) && p.vec) {
         lora::ExpandLaunch u;
         u.x = x;
         for (int s = 0; s < LORA_MAX_SLICES; ++s) {
