@@ -25,7 +25,7 @@ from . import _lib
 from ._lib import LoraError, LORA_MAX_LORAS, LORA_MAX_RANK, LORA_MAX_SLICES  # noqa: F401
 
 __all__ = ["LoRAKernelMeta", "lora_meta_prepare", "lora_shrink", "lora_expand",
-           "add_lora_linear", "LoraError", "library", "build"]
+           "lora_linear", "add_lora_linear", "LoraError", "library", "build"]
 
 
 def library():
@@ -223,3 +223,55 @@ def add_lora_linear(y: torch.Tensor, x: torch.Tensor, lora_a_stacked, lora_b_sta
                              device=x.device)
     lora_shrink(x2, A, buffer, meta, scale)
     lora_expand(buffer, B, y, meta, 0, True, lora_bias_stacked)
+
+
+def lora_linear(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_a_stacked,
+                lora_b_stacked, lora_bias_stacked, scale: float, buffer: torch.Tensor,
+                y: torch.Tensor, meta: LoRAKernelMeta) -> None:
+    """Metadata + shrink + expand of one LoRA layer in one library call
+    (PunicaWrapperGPU.update_metadata followed by add_lora_linear).  Small
+    batches run as one fused kernel; see include/lora_punica.h."""
+    m = token_lora_mapping
+    _need(m, "token_lora_mapping", torch.int32)
+    _need(x, "x", torch.bfloat16)
+    _need(buffer, "buffer", torch.float32)
+    _need(y, "y", torch.bfloat16)
+    x2 = x.view(-1, x.shape[-1]) if x.dim() != 2 else x
+    y2 = y.view(-1, y.shape[-1]) if y.dim() != 2 else y
+    A = _weights(lora_a_stacked, "lora_a_stacked")
+    B = _weights(lora_b_stacked, "lora_b_stacked")
+    T, H = x2.shape
+    if m.dim() != 1 or m.numel() != T or not m.is_contiguous():
+        raise ValueError("token_lora_mapping must be a contiguous [T] tensor")
+    if x2.stride(1) != 1 or y2.stride(1) != 1 or y2.size(0) != T:
+        raise ValueError("x and y need contiguous rows and T rows")
+    if len(A) != len(B):
+        raise ValueError("lora_a_stacked and lora_b_stacked differ in length")
+    L, r, Ha = A[0].shape
+    if Ha != H or any(a.shape != A[0].shape for a in A):
+        raise ValueError("lora_a_stacked shapes must all be [L, r, %d]" % H)
+    if L < meta.max_loras or B[0].size(0) < meta.max_loras:
+        raise ValueError("weights hold fewer LoRAs than the metadata expects")
+    for i, b in enumerate(B):
+        if b.size(2) != r:
+            raise ValueError("lora_b_stacked[%d] must be [L, n, %d]" % (i, r))
+    if tuple(buffer.shape) != (len(A), T, r) or not buffer.is_contiguous():
+        raise ValueError("buffer must be a contiguous fp32 [%d, %d, %d] tensor" % (len(A), T, r))
+    sizes = [b.size(1) for b in B]
+    bias_arr = None
+    if lora_bias_stacked is not None:
+        if len(lora_bias_stacked) != len(B):
+            raise ValueError("lora_bias_stacked needs one entry per slice")
+        for i, (bb, n) in enumerate(zip(lora_bias_stacked, sizes)):
+            if bb is not None:
+                _need(bb, "lora_bias_stacked[%d]" % i, torch.bfloat16)
+                if not bb.is_contiguous() or bb.numel() != B[0].size(0) * n:
+                    raise ValueError("lora_bias_stacked[%d] must be [L, %d]" % (i, n))
+        bias_arr = _ptr_array(list(lora_bias_stacked))
+    size_arr = (ctypes.c_int32 * len(B))(*sizes)
+    st = _lib.load().lora_linear(m.data_ptr(), T, x2.data_ptr(), H, x2.stride(0), _ptr_array(A),
+                                 _ptr_array(B), bias_arr, size_arr, len(B), r, float(scale),
+                                 buffer.data_ptr(), y2.data_ptr(), y2.stride(0),
+                                 ctypes.byref(meta.c), _stream_handle(x.device))
+    _lib.check("lora_linear", st)
+

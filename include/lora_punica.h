@@ -178,6 +178,33 @@ int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
                 int32_t offset_start, int32_t add_inputs,
                 const lora_meta_t *meta, void *stream);
 
+/*
+ * lora_linear -- one LoRA layer applied to a batch, metadata included: the
+ * result of lora_meta_prepare(token_lora_mapping), then lora_shrink(x ->
+ * buf, scale), then lora_expand(buf -> y, lora_bias, offset_start = 0,
+ * add_inputs = 1) (page "vllm.lora.punica_wrapper.punica_gpu",
+ * PunicaWrapperGPU.update_metadata + add_lora_linear: add_shrink into the
+ * fp32 buffer, then add_expand).  Arguments mean what they mean in those
+ * three calls; `buf` is accumulated into like lora_shrink's y, and every
+ * metadata buffer of `meta` is written as lora_meta_prepare writes it.
+ *
+ * Batches of at most 512 tokens (max_loras <= 256, num_slices * padded
+ * rank <= 128, 16-byte-aligned rows, offsets and widths) run as ONE kernel:
+ * a thread-block cluster per (LoRA segment, 64-token tile) builds the
+ * metadata in shared memory, splits the shrink over the hidden dimension,
+ * sums the rank-r partials through distributed shared memory and expands
+ * its share of the output columns.  Other batches run the three kernels in
+ * sequence.  Either way the results equal the three calls' (the fused
+ * shrink sums its partials in a different order).  LORA_PUNICA_FUSED=0 in
+ * the environment forces the three-kernel sequence.
+ */
+int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
+                const lora_bf16_t *x, int32_t hidden, int64_t x_ld,
+                const lora_bf16_t *const *lora_a, const lora_bf16_t *const *lora_b,
+                const lora_bf16_t *const *lora_bias, const int32_t *slice_sizes,
+                int32_t num_slices, int32_t rank, float scale, float *buf,
+                lora_bf16_t *y, int64_t y_ld, const lora_meta_t *meta, void *stream);
+
 /* Human-readable name of a status (negative LORA_ERR_* or cudaError_t). */
 const char *lora_status_string(int status);
 

@@ -1,0 +1,118 @@
+"""GPU parity of lora_linear (metadata + shrink + expand in one call) against
+the oracle composition, with the fused single-kernel path and with the
+three-kernel sequence."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from gpu_helpers import (EXPAND_ATOL, EXPAND_RTOL, SHRINK_ATOL, SHRINK_RTOL, assert_close,
+                         bits_to_f64, dev_bf16, dev_f32, dev_i32, host_bits)
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [pytest.param("1", id="fused"), pytest.param("0", id="three_kernels")]
+
+
+def _check_linear(oracle_mod, inp, ids=None, buf0=None, L=None):
+    import expand_gemm_gb300 as eg
+    w = inp.workload
+    ids = inp.ids if ids is None else ids
+    L = w.max_loras if L is None else L
+    T = ids.shape[0]
+    b0 = inp.buf if buf0 is None else buf0
+    x = dev_bf16(inp.x)
+    A = [dev_bf16(a) for a in inp.lora_a]
+    B = [dev_bf16(b) for b in inp.lora_b]
+    bias = None if inp.lora_bias is None else [dev_bf16(b) for b in inp.lora_bias]
+    y = dev_bf16(inp.y)
+    buf = dev_f32(b0)
+    meta = eg.LoRAKernelMeta.make(L, T, "cuda")
+    eg.lora_linear(dev_i32(ids), x, A, B, bias, w.scale, buf, y, meta)
+    torch.cuda.synchronize()
+
+    o = oracle_mod.meta_prepare(ids, L)
+    assert int(meta.no_lora_flag.item()) == int(o.no_lora_flag[0])
+    np.testing.assert_array_equal(meta.active_lora_ids.cpu().numpy(), o.active_lora_ids)
+    np.testing.assert_array_equal(meta.num_tokens_per_lora.cpu().numpy(), o.num_tokens_per_lora)
+    np.testing.assert_array_equal(meta.lora_token_start_loc.cpu().numpy(), o.lora_token_start_loc)
+    assert int(meta.error_word.item()) & ~(1 << 30) == o.invalid_ids
+    assert int(meta.error_word.item()) & (1 << 30) == 0
+    if not o.no_lora_flag[0]:
+        np.testing.assert_array_equal(meta.token_indices_sorted_by_lora_ids[:T].cpu().numpy(),
+                                      o.token_indices_sorted_by_lora_ids[:T])
+        np.testing.assert_array_equal(meta.token_lora_mapping[:T].cpu().numpy(), ids)
+
+    ref_buf = oracle_mod.shrink(inp.x, inp.lora_a, ids, w.scale, b0)
+    got_buf = buf.cpu().numpy()
+    assert_close(got_buf, ref_buf, SHRINK_ATOL, SHRINK_RTOL, "lora_linear buffer")
+    ref_y = oracle_mod.expand(ref_buf.astype(np.float32), inp.lora_b, ids, inp.y, w.slices,
+                              0, True, inp.lora_bias)
+    got_y = host_bits(y)
+    assert_close(bits_to_f64(got_y), ref_y, EXPAND_ATOL, EXPAND_RTOL, "lora_linear y")
+    none = (ids < 0) | (ids >= L)
+    np.testing.assert_array_equal(got_y[none], inp.y[none])
+    np.testing.assert_array_equal(got_buf[:, none], b0[:, none])
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("mlp", 200)])
+def test_linear_workloads(oracle_mod, monkeypatch, path, name, T):
+    monkeypatch.setenv("LORA_PUNICA_FUSED", path)
+    _check_linear(oracle_mod, W.generate(name, num_tokens=T))
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("T,H,r,L,slices,bias,ids", [
+    (1, 64, 16, 1, (128,), False, "uniform"),              # single token
+    (37, 320, 8, 3, (64, 200, 8), True, "uniform"),        # rank 8, ragged hidden blocks
+    (130, 512, 24, 5, (256, 136), True, "uniform"),        # padded rank, two tiles per LoRA
+    (300, 1024, 32, 4, (128, 128, 128, 128), False, "zipf_seq"),   # four slices, S*rp = 128
+    (512, 2048, 64, 2, (512, 256), True, "zipf_seq"),      # the largest fused batch
+    (513, 256, 16, 3, (128,), False, "uniform"),           # one past it: three kernels
+    (200, 256, 16, 300, (64,), False, "uniform"),          # many LoRAs: three kernels
+])
+def test_linear_shapes(oracle_mod, monkeypatch, path, T, H, r, L, slices, bias, ids):
+    monkeypatch.setenv("LORA_PUNICA_FUSED", path)
+    w = W.Workload("lin", T + H + r, T, H, r, L, slices, ids, p_none=0.2, seq_len=(20, 90),
+                   bias=bias, scale=0.8)
+    inp = W.generate(w)
+    b0 = np.random.default_rng(T).standard_normal(inp.buf.shape).astype(np.float32)
+    _check_linear(oracle_mod, inp, buf0=b0)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_linear_no_lora_and_invalid_ids(oracle_mod, monkeypatch, path):
+    monkeypatch.setenv("LORA_PUNICA_FUSED", path)
+    inp = W.generate("decode")
+    _check_linear(oracle_mod, inp, ids=np.full(256, -1, np.int32))
+    ids = inp.ids.copy()
+    ids[::9] = 8
+    ids[::13] = -3
+    _check_linear(oracle_mod, inp, ids=ids)
+
+
+def test_linear_repeated_calls_accumulate(oracle_mod):
+    """Two calls in a row on the same buffers (the buffer accumulates)."""
+    import expand_gemm_gb300 as eg
+    inp = W.generate("tiny")
+    w = inp.workload
+    x, y = dev_bf16(inp.x), dev_bf16(inp.y)
+    A = [dev_bf16(a) for a in inp.lora_a]
+    B = [dev_bf16(b) for b in inp.lora_b]
+    bias = [dev_bf16(b) for b in inp.lora_bias]
+    buf = dev_f32(inp.buf)
+    meta = eg.LoRAKernelMeta.make(w.max_loras, w.num_tokens, "cuda")
+    ids = dev_i32(inp.ids)
+    for _ in range(2):
+        eg.lora_linear(ids, x, A, B, bias, w.scale, buf, y, meta)
+    torch.cuda.synchronize()
+    b1 = oracle_mod.shrink(inp.x, inp.lora_a, inp.ids, w.scale, inp.buf)
+    y1 = oracle_mod.expand(b1.astype(np.float32), inp.lora_b, inp.ids, inp.y, w.slices, 0, True,
+                           inp.lora_bias)
+    y1_bits = W.bf16_bits(y1.astype(np.float32))
+    b2 = oracle_mod.shrink(inp.x, inp.lora_a, inp.ids, w.scale, b1.astype(np.float32))
+    y2 = oracle_mod.expand(b2.astype(np.float32), inp.lora_b, inp.ids, y1_bits, w.slices, 0,
+                           True, inp.lora_bias)
+    assert_close(buf.cpu().numpy(), b2, SHRINK_ATOL, SHRINK_RTOL, "buffer after two calls")
+    assert_close(bits_to_f64(host_bits(y)), y2, 2 * EXPAND_ATOL, 2 * EXPAND_RTOL, "y after two calls")
