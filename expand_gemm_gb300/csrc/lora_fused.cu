@@ -55,6 +55,7 @@ struct FusedArgs {
     uint16_t *y;
     int64_t y_ld;
     int32_t hper;                        // hidden elements per CTA (multiple of 64)
+    int32_t nst;                         // expand stages (1..8)
     // metadata outputs
     int32_t *mapping_copy;
     int32_t *sorted;
@@ -75,7 +76,7 @@ struct FuLayout {
     int aop_off, stage_off, stage_bytes;
 };
 
-__host__ __device__ inline FuLayout fu_layout(int S, int rp, int nbins, int hper)
+__host__ __device__ inline FuLayout fu_layout(int S, int rp, int nbins, int hper, int nst)
 {
     FuLayout l;
     const int M = S * rp;                                   // stacked A rows
@@ -93,14 +94,28 @@ __host__ __device__ inline FuLayout fu_layout(int S, int rp, int nbins, int hper
     // shrink: x tile [FU_TT][hper] and A tile [M][hper], 64-column blocks
     l.xs_off = l.work_off;
     l.as_off = l.xs_off + FU_TT * hper * 2;
-    const int shrink_end = l.as_off + M * hper * 2;
-    // expand: A operand [FU_TT][rp] bf16, then 2 stages of y tile + B tile + bias
-    l.aop_off = l.work_off;
+    // expand (its own region, so its loads can fly during the shrink):
+    // A operand [FU_TT][rp] bf16, then nst stages of y tile + B tile + bias
+    l.aop_off = (l.as_off + M * hper * 2 + 127) & ~127;
     l.stage_bytes = (FU_TT * FU_Y_LD + FU_BN * rp * 2 + FU_BN * 2 + 127) & ~127;
     l.stage_off = (l.aop_off + FU_TT * rp * 2 + 127) & ~127;
-    const int expand_end = l.stage_off + 2 * l.stage_bytes;
-    l.total = (shrink_end > expand_end ? shrink_end : expand_end) + 128;
+    l.total = l.stage_off + nst * l.stage_bytes + 128;
     return l;
+}
+
+__device__ __forceinline__ void cp_async_wait_dyn(int n)
+{
+    switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    case 7: cp_async_wait<7>(); break;
+    default: cp_async_wait<8>(); break;
+    }
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -127,8 +142,8 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank)
 __device__ __forceinline__ float4 ld_peer_f4(uint32_t addr)
 {
     float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+    asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
     return v;
 }
 
@@ -139,7 +154,7 @@ __global__ void __launch_bounds__(FU_THREADS, 1) fused_kernel(FusedArgs p)
     const int S = p.num_slices, RP = p.rp, R = p.rank, T = p.num_tokens;
     const int M = S * RP, MT = M / 16;
     const int nbins = p.max_loras + 1;
-    const FuLayout Ly = fu_layout(S, RP, nbins, p.hper);
+    const FuLayout Ly = fu_layout(S, RP, nbins, p.hper, p.nst);
     int32_t *cnt = reinterpret_cast<int32_t *>(smem + Ly.cnt_off);
     int32_t *tot = reinterpret_cast<int32_t *>(smem + Ly.tot_off);
     int32_t *basev = reinterpret_cast<int32_t *>(smem + Ly.base_off);
@@ -281,6 +296,37 @@ __global__ void __launch_bounds__(FU_THREADS, 1) fused_kernel(FusedArgs p)
         const int r0 = basev[b] + u * FU_TT;
         const int nt = min(FU_TT, basev[b] + tot[b] - r0);
         const int32_t *tok = srt + r0;                        // nt tokens (shared)
+        const int CPR = RP / 8;
+        const int nmine = max(0, ce - cb);                    // expand chunks of this CTA
+        int issued = 0;
+        auto load_chunk = [&](int slot, int c) {
+            int s = 0;
+            while (s + 1 < S && p.chunk0[s + 1] <= c) ++s;
+            const int n_s = p.n[s];
+            const int c0 = (c - p.chunk0[s]) * FU_BN;
+            const int ncols = min(FU_BN, n_s - c0);
+            const uint32_t sy = smem_addr(smem + Ly.stage_off + slot * Ly.stage_bytes);
+            const uint32_t sb = sy + FU_TT * FU_Y_LD;
+            const uint32_t sbias = sb + FU_BN * RP * 2;
+            uint16_t *yslice = p.y + p.col0[s];
+            for (int i = tid; i < FU_TT * (FU_BN / 8); i += FU_THREADS) {
+                const int r = i >> 4, cc = i & 15;
+                const bool ok = r < nt && cc * 8 < ncols;
+                cp_async16(sy + r * FU_Y_LD + cc * 16,
+                           ok ? yslice + int64_t(tok[r]) * p.y_ld + c0 + cc * 8 : p.y, ok);
+            }
+            const uint16_t *bbase = p.b[s] + (int64_t(id) * n_s + c0) * R;
+            for (int i = tid; i < FU_BN * CPR; i += FU_THREADS) {
+                const int r = i / CPR, cc = i - r * CPR;
+                const bool ok = r < ncols && cc * 8 < R;
+                const uint32_t dst = (RP == 16) ? sb + swz<2>(r, cc)
+                                   : (RP == 32) ? sb + swz<4>(r, cc) : sb + swz<8>(r, cc);
+                cp_async16(dst, ok ? bbase + int64_t(r) * R + cc * 8 : p.b[s], ok);
+            }
+            const uint16_t *bias_row = p.bias[s] ? p.bias[s] + int64_t(id) * n_s + c0 : nullptr;
+            if (bias_row != nullptr && tid < FU_BN / 8 && tid * 8 < ncols)
+                cp_async16(sbias + tid * 16, bias_row + tid * 8, true);
+        };
 
         // ------------------------------------------------ 2. shrink partial
         {
@@ -303,8 +349,13 @@ __global__ void __launch_bounds__(FU_THREADS, 1) fused_kernel(FusedArgs p)
                 cp_async16(as + kb * (M * 128) + swz<8>(row, c),
                            ok ? p.a[s] + (int64_t(id) * R + ri) * p.hidden + h : p.x, ok);
             }
-            cp_async_commit();
-            cp_async_wait<0>();
+            cp_async_commit();                                // group: shrink tiles
+            // prefetch the first expand chunks (they need only tokens and id)
+            for (; issued < nmine && issued < p.nst; ++issued) {
+                load_chunk(issued % p.nst, cb + issued);
+                cp_async_commit();
+            }
+            cp_async_wait_dyn(issued);                         // shrink tiles landed
             __syncthreads();
             // warp w: tokens [8w, 8w + 8), all MT row tiles
             float acc[8][4];
@@ -358,11 +409,14 @@ __global__ void __launch_bounds__(FU_THREADS, 1) fused_kernel(FusedArgs p)
             const int e0 = int(rank) * per, e1 = min(E, e0 + per);
             const uint32_t pa = smem_addr(P);
             for (int e = e0 + tid * 4; e < e1; e += FU_THREADS * 4) {
+                // all CL remote loads in flight before the first add
+                float4 v[CL];
+#pragma unroll
+                for (int j = 0; j < CL; ++j) v[j] = ld_peer_f4(map_peer(pa + e * 4, uint32_t(j)));
                 float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < CL; ++j) {
-                    const float4 v = ld_peer_f4(map_peer(pa + e * 4, uint32_t(j)));
-                    s4.x += v.x; s4.y += v.y; s4.z += v.z; s4.w += v.w;
+                    s4.x += v[j].x; s4.y += v[j].y; s4.z += v[j].z; s4.w += v[j].w;
                 }
                 // the owner updates the fp32 buffer (buf += scale * sum) and keeps
                 // the updated value: that is what expand reads from the buffer
@@ -400,46 +454,13 @@ __global__ void __launch_bounds__(FU_THREADS, 1) fused_kernel(FusedArgs p)
         cluster_sync_all();                                   // peers done reading P / RED
 
         // ------------------------------------------------ 4. expand
-        if (cb < ce) {
+        if (nmine > 0) {
             uint8_t *aop = smem + Ly.aop_off;
             const uint32_t aopa = smem_addr(aop);
-            const int CPR = RP / 8;
             int cur_s = -1;
-            auto load_chunk = [&](int slot, int c) {
-                int s = 0;
-                while (s + 1 < S && p.chunk0[s + 1] <= c) ++s;
-                const int n_s = p.n[s];
-                const int c0 = (c - p.chunk0[s]) * FU_BN;
-                const int ncols = min(FU_BN, n_s - c0);
-                const uint32_t sy = smem_addr(smem + Ly.stage_off + slot * Ly.stage_bytes);
-                const uint32_t sb = sy + FU_TT * FU_Y_LD;
-                const uint32_t sbias = sb + FU_BN * RP * 2;
-                uint16_t *yslice = p.y + p.col0[s];
-                for (int i = tid; i < FU_TT * (FU_BN / 8); i += FU_THREADS) {
-                    const int r = i >> 4, cc = i & 15;
-                    const bool ok = r < nt && cc * 8 < ncols;
-                    cp_async16(sy + r * FU_Y_LD + cc * 16,
-                               ok ? yslice + int64_t(tok[r]) * p.y_ld + c0 + cc * 8 : p.y, ok);
-                }
-                const uint16_t *bbase = p.b[s] + (int64_t(id) * n_s + c0) * R;
-                for (int i = tid; i < FU_BN * CPR; i += FU_THREADS) {
-                    const int r = i / CPR, cc = i - r * CPR;
-                    const bool ok = r < ncols && cc * 8 < R;
-                    const uint32_t dst = (RP == 16) ? sb + swz<2>(r, cc)
-                                       : (RP == 32) ? sb + swz<4>(r, cc) : sb + swz<8>(r, cc);
-                    cp_async16(dst, ok ? bbase + int64_t(r) * R + cc * 8 : p.b[s], ok);
-                }
-                const uint16_t *bias_row = p.bias[s] ? p.bias[s] + int64_t(id) * n_s + c0 : nullptr;
-                if (bias_row != nullptr && tid < FU_BN / 8 && tid * 8 < ncols)
-                    cp_async16(sbias + tid * 16, bias_row + tid * 8, true);
-            };
-            load_chunk(0, cb);
-            cp_async_commit();
             const int wm = warp >> 2, wn = warp & 3;         // 2 x 4 warps, 32 x 32 each
-            for (int c = cb; c < ce; ++c) {
-                const int slot = (c - cb) & 1;
-                if (c + 1 < ce) load_chunk(slot ^ 1, c + 1);
-                cp_async_commit();
+            for (int i = 0; i < nmine; ++i) {
+                const int c = cb + i, slot = i % p.nst;
                 int s = 0;
                 while (s + 1 < S && p.chunk0[s + 1] <= c) ++s;
                 if (s != cur_s) {
@@ -460,7 +481,7 @@ __global__ void __launch_bounds__(FU_THREADS, 1) fused_kernel(FusedArgs p)
                     }
                     cur_s = s;
                 }
-                cp_async_wait<1>();
+                cp_async_wait_dyn(issued - (i + 1));          // chunk i landed
                 __syncthreads();
                 const int n_s = p.n[s];
                 const int c0 = (c - p.chunk0[s]) * FU_BN;
@@ -526,10 +547,15 @@ __global__ void __launch_bounds__(FU_THREADS, 1) fused_kernel(FusedArgs p)
                     *reinterpret_cast<uint4 *>(yslice + int64_t(tok[r]) * p.y_ld + c0 + cc * 8) = v;
                 }
                 __syncthreads();
+                if (issued < nmine) {                          // refill the slot just used
+                    load_chunk(issued % p.nst, cb + issued);
+                    cp_async_commit();
+                    ++issued;
+                }
             }
-            cp_async_wait<0>();
-            __syncthreads();
         }
+        cp_async_wait<0>();
+        __syncthreads();
     }
 }
 
@@ -617,7 +643,12 @@ int launch_fused(FusedArgs &p, cudaStream_t stream)
     const int cl = cl_cache[dev];
     if (cl <= 0) return 0;
     p.hper = hper_for(cl);
-    const FuLayout L = fu_layout(p.num_slices, rp, nbins, p.hper);
+    int chunks_total = p.chunk0[p.num_slices];
+    const int cper = (chunks_total + cl - 1) / cl;
+    p.nst = 8;
+    if (p.nst > cper) p.nst = max(1, cper);
+    while (p.nst > 1 && fu_layout(p.num_slices, rp, nbins, p.hper, p.nst).total > 227 * 1024) --p.nst;
+    const FuLayout L = fu_layout(p.num_slices, rp, nbins, p.hper, p.nst);
     if (L.total > 227 * 1024) return 0;
     // units: at most ceil(T / 64) + (number of distinct ids)
     const int units_max = (p.num_tokens + FU_TT - 1) / FU_TT + min(p.max_loras, p.num_tokens);
