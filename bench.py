@@ -80,9 +80,10 @@ def _padded_rank(r: int) -> int:
 
 def fused_path(w) -> bool:
     """lora_linear's rule for its single fused kernel (include/lora_punica.h)."""
-    return (w.num_tokens <= 512 and w.max_loras <= 256 and _padded_rank(w.rank) <= 64
-            and w.num_slices * _padded_rank(w.rank) <= 128
-            and os.environ.get("LORA_PUNICA_FUSED", "1") != "0")
+    mode = os.environ.get("LORA_PUNICA_FUSED", "")
+    limit = 512 if mode == "1" else int(os.environ.get("LORA_PUNICA_FUSED_MAX_TOKENS", "128"))
+    return (w.num_tokens <= limit and w.max_loras <= 256 and _padded_rank(w.rank) <= 64
+            and w.num_slices * _padded_rank(w.rank) <= 128 and mode != "0")
 
 
 def umma_shrink_path(w) -> bool:

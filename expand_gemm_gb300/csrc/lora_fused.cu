@@ -676,8 +676,16 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     // One fused kernel for small batches when every layout rule of the
-    // vector paths holds; LORA_PUNICA_FUSED=0 turns it off.
-    bool fused = lora::env_int("LORA_PUNICA_FUSED", 1) != 0 && num_tokens > 0 &&
+    // vector paths holds.  By default it is taken for batches of at most
+    // LORA_PUNICA_FUSED_MAX_TOKENS (128) tokens: measured on decode-sized
+    // batches (256 tokens, 8 LoRAs) the per-unit chain of cluster syncs and
+    // shared-memory reductions made it slower than the three kernels, on 64
+    // tokens faster.  LORA_PUNICA_FUSED=1 takes it up to 512 tokens,
+    // LORA_PUNICA_FUSED=0 never.
+    const int fused_mode = lora::env_int("LORA_PUNICA_FUSED", -1);
+    const int fused_max = fused_mode == 1 ? lora::FU_TMAX
+                        : lora::env_int("LORA_PUNICA_FUSED_MAX_TOKENS", 128);
+    bool fused = fused_mode != 0 && num_tokens > 0 && num_tokens <= fused_max &&
                  token_lora_mapping != nullptr && x != nullptr && buf != nullptr && y != nullptr &&
                  hidden > 0 && hidden % 8 == 0 && x_ld % 8 == 0 && y_ld % 8 == 0 &&
                  meta->max_loras >= 1 && meta->max_loras <= lora::FU_MAX_LORAS &&

@@ -188,15 +188,17 @@ int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
  * three calls; `buf` is accumulated into like lora_shrink's y, and every
  * metadata buffer of `meta` is written as lora_meta_prepare writes it.
  *
- * Batches of at most 512 tokens (max_loras <= 256, num_slices * padded
- * rank <= 128, 16-byte-aligned rows, offsets and widths) run as ONE kernel:
- * a thread-block cluster per (LoRA segment, 64-token tile) builds the
- * metadata in shared memory, splits the shrink over the hidden dimension,
- * sums the rank-r partials through distributed shared memory and expands
- * its share of the output columns.  Other batches run the three kernels in
- * sequence.  Either way the results equal the three calls' (the fused
- * shrink sums its partials in a different order).  LORA_PUNICA_FUSED=0 in
- * the environment forces the three-kernel sequence.
+ * Small batches (by default at most 128 tokens; max_loras <= 256,
+ * num_slices * padded rank <= 128, 16-byte-aligned rows, offsets and
+ * widths) run as ONE kernel: a thread-block cluster per (LoRA segment,
+ * 64-token tile) builds the metadata in shared memory, splits the shrink
+ * over the hidden dimension, sums the rank-r partials through distributed
+ * shared memory and expands its share of the output columns.  Other
+ * batches run the three kernels in sequence.  Either way the results equal
+ * the three calls' (the fused shrink sums its partials in a different
+ * order).  Environment: LORA_PUNICA_FUSED=0 forces the three kernels,
+ * LORA_PUNICA_FUSED=1 allows the fused kernel up to 512 tokens,
+ * LORA_PUNICA_FUSED_MAX_TOKENS sets the default limit.
  */
 int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
                 const lora_bf16_t *x, int32_t hidden, int64_t x_ld,
