@@ -189,6 +189,164 @@ __device__ __forceinline__ int load_segments(const int32_t *no_lora, const int32
     return t.tile[nbins];
 }
 
+// Stable counting sort of a small batch's LoRA ids inside one CTA of NW
+// warps (the metadata step of LoRAKernelMeta.prepare_tensors, computed in
+// shared memory).  Bin 0 holds id -1 and invalid ids, bin b holds id b - 1.
+// Shared arrays: cnt[NW * nbins], tot[nbins], base[nbins], pos[nbins],
+// srt[T] (the permutation), misc[2] (invalid ids, number of non-empty bins).
+// Each warp owns a contiguous run of tokens, so warp order, group order and
+// lane order together give token order inside every bin.  Returns the
+// no-LoRA flag to every thread; srt is only filled when it is false.
+template <int NW>
+__device__ __forceinline__ bool block_sort_ids(const int32_t *map, int T, int max_loras,
+                                               int *cnt, int *tot, int *base, int *pos,
+                                               int *srt, int *misc)
+{
+    const int nbins = max_loras + 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < NW * nbins; i += NW * 32) cnt[i] = 0;
+    if (tid == 0) misc[0] = 0;
+    __syncthreads();
+    const int per_warp = ((T + NW * 32 - 1) / (NW * 32)) * 32;
+    const int t0 = min(T, warp * per_warp), t1 = min(T, t0 + per_warp);
+    int bad = 0;
+    for (int g = t0; g < t1; g += 32) {
+        const int t = g + lane;
+        const bool has = t < t1;
+        int b = -1;
+        if (has) {
+            const int32_t id = map[t];
+            if (id >= 0 && id < max_loras) b = id + 1;
+            else { b = 0; if (id != -1) ++bad; }
+        }
+        const unsigned grp = __match_any_sync(0xffffffffu, b);
+        if (has && lane == __ffs(grp) - 1) cnt[warp * nbins + b] += __popc(grp);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if (lane == 0 && bad) atomicAdd(&misc[0], bad);
+    __syncthreads();
+    for (int b = tid; b < nbins; b += NW * 32) {
+        int run = 0;
+        for (int w = 0; w < NW; ++w) {
+            const int c = cnt[w * nbins + b];
+            cnt[w * nbins + b] = run;
+            run += c;
+        }
+        tot[b] = run;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int ct = 0, cp = 0;
+        for (int b0 = 0; b0 < nbins; b0 += 32) {
+            const int b = b0 + lane;
+            const int v = (b < nbins) ? tot[b] : 0;
+            const int f = v > 0 ? 1 : 0;
+            int iv = v, jf = f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, iv, o);
+                const int w = __shfl_up_sync(0xffffffffu, jf, o);
+                if (lane >= o) { iv += u; jf += w; }
+            }
+            if (b < nbins) { base[b] = ct + iv - v; pos[b] = cp + jf - f; }
+            ct += __shfl_sync(0xffffffffu, iv, 31);
+            cp += __shfl_sync(0xffffffffu, jf, 31);
+        }
+        if (lane == 0) misc[1] = cp;
+    }
+    __syncthreads();
+    const bool no_lora = (tot[0] == T);
+    if (!no_lora) {
+        for (int g = t0; g < t1; g += 32) {
+            const int t = g + lane;
+            const bool has = t < t1;
+            int b = -1;
+            if (has) {
+                const int32_t id = map[t];
+                b = (id >= 0 && id < max_loras) ? id + 1 : 0;
+            }
+            const unsigned grp = __match_any_sync(0xffffffffu, b);
+            const int rk = __popc(grp & ((1u << lane) - 1u));
+            if (has) srt[base[b] + cnt[warp * nbins + b] + rk] = t;
+            __syncwarp();
+            if (has && rk == 0) cnt[warp * nbins + b] += __popc(grp);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    return no_lora;
+}
+
+// Writes the metadata buffers from a block_sort_ids result (one CTA calls it).
+__device__ __forceinline__ void write_meta(const int32_t *map, int T, int max_loras, bool no_lora,
+                                           const int *tot, const int *base, const int *pos,
+                                           const int *srt, const int *misc,
+                                           int32_t *mapping_copy, int32_t *sorted, int32_t *counts,
+                                           int32_t *start_loc, int32_t *active, int32_t *flag,
+                                           int32_t *error_word)
+{
+    const int nbins = max_loras + 1;
+    const int nact = no_lora ? 0 : misc[1];
+    for (int k = threadIdx.x; k < nbins; k += blockDim.x)
+        if (k >= nact) { active[k] = -1; counts[k] = 0; start_loc[k + 1] = 0; }
+    if (threadIdx.x == 0) {
+        start_loc[0] = 0;
+        *flag = no_lora ? 1 : 0;
+        *error_word = misc[0];
+    }
+    if (no_lora) return;
+    for (int b = threadIdx.x; b < nbins; b += blockDim.x) {
+        const int c = tot[b];
+        if (c > 0) {
+            const int k = pos[b];
+            active[k] = b - 1;
+            counts[k] = c;
+            start_loc[k + 1] = base[b] + c;
+        }
+    }
+    for (int t = threadIdx.x; t < T; t += blockDim.x) {
+        sorted[t] = srt[t];
+        mapping_copy[t] = map[t];
+    }
+}
+
+// Fills a segment table from a block_sort_ids result (segment k = bin k)
+// and scans it into tiles of `tile_rows`; returns the total tile count.
+__device__ __forceinline__ int segments_from_sort(const int *tot, const int *base, int nbins,
+                                                  int tile_rows, SegTab t)
+{
+    for (int k = threadIdx.x; k < nbins; k += blockDim.x) {
+        t.id[k] = (k >= 1 && tot[k] > 0) ? k - 1 : -1;
+        t.count[k] = tot[k];
+        t.start[k] = base[k];
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int carry = 0;
+        for (int b0 = 0; b0 < nbins; b0 += 32) {
+            const int k = b0 + lane;
+            int n = 0;
+            if (k < nbins) {
+                const int c = t.count[k];
+                n = (t.id[k] >= 0 && c > 0) ? (c + tile_rows - 1) / tile_rows : 0;
+            }
+            int v = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (k < nbins) t.tile[k] = carry + v - n;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) t.tile[nbins] = carry;
+    }
+    __syncthreads();
+    return t.tile[nbins];
+}
+
 // Segment that holds global tile `tile`: the last k with s_tile[k] <= tile.
 // Segments with no tiles (id -1, or no tokens) share their successor's
 // prefix value and are skipped by the search.
@@ -230,6 +388,10 @@ struct ShrinkLaunch {
     int32_t *error_word;
 };
 int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream);
+int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_tokens,
+                     int32_t hidden, int64_t x_ld, const lora_bf16_t *const *lora_a,
+                     int32_t num_slices, int32_t rank, float *y, const lora_meta_t *meta,
+                     float scale, cudaStream_t st);
 
 // Host-side description of one lora_expand call for its tensor-core path.
 struct ExpandLaunch {

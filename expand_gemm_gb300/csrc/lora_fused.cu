@@ -747,10 +747,21 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
             if (r != 0) return r;
         }
     }
-    int r = lora_meta_prepare(token_lora_mapping, num_tokens, meta, stream);
-    if (r != 0) return r;
-    r = lora_shrink(x, num_tokens, hidden, x_ld, lora_a, num_slices, rank, buf, meta, scale, stream);
-    if (r != 0) return r;
+    // Two kernels for small batches (the shrink sorts the ids itself and
+    // writes the metadata), three otherwise.  LORA_PUNICA_SELF_META=0 keeps
+    // the separate metadata kernel.
+    int r = 0;
+    if (lora::env_int("LORA_PUNICA_SELF_META", 1) != 0)
+        r = lora::shrink_self_meta(token_lora_mapping, x, num_tokens, hidden, x_ld, lora_a,
+                                   num_slices, rank, buf, meta, scale, st);
+    if (r < 0 || r > 1) return r;
+    if (r == 0) {
+        r = lora_meta_prepare(token_lora_mapping, num_tokens, meta, stream);
+        if (r != 0) return r;
+        r = lora_shrink(x, num_tokens, hidden, x_ld, lora_a, num_slices, rank, buf, meta, scale,
+                        stream);
+        if (r != 0) return r;
+    }
     return lora_expand(buf, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld, num_tokens,
                        0, 1, meta, stream);
 }

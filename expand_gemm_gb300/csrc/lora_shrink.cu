@@ -42,7 +42,25 @@ struct ShrinkArgs {
     const int32_t *no_lora;
     int32_t nbins;                 // max_loras + 1
     int32_t skip_rows;             // rows per segment left to the tensor-core path
+    // Self-built metadata (small batches, lora_linear): every CTA sorts the
+    // raw id map in shared memory; CTA 0 also writes the metadata buffers.
+    const int32_t *map;            // non-null selects this mode
+    int32_t *mapping_copy;
+    int32_t *sorted_out;
+    int32_t *counts_out;
+    int32_t *start_out;
+    int32_t *active_out;
+    int32_t *no_lora_out;
+    int32_t *error_out;
 };
+
+constexpr int SH_SELF_META_MAX_TOKENS = 512;
+
+// Extra shared memory of the self-built-metadata mode.
+size_t shrink_self_meta_bytes(int nbins)
+{
+    return size_t(4 * nbins + 3 * nbins + SH_SELF_META_MAX_TOKENS + 4) * sizeof(int);
+}
 
 template <int MT>
 struct ShrinkTile {
@@ -79,8 +97,25 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
     pdl_launch_dependents();
 
     const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + Cfg::RING_BYTES), p.nbins);
-    const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
-                                          p.nbins, SH_BN, tab, false, p.skip_rows);
+    const int32_t *tokens = p.sorted;
+    int total_tiles;
+    if (p.map != nullptr) {
+        int *mm = reinterpret_cast<int *>(smem + Cfg::RING_BYTES + seg_tab_bytes(p.nbins));
+        int *cnt = mm, *tot = cnt + 4 * p.nbins, *base = tot + p.nbins, *pos = base + p.nbins;
+        int *srt = pos + p.nbins, *misc = srt + SH_SELF_META_MAX_TOKENS;
+        const bool nl = block_sort_ids<SH_THREADS / 32>(p.map, p.num_tokens, p.nbins - 1, cnt,
+                                                        tot, base, pos, srt, misc);
+        if (blockIdx.x == 0)
+            write_meta(p.map, p.num_tokens, p.nbins - 1, nl, tot, base, pos, srt, misc,
+                       p.mapping_copy, p.sorted_out, p.counts_out, p.start_out, p.active_out,
+                       p.no_lora_out, p.error_out);
+        if (nl) return;
+        total_tiles = segments_from_sort(tot, base, p.nbins, SH_BN, tab);
+        tokens = srt;
+    } else {
+        total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
+                                    p.nbins, SH_BN, tab, false, p.skip_rows);
+    }
     if (total_tiles == 0) return;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -112,7 +147,7 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
         const int id = tab.id[seg];
         const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * SH_BN;
         const int nrows = min(SH_BN, tab.start[seg] + tab.count[seg] - row0);
-        if (tid < SH_BN) s_tok[tid] = (tid < nrows) ? p.sorted[row0 + tid] : -1;
+        if (tid < SH_BN) s_tok[tid] = (tid < nrows) ? tokens[row0 + tid] : -1;
         __syncthreads();
 
         const int k_first = kc * steps_per_chunk;
@@ -239,7 +274,8 @@ static int launch_shrink_mt(const ShrinkArgs &p, cudaStream_t stream)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return int(e);
-    const size_t smem = shrink_smem_bytes(MT, LORA_MAX_LORAS + 1);
+    const size_t smem = shrink_smem_bytes(MT, LORA_MAX_LORAS + 1) +
+                        shrink_self_meta_bytes(LORA_MAX_LORAS + 1);
     int grid = (dev < 64) ? grid_cache[dev] : 0;
     if (grid == 0) {
         e = cudaFuncSetAttribute(shrink_kernel<MT>,
@@ -252,8 +288,9 @@ static int launch_shrink_mt(const ShrinkArgs &p, cudaStream_t stream)
         grid = device_sm_count() * max(occ, 1);
         if (dev < 64) grid_cache[dev] = grid;
     }
-    e = launch_kernel(shrink_kernel<MT>, dim3(grid), dim3(SH_THREADS),
-                      shrink_smem_bytes(MT, p.nbins), stream, p);
+    const size_t used = shrink_smem_bytes(MT, p.nbins) +
+                        (p.map != nullptr ? shrink_self_meta_bytes(p.nbins) : 0);
+    e = launch_kernel(shrink_kernel<MT>, dim3(grid), dim3(SH_THREADS), used, stream, p);
     return int(e);
 }
 
@@ -301,6 +338,7 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
     p.no_lora = meta->no_lora_flag;
     p.nbins = meta->max_loras + 1;
     p.skip_rows = 0;
+    p.map = nullptr;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -340,3 +378,65 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
     if (rank <= 64) return lora::launch_shrink_mt<4>(p, st);
     return lora::launch_shrink_mt<8>(p, st);
 }
+
+namespace lora {
+
+// lora_shrink for lora_linear on small batches: the kernel sorts the raw id
+// map itself (no separate metadata kernel) and CTA 0 writes the metadata
+// buffers exactly as lora_meta_prepare would.  Returns 0 when it does not
+// apply (the caller then runs the metadata kernel and lora_shrink), 1 when
+// launched, or an error status.
+int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_tokens,
+                     int32_t hidden, int64_t x_ld, const lora_bf16_t *const *lora_a,
+                     int32_t num_slices, int32_t rank, float *y, const lora_meta_t *meta,
+                     float scale, cudaStream_t st)
+{
+    if (num_tokens < 1 || num_tokens > SH_SELF_META_MAX_TOKENS || meta->max_loras > 256)
+        return 0;
+    if (num_slices < 1 || num_slices > LORA_MAX_SLICES || rank < 8 || rank > LORA_MAX_RANK ||
+        rank % 8 != 0 || hidden < 8 || hidden % 8 != 0 || x_ld % 8 != 0 || x_ld < hidden)
+        return 0;
+    if (!map || !x || !y || !meta->token_lora_mapping || !meta->token_indices_sorted_by_lora_ids ||
+        !meta->num_tokens_per_lora || !meta->lora_token_start_loc || !meta->active_lora_ids ||
+        !meta->no_lora_flag || !meta->error_word)
+        return 0;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) return 0;
+    ShrinkArgs p;
+    for (int s = 0; s < LORA_MAX_SLICES; ++s) p.a[s] = nullptr;
+    for (int s = 0; s < num_slices; ++s) {
+        if (lora_a[s] == nullptr || (reinterpret_cast<uintptr_t>(lora_a[s]) & 15u)) return 0;
+        p.a[s] = lora_a[s];
+    }
+    p.x = x;
+    p.x_ld = x_ld;
+    p.hidden = hidden;
+    p.num_tokens = num_tokens;
+    p.num_slices = num_slices;
+    p.rank = rank;
+    p.y = y;
+    p.scale = scale;
+    p.sorted = nullptr;
+    p.counts = nullptr;
+    p.start_loc = nullptr;
+    p.active = nullptr;
+    p.no_lora = nullptr;
+    p.nbins = meta->max_loras + 1;
+    p.skip_rows = 0;
+    p.map = map;
+    p.mapping_copy = meta->token_lora_mapping;
+    p.sorted_out = meta->token_indices_sorted_by_lora_ids;
+    p.counts_out = meta->num_tokens_per_lora;
+    p.start_out = meta->lora_token_start_loc;
+    p.active_out = meta->active_lora_ids;
+    p.no_lora_out = meta->no_lora_flag;
+    p.error_out = meta->error_word;
+    int r;
+    if (rank <= 16) r = launch_shrink_mt<1>(p, st);
+    else if (rank <= 32) r = launch_shrink_mt<2>(p, st);
+    else if (rank <= 64) r = launch_shrink_mt<4>(p, st);
+    else r = launch_shrink_mt<8>(p, st);
+    return r == 0 ? 1 : r;
+}
+
+}  // namespace lora
+

@@ -11,7 +11,15 @@ from gpu_helpers import (EXPAND_ATOL, EXPAND_RTOL, SHRINK_ATOL, SHRINK_RTOL, ass
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [pytest.param("1", id="fused"), pytest.param("0", id="three_kernels")]
+# (LORA_PUNICA_FUSED, LORA_PUNICA_SELF_META): one fused kernel; the shrink
+# sorting the ids itself + expand; metadata kernel + shrink + expand.
+PATHS = [pytest.param(("1", "1"), id="fused"), pytest.param(("0", "1"), id="two_kernels"),
+         pytest.param(("0", "0"), id="three_kernels")]
+
+
+def _set_path(monkeypatch, path):
+    monkeypatch.setenv("LORA_PUNICA_FUSED", path[0])
+    monkeypatch.setenv("LORA_PUNICA_SELF_META", path[1])
 
 
 def _check_linear(oracle_mod, inp, ids=None, buf0=None, L=None):
@@ -58,7 +66,7 @@ def _check_linear(oracle_mod, inp, ids=None, buf0=None, L=None):
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("mlp", 200)])
 def test_linear_workloads(oracle_mod, monkeypatch, path, name, T):
-    monkeypatch.setenv("LORA_PUNICA_FUSED", path)
+    _set_path(monkeypatch, path)
     _check_linear(oracle_mod, W.generate(name, num_tokens=T))
 
 
@@ -73,7 +81,7 @@ def test_linear_workloads(oracle_mod, monkeypatch, path, name, T):
     (200, 256, 16, 300, (64,), False, "uniform"),          # many LoRAs: three kernels
 ])
 def test_linear_shapes(oracle_mod, monkeypatch, path, T, H, r, L, slices, bias, ids):
-    monkeypatch.setenv("LORA_PUNICA_FUSED", path)
+    _set_path(monkeypatch, path)
     w = W.Workload("lin", T + H + r, T, H, r, L, slices, ids, p_none=0.2, seq_len=(20, 90),
                    bias=bias, scale=0.8)
     inp = W.generate(w)
@@ -83,7 +91,7 @@ def test_linear_shapes(oracle_mod, monkeypatch, path, T, H, r, L, slices, bias, 
 
 @pytest.mark.parametrize("path", PATHS)
 def test_linear_no_lora_and_invalid_ids(oracle_mod, monkeypatch, path):
-    monkeypatch.setenv("LORA_PUNICA_FUSED", path)
+    _set_path(monkeypatch, path)
     inp = W.generate("decode")
     _check_linear(oracle_mod, inp, ids=np.full(256, -1, np.int32))
     ids = inp.ids.copy()
