@@ -391,7 +391,11 @@ int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream);
 int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_tokens,
                      int32_t hidden, int64_t x_ld, const lora_bf16_t *const *lora_a,
                      int32_t num_slices, int32_t rank, float *y, const lora_meta_t *meta,
-                     float scale, cudaStream_t st);
+                     float scale, cudaStream_t st, int early);
+int expand_early(const float *x, const lora_bf16_t *const *lora_b,
+                 const lora_bf16_t *const *lora_bias, const int32_t *slice_sizes,
+                 int32_t num_slices, int32_t rank, lora_bf16_t *y, int64_t y_ld,
+                 int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st);
 
 // Host-side description of one lora_expand call for its tensor-core path.
 struct ExpandLaunch {

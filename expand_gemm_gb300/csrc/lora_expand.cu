@@ -47,6 +47,14 @@ struct ExpandArgs {
     const int32_t *active;
     const int32_t *no_lora;
     int32_t nbins;
+    // Early mode (set only by lora_linear, whose preceding kernel is its own
+    // shrink): the segment table, the token list and the y / B / bias loads
+    // of the first tile are issued before the grid-dependency wait; only the
+    // shrink output (x) is read after it.  Safe because the shrink lets its
+    // dependents launch only after its own wait, i.e. once the metadata
+    // kernel and everything before it in the stream have completed, and the
+    // shrink writes neither the metadata, y, B nor bias.
+    int32_t early;
 };
 
 template <int KT>
@@ -94,8 +102,12 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 2) ? 3 : 2) expand_kernel(E
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_tok[EX_BM];
 
-    pdl_wait();
-    pdl_launch_dependents();
+    bool waited = false;
+    if (!p.early) {
+        pdl_wait();
+        pdl_launch_dependents();
+        waited = true;
+    }
 
     uint8_t *sA = smem + EX_STAGES * Cfg::STAGE_BYTES;
     const SegTab tab = seg_tab(reinterpret_cast<int *>(sA + Cfg::A_BYTES), p.nbins);
@@ -166,6 +178,11 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 2) ? 3 : 2) expand_kernel(E
             cp_async_commit();
         }
 
+        if (!waited) {                        // the shrink output is read from here on
+            pdl_wait();
+            pdl_launch_dependents();
+            waited = true;
+        }
         // x rows of this tile and slice -> bf16 A operand (overlaps the ring fill)
         {
             const float *xs = p.x + int64_t(s) * T * R;
@@ -332,12 +349,34 @@ static int slice_chunks(int n, int rank)
 
 }  // namespace lora
 
+namespace lora {
+int expand_dispatch(ExpandArgs &p, const float *x, const lora_meta_t *meta, cudaStream_t st);
+static int lora_expand_impl(const float *x, const lora_bf16_t *const *lora_b,
+                            const lora_bf16_t *const *lora_bias,
+                            const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
+                            lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
+                            int32_t offset_start, int32_t add_inputs,
+                            const lora_meta_t *meta, cudaStream_t stream, int early);
+}  // namespace lora
+
 LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
                          const lora_bf16_t *const *lora_bias,
                          const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
                          lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
                          int32_t offset_start, int32_t add_inputs,
                          const lora_meta_t *meta, void *stream)
+{
+    return lora::lora_expand_impl(x, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
+                                  num_tokens, offset_start, add_inputs, meta,
+                                  static_cast<cudaStream_t>(stream), 0);
+}
+
+static int lora::lora_expand_impl(const float *x, const lora_bf16_t *const *lora_b,
+                                  const lora_bf16_t *const *lora_bias,
+                                  const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
+                                  lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
+                                  int32_t offset_start, int32_t add_inputs,
+                                  const lora_meta_t *meta, cudaStream_t stream, int early)
 {
     if (meta == nullptr || lora_b == nullptr || slice_sizes == nullptr) return LORA_ERR_NULL;
     if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SLICES;
@@ -398,8 +437,17 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
     p.active = meta->active_lora_ids;
     p.no_lora = meta->no_lora_flag;
     p.nbins = meta->max_loras + 1;
+    p.early = early;
+    return lora::expand_dispatch(p, x, meta, stream);
+}
 
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+namespace lora {
+
+int expand_dispatch(ExpandArgs &p, const float *x, const lora_meta_t *meta, cudaStream_t st)
+{
+    const int num_slices = p.num_slices, rank = p.rank, num_tokens = p.num_tokens;
+    lora_bf16_t *y = p.y;
+    const int64_t y_ld = p.y_ld;
 
     // Tensor-core path (tcgen05, TMEM accumulators, TMA for B and for y over
     // runs of consecutive tokens) for 16-byte-aligned outputs.  Opt-in with
@@ -440,3 +488,15 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
     if (rank <= 64) return lora::launch_expand_kt<4>(p, st);
     return lora::launch_expand_kt<8>(p, st);
 }
+
+// lora_expand for lora_linear: the same call in early mode (see ExpandArgs).
+int expand_early(const float *x, const lora_bf16_t *const *lora_b,
+                 const lora_bf16_t *const *lora_bias, const int32_t *slice_sizes,
+                 int32_t num_slices, int32_t rank, lora_bf16_t *y, int64_t y_ld,
+                 int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st)
+{
+    return lora_expand_impl(x, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
+                            num_tokens, 0, 1, meta, st, 1);
+}
+
+}  // namespace lora

@@ -747,14 +747,33 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
             if (r != 0) return r;
         }
     }
-    // Two kernels for small batches (the shrink sorts the ids itself and
-    // writes the metadata), three otherwise.  LORA_PUNICA_SELF_META=0 keeps
-    // the separate metadata kernel.
+    // Small batches: the metadata kernel, then the shrink in early mode
+    // (it sorts the ids itself and starts its loads while the metadata
+    // kernel runs), then the expand in early mode (it fetches the metadata,
+    // y and B while the shrink runs).  LORA_PUNICA_SELF_META=1 instead drops
+    // the metadata kernel (the shrink writes the metadata); =0 runs the
+    // plain three calls.
+    const int self_meta = lora::env_int("LORA_PUNICA_SELF_META", -1);
     int r = 0;
-    if (lora::env_int("LORA_PUNICA_SELF_META", 1) != 0)
+    bool early = false;
+    if (self_meta == 1) {
         r = lora::shrink_self_meta(token_lora_mapping, x, num_tokens, hidden, x_ld, lora_a,
-                                   num_slices, rank, buf, meta, scale, st);
-    if (r < 0 || r > 1) return r;
+                                   num_slices, rank, buf, meta, scale, st, 0);
+        if (r < 0 || r > 1) return r;
+    } else if (self_meta == -1) {
+        r = lora_meta_prepare(token_lora_mapping, num_tokens, meta, stream);
+        if (r != 0) return r;
+        r = lora::shrink_self_meta(token_lora_mapping, x, num_tokens, hidden, x_ld, lora_a,
+                                   num_slices, rank, buf, meta, scale, st, 1);
+        if (r < 0 || r > 1) return r;
+        if (r == 0) {
+            r = lora_shrink(x, num_tokens, hidden, x_ld, lora_a, num_slices, rank, buf, meta,
+                            scale, stream);
+            if (r != 0) return r;
+        }
+        early = true;
+        r = 1;
+    }
     if (r == 0) {
         r = lora_meta_prepare(token_lora_mapping, num_tokens, meta, stream);
         if (r != 0) return r;
@@ -762,6 +781,9 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
                         stream);
         if (r != 0) return r;
     }
+    if (early)
+        return lora::expand_early(buf, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
+                                  num_tokens, meta, st);
     return lora_expand(buf, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld, num_tokens,
                        0, 1, meta, stream);
 }

@@ -52,6 +52,14 @@ struct ShrinkArgs {
     int32_t *active_out;
     int32_t *no_lora_out;
     int32_t *error_out;
+    int32_t write_meta;            // CTA 0 writes the metadata buffers
+    // Early mode (lora_linear, after its metadata kernel): the ids are sorted
+    // and the first tile's loads issued before the grid-dependency wait.
+    // Safe because the metadata kernel lets its dependents launch only after
+    // its own wait (so the id map, x and A are final), and this kernel reads
+    // nothing the metadata kernel writes; it lets its own dependents launch
+    // only after that wait, which is what lora_linear's expand relies on.
+    int32_t early;
 };
 
 constexpr int SH_SELF_META_MAX_TOKENS = 512;
@@ -93,8 +101,12 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_tok[SH_BN];
 
-    pdl_wait();
-    pdl_launch_dependents();
+    bool waited = false;
+    if (!p.early) {
+        pdl_wait();
+        pdl_launch_dependents();
+        waited = true;
+    }
 
     const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + Cfg::RING_BYTES), p.nbins);
     const int32_t *tokens = p.sorted;
@@ -105,7 +117,7 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
         int *srt = pos + p.nbins, *misc = srt + SH_SELF_META_MAX_TOKENS;
         const bool nl = block_sort_ids<SH_THREADS / 32>(p.map, p.num_tokens, p.nbins - 1, cnt,
                                                         tot, base, pos, srt, misc);
-        if (blockIdx.x == 0)
+        if (blockIdx.x == 0 && p.write_meta)
             write_meta(p.map, p.num_tokens, p.nbins - 1, nl, tot, base, pos, srt, misc,
                        p.mapping_copy, p.sorted_out, p.counts_out, p.start_out, p.active_out,
                        p.no_lora_out, p.error_out);
@@ -199,6 +211,11 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
             cp_async_commit();
         }
 
+        if (!waited) {                        // y (the buffer) is written from here on
+            pdl_wait();
+            pdl_launch_dependents();
+            waited = true;
+        }
         for (int ks = 0; ks < k_steps; ++ks) {
             cp_async_wait<SH_STAGES - 2>();
             __syncthreads();
@@ -339,6 +356,8 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
     p.nbins = meta->max_loras + 1;
     p.skip_rows = 0;
     p.map = nullptr;
+    p.write_meta = 0;
+    p.early = 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -382,14 +401,16 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
 namespace lora {
 
 // lora_shrink for lora_linear on small batches: the kernel sorts the raw id
-// map itself (no separate metadata kernel) and CTA 0 writes the metadata
-// buffers exactly as lora_meta_prepare would.  Returns 0 when it does not
+// map itself.  early == 0: no separate metadata kernel runs and CTA 0 writes
+// the metadata buffers exactly as lora_meta_prepare would.  early == 1: the
+// metadata kernel runs just before and writes them; this kernel sorts and
+// starts loading while it runs (see ShrinkArgs::early).  Returns 0 when it does not
 // apply (the caller then runs the metadata kernel and lora_shrink), 1 when
 // launched, or an error status.
 int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_tokens,
                      int32_t hidden, int64_t x_ld, const lora_bf16_t *const *lora_a,
                      int32_t num_slices, int32_t rank, float *y, const lora_meta_t *meta,
-                     float scale, cudaStream_t st)
+                     float scale, cudaStream_t st, int early)
 {
     if (num_tokens < 1 || num_tokens > SH_SELF_META_MAX_TOKENS || meta->max_loras > 256)
         return 0;
@@ -430,6 +451,9 @@ int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_token
     p.active_out = meta->active_lora_ids;
     p.no_lora_out = meta->no_lora_flag;
     p.error_out = meta->error_word;
+    // early: the metadata kernel writes the buffers; otherwise CTA 0 does
+    p.write_meta = early ? 0 : 1;
+    p.early = early ? 1 : 0;
     int r;
     if (rank <= 16) r = launch_shrink_mt<1>(p, st);
     else if (rank <= 32) r = launch_shrink_mt<2>(p, st);

@@ -11,10 +11,12 @@ from gpu_helpers import (EXPAND_ATOL, EXPAND_RTOL, SHRINK_ATOL, SHRINK_RTOL, ass
 
 pytestmark = pytest.mark.gpu
 
-# (LORA_PUNICA_FUSED, LORA_PUNICA_SELF_META): one fused kernel; the shrink
-# sorting the ids itself + expand; metadata kernel + shrink + expand.
-PATHS = [pytest.param(("1", "1"), id="fused"), pytest.param(("0", "1"), id="two_kernels"),
-         pytest.param(("0", "0"), id="three_kernels")]
+# (LORA_PUNICA_FUSED, LORA_PUNICA_SELF_META): one fused kernel; the default
+# (metadata kernel, then shrink and expand each loading before their
+# grid-dependency wait); the shrink sorting the ids itself and writing the
+# metadata + expand; the plain metadata kernel + shrink + expand.
+PATHS = [pytest.param(("1", ""), id="fused"), pytest.param(("0", ""), id="early"),
+         pytest.param(("0", "1"), id="two_kernels"), pytest.param(("0", "0"), id="three_kernels")]
 
 
 def _set_path(monkeypatch, path):
