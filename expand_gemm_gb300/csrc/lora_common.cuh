@@ -197,16 +197,21 @@ __device__ __forceinline__ int load_segments(const int32_t *no_lora, const int32
 // Each warp owns a contiguous run of tokens, so warp order, group order and
 // lane order together give token order inside every bin.  Returns the
 // no-LoRA flag to every thread; srt is only filled when it is false.
+//
+// The id map is first copied into shared memory (ids[T], one round of
+// independent global loads), so both passes read shared memory.
 template <int NW>
-__device__ __forceinline__ bool block_sort_ids(const int32_t *map, int T, int max_loras,
+__device__ __forceinline__ bool block_sort_ids(const int32_t *map_g, int T, int max_loras,
                                                int *cnt, int *tot, int *base, int *pos,
-                                               int *srt, int *misc)
+                                               int *srt, int *misc, int *ids)
 {
     const int nbins = max_loras + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int t = tid; t < T; t += NW * 32) ids[t] = map_g[t];
     for (int i = tid; i < NW * nbins; i += NW * 32) cnt[i] = 0;
     if (tid == 0) misc[0] = 0;
     __syncthreads();
+    const int32_t *map = ids;
     const int per_warp = ((T + NW * 32 - 1) / (NW * 32)) * 32;
     const int t0 = min(T, warp * per_warp), t1 = min(T, t0 + per_warp);
     int bad = 0;
@@ -395,7 +400,8 @@ int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_token
 int expand_early(const float *x, const lora_bf16_t *const *lora_b,
                  const lora_bf16_t *const *lora_bias, const int32_t *slice_sizes,
                  int32_t num_slices, int32_t rank, lora_bf16_t *y, int64_t y_ld,
-                 int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st);
+                 int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st,
+                 const int32_t *map);
 
 // Host-side description of one lora_expand call for its tensor-core path.
 struct ExpandLaunch {

@@ -55,7 +55,20 @@ struct ExpandArgs {
     // kernel and everything before it in the stream have completed, and the
     // shrink writes neither the metadata, y, B nor bias.
     int32_t early;
+    // With `map` (early mode, small batches) every CTA sorts the id map
+    // itself instead of reading the segment table and token list: one round
+    // trip instead of two.  The result is the metadata the metadata kernel
+    // writes, so the two agree.
+    const int32_t *map;
 };
+
+constexpr int EX_SELF_SORT_MAX_TOKENS = 512;
+constexpr int EX_SELF_SORT_MAX_LORAS = 256;
+
+size_t expand_self_sort_bytes(int nbins)
+{
+    return size_t(8 * nbins + 3 * nbins + 2 * EX_SELF_SORT_MAX_TOKENS + 4) * sizeof(int);
+}
 
 template <int KT>
 struct ExpandTile {
@@ -95,7 +108,7 @@ size_t expand_smem_bytes(int kt, int nbins)
 }
 
 template <int KT>
-__global__ void __launch_bounds__(EX_THREADS, (KT <= 2) ? 3 : 2) expand_kernel(ExpandArgs p)
+__global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(ExpandArgs p)
 {
     using Cfg = ExpandTile<KT>;
     constexpr int CPR = Cfg::CPR, BN = Cfg::BN, MI = Cfg::MI, NI = Cfg::NI, YCH = Cfg::YCH;
@@ -111,8 +124,22 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 2) ? 3 : 2) expand_kernel(E
 
     uint8_t *sA = smem + EX_STAGES * Cfg::STAGE_BYTES;
     const SegTab tab = seg_tab(reinterpret_cast<int *>(sA + Cfg::A_BYTES), p.nbins);
-    const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
-                                          p.nbins, EX_BM, tab);
+    const int32_t *tokens = p.sorted;
+    int total_tiles;
+    if (p.map != nullptr) {
+        int *mm = reinterpret_cast<int *>(sA + Cfg::A_BYTES + seg_tab_bytes(p.nbins));
+        int *cnt = mm, *tot = cnt + 8 * p.nbins, *base = tot + p.nbins, *pos = base + p.nbins;
+        int *srt = pos + p.nbins, *ids = srt + EX_SELF_SORT_MAX_TOKENS;
+        int *misc = ids + EX_SELF_SORT_MAX_TOKENS;
+        if (block_sort_ids<EX_THREADS / 32>(p.map, p.num_tokens, p.nbins - 1, cnt, tot, base,
+                                            pos, srt, misc, ids))
+            return;
+        total_tiles = segments_from_sort(tot, base, p.nbins, EX_BM, tab);
+        tokens = srt;
+    } else {
+        total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc, p.nbins, EX_BM,
+                                    tab);
+    }
     if (total_tiles == 0) return;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -143,7 +170,7 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 2) ? 3 : 2) expand_kernel(E
         const uint16_t *bias_row = p.bias[s] ? p.bias[s] + int64_t(id) * n_s : nullptr;
         uint16_t *yslice = p.y + p.col0[s];
 
-        if (tid < EX_BM) s_tok[tid] = (tid < nrows) ? p.sorted[row0 + tid] : -1;
+        if (tid < EX_BM) s_tok[tid] = (tid < nrows) ? tokens[row0 + tid] : -1;
         __syncthreads();
 
         auto load_chunk = [&](int slot, int c) {
@@ -322,7 +349,8 @@ static int launch_expand_kt(const ExpandArgs &p, cudaStream_t stream)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return int(e);
-    const size_t smem = expand_smem_bytes(KT, LORA_MAX_LORAS + 1);
+    const size_t smem = expand_smem_bytes(KT, LORA_MAX_LORAS + 1) +
+                        expand_self_sort_bytes(EX_SELF_SORT_MAX_LORAS + 1);
     int grid = (dev < 64) ? grid_cache[dev] : 0;
     if (grid == 0) {
         e = cudaFuncSetAttribute(expand_kernel<KT>,
@@ -335,8 +363,9 @@ static int launch_expand_kt(const ExpandArgs &p, cudaStream_t stream)
         grid = device_sm_count() * max(occ, 1);
         if (dev < 64) grid_cache[dev] = grid;
     }
-    e = launch_kernel(expand_kernel<KT>, dim3(grid), dim3(EX_THREADS),
-                      expand_smem_bytes(KT, p.nbins), stream, p);
+    const size_t used = expand_smem_bytes(KT, p.nbins) +
+                        (p.map != nullptr ? expand_self_sort_bytes(p.nbins) : 0);
+    e = launch_kernel(expand_kernel<KT>, dim3(grid), dim3(EX_THREADS), used, stream, p);
     return int(e);
 }
 
@@ -356,7 +385,8 @@ static int lora_expand_impl(const float *x, const lora_bf16_t *const *lora_b,
                             const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
                             lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
                             int32_t offset_start, int32_t add_inputs,
-                            const lora_meta_t *meta, cudaStream_t stream, int early);
+                            const lora_meta_t *meta, cudaStream_t stream, int early,
+                            const int32_t *map);
 }  // namespace lora
 
 LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
@@ -368,7 +398,7 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
 {
     return lora::lora_expand_impl(x, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
                                   num_tokens, offset_start, add_inputs, meta,
-                                  static_cast<cudaStream_t>(stream), 0);
+                                  static_cast<cudaStream_t>(stream), 0, nullptr);
 }
 
 static int lora::lora_expand_impl(const float *x, const lora_bf16_t *const *lora_b,
@@ -376,7 +406,8 @@ static int lora::lora_expand_impl(const float *x, const lora_bf16_t *const *lora
                                   const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
                                   lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
                                   int32_t offset_start, int32_t add_inputs,
-                                  const lora_meta_t *meta, cudaStream_t stream, int early)
+                                  const lora_meta_t *meta, cudaStream_t stream, int early,
+                                  const int32_t *map)
 {
     if (meta == nullptr || lora_b == nullptr || slice_sizes == nullptr) return LORA_ERR_NULL;
     if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SLICES;
@@ -438,6 +469,7 @@ static int lora::lora_expand_impl(const float *x, const lora_bf16_t *const *lora
     p.no_lora = meta->no_lora_flag;
     p.nbins = meta->max_loras + 1;
     p.early = early;
+    p.map = map;
     return lora::expand_dispatch(p, x, meta, stream);
 }
 
@@ -493,10 +525,13 @@ int expand_dispatch(ExpandArgs &p, const float *x, const lora_meta_t *meta, cuda
 int expand_early(const float *x, const lora_bf16_t *const *lora_b,
                  const lora_bf16_t *const *lora_bias, const int32_t *slice_sizes,
                  int32_t num_slices, int32_t rank, lora_bf16_t *y, int64_t y_ld,
-                 int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st)
+                 int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st,
+                 const int32_t *map)
 {
+    const bool self_sort = map != nullptr && num_tokens <= EX_SELF_SORT_MAX_TOKENS &&
+                           meta->max_loras <= EX_SELF_SORT_MAX_LORAS;
     return lora_expand_impl(x, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
-                            num_tokens, 0, 1, meta, st, 1);
+                            num_tokens, 0, 1, meta, st, 1, self_sort ? map : nullptr);
 }
 
 }  // namespace lora

@@ -783,7 +783,7 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
     }
     if (early)
         return lora::expand_early(buf, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
-                                  num_tokens, meta, st);
+                                  num_tokens, meta, st, token_lora_mapping);
     return lora_expand(buf, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld, num_tokens,
                        0, 1, meta, stream);
 }

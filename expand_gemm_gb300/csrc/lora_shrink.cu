@@ -67,7 +67,7 @@ constexpr int SH_SELF_META_MAX_TOKENS = 512;
 // Extra shared memory of the self-built-metadata mode.
 size_t shrink_self_meta_bytes(int nbins)
 {
-    return size_t(4 * nbins + 3 * nbins + SH_SELF_META_MAX_TOKENS + 4) * sizeof(int);
+    return size_t(4 * nbins + 3 * nbins + 2 * SH_SELF_META_MAX_TOKENS + 4) * sizeof(int);
 }
 
 template <int MT>
@@ -114,9 +114,10 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
     if (p.map != nullptr) {
         int *mm = reinterpret_cast<int *>(smem + Cfg::RING_BYTES + seg_tab_bytes(p.nbins));
         int *cnt = mm, *tot = cnt + 4 * p.nbins, *base = tot + p.nbins, *pos = base + p.nbins;
-        int *srt = pos + p.nbins, *misc = srt + SH_SELF_META_MAX_TOKENS;
+        int *srt = pos + p.nbins, *ids = srt + SH_SELF_META_MAX_TOKENS;
+        int *misc = ids + SH_SELF_META_MAX_TOKENS;
         const bool nl = block_sort_ids<SH_THREADS / 32>(p.map, p.num_tokens, p.nbins - 1, cnt,
-                                                        tot, base, pos, srt, misc);
+                                                        tot, base, pos, srt, misc, ids);
         if (blockIdx.x == 0 && p.write_meta)
             write_meta(p.map, p.num_tokens, p.nbins - 1, nl, tot, base, pos, srt, misc,
                        p.mapping_copy, p.sorted_out, p.counts_out, p.start_out, p.active_out,
@@ -307,6 +308,9 @@ static int launch_shrink_mt(const ShrinkArgs &p, cudaStream_t stream)
     }
     const size_t used = shrink_smem_bytes(MT, p.nbins) +
                         (p.map != nullptr ? shrink_self_meta_bytes(p.nbins) : 0);
+    // In early mode (small batches inside lora_linear) at most three CTAs
+    // per SM, so that the expand that follows finds room to start loading.
+    if (p.early) grid = min(grid, 3 * device_sm_count());
     e = launch_kernel(shrink_kernel<MT>, dim3(grid), dim3(SH_THREADS), used, stream, p);
     return int(e);
 }
