@@ -782,8 +782,14 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
         if (r != 0) return r;
     }
     if (early)
+        // The expand reads the segment table and token list the metadata
+        // kernel wrote (two round trips); sorting the ids in every expand
+        // CTA was measured slower on decode batches, so it is opt-in
+        // (LORA_PUNICA_EXPAND_SELF_SORT=1).
         return lora::expand_early(buf, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
-                                  num_tokens, meta, st, token_lora_mapping);
+                                  num_tokens, meta, st,
+                                  lora::env_int("LORA_PUNICA_EXPAND_SELF_SORT", 0)
+                                      ? token_lora_mapping : nullptr);
     return lora_expand(buf, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld, num_tokens,
                        0, 1, meta, stream);
 }

@@ -11,17 +11,21 @@ from gpu_helpers import (EXPAND_ATOL, EXPAND_RTOL, SHRINK_ATOL, SHRINK_RTOL, ass
 
 pytestmark = pytest.mark.gpu
 
-# (LORA_PUNICA_FUSED, LORA_PUNICA_SELF_META): one fused kernel; the default
-# (metadata kernel, then shrink and expand each loading before their
-# grid-dependency wait); the shrink sorting the ids itself and writing the
+# (LORA_PUNICA_FUSED, LORA_PUNICA_SELF_META, LORA_PUNICA_EXPAND_SELF_SORT):
+# one fused kernel; the default (metadata kernel, then shrink and expand each
+# loading before their grid-dependency wait); the same with the expand
+# sorting the ids itself; the shrink sorting the ids itself and writing the
 # metadata + expand; the plain metadata kernel + shrink + expand.
-PATHS = [pytest.param(("1", ""), id="fused"), pytest.param(("0", ""), id="early"),
-         pytest.param(("0", "1"), id="two_kernels"), pytest.param(("0", "0"), id="three_kernels")]
+PATHS = [pytest.param(("1", "", ""), id="fused"), pytest.param(("0", "", ""), id="early"),
+         pytest.param(("0", "", "1"), id="early_self_sort"),
+         pytest.param(("0", "1", ""), id="two_kernels"),
+         pytest.param(("0", "0", ""), id="three_kernels")]
 
 
 def _set_path(monkeypatch, path):
     monkeypatch.setenv("LORA_PUNICA_FUSED", path[0])
     monkeypatch.setenv("LORA_PUNICA_SELF_META", path[1])
+    monkeypatch.setenv("LORA_PUNICA_EXPAND_SELF_SORT", path[2])
 
 
 def _check_linear(oracle_mod, inp, ids=None, buf0=None, L=None):
