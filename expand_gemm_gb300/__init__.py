@@ -22,10 +22,12 @@ from typing import Optional, Sequence
 import torch
 
 from . import _lib
-from ._lib import LoraError, LORA_MAX_LORAS, LORA_MAX_RANK, LORA_MAX_SLICES  # noqa: F401
+from ._lib import (LoraError, LORA_MAX_LORAS, LORA_MAX_RANK, LORA_MAX_SLICES,  # noqa: F401
+                   LORA_NOALLOC_MAX_FLOATS)
 
 __all__ = ["LoRAKernelMeta", "lora_meta_prepare", "lora_shrink", "lora_expand",
-           "lora_linear", "add_lora_linear", "LoraError", "library", "build"]
+           "lora_linear", "lora_linear_noalloc", "add_lora_linear", "LoraError", "library",
+           "build"]
 
 
 def library():
@@ -225,16 +227,14 @@ def add_lora_linear(y: torch.Tensor, x: torch.Tensor, lora_a_stacked, lora_b_sta
     lora_expand(buffer, B, y, meta, 0, True, lora_bias_stacked)
 
 
-def lora_linear(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_a_stacked,
-                lora_b_stacked, lora_bias_stacked, scale: float, buffer: torch.Tensor,
-                y: torch.Tensor, meta: LoRAKernelMeta) -> None:
-    """Metadata + shrink + expand of one LoRA layer in one library call
-    (PunicaWrapperGPU.update_metadata followed by add_lora_linear).  Small
-    batches run as one fused kernel; see include/lora_punica.h."""
+def _linear_args(token_lora_mapping, x, lora_a_stacked, lora_b_stacked, lora_bias_stacked,
+                 buffer, y):
+    """Checks shared by lora_linear and lora_linear_noalloc; returns the
+    marshalled C arguments in lora_linear's order (buffer pointer None when
+    no buffer is given)."""
     m = token_lora_mapping
     _need(m, "token_lora_mapping", torch.int32)
     _need(x, "x", torch.bfloat16)
-    _need(buffer, "buffer", torch.float32)
     _need(y, "y", torch.bfloat16)
     x2 = x.view(-1, x.shape[-1]) if x.dim() != 2 else x
     y2 = y.view(-1, y.shape[-1]) if y.dim() != 2 else y
@@ -250,13 +250,14 @@ def lora_linear(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_a_stacke
     L, r, Ha = A[0].shape
     if Ha != H or any(a.shape != A[0].shape for a in A):
         raise ValueError("lora_a_stacked shapes must all be [L, r, %d]" % H)
-    if L < meta.max_loras or B[0].size(0) < meta.max_loras:
-        raise ValueError("weights hold fewer LoRAs than the metadata expects")
     for i, b in enumerate(B):
         if b.size(2) != r:
             raise ValueError("lora_b_stacked[%d] must be [L, n, %d]" % (i, r))
-    if tuple(buffer.shape) != (len(A), T, r) or not buffer.is_contiguous():
-        raise ValueError("buffer must be a contiguous fp32 [%d, %d, %d] tensor" % (len(A), T, r))
+    if buffer is not None:
+        _need(buffer, "buffer", torch.float32)
+        if tuple(buffer.shape) != (len(A), T, r) or not buffer.is_contiguous():
+            raise ValueError("buffer must be a contiguous fp32 [%d, %d, %d] tensor"
+                             % (len(A), T, r))
     sizes = [b.size(1) for b in B]
     bias_arr = None
     if lora_bias_stacked is not None:
@@ -269,9 +270,42 @@ def lora_linear(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_a_stacke
                     raise ValueError("lora_bias_stacked[%d] must be [L, %d]" % (i, n))
         bias_arr = _ptr_array(list(lora_bias_stacked))
     size_arr = (ctypes.c_int32 * len(B))(*sizes)
-    st = _lib.load().lora_linear(m.data_ptr(), T, x2.data_ptr(), H, x2.stride(0), _ptr_array(A),
-                                 _ptr_array(B), bias_arr, size_arr, len(B), r, float(scale),
-                                 buffer.data_ptr(), y2.data_ptr(), y2.stride(0),
+    return dict(L=L, nb=B[0].size(0),
+                head=(m.data_ptr(), T, x2.data_ptr(), H, x2.stride(0), _ptr_array(A),
+                      _ptr_array(B), bias_arr, size_arr, len(B), r),
+                buf=None if buffer is None else buffer.data_ptr(),
+                tail=(y2.data_ptr(), y2.stride(0)))
+
+
+def lora_linear(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_a_stacked,
+                lora_b_stacked, lora_bias_stacked, scale: float, buffer: torch.Tensor,
+                y: torch.Tensor, meta: LoRAKernelMeta) -> None:
+    """Metadata + shrink + expand of one LoRA layer in one library call
+    (PunicaWrapperGPU.update_metadata followed by add_lora_linear).  Small
+    batches run as one fused kernel; see include/lora_punica.h."""
+    if not isinstance(buffer, torch.Tensor):
+        raise TypeError("buffer must be a torch.Tensor (lora_linear_noalloc needs none)")
+    a = _linear_args(token_lora_mapping, x, lora_a_stacked, lora_b_stacked, lora_bias_stacked,
+                     buffer, y)
+    if a["L"] < meta.max_loras or a["nb"] < meta.max_loras:
+        raise ValueError("weights hold fewer LoRAs than the metadata expects")
+    st = _lib.load().lora_linear(*a["head"], float(scale), a["buf"], *a["tail"],
                                  ctypes.byref(meta.c), _stream_handle(x.device))
     _lib.check("lora_linear", st)
 
+
+def lora_linear_noalloc(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_a_stacked,
+                        lora_b_stacked, lora_bias_stacked, scale: float, y: torch.Tensor,
+                        meta: LoRAKernelMeta) -> None:
+    """lora_linear without a caller buffer: the fp32 intermediate lives in a
+    fixed array the library owns on each device (at most
+    LORA_NOALLOC_MAX_FLOATS = slices x tokens x rank floats), cleared by each
+    call, so no device memory is allocated.  Calls on one device share that
+    array and must not overlap; see include/lora_punica.h."""
+    a = _linear_args(token_lora_mapping, x, lora_a_stacked, lora_b_stacked, lora_bias_stacked,
+                     None, y)
+    if a["L"] < meta.max_loras or a["nb"] < meta.max_loras:
+        raise ValueError("weights hold fewer LoRAs than the metadata expects")
+    st = _lib.load().lora_linear_noalloc(*a["head"], float(scale), *a["tail"],
+                                         ctypes.byref(meta.c), _stream_handle(x.device))
+    _lib.check("lora_linear_noalloc", st)

@@ -14,11 +14,12 @@ LIB_PATH = os.path.join(PKG, "liblora_punica.so")
 
 # Public entry points of include/lora_punica.h (checked by the test suite).
 EXPORTS = ("lora_meta_prepare", "lora_shrink", "lora_expand", "lora_linear",
-           "lora_status_string", "lora_version")
+           "lora_linear_noalloc", "lora_status_string", "lora_version")
 
 LORA_MAX_SLICES = 8
 LORA_MAX_LORAS = 1024
 LORA_MAX_RANK = 128
+LORA_NOALLOC_MAX_FLOATS = 1 << 20
 
 
 class LoraMetaC(ctypes.Structure):
@@ -73,6 +74,10 @@ def load(path: str | None = None):
         lib.lora_linear.argtypes = [_P, _I32, _P, _I32, _I64, _P, _P, _P, _P, _I32, _I32,
                                     ctypes.c_float, _P, _P, _I64, ctypes.POINTER(LoraMetaC), _P]
         lib.lora_linear.restype = ctypes.c_int
+        lib.lora_linear_noalloc.argtypes = [_P, _I32, _P, _I32, _I64, _P, _P, _P, _P, _I32,
+                                            _I32, ctypes.c_float, _P, _I64,
+                                            ctypes.POINTER(LoraMetaC), _P]
+        lib.lora_linear_noalloc.restype = ctypes.c_int
         lib.lora_status_string.argtypes = [ctypes.c_int]
         lib.lora_status_string.restype = ctypes.c_char_p
         lib.lora_version.argtypes = []

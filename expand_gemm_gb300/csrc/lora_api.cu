@@ -54,6 +54,7 @@ LORA_API const char *lora_status_string(int status)
     case LORA_ERR_TOKENS: return "num_tokens exceeds meta->max_num_tokens";
     case LORA_ERR_WIDTH: return "offset_start + sum(slice_sizes) exceeds y_ld";
     case LORA_ERR_DEVICE: return "no usable CUDA device";
+    case LORA_ERR_SCRATCH: return "num_slices * num_tokens * rank exceeds the fixed buffer of lora_linear_noalloc";
     default: break;
     }
     if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));

@@ -55,6 +55,7 @@ typedef uint16_t lora_bf16_t;
 #define LORA_MAX_SLICES 8      /* slices per shrink/expand call          */
 #define LORA_MAX_LORAS 1024    /* max_loras accepted by the metadata step */
 #define LORA_MAX_RANK 128      /* rank r: a multiple of 8, 8 <= r <= 128 */
+#define LORA_NOALLOC_MAX_FLOATS (1 << 20)  /* lora_linear_noalloc buffer: 4 MiB */
 
 enum lora_status {
     LORA_OK = 0,
@@ -65,7 +66,9 @@ enum lora_status {
     LORA_ERR_SLICES = -5,      /* num_slices not in [1, LORA_MAX_SLICES]    */
     LORA_ERR_TOKENS = -6,      /* num_tokens > meta->max_num_tokens         */
     LORA_ERR_WIDTH = -7,       /* offset_start + sum(slice_sizes) > y_ld    */
-    LORA_ERR_DEVICE = -8       /* no usable CUDA device / wrong architecture */
+    LORA_ERR_DEVICE = -8,      /* no usable CUDA device / wrong architecture */
+    LORA_ERR_SCRATCH = -9      /* num_slices * num_tokens * rank exceeds
+                                  LORA_NOALLOC_MAX_FLOATS (lora_linear_noalloc) */
 };
 
 /*
@@ -206,6 +209,34 @@ int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
                 const lora_bf16_t *const *lora_bias, const int32_t *slice_sizes,
                 int32_t num_slices, int32_t rank, float scale, float *buf,
                 lora_bf16_t *y, int64_t y_ld, const lora_meta_t *meta, void *stream);
+
+/*
+ * lora_linear_noalloc -- lora_linear for callers that cannot allocate
+ * device memory (code running where cudaMalloc is unavailable or forbidden:
+ * inside an allocator or memory-pool callback, a plugin whose host owns
+ * every allocation, a process that must not grow after start-up).  The
+ * pages have no counterpart: this is an addition of this library.
+ *
+ * Same arguments and results as lora_linear, without `buf`: the fp32
+ * buffer between shrink and expand lives in a fixed array of
+ * LORA_NOALLOC_MAX_FLOATS floats (4 MiB) that the library holds on every
+ * GPU that loads it, until the process exits.  Each call clears the
+ * num_slices * num_tokens * rank floats it uses, so the shrink starts from
+ * zero (as add_lora_linear's own zeroed buffer does); larger calls return
+ * LORA_ERR_SCRATCH.  No cudaMalloc, cudaFree or allocating library routine
+ * is called.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make it before any stream capture.  All calls on a
+ * device share the array: calls that may overlap on the GPU (other streams
+ * or threads) race on it and must be serialised by the caller.
+ */
+int lora_linear_noalloc(const int32_t *token_lora_mapping, int32_t num_tokens,
+                        const lora_bf16_t *x, int32_t hidden, int64_t x_ld,
+                        const lora_bf16_t *const *lora_a, const lora_bf16_t *const *lora_b,
+                        const lora_bf16_t *const *lora_bias, const int32_t *slice_sizes,
+                        int32_t num_slices, int32_t rank, float scale, lora_bf16_t *y,
+                        int64_t y_ld, const lora_meta_t *meta, void *stream);
 
 /* Human-readable name of a status (negative LORA_ERR_* or cudaError_t). */
 const char *lora_status_string(int status);

@@ -54,7 +54,7 @@ def test_library_exports_every_declared_symbol_and_nothing_else(lib):
 def test_version_and_status_strings(lib):
     assert lib.lora_version() == 1
     assert lib.lora_status_string(0) == b"ok"
-    for code in range(-1, -9, -1):
+    for code in range(-1, -10, -1):
         s = lib.lora_status_string(code)
         assert s and s != b"unknown status"
     assert lib.lora_status_string(-99) == b"unknown status"
@@ -123,3 +123,24 @@ def test_expand_rejects_bad_arguments(lib):
     assert call(B=(ctypes.c_void_p * 2)(0, 0x3000)) == -1
     assert call(x=0x4004) == -3
     assert call(T=0) == 0
+
+
+def test_linear_noalloc_rejects_sizes_above_its_buffer(lib):
+    """Checked on the host before any CUDA call: slices, rank, and
+    num_slices * num_tokens * rank against the fixed buffer."""
+    from expand_gemm_gb300 import _lib
+    m = _meta(max_tokens=1 << 20)
+    A = (ctypes.c_void_p * 2)(0x2000, 0x3000)
+    B = (ctypes.c_void_p * 2)(0x6000, 0x7000)
+    sizes = (ctypes.c_int32 * 2)(64, 64)
+
+    def call(T, S=2, r=16):
+        return lib.lora_linear_noalloc(0x1000, T, 0x4000, 64, 64, A, B, None, sizes, S, r, 1.0,
+                                       0x5000, 128, ctypes.byref(m), None)
+    cap = _lib.LORA_NOALLOC_MAX_FLOATS
+    assert call(cap // 32 + 1) == -9
+    assert call(cap // 16 + 1, S=1) == -9
+    assert call(1 << 20, S=2, r=128) == -9
+    assert call(8, S=0) == -5
+    assert call(8, S=2, r=12) == -4
+    assert call(-1) == -2
