@@ -10,9 +10,11 @@ Names follow vLLM's API pages:
 
 * :class:`LoRAKernelMeta` -- page ``vllm.lora.ops.triton_ops.lora_kernel_metadata``
   (``make``, ``prepare_tensors``, ``meta_args``).
-* :func:`lora_shrink`, :func:`lora_expand`, :func:`add_lora_linear` -- page
+* :func:`lora_shrink`, :func:`lora_expand`, :func:`add_lora_linear`,
+  :func:`add_lora_embedding`, :func:`add_lora_logits` -- page
   ``vllm.lora.punica_wrapper.punica_gpu`` (``PunicaWrapperGPU.add_shrink``,
-  ``add_expand``, ``add_lora_linear``).
+  ``add_expand``, ``add_lora_linear``, ``add_lora_embedding``,
+  ``add_lora_logits``).
 """
 from __future__ import annotations
 
@@ -26,8 +28,8 @@ from ._lib import (LoraError, LORA_MAX_LORAS, LORA_MAX_RANK, LORA_MAX_SLICES,  #
                    LORA_NOALLOC_MAX_FLOATS)
 
 __all__ = ["LoRAKernelMeta", "lora_meta_prepare", "lora_shrink", "lora_expand",
-           "lora_linear", "lora_linear_noalloc", "add_lora_linear", "LoraError", "library",
-           "build"]
+           "lora_linear", "lora_linear_noalloc", "add_lora_linear", "add_lora_embedding",
+           "add_lora_logits", "LoraError", "library", "build"]
 
 
 def library():
@@ -165,12 +167,17 @@ def lora_shrink(x: torch.Tensor, lora_a_stacked, y: torch.Tensor,
 def lora_expand(x: torch.Tensor, lora_b_stacked, y: torch.Tensor,
                 meta: LoRAKernelMeta, offset_start: int = 0, add_inputs: bool = True,
                 lora_bias_stacked: Optional[Sequence[Optional[torch.Tensor]]] = None) -> None:
-    """y[:, off_s:off_s+n_s] (+)= x[s] @ lora_b_stacked[s][id]^T (+ bias)."""
-    _need(x, "x", torch.float32)
+    """y[:, off_s:off_s+n_s] (+)= x[s] @ lora_b_stacked[s][id]^T (+ bias).
+
+    x is fp32 (the shrink's buffer; rounded to bf16 for the tensor cores) or
+    bf16 (taken as it is: lora_expand_bf16)."""
+    if not isinstance(x, torch.Tensor) or x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x must be a float32 or bfloat16 torch.Tensor")
+    _need(x, "x", x.dtype)
     _need(y, "y", torch.bfloat16)
     B = _weights(lora_b_stacked, "lora_b_stacked")
     if x.dim() != 3 or not x.is_contiguous() or x.size(0) != len(B):
-        raise ValueError("x must be a contiguous fp32 [num_slices, T, r] tensor")
+        raise ValueError("x must be a contiguous [num_slices, T, r] tensor")
     S, T, r = x.shape
     L = B[0].size(0)
     if L < meta.max_loras:
@@ -197,11 +204,40 @@ def lora_expand(x: torch.Tensor, lora_b_stacked, y: torch.Tensor,
             bl.append(bb)
         bias_arr = _ptr_array(bl)
     size_arr = (ctypes.c_int32 * S)(*sizes)
-    st = _lib.load().lora_expand(x.data_ptr(), _ptr_array(B), bias_arr, size_arr, S, r,
-                                 y2.data_ptr(), y2.stride(0), T, int(offset_start),
-                                 1 if add_inputs else 0, ctypes.byref(meta.c),
-                                 _stream_handle(x.device))
-    _lib.check("lora_expand", st)
+    fn = "lora_expand_bf16" if x.dtype == torch.bfloat16 else "lora_expand"
+    st = getattr(_lib.load(), fn)(x.data_ptr(), _ptr_array(B), bias_arr, size_arr, S, r,
+                                  y2.data_ptr(), y2.stride(0), T, int(offset_start),
+                                  1 if add_inputs else 0, ctypes.byref(meta.c),
+                                  _stream_handle(x.device))
+    _lib.check(fn, st)
+
+
+def add_lora_embedding(y: torch.Tensor, x: torch.Tensor, lora_b_stacked,
+                       meta: LoRAKernelMeta, add_inputs: bool = True) -> None:
+    """PunicaWrapperGPU.add_lora_embedding: y (+)= x @ lora_b_stacked[id]^T,
+    where x is bf16 [T, r] (the embedding LoRA's A rows looked up per
+    token) and add_inputs is passed through."""
+    _need(x, "x", torch.bfloat16)
+    x2 = x.view(-1, x.shape[-1])
+    lora_expand(x2.unsqueeze(0), lora_b_stacked, y, meta, 0, add_inputs)
+
+
+def add_lora_logits(y: torch.Tensor, x: torch.Tensor, lora_a_stacked, lora_b_stacked,
+                    scale: float, meta: LoRAKernelMeta, *,
+                    buffer: Optional[torch.Tensor] = None) -> None:
+    """PunicaWrapperGPU.add_lora_logits: buffer = scale * x @ A[id]^T, then
+    y += buffer @ B[id]^T, both driven by ``meta`` (the prompt/sampler
+    metadata instance, one id per logits row)."""
+    y2 = y.view(-1, y.shape[-1])
+    x2 = x.view(-1, x.shape[-1])
+    B = _weights(lora_b_stacked, "lora_b_stacked")
+    if len(B) != 1:
+        raise ValueError("add_lora_logits takes one lora_b tensor")
+    r = B[0].size(-1)
+    if buffer is None:
+        buffer = torch.zeros((x2.size(0), r), dtype=torch.float32, device=x.device)
+    lora_shrink(x2, lora_a_stacked, buffer.unsqueeze(0), meta, scale)
+    lora_expand(buffer.unsqueeze(0), B, y2, meta, 0, True)
 
 
 def add_lora_linear(y: torch.Tensor, x: torch.Tensor, lora_a_stacked, lora_b_stacked,

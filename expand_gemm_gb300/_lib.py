@@ -13,8 +13,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "liblora_punica.so")
 
 # Public entry points of include/lora_punica.h (checked by the test suite).
-EXPORTS = ("lora_meta_prepare", "lora_shrink", "lora_expand", "lora_linear",
-           "lora_linear_noalloc", "lora_status_string", "lora_version")
+EXPORTS = ("lora_meta_prepare", "lora_shrink", "lora_expand", "lora_expand_bf16",
+           "lora_linear", "lora_linear_noalloc", "lora_status_string", "lora_version")
 
 LORA_MAX_SLICES = 8
 LORA_MAX_LORAS = 1024
@@ -71,6 +71,8 @@ def load(path: str | None = None):
         lib.lora_expand.argtypes = [_P, _P, _P, _P, _I32, _I32, _P, _I64, _I32,
                                     _I32, _I32, ctypes.POINTER(LoraMetaC), _P]
         lib.lora_expand.restype = ctypes.c_int
+        lib.lora_expand_bf16.argtypes = lib.lora_expand.argtypes
+        lib.lora_expand_bf16.restype = ctypes.c_int
         lib.lora_linear.argtypes = [_P, _I32, _P, _I32, _I64, _P, _P, _P, _P, _I32, _I32,
                                     ctypes.c_float, _P, _P, _I64, ctypes.POINTER(LoraMetaC), _P]
         lib.lora_linear.restype = ctypes.c_int

@@ -27,7 +27,8 @@ constexpr int EX_THREADS = 256;    // 8 warps
 constexpr int EX_STAGES = 3;
 
 struct ExpandArgs {
-    const float *x;
+    const void *x;                       // [S, T, r]: fp32, or bf16 when x_bf16
+    int32_t x_bf16;
     const uint16_t *b[LORA_MAX_SLICES];
     const uint16_t *bias[LORA_MAX_SLICES];
     int32_t n[LORA_MAX_SLICES];          // slice widths
@@ -210,20 +211,27 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
             pdl_launch_dependents();
             waited = true;
         }
-        // x rows of this tile and slice -> bf16 A operand (overlaps the ring fill)
+        // x rows of this tile and slice -> bf16 A operand (overlaps the ring
+        // fill): fp32 rows are rounded to bf16, bf16 rows are copied as they are
         {
-            const float *xs = p.x + int64_t(s) * T * R;
+            const int64_t xoff = int64_t(s) * T * R;
             for (int i = tid; i < EX_BM * CPR; i += EX_THREADS) {
                 const int r = i / CPR, cc = i - r * CPR;
                 const int tok = s_tok[r];
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (tok >= 0 && cc * 8 < R) {
-                    const float4 *src = reinterpret_cast<const float4 *>(xs + int64_t(tok) * R + cc * 8);
-                    const float4 u = src[0], q = src[1];
-                    v.x = pack_bf16x2(u.x, u.y);
-                    v.y = pack_bf16x2(u.z, u.w);
-                    v.z = pack_bf16x2(q.x, q.y);
-                    v.w = pack_bf16x2(q.z, q.w);
+                    const int64_t e = xoff + int64_t(tok) * R + cc * 8;
+                    if (p.x_bf16) {
+                        v = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.x) + e);
+                    } else {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            static_cast<const float *>(p.x) + e);
+                        const float4 u = src[0], q = src[1];
+                        v.x = pack_bf16x2(u.x, u.y);
+                        v.y = pack_bf16x2(u.z, u.w);
+                        v.z = pack_bf16x2(q.x, q.y);
+                        v.w = pack_bf16x2(q.z, q.w);
+                    }
                 }
                 *reinterpret_cast<uint4 *>(sA + swz<CPR>(r, cc)) = v;
             }
@@ -379,8 +387,8 @@ static int slice_chunks(int n, int rank)
 }  // namespace lora
 
 namespace lora {
-int expand_dispatch(ExpandArgs &p, const float *x, const lora_meta_t *meta, cudaStream_t st);
-static int lora_expand_impl(const float *x, const lora_bf16_t *const *lora_b,
+int expand_dispatch(ExpandArgs &p, const lora_meta_t *meta, cudaStream_t st);
+static int lora_expand_impl(const void *x, int x_bf16, const lora_bf16_t *const *lora_b,
                             const lora_bf16_t *const *lora_bias,
                             const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
                             lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
@@ -396,12 +404,27 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
                          int32_t offset_start, int32_t add_inputs,
                          const lora_meta_t *meta, void *stream)
 {
-    return lora::lora_expand_impl(x, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
-                                  num_tokens, offset_start, add_inputs, meta,
+    return lora::lora_expand_impl(x, 0, lora_b, lora_bias, slice_sizes, num_slices, rank, y,
+                                  y_ld, num_tokens, offset_start, add_inputs, meta,
                                   static_cast<cudaStream_t>(stream), 0, nullptr);
 }
 
-static int lora::lora_expand_impl(const float *x, const lora_bf16_t *const *lora_b,
+// The same product over a bf16 input, which the MMA takes as it is (page
+// "vllm.lora.punica_wrapper.punica_gpu", PunicaWrapperGPU.add_lora_embedding:
+// the expand of the looked-up rows of an embedding LoRA's A).
+LORA_API int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lora_b,
+                              const lora_bf16_t *const *lora_bias,
+                              const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
+                              lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
+                              int32_t offset_start, int32_t add_inputs,
+                              const lora_meta_t *meta, void *stream)
+{
+    return lora::lora_expand_impl(x, 1, lora_b, lora_bias, slice_sizes, num_slices, rank, y,
+                                  y_ld, num_tokens, offset_start, add_inputs, meta,
+                                  static_cast<cudaStream_t>(stream), 0, nullptr);
+}
+
+static int lora::lora_expand_impl(const void *x, int x_bf16, const lora_bf16_t *const *lora_b,
                                   const lora_bf16_t *const *lora_bias,
                                   const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
                                   lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
@@ -454,6 +477,7 @@ static int lora::lora_expand_impl(const float *x, const lora_bf16_t *const *lora
     if (reinterpret_cast<uintptr_t>(x) & 15u) return LORA_ERR_ALIGN;
 
     p.x = x;
+    p.x_bf16 = x_bf16 ? 1 : 0;
     p.num_slices = num_slices;
     p.rank = rank;
     p.y = y;
@@ -470,12 +494,12 @@ static int lora::lora_expand_impl(const float *x, const lora_bf16_t *const *lora
     p.nbins = meta->max_loras + 1;
     p.early = early;
     p.map = map;
-    return lora::expand_dispatch(p, x, meta, stream);
+    return lora::expand_dispatch(p, meta, stream);
 }
 
 namespace lora {
 
-int expand_dispatch(ExpandArgs &p, const float *x, const lora_meta_t *meta, cudaStream_t st)
+int expand_dispatch(ExpandArgs &p, const lora_meta_t *meta, cudaStream_t st)
 {
     const int num_slices = p.num_slices, rank = p.rank, num_tokens = p.num_tokens;
     lora_bf16_t *y = p.y;
@@ -486,9 +510,9 @@ int expand_dispatch(ExpandArgs &p, const float *x, const lora_meta_t *meta, cuda
     // LORA_PUNICA_EXPAND_UMMA=1: on these workloads it was measured slower
     // than the mma.sync kernel (a TMA box per scattered token row costs far
     // more than the cp.async gather), so the default stays on mma.sync.
-    if (lora::env_int("LORA_PUNICA_EXPAND_UMMA", 0) && p.vec) {
+    if (lora::env_int("LORA_PUNICA_EXPAND_UMMA", 0) && p.vec && !p.x_bf16) {
         lora::ExpandLaunch u;
-        u.x = x;
+        u.x = static_cast<const float *>(p.x);
         for (int s = 0; s < LORA_MAX_SLICES; ++s) {
             u.b[s] = p.b[s];
             u.bias[s] = p.bias[s];
@@ -530,7 +554,7 @@ int expand_early(const float *x, const lora_bf16_t *const *lora_b,
 {
     const bool self_sort = map != nullptr && num_tokens <= EX_SELF_SORT_MAX_TOKENS &&
                            meta->max_loras <= EX_SELF_SORT_MAX_LORAS;
-    return lora_expand_impl(x, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
+    return lora_expand_impl(x, 0, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
                             num_tokens, 0, 1, meta, st, 1, self_sort ? map : nullptr);
 }
 

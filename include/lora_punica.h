@@ -182,6 +182,25 @@ int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
                 const lora_meta_t *meta, void *stream);
 
 /*
+ * lora_expand_bf16 -- lora_expand over a bf16 input, for the embedding LoRA
+ * (page "vllm.lora.punica_wrapper.punica_gpu",
+ * PunicaWrapperGPU.add_lora_embedding: y (+)= x @ lora_b, where x holds the
+ * rows of the embedding LoRA's A looked up for each token, and add_inputs
+ * is passed through from the caller).
+ *
+ *   x   device bf16 [num_slices, num_tokens, rank], 16-byte aligned; the
+ *       tensor cores take it as it is (no rounding of the input).
+ * Every other argument, the results and the errors are those of
+ * lora_expand.
+ */
+int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lora_b,
+                     const lora_bf16_t *const *lora_bias,
+                     const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
+                     lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
+                     int32_t offset_start, int32_t add_inputs,
+                     const lora_meta_t *meta, void *stream);
+
+/*
  * lora_linear -- one LoRA layer applied to a batch, metadata included: the
  * result of lora_meta_prepare(token_lora_mapping), then lora_shrink(x ->
  * buf, scale), then lora_expand(buf -> y, lora_bias, offset_start = 0,

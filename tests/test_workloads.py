@@ -69,3 +69,21 @@ def test_unique_bytes_counts_active_rows_and_loras():
     assert ub["t_active"] == 3 and ub["distinct"] == 2
     assert ub["shrink"] == 3 * 4096 * 2 + 2 * 3 * 16 * 4096 * 2 + 2 * 3 * 3 * 16 * 4
     assert ub["expand"] == 3 * 3 * 16 * 4 + 2 * 12288 * 16 * 2 + 3 * 12288 * 2 * 2
+
+
+def test_embedding_workload_has_a_bf16_rank_wide_input_and_no_a():
+    inp = W.generate("embedding")
+    w = inp.workload
+    assert inp.x.shape == (w.num_tokens, w.rank) and inp.x.dtype == np.uint16
+    assert inp.lora_a == [] and inp.lora_b[0].shape == (w.max_loras, 4096, w.rank)
+    ub = W.unique_bytes(w, inp.ids)
+    assert ub["shrink"] == 0 and ub["flops_shrink"] == 0
+    t, d = ub["t_active"], ub["distinct"]
+    assert ub["expand"] == t * w.rank * 2 + d * 4096 * w.rank * 2 + t * 4096 * 4
+
+
+def test_logits_workload_is_one_vocabulary_wide_slice():
+    inp = W.generate("logits")
+    w = inp.workload
+    assert w.slices == (32000,) and inp.y.shape == (256, 32000)
+    assert inp.lora_a[0].shape == (8, 16, 4096)

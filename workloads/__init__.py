@@ -4,8 +4,9 @@ This module draws random numbers and nothing else: it holds none of the
 method's arithmetic, so both the CUDA path and the CPU oracle can take their
 inputs from it without sharing any computation.
 
-Five workloads (sizes and distributions as stated for each below) plus an
-all-no-LoRA batch.  Values: x ~ N(0, 1), A and B ~ N(0, 0.02^2), bias ~
+Five workloads of one linear LoRA layer (sizes and distributions as stated
+for each below), an all-no-LoRA batch, and one workload each for the logits
+and the embedding LoRA.  Values: x ~ N(0, 1), A and B ~ N(0, 0.02^2), bias ~
 N(0, 0.01^2), y_in ~ N(0, 1), each rounded to bf16 (round to nearest even)
 and stored as raw uint16 bit patterns; the shrink buffer starts at zero.
 LoRA ids: per token uniform, or per sequence drawn from a truncated Zipf law
@@ -38,6 +39,11 @@ class Workload:
     scale: float = 1.0
     offset_start: int = 0
     add_inputs: bool = True
+    # "linear": shrink + expand of one LoRA layer; "logits": the same over
+    # the logits rows (one id per sampled position, the vocabulary as the one
+    # slice); "embedding": expand only, from a bf16 [T, r] input (the
+    # embedding LoRA's A rows looked up per token), no A.
+    kind: str = "linear"
     description: str = field(default="", compare=False)
 
     @property
@@ -80,6 +86,17 @@ WORKLOADS = {
     "none": Workload(
         "none", 5, 16384, 8192, 128, 64, (8192, 1024, 1024), "none",
         description="large-workload shapes with every id -1 (no-LoRA batch)"),
+    "logits": Workload(
+        "logits", 6, 256, 4096, 16, 8, (32000,), "uniform", kind="logits",
+        description="logits of 256 sampled positions (one per decode "
+                    "sequence): hidden 4096, rank 16, 8 LoRAs, vocabulary "
+                    "32000 as one slice, sampler ids uniform in {-1..7}"),
+    "embedding": Workload(
+        "embedding", 7, 2048, 16, 16, 8, (4096,), "uniform_p", p_none=0.1,
+        kind="embedding",
+        description="embedding LoRA of 2048 tokens: bf16 input [T, 16] (the "
+                    "looked-up A rows), rank 16, 8 LoRAs, embedding width "
+                    "4096, per-token ids uniform with 10% -1"),
 }
 
 
@@ -141,8 +158,8 @@ def normal_bf16(rng: np.random.Generator, shape, std: float) -> np.ndarray:
 class Inputs:
     workload: Workload
     ids: np.ndarray                 # int32 [T]
-    x: np.ndarray                   # uint16 (bf16) [T, H]
-    lora_a: list                    # S x uint16 [L, r, H]
+    x: np.ndarray                   # uint16 (bf16) [T, H] ([T, r] for "embedding")
+    lora_a: list                    # S x uint16 [L, r, H] (empty for "embedding")
     lora_b: list                    # S x uint16 [L, n_s, r]
     lora_bias: list | None          # S x uint16 [L, n_s] or None
     y: np.ndarray                   # uint16 (bf16) [T, y_ld]
@@ -154,7 +171,8 @@ def generate(w: Workload | str, seed: int | None = None,
     """Draw one batch of inputs for workload ``w``.
 
     ``num_tokens`` overrides T (the id law is unchanged); ``seed`` overrides
-    the workload's own seed.  Draw order is fixed: ids, x, A, B, bias, y.
+    the workload's own seed.  Draw order is fixed: ids, x, A, B, bias, y
+    (no A for an embedding workload).
     """
     if isinstance(w, str):
         w = WORKLOADS[w]
@@ -166,7 +184,10 @@ def generate(w: Workload | str, seed: int | None = None,
     T, H, r, L, S = w.num_tokens, w.hidden, w.rank, w.max_loras, w.num_slices
     ids = token_ids(w, rng)
     x = normal_bf16(rng, (T, H), 1.0)
-    lora_a = [normal_bf16(rng, (L, r, H), 0.02) for _ in range(S)]
+    if w.kind == "embedding":
+        lora_a = []
+    else:
+        lora_a = [normal_bf16(rng, (L, r, H), 0.02) for _ in range(S)]
     lora_b = [normal_bf16(rng, (L, n, r), 0.02) for n in w.slices]
     lora_bias = [normal_bf16(rng, (L, n), 0.01) for n in w.slices] if w.bias else None
     y = normal_bf16(rng, (T, w.y_ld), 1.0)
@@ -188,11 +209,15 @@ def unique_bytes(w: Workload, ids: np.ndarray) -> dict:
     d = int(np.unique(ids[act]).size)
     S, r, H = w.num_slices, w.rank, w.hidden
     n_tot = sum(w.slices)
-    shrink = t_act * H * 2 + d * S * r * H * 2 + 2 * S * t_act * r * 4
-    expand = (S * t_act * r * 4 + d * n_tot * r * 2
+    if w.kind == "embedding":                  # expand only, bf16 input
+        shrink, x_bytes = 0, S * t_act * r * 2
+    else:
+        shrink = t_act * H * 2 + d * S * r * H * 2 + 2 * S * t_act * r * 4
+        x_bytes = S * t_act * r * 4
+    expand = (x_bytes + d * n_tot * r * 2
               + (d * n_tot * 2 if w.bias else 0)
               + t_act * n_tot * 2 * (2 if w.add_inputs else 1))
-    flops_shrink = 2 * t_act * S * r * H
+    flops_shrink = 0 if w.kind == "embedding" else 2 * t_act * S * r * H
     flops_expand = 2 * t_act * n_tot * r
     return {"t_active": t_act, "distinct": d, "shrink": shrink, "expand": expand,
             "flops_shrink": flops_shrink, "flops_expand": flops_expand}
