@@ -3,9 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
     python bench.py --impl reference ...     # the fp64 CPU oracle, timed
 
-One step = one pass of the whole path over one batch: lora_meta_prepare,
-lora_shrink and lora_expand (through the C ABI), on inputs already resident
-in HBM.  Input sets (ids, x, A, B, bias, y, buffer) are replicated until
+One step = one pass of the whole path over one batch: metadata, shrink and
+expand through the C ABI (lora_linear), or metadata and the expand of a
+bf16 input for the embedding workload, on inputs already resident in HBM.  Input sets (ids, x, A, B, bias, y, buffer) are replicated until
 they total at least 4x the L2 cache, and consecutive steps rotate through
 them, so every step reads from HBM.  Steps are captured in CUDA graphs (one
 graph per rotation), warm-up steps run first, and exactly K steps are timed
@@ -215,10 +215,18 @@ def run_ours(args, rank, world):
     n_sets = max(2, -(-4 * l2 // base.nbytes))
     sets = [base] + [base.clone(eg) for _ in range(n_sets - 1)]
 
+    emb = w.kind == "embedding"
+
     def step(s: DeviceSet):
-        # metadata + shrink + expand of one layer: one C-ABI call (fused into
-        # a single kernel for small batches, three kernels otherwise)
-        eg.lora_linear(s.ids, s.x, s.A, s.B, s.bias, w.scale, s.buf, s.y, s.meta)
+        if emb:
+            # metadata + expand of the looked-up bf16 rows (embedding LoRA)
+            s.meta.prepare_tensors(s.ids)
+            eg.add_lora_embedding(s.y, s.x, s.B[0], s.meta, w.add_inputs)
+        else:
+            # metadata + shrink + expand of one layer (or of the logits): one
+            # C-ABI call (fused into a single kernel for small batches, three
+            # kernels otherwise)
+            eg.lora_linear(s.ids, s.x, s.A, s.B, s.bias, w.scale, s.buf, s.y, s.meta)
 
     stream = torch.cuda.Stream(dev)
     # eager pass first: configures kernels (smem attributes, occupancy) before capture
@@ -301,14 +309,22 @@ def run_ours(args, rank, world):
 
     k_step = time_kernel(mk_step, args.kernel_seconds)
     k_meta = time_kernel(lambda s: (lambda: s.meta.prepare_tensors(s.ids)), args.kernel_seconds)
-    k_shrink = time_kernel(lambda s: (lambda: eg.lora_shrink(s.x, s.A, s.buf, s.meta, w.scale)),
-                           args.kernel_seconds)
-    k_expand = time_kernel(lambda s: (lambda: eg.lora_expand(
-        s.buf, s.B, s.y, s.meta, w.offset_start, w.add_inputs, s.bias)), args.kernel_seconds)
+    if emb:
+        k_shrink = 0.0
+        k_expand = time_kernel(lambda s: (lambda: eg.lora_expand(
+            s.x.unsqueeze(0), s.B, s.y, s.meta, w.offset_start, w.add_inputs, s.bias)),
+            args.kernel_seconds)
+    else:
+        k_shrink = time_kernel(lambda s: (lambda: eg.lora_shrink(s.x, s.A, s.buf, s.meta,
+                                                                 w.scale)),
+                               args.kernel_seconds)
+        k_expand = time_kernel(lambda s: (lambda: eg.lora_expand(
+            s.buf, s.B, s.y, s.meta, w.offset_start, w.add_inputs, s.bias)),
+            args.kernel_seconds)
     clocks.stop()
 
     # ---- end to end through the public API, host buffers, copies timed
-    e2e = run_e2e(args, inp, w, dev, eg, stream)
+    e2e = run_e2e(args, inp, w, dev, eg, stream, step)
 
     if rank != 0:
         if dist:
@@ -319,11 +335,14 @@ def run_ours(args, rank, world):
     ms_per_step = elapsed_ms / args.steps
     value = world * T * args.steps / (elapsed_ms / 1e3)
     hbm, peak_src = peaks()
-    kern = {"meta": k_meta, "shrink": k_shrink, "expand": k_expand, "lora_linear": k_step}
-    shrink_gbs = ub["shrink"] / (k_shrink * 1e-3) / 1e9
+    kern = {"meta": k_meta, "shrink": k_shrink, "expand": k_expand,
+            ("embedding_step" if emb else "lora_linear"): k_step}
+    if emb:
+        del kern["shrink"]
+    shrink_gbs = ub["shrink"] / (k_shrink * 1e-3) / 1e9 if k_shrink else None
     expand_gbs = ub["expand"] / (k_expand * 1e-3) / 1e9
     step_bytes = ub["shrink"] + ub["expand"]
-    fused = fused_path(w)
+    fused = fused_path(w) and not emb
     if fused:
         # the whole step is one kernel: its bytes are the step's bytes
         dominant, dom_bytes, dom_ms, src = "linear_fused", step_bytes, k_step, "lora_fused.cu"
@@ -356,8 +375,9 @@ def run_ours(args, rank, world):
                   "(%.0f MB total, L2 %.0f MB)" % (n_sets, base.nbytes / 1e6,
                                                    n_sets * base.nbytes / 1e6, l2 / 1e6),
             "timing": "CUDA graphs of one rotation of steps, CUDA events on the launch stream",
-            "step": "lora_linear (metadata + shrink + expand): %s" % (
-                "one fused cluster kernel" if fused else "three kernels"),
+            "step": ("metadata + expand of a bf16 input (add_lora_embedding): two kernels"
+                     if emb else "lora_linear (metadata + shrink + expand): %s" % (
+                         "one fused cluster kernel" if fused else "three kernels")),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "effective_gbps": step_bytes / (ms_per_step * 1e-3) / 1e9,
@@ -367,7 +387,7 @@ def run_ours(args, rank, world):
         "roofline": {
             "bound": "hbm", "kernel": "lora_" + dominant,
             "note": ("fused kernel: algorithmic bytes of shrink + expand per launch"
-                     if fused else "largest of the three kernels"),
+                     if fused else "the step's longest kernel"),
             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": traffic,
             "algorithmic_bytes_per_launch": dom_bytes,
@@ -375,7 +395,8 @@ def run_ours(args, rank, world):
             "peak_source": peak_src + " (of measured)" if "measured" in peak_src else peak_src,
         },
         "hbm_frac_step": (step_bytes / (ms_per_step * 1e-3) / 1e9) / hbm,
-        "gpu_launches": args.steps * (1 if fused else 3 + (1 if umma_shrink_path(w) else 0)),
+        "gpu_launches": args.steps * (2 if emb else 1 if fused
+                                      else 3 + (1 if umma_shrink_path(w) else 0)),
         "clocks": clocks.summary(),
         "e2e": e2e,
         "wall_s_timed": wall,
@@ -389,9 +410,9 @@ def run_ours(args, rank, world):
     return out
 
 
-def run_e2e(args, inp, w, dev, eg, stream):
+def run_e2e(args, inp, w, dev, eg, stream, step):
     """Same step through the public API from pinned host buffers: H2D of the
-    step's ids, x and y, the three calls, D2H of y; all inside the timing."""
+    step's ids, x and y, the step's calls, D2H of y; all inside the timing."""
     import torch
     ids_h = torch.from_numpy(inp.ids).pin_memory()
     x_h = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).pin_memory()
@@ -405,7 +426,7 @@ def run_e2e(args, inp, w, dev, eg, stream):
         s.ids.copy_(ids_h, non_blocking=True)
         x_d.copy_(x_h, non_blocking=True)
         y_d.copy_(y_h, non_blocking=True)
-        eg.lora_linear(s.ids, s.x, s.A, s.B, s.bias, w.scale, s.buf, s.y, s.meta)
+        step(s)
         out_h.copy_(y_d, non_blocking=True)
 
     n = max(3, args.e2e_steps)
@@ -437,11 +458,15 @@ def _cores():
 
 
 def _oracle_step(oracle, w, inp, sel):
-    """One oracle pass: metadata on the whole map, shrink + expand on tokens sel."""
+    """One oracle pass: metadata on the whole map, shrink + expand (expand of
+    the bf16 input for an embedding workload) on tokens sel."""
     oracle.meta_prepare(inp.ids, w.max_loras)
     ids = inp.ids[sel]
-    buf = np.zeros((w.num_slices, sel.size, w.rank), np.float32)
-    b = oracle.shrink(inp.x[sel], inp.lora_a, ids, w.scale, buf)
+    if w.kind == "embedding":
+        b = oracle.bf16_to_f64(inp.x[sel])[None]
+    else:
+        buf = np.zeros((w.num_slices, sel.size, w.rank), np.float32)
+        b = oracle.shrink(inp.x[sel], inp.lora_a, ids, w.scale, buf)
     oracle.expand(b.astype(np.float32), inp.lora_b, ids, inp.y[sel], w.slices,
                   w.offset_start, w.add_inputs, inp.lora_bias)
 
@@ -463,7 +488,7 @@ def cpu_baseline(w, inp, target_s=10.0):
         _oracle_step(oracle, w, inp, sel)
         done += sel.size
         el = time.perf_counter() - t0
-        if el >= target_s * 0.5 or done >= 64 * T:
+        if el >= target_s:
             break
     return {"value": done / el, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
             "sample": "%d of %d tokens of the %s batch per pass (metadata on the full map), "
