@@ -90,7 +90,17 @@ struct ExpandTile {
     static constexpr int STAGE_BYTES = Y_BYTES + B_BYTES + BIAS_BYTES;
     static constexpr int A_BYTES = EX_BM * RP * 2;
     static constexpr int BYTES = EX_STAGES * STAGE_BYTES + A_BYTES;
+    // Copy shapes: y pieces (16 bytes) of one row are taken by YCH
+    // consecutive threads, so one pass covers Y_RPP rows and every thread
+    // keeps the same Y_PASSES rows for a whole tile; B likewise with CPR
+    // threads per row and B_RPP rows per pass.
+    static constexpr int Y_RPP = EX_THREADS / YCH;
+    static constexpr int Y_PASSES = EX_BM / Y_RPP;
+    static constexpr int B_RPP = EX_THREADS / CPR;
+    static constexpr int B_PASSES = (BN + B_RPP - 1) / B_RPP;
     static_assert(WN == 32 && MI >= 1, "warp tile");
+    static_assert(EX_THREADS % YCH == 0 && EX_BM % Y_RPP == 0, "y copy shape");
+    static_assert(EX_THREADS % CPR == 0 && B_RPP % 8 == 0, "B copy shape (swizzle period)");
 };
 
 template <int KT>
@@ -174,25 +184,41 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
         if (tid < EX_BM) s_tok[tid] = (tid < nrows) ? tokens[row0 + tid] : -1;
         __syncthreads();
 
+        // This thread's y rows for the whole tile (piece ycc of rows
+        // yr0 + j * Y_RPP), and its B row / piece of every chunk.
+        const int ycc = tid % YCH, yr0 = tid / YCH;
+        int ytok[Cfg::Y_PASSES];
+#pragma unroll
+        for (int j = 0; j < Cfg::Y_PASSES; ++j) ytok[j] = s_tok[yr0 + j * Cfg::Y_RPP];
+        uint16_t *const ybase = yslice + ycc * 8;
+        const uint32_t y_soff = yr0 * Cfg::Y_LD + ycc * 16;
+        const int bcc = tid % CPR, br0 = tid / CPR;
+        const bool b_kin = bcc * 8 < R;
+        const uint16_t *brow = bslice + int64_t(br0) * R + bcc * 8;
+        const uint32_t b_soff = swz<CPR>(br0, bcc);
+
         auto load_chunk = [&](int slot, int c) {
             const int c0 = (c - p.chunk0[s]) * BN;
             const int ncols = min(BN, n_s - c0);
             const uint32_t sy = ring + slot * Cfg::STAGE_BYTES;
             const uint32_t sb = sy + Cfg::Y_BYTES;
             if (prefetch_y) {
-                for (int i = tid; i < EX_BM * YCH; i += EX_THREADS) {
-                    const int r = i / YCH, cc = i - r * YCH;
-                    const int tok = s_tok[r];
-                    const bool ok = tok >= 0 && cc * 8 < ncols;
-                    cp_async16(sy + r * Cfg::Y_LD + cc * 16,
-                               ok ? yslice + int64_t(tok) * p.y_ld + c0 + cc * 8 : p.y, ok);
+                const bool cin = ycc * 8 < ncols;
+#pragma unroll
+                for (int j = 0; j < Cfg::Y_PASSES; ++j) {
+                    const bool ok = cin && ytok[j] >= 0;
+                    cp_async16(sy + y_soff + j * Cfg::Y_RPP * Cfg::Y_LD,
+                               ok ? ybase + (int64_t(ytok[j]) * p.y_ld + c0) : p.y, ok);
                 }
             }
-            for (int i = tid; i < BN * CPR; i += EX_THREADS) {
-                const int r = i / CPR, cc = i - r * CPR;
-                const bool ok = r < ncols && cc * 8 < R;
-                cp_async16(sb + swz<CPR>(r, cc),
-                           ok ? bslice + int64_t(c0 + r) * R + cc * 8 : p.b[s], ok);
+            const uint16_t *bc = brow + int64_t(c0) * R;
+#pragma unroll
+            for (int j = 0; j < Cfg::B_PASSES; ++j) {
+                const int r = br0 + j * Cfg::B_RPP;
+                if (Cfg::B_PASSES * Cfg::B_RPP > BN && r >= BN) break;
+                const bool ok = b_kin && r < ncols;
+                cp_async16(sb + b_soff + j * Cfg::B_RPP * CPR * 16,
+                           ok ? bc + int64_t(j) * Cfg::B_RPP * R : p.b[s], ok);
             }
             if (bias_row != nullptr && p.bias_vec && tid < BN / 8) {
                 const bool ok = tid * 8 < ncols;
@@ -277,13 +303,14 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
                     bv[n][h] = b;
                 }
 
+            // the accumulators start at the bias, so the product lands on it
             float acc[MI][NI][4];
 #pragma unroll
             for (int m = 0; m < MI; ++m)
 #pragma unroll
                 for (int n = 0; n < NI; ++n)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[m][n][q] = 0.f;
+                    for (int q = 0; q < 4; ++q) acc[m][n][q] = bv[n][q & 1];
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk)
 #pragma unroll
@@ -310,8 +337,8 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
                             const int r = wm * Cfg::WM + m * 16 + (lane >> 2) + 8 * h;
                             const int c = wn * Cfg::WN + n * 8 + 2 * (lane & 3);
                             uint32_t *cell = reinterpret_cast<uint32_t *>(sy + r * Cfg::Y_LD + c * 2);
-                            float v0 = acc[m][n][2 * h] + bv[n][0];
-                            float v1 = acc[m][n][2 * h + 1] + bv[n][1];
+                            float v0 = acc[m][n][2 * h];
+                            float v1 = acc[m][n][2 * h + 1];
                             if (p.add_inputs) {
                                 const uint32_t old = *cell;
                                 v0 += bf16_lo(old);
@@ -320,12 +347,14 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
                             *cell = pack_bf16x2(v0, v1);
                         }
                 __syncthreads();
-                for (int j = tid; j < EX_BM * YCH; j += EX_THREADS) {
-                    const int r = j / YCH, cc = j - r * YCH;
-                    const int tok = s_tok[r];
-                    if (tok < 0 || cc * 8 >= ncols) continue;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(sy + r * Cfg::Y_LD + cc * 16);
-                    *reinterpret_cast<uint4 *>(yslice + int64_t(tok) * p.y_ld + c0 + cc * 8) = v;
+                if (ycc * 8 < ncols) {
+#pragma unroll
+                    for (int j = 0; j < Cfg::Y_PASSES; ++j) {
+                        if (ytok[j] < 0) continue;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(
+                            sy + y_soff + j * Cfg::Y_RPP * Cfg::Y_LD);
+                        *reinterpret_cast<uint4 *>(ybase + (int64_t(ytok[j]) * p.y_ld + c0)) = v;
+                    }
                 }
             } else {
 #pragma unroll
@@ -339,7 +368,7 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
                             const int tok = s_tok[r];
                             if (tok < 0 || c >= ncols) continue;
                             uint16_t *dst = yslice + int64_t(tok) * p.y_ld + c0 + c;
-                            float v = acc[m][n][q] + bv[n][q & 1];
+                            float v = acc[m][n][q];
                             if (p.add_inputs) v += bf16_to_f32(*dst);
                             *dst = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
                         }
