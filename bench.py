@@ -78,8 +78,18 @@ def _padded_rank(r: int) -> int:
     return rp
 
 
+def coop_path(w) -> bool:
+    """lora_linear's rule for its single cooperative kernel (lora_linear_coop.cu)."""
+    mode = os.environ.get("LORA_PUNICA_COOP", "")
+    wanted = mode == "1" or (mode != "0" and w.num_tokens * w.num_slices <= 256)
+    return (wanted and 1 <= w.num_tokens <= 512 and w.max_loras <= 256 and w.rank <= 64
+            and w.hidden % 8 == 0)
+
+
 def fused_path(w) -> bool:
     """lora_linear's rule for its single fused kernel (include/lora_punica.h)."""
+    if coop_path(w):
+        return False
     mode = os.environ.get("LORA_PUNICA_FUSED", "")
     limit = 512 if mode == "1" else int(os.environ.get("LORA_PUNICA_FUSED_MAX_TOKENS", "128"))
     return (w.num_tokens <= limit and w.max_loras <= 256 and _padded_rank(w.rank) <= 64
@@ -342,9 +352,13 @@ def run_ours(args, rank, world):
     shrink_gbs = ub["shrink"] / (k_shrink * 1e-3) / 1e9 if k_shrink else None
     expand_gbs = ub["expand"] / (k_expand * 1e-3) / 1e9
     step_bytes = ub["shrink"] + ub["expand"]
-    fused = fused_path(w) and not emb
-    if fused:
+    coop = coop_path(w) and not emb
+    fused = (fused_path(w) and not emb) or coop
+    if coop:
         # the whole step is one kernel: its bytes are the step's bytes
+        dominant, dom_bytes, dom_ms, src = ("linear_coop", step_bytes, k_step,
+                                            "lora_linear_coop.cu")
+    elif fused:
         dominant, dom_bytes, dom_ms, src = "linear_fused", step_bytes, k_step, "lora_fused.cu"
     else:
         dominant = "expand" if k_expand >= k_shrink else "shrink"
@@ -377,6 +391,7 @@ def run_ours(args, rank, world):
             "timing": "CUDA graphs of one rotation of steps, CUDA events on the launch stream",
             "step": ("metadata + expand of a bf16 input (add_lora_embedding): two kernels"
                      if emb else "lora_linear (metadata + shrink + expand): %s" % (
+                         "one cooperative kernel" if coop else
                          "one fused cluster kernel" if fused else "three kernels")),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
@@ -386,7 +401,7 @@ def run_ours(args, rank, world):
         "kernels_gbps": {"shrink": shrink_gbs, "expand": expand_gbs},
         "roofline": {
             "bound": "hbm", "kernel": "lora_" + dominant,
-            "note": ("fused kernel: algorithmic bytes of shrink + expand per launch"
+            "note": ("single kernel: algorithmic bytes of shrink + expand per launch"
                      if fused else "the step's longest kernel"),
             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": traffic,

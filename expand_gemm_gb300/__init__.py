@@ -85,6 +85,8 @@ class LoRAKernelMeta:
         self.lora_token_start_loc = torch.zeros(max_loras + 2, **i32)
         self.no_lora_flag = torch.ones(1, **i32)
         self.error_word = torch.zeros(1, **i32)
+        # grid barrier of lora_linear's single-kernel path (left zero by every call)
+        self.grid_sync = torch.zeros(2, **i32)
         self.c = _lib.LoraMetaC(
             self.token_lora_mapping.data_ptr(),
             self.token_indices_sorted_by_lora_ids.data_ptr(),
@@ -93,7 +95,8 @@ class LoRAKernelMeta:
             self.active_lora_ids.data_ptr(),
             self.no_lora_flag.data_ptr(),
             self.error_word.data_ptr(),
-            self.max_loras, self.max_num_tokens)
+            self.max_loras, self.max_num_tokens,
+            self.grid_sync.data_ptr())
         self.device = dev
 
     @staticmethod

@@ -34,6 +34,7 @@ class LoraMetaC(ctypes.Structure):
         ("error_word", ctypes.c_void_p),
         ("max_loras", ctypes.c_int32),
         ("max_num_tokens", ctypes.c_int32),
+        ("grid_sync", ctypes.c_void_p),
     ]
 
 

@@ -402,6 +402,14 @@ int expand_early(const float *x, const lora_bf16_t *const *lora_b,
                  int32_t num_slices, int32_t rank, lora_bf16_t *y, int64_t y_ld,
                  int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st,
                  const int32_t *map);
+// lora_linear as one cooperative kernel (small batches).  Returns 1 when
+// launched, 0 when the batch or its layout does not fit that path.
+int linear_coop(const int32_t *map, int32_t num_tokens, const lora_bf16_t *x, int32_t hidden,
+                int64_t x_ld, const lora_bf16_t *const *lora_a,
+                const lora_bf16_t *const *lora_b, const lora_bf16_t *const *lora_bias,
+                const int32_t *slice_sizes, int32_t num_slices, int32_t rank, float scale,
+                float *buf, lora_bf16_t *y, int64_t y_ld, const lora_meta_t *meta,
+                cudaStream_t st);
 
 // Host-side description of one lora_expand call for its tensor-core path.
 struct ExpandLaunch {

@@ -18,119 +18,20 @@
 // y tile, and the tile leaves with 128-bit coalesced stores.  When y, its
 // stride, the offsets or a slice width are not multiples of 8 elements, y
 // is not prefetched and a scalar epilogue reads and writes it per element.
-#include "lora_common.cuh"
+#include "lora_expand.cuh"
 
 namespace lora {
-
-constexpr int EX_BM = 64;          // tokens per tile
-constexpr int EX_THREADS = 256;    // 8 warps
-constexpr int EX_STAGES = 3;
-
-struct ExpandArgs {
-    const void *x;                       // [S, T, r]: fp32, or bf16 when x_bf16
-    int32_t x_bf16;
-    const uint16_t *b[LORA_MAX_SLICES];
-    const uint16_t *bias[LORA_MAX_SLICES];
-    int32_t n[LORA_MAX_SLICES];          // slice widths
-    int32_t col0[LORA_MAX_SLICES];       // off_s
-    int32_t chunk0[LORA_MAX_SLICES + 1]; // first column chunk of each slice
-    int32_t num_slices;
-    int32_t rank;
-    uint16_t *y;
-    int64_t y_ld;
-    int32_t num_tokens;
-    int32_t add_inputs;
-    int32_t vec;                         // 16-byte y path allowed
-    int32_t bias_vec;                    // 16-byte bias loads allowed (every bias)
-    const int32_t *sorted;
-    const int32_t *counts;
-    const int32_t *start_loc;
-    const int32_t *active;
-    const int32_t *no_lora;
-    int32_t nbins;
-    // Early mode (set only by lora_linear, whose preceding kernel is its own
-    // shrink): the segment table, the token list and the y / B / bias loads
-    // of the first tile are issued before the grid-dependency wait; only the
-    // shrink output (x) is read after it.  Safe because the shrink lets its
-    // dependents launch only after its own wait, i.e. once the metadata
-    // kernel and everything before it in the stream have completed, and the
-    // shrink writes neither the metadata, y, B nor bias.
-    int32_t early;
-    // With `map` (early mode, small batches) every CTA sorts the id map
-    // itself instead of reading the segment table and token list: one round
-    // trip instead of two.  The result is the metadata the metadata kernel
-    // writes, so the two agree.
-    const int32_t *map;
-};
-
-constexpr int EX_SELF_SORT_MAX_TOKENS = 512;
-constexpr int EX_SELF_SORT_MAX_LORAS = 256;
-
-size_t expand_self_sort_bytes(int nbins)
-{
-    return size_t(8 * nbins + 3 * nbins + 2 * EX_SELF_SORT_MAX_TOKENS + 4) * sizeof(int);
-}
-
-template <int KT>
-struct ExpandTile {
-    static constexpr int RP = 16 * KT;                 // padded rank
-    static constexpr int CPR = RP / 8;                 // 16-byte chunks per row
-    static constexpr int BN = (KT >= 8) ? 64 : 128;    // columns per chunk
-    static constexpr int WARPS_M = (BN == 128) ? 2 : 4;
-    static constexpr int WARPS_N = 8 / WARPS_M;
-    static constexpr int WM = EX_BM / WARPS_M;         // rows per warp
-    static constexpr int WN = BN / WARPS_N;            // columns per warp (32)
-    static constexpr int MI = WM / 16;
-    static constexpr int NI = WN / 8;
-    static constexpr int YCH = BN / 8;                 // 16-byte chunks per y row
-    static constexpr int Y_LD = BN * 2 + 16;           // padded shared y row (bytes)
-    static constexpr int Y_BYTES = EX_BM * Y_LD;
-    static constexpr int B_BYTES = BN * RP * 2;
-    static constexpr int BIAS_BYTES = BN * 2;                // bf16 bias chunk
-    static constexpr int STAGE_BYTES = Y_BYTES + B_BYTES + BIAS_BYTES;
-    static constexpr int A_BYTES = EX_BM * RP * 2;
-    static constexpr int BYTES = EX_STAGES * STAGE_BYTES + A_BYTES;
-    // Copy shapes: y pieces (16 bytes) of one row are taken by YCH
-    // consecutive threads, so one pass covers Y_RPP rows and every thread
-    // keeps the same Y_PASSES rows for a whole tile; B likewise with CPR
-    // threads per row and B_RPP rows per pass.
-    static constexpr int Y_RPP = EX_THREADS / YCH;
-    static constexpr int Y_PASSES = EX_BM / Y_RPP;
-    static constexpr int B_RPP = EX_THREADS / CPR;
-    static constexpr int B_PASSES = (BN + B_RPP - 1) / B_RPP;
-    static_assert(WN == 32 && MI >= 1, "warp tile");
-    static_assert(EX_THREADS % YCH == 0 && EX_BM % Y_RPP == 0, "y copy shape");
-    static_assert(EX_THREADS % CPR == 0 && B_RPP % 8 == 0, "B copy shape (swizzle period)");
-};
-
-template <int KT>
-constexpr int expand_bn() { return ExpandTile<KT>::BN; }
-
-size_t expand_smem_bytes(int kt, int nbins)
-{
-    size_t t = 0;
-    switch (kt) {
-    case 1: t = ExpandTile<1>::BYTES; break;
-    case 2: t = ExpandTile<2>::BYTES; break;
-    case 4: t = ExpandTile<4>::BYTES; break;
-    default: t = ExpandTile<8>::BYTES; break;
-    }
-    return t + seg_tab_bytes(nbins);
-}
 
 template <int KT>
 __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(ExpandArgs p)
 {
     using Cfg = ExpandTile<KT>;
-    constexpr int CPR = Cfg::CPR, BN = Cfg::BN, MI = Cfg::MI, NI = Cfg::NI, YCH = Cfg::YCH;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_tok[EX_BM];
 
-    bool waited = false;
     if (!p.early) {
         pdl_wait();
         pdl_launch_dependents();
-        waited = true;
     }
 
     uint8_t *sA = smem + EX_STAGES * Cfg::STAGE_BYTES;
@@ -152,231 +53,15 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
                                     tab);
     }
     if (total_tiles == 0) return;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int wm = warp / Cfg::WARPS_N, wn = warp % Cfg::WARPS_N;
-    const int S = p.num_slices, R = p.rank, T = p.num_tokens;
-    const int nchunks = p.chunk0[S];
-    const int64_t total = int64_t(total_tiles) * nchunks;
-    int64_t w = int64_t(blockIdx.x) * total / gridDim.x;
-    const int64_t w_end = int64_t(blockIdx.x + 1) * total / gridDim.x;
-    const uint32_t ring = smem_addr(smem), aA = smem_addr(sA);
-    const bool prefetch_y = p.vec && p.add_inputs;
-
-    while (w < w_end) {
-        // ---- one row item: token tile `tile`, slice s, chunks [cb, ce)
-        const int tile = int(w / nchunks);
-        const int cb = int(w - int64_t(tile) * nchunks);
-        int s = 0;
-        while (s + 1 < S && p.chunk0[s + 1] <= cb) ++s;
-        const int ce = int(min(int64_t(p.chunk0[s + 1]), int64_t(cb) + (w_end - w)));
-        w += ce - cb;
-
-        const int seg = find_segment(tab.tile, p.nbins, tile);
-        const int id = tab.id[seg];
-        const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * EX_BM;
-        const int nrows = min(EX_BM, tab.start[seg] + tab.count[seg] - row0);
-        const int n_s = p.n[s];
-        const uint16_t *bslice = p.b[s] + int64_t(id) * n_s * R;
-        const uint16_t *bias_row = p.bias[s] ? p.bias[s] + int64_t(id) * n_s : nullptr;
-        uint16_t *yslice = p.y + p.col0[s];
-
-        if (tid < EX_BM) s_tok[tid] = (tid < nrows) ? tokens[row0 + tid] : -1;
-        __syncthreads();
-
-        // This thread's y rows for the whole tile (piece ycc of rows
-        // yr0 + j * Y_RPP), and its B row / piece of every chunk.
-        const int ycc = tid % YCH, yr0 = tid / YCH;
-        int ytok[Cfg::Y_PASSES];
-#pragma unroll
-        for (int j = 0; j < Cfg::Y_PASSES; ++j) ytok[j] = s_tok[yr0 + j * Cfg::Y_RPP];
-        uint16_t *const ybase = yslice + ycc * 8;
-        const uint32_t y_soff = yr0 * Cfg::Y_LD + ycc * 16;
-        const int bcc = tid % CPR, br0 = tid / CPR;
-        const bool b_kin = bcc * 8 < R;
-        const uint16_t *brow = bslice + int64_t(br0) * R + bcc * 8;
-        const uint32_t b_soff = swz<CPR>(br0, bcc);
-
-        auto load_chunk = [&](int slot, int c) {
-            const int c0 = (c - p.chunk0[s]) * BN;
-            const int ncols = min(BN, n_s - c0);
-            const uint32_t sy = ring + slot * Cfg::STAGE_BYTES;
-            const uint32_t sb = sy + Cfg::Y_BYTES;
-            if (prefetch_y) {
-                const bool cin = ycc * 8 < ncols;
-#pragma unroll
-                for (int j = 0; j < Cfg::Y_PASSES; ++j) {
-                    const bool ok = cin && ytok[j] >= 0;
-                    cp_async16(sy + y_soff + j * Cfg::Y_RPP * Cfg::Y_LD,
-                               ok ? ybase + (int64_t(ytok[j]) * p.y_ld + c0) : p.y, ok);
-                }
-            }
-            const uint16_t *bc = brow + int64_t(c0) * R;
-#pragma unroll
-            for (int j = 0; j < Cfg::B_PASSES; ++j) {
-                const int r = br0 + j * Cfg::B_RPP;
-                if (Cfg::B_PASSES * Cfg::B_RPP > BN && r >= BN) break;
-                const bool ok = b_kin && r < ncols;
-                cp_async16(sb + b_soff + j * Cfg::B_RPP * CPR * 16,
-                           ok ? bc + int64_t(j) * Cfg::B_RPP * R : p.b[s], ok);
-            }
-            if (bias_row != nullptr && p.bias_vec && tid < BN / 8) {
-                const bool ok = tid * 8 < ncols;
-                cp_async16(sb + Cfg::B_BYTES + tid * 16, ok ? bias_row + c0 + tid * 8 : bias_row, ok);
-            }
-        };
-
-#pragma unroll
-        for (int st = 0; st < EX_STAGES - 1; ++st) {
-            if (cb + st < ce) load_chunk(st, cb + st);
-            cp_async_commit();
-        }
-
-        if (!waited) {                        // the shrink output is read from here on
+    // early mode: the grid-dependency wait sits right before the first read
+    // of the shrink output
+    expand_items<KT>(p, tab, tokens, total_tiles, smem, s_tok, [&]() {
+        if (p.early) {
             pdl_wait();
             pdl_launch_dependents();
-            waited = true;
         }
-        // x rows of this tile and slice -> bf16 A operand (overlaps the ring
-        // fill): fp32 rows are rounded to bf16, bf16 rows are copied as they are
-        {
-            const int64_t xoff = int64_t(s) * T * R;
-            for (int i = tid; i < EX_BM * CPR; i += EX_THREADS) {
-                const int r = i / CPR, cc = i - r * CPR;
-                const int tok = s_tok[r];
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (tok >= 0 && cc * 8 < R) {
-                    const int64_t e = xoff + int64_t(tok) * R + cc * 8;
-                    if (p.x_bf16) {
-                        v = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.x) + e);
-                    } else {
-                        const float4 *src = reinterpret_cast<const float4 *>(
-                            static_cast<const float *>(p.x) + e);
-                        const float4 u = src[0], q = src[1];
-                        v.x = pack_bf16x2(u.x, u.y);
-                        v.y = pack_bf16x2(u.z, u.w);
-                        v.z = pack_bf16x2(q.x, q.y);
-                        v.w = pack_bf16x2(q.z, q.w);
-                    }
-                }
-                *reinterpret_cast<uint4 *>(sA + swz<CPR>(r, cc)) = v;
-            }
-        }
-        __syncthreads();
-        uint32_t af[MI][KT][4];
-#pragma unroll
-        for (int m = 0; m < MI; ++m)
-#pragma unroll
-            for (int kk = 0; kk < KT; ++kk) {
-                const int r = wm * Cfg::WM + m * 16 + (lane & 15);
-                const int c = kk * 2 + (lane >> 4);
-                ldmatrix_x4(aA + swz<CPR>(r, c), af[m][kk][0], af[m][kk][1], af[m][kk][2],
-                            af[m][kk][3]);
-            }
-
-        for (int i = 0; cb + i < ce; ++i) {
-            cp_async_wait<EX_STAGES - 2>();
-            __syncthreads();
-            {
-                const int nxt = i + EX_STAGES - 1;
-                if (cb + nxt < ce) load_chunk(nxt % EX_STAGES, cb + nxt);
-                cp_async_commit();
-            }
-            const int slot = i % EX_STAGES;
-            const int c0 = (cb + i - p.chunk0[s]) * BN;
-            const int ncols = min(BN, n_s - c0);
-            uint8_t *sy = smem + slot * Cfg::STAGE_BYTES;
-            const uint32_t sb = ring + slot * Cfg::STAGE_BYTES + Cfg::Y_BYTES;
-
-            // bias of this chunk: staged with the chunk when aligned, else read here
-            float bv[NI][2];
-            const uint16_t *sbias = reinterpret_cast<const uint16_t *>(
-                smem + slot * Cfg::STAGE_BYTES + Cfg::Y_BYTES + Cfg::B_BYTES);
-#pragma unroll
-            for (int n = 0; n < NI; ++n)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c = wn * Cfg::WN + n * 8 + 2 * (lane & 3) + h;
-                    float b = 0.f;
-                    if (bias_row != nullptr && c < ncols)
-                        b = bf16_to_f32(p.bias_vec ? sbias[c] : bias_row[c0 + c]);
-                    bv[n][h] = b;
-                }
-
-            // the accumulators start at the bias, so the product lands on it
-            float acc[MI][NI][4];
-#pragma unroll
-            for (int m = 0; m < MI; ++m)
-#pragma unroll
-                for (int n = 0; n < NI; ++n)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[m][n][q] = bv[n][q & 1];
-#pragma unroll
-            for (int kk = 0; kk < KT; ++kk)
-#pragma unroll
-                for (int n2 = 0; n2 < NI / 2; ++n2) {
-                    uint32_t b[4];
-                    const int q = lane >> 3;
-                    const int r = wn * Cfg::WN + n2 * 16 + (q >> 1) * 8 + (lane & 7);
-                    const int c = kk * 2 + (q & 1);
-                    ldmatrix_x4(sb + swz<CPR>(r, c), b[0], b[1], b[2], b[3]);
-#pragma unroll
-                    for (int m = 0; m < MI; ++m) {
-                        mma_bf16_16816(acc[m][2 * n2], af[m][kk], b[0], b[1]);
-                        mma_bf16_16816(acc[m][2 * n2 + 1], af[m][kk], b[2], b[3]);
-                    }
-                }
-
-            if (p.vec) {
-#pragma unroll
-                for (int m = 0; m < MI; ++m)
-#pragma unroll
-                    for (int n = 0; n < NI; ++n)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int r = wm * Cfg::WM + m * 16 + (lane >> 2) + 8 * h;
-                            const int c = wn * Cfg::WN + n * 8 + 2 * (lane & 3);
-                            uint32_t *cell = reinterpret_cast<uint32_t *>(sy + r * Cfg::Y_LD + c * 2);
-                            float v0 = acc[m][n][2 * h];
-                            float v1 = acc[m][n][2 * h + 1];
-                            if (p.add_inputs) {
-                                const uint32_t old = *cell;
-                                v0 += bf16_lo(old);
-                                v1 += bf16_hi(old);
-                            }
-                            *cell = pack_bf16x2(v0, v1);
-                        }
-                __syncthreads();
-                if (ycc * 8 < ncols) {
-#pragma unroll
-                    for (int j = 0; j < Cfg::Y_PASSES; ++j) {
-                        if (ytok[j] < 0) continue;
-                        const uint4 v = *reinterpret_cast<const uint4 *>(
-                            sy + y_soff + j * Cfg::Y_RPP * Cfg::Y_LD);
-                        *reinterpret_cast<uint4 *>(ybase + (int64_t(ytok[j]) * p.y_ld + c0)) = v;
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int m = 0; m < MI; ++m)
-#pragma unroll
-                    for (int n = 0; n < NI; ++n)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int r = wm * Cfg::WM + m * 16 + (lane >> 2) + 8 * (q >> 1);
-                            const int c = wn * Cfg::WN + n * 8 + 2 * (lane & 3) + (q & 1);
-                            const int tok = s_tok[r];
-                            if (tok < 0 || c >= ncols) continue;
-                            uint16_t *dst = yslice + int64_t(tok) * p.y_ld + c0 + c;
-                            float v = acc[m][n][q];
-                            if (p.add_inputs) v += bf16_to_f32(*dst);
-                            *dst = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
-                        }
-            }
-        }
-        cp_async_wait<0>();
-        __syncthreads();
-    }
+        return true;
+    });
 }
 
 template <int KT>
@@ -453,13 +138,11 @@ LORA_API int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lo
                                   static_cast<cudaStream_t>(stream), 0, nullptr);
 }
 
-static int lora::lora_expand_impl(const void *x, int x_bf16, const lora_bf16_t *const *lora_b,
-                                  const lora_bf16_t *const *lora_bias,
-                                  const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
-                                  lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
-                                  int32_t offset_start, int32_t add_inputs,
-                                  const lora_meta_t *meta, cudaStream_t stream, int early,
-                                  const int32_t *map)
+int lora::expand_setup(ExpandArgs &p, const void *x, int x_bf16,
+                       const lora_bf16_t *const *lora_b, const lora_bf16_t *const *lora_bias,
+                       const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
+                       lora_bf16_t *y, int64_t y_ld, int32_t num_tokens, int32_t offset_start,
+                       int32_t add_inputs, const lora_meta_t *meta)
 {
     if (meta == nullptr || lora_b == nullptr || slice_sizes == nullptr) return LORA_ERR_NULL;
     if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SLICES;
@@ -468,7 +151,6 @@ static int lora::lora_expand_impl(const void *x, int x_bf16, const lora_bf16_t *
     if (meta->max_loras < 1 || meta->max_loras > LORA_MAX_LORAS) return LORA_ERR_SIZE;
     if (num_tokens > meta->max_num_tokens) return LORA_ERR_TOKENS;
 
-    lora::ExpandArgs p;
     int64_t col = offset_start;
     int chunks = 0;
     bool vec = ((reinterpret_cast<uintptr_t>(y) & 15u) == 0) && (y_ld % 8 == 0) &&
@@ -499,7 +181,7 @@ static int lora::lora_expand_impl(const void *x, int x_bf16, const lora_bf16_t *
     }
     p.chunk0[num_slices] = chunks;
     if (col > y_ld) return LORA_ERR_WIDTH;
-    if (num_tokens == 0 || chunks == 0) return LORA_OK;
+    if (num_tokens == 0 || chunks == 0) return 1;
     if (!x || !y || !meta->token_indices_sorted_by_lora_ids || !meta->num_tokens_per_lora ||
         !meta->lora_token_start_loc || !meta->active_lora_ids || !meta->no_lora_flag)
         return LORA_ERR_NULL;
@@ -521,6 +203,24 @@ static int lora::lora_expand_impl(const void *x, int x_bf16, const lora_bf16_t *
     p.active = meta->active_lora_ids;
     p.no_lora = meta->no_lora_flag;
     p.nbins = meta->max_loras + 1;
+    p.early = 0;
+    p.map = nullptr;
+    return LORA_OK;
+}
+
+static int lora::lora_expand_impl(const void *x, int x_bf16, const lora_bf16_t *const *lora_b,
+                                  const lora_bf16_t *const *lora_bias,
+                                  const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
+                                  lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
+                                  int32_t offset_start, int32_t add_inputs,
+                                  const lora_meta_t *meta, cudaStream_t stream, int early,
+                                  const int32_t *map)
+{
+    lora::ExpandArgs p;
+    const int r = lora::expand_setup(p, x, x_bf16, lora_b, lora_bias, slice_sizes, num_slices,
+                                     rank, y, y_ld, num_tokens, offset_start, add_inputs, meta);
+    if (r == 1) return LORA_OK;              // nothing to do
+    if (r != LORA_OK) return r;
     p.early = early;
     p.map = map;
     return lora::expand_dispatch(p, meta, stream);

@@ -675,6 +675,24 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
     if (num_tokens > meta->max_num_tokens) return LORA_ERR_TOKENS;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+    // Small batches as one cooperative kernel (metadata, shrink, grid
+    // barrier, expand), when the layout fits it (lora_linear_coop.cu).  By
+    // default it takes batches with num_tokens * num_slices <= 256 (the
+    // shrink rows): measured faster than the other paths on 64 tokens x 1
+    // slice and on 256 x 1 (logits-like), slower on 256 x 3 (q/k/v decode),
+    // where the shrink phase and the barrier cost more than the launches
+    // they replace.  LORA_PUNICA_COOP=1 takes it for every batch that fits
+    // (up to 512 tokens), LORA_PUNICA_COOP=0 never.
+    const int coop_mode = lora::env_int("LORA_PUNICA_COOP", -1);
+    if (coop_mode == 1 ||
+        (coop_mode != 0 && int64_t(num_tokens) * num_slices <= 256)) {
+        const int r = lora::linear_coop(token_lora_mapping, num_tokens, x, hidden, x_ld, lora_a,
+                                        lora_b, lora_bias, slice_sizes, num_slices, rank, scale,
+                                        buf, y, y_ld, meta, st);
+        if (r == 1) return LORA_OK;
+        if (r != 0) return r;
+    }
+
     // One fused kernel for small batches when every layout rule of the
     // vector paths holds.  By default it is taken for batches of at most
     // LORA_PUNICA_FUSED_MAX_TOKENS (128) tokens: measured on decode-sized

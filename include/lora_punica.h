@@ -83,6 +83,10 @@ enum lora_status {
  *   active_lora_ids                   [max_loras + 1]   ascending, pad -1
  *   no_lora_flag                      [1]               1 = every id is -1
  *   error_word                        [1]               invalid ids counted
+ *   grid_sync                         [2]               zero-filled once by
+ *       the caller; the grid barrier of lora_linear's single-kernel path
+ *       (every call leaves it zero again).  May be NULL, which turns that
+ *       path off.  Calls that share a struct must be stream-ordered.
  * The same struct (by pointer) is then handed to lora_shrink/lora_expand;
  * they read it on the device.  The struct itself is host memory and is only
  * read during each call.
@@ -97,6 +101,7 @@ typedef struct lora_meta {
     int32_t *error_word;
     int32_t max_loras;
     int32_t max_num_tokens;
+    int32_t *grid_sync;
 } lora_meta_t;
 
 /*

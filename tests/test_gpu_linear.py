@@ -1,6 +1,5 @@
 """GPU parity of lora_linear (metadata + shrink + expand in one call) against
-the oracle composition, with the fused single-kernel path and with the
-three-kernel sequence."""
+the oracle composition, on each of its launch paths."""
 import numpy as np
 import pytest
 import torch
@@ -11,21 +10,26 @@ from gpu_helpers import (EXPAND_ATOL, EXPAND_RTOL, SHRINK_ATOL, SHRINK_RTOL, ass
 
 pytestmark = pytest.mark.gpu
 
-# (LORA_PUNICA_FUSED, LORA_PUNICA_SELF_META, LORA_PUNICA_EXPAND_SELF_SORT):
-# one fused kernel; the default (metadata kernel, then shrink and expand each
-# loading before their grid-dependency wait); the same with the expand
-# sorting the ids itself; the shrink sorting the ids itself and writing the
-# metadata + expand; the plain metadata kernel + shrink + expand.
-PATHS = [pytest.param(("1", "", ""), id="fused"), pytest.param(("0", "", ""), id="early"),
-         pytest.param(("0", "", "1"), id="early_self_sort"),
-         pytest.param(("0", "1", ""), id="two_kernels"),
-         pytest.param(("0", "0", ""), id="three_kernels")]
+# (LORA_PUNICA_COOP, LORA_PUNICA_FUSED, LORA_PUNICA_SELF_META,
+#  LORA_PUNICA_EXPAND_SELF_SORT): one cooperative kernel (metadata, shrink,
+# grid barrier, expand); one cluster kernel; the metadata kernel, then
+# shrink and expand each loading before their grid-dependency wait; the
+# same with the expand sorting the ids itself; the shrink sorting the ids
+# itself and writing the metadata + expand; the plain metadata kernel +
+# shrink + expand.  Batches a path does not take fall through to the next.
+PATHS = [pytest.param(("1", "0", "", ""), id="coop"),
+         pytest.param(("0", "1", "", ""), id="fused"),
+         pytest.param(("0", "0", "", ""), id="early"),
+         pytest.param(("0", "0", "", "1"), id="early_self_sort"),
+         pytest.param(("0", "0", "1", ""), id="two_kernels"),
+         pytest.param(("0", "0", "0", ""), id="three_kernels")]
 
 
 def _set_path(monkeypatch, path):
-    monkeypatch.setenv("LORA_PUNICA_FUSED", path[0])
-    monkeypatch.setenv("LORA_PUNICA_SELF_META", path[1])
-    monkeypatch.setenv("LORA_PUNICA_EXPAND_SELF_SORT", path[2])
+    monkeypatch.setenv("LORA_PUNICA_COOP", path[0])
+    monkeypatch.setenv("LORA_PUNICA_FUSED", path[1])
+    monkeypatch.setenv("LORA_PUNICA_SELF_META", path[2])
+    monkeypatch.setenv("LORA_PUNICA_EXPAND_SELF_SORT", path[3])
 
 
 def _check_linear(oracle_mod, inp, ids=None, buf0=None, L=None):
@@ -52,6 +56,7 @@ def _check_linear(oracle_mod, inp, ids=None, buf0=None, L=None):
     np.testing.assert_array_equal(meta.lora_token_start_loc.cpu().numpy(), o.lora_token_start_loc)
     assert int(meta.error_word.item()) & ~(1 << 30) == o.invalid_ids
     assert int(meta.error_word.item()) & (1 << 30) == 0
+    assert meta.grid_sync.cpu().tolist() == [0, 0]      # barrier words left clean
     if not o.no_lora_flag[0]:
         np.testing.assert_array_equal(meta.token_indices_sorted_by_lora_ids[:T].cpu().numpy(),
                                       o.token_indices_sorted_by_lora_ids[:T])
@@ -130,3 +135,46 @@ def test_linear_repeated_calls_accumulate(oracle_mod):
                            True, inp.lora_bias)
     assert_close(buf.cpu().numpy(), b2, SHRINK_ATOL, SHRINK_RTOL, "buffer after two calls")
     assert_close(bits_to_f64(host_bits(y)), y2, 2 * EXPAND_ATOL, 2 * EXPAND_RTOL, "y after two calls")
+
+
+def test_coop_barrier_timeout_reports_and_recovers(oracle_mod, monkeypatch):
+    """The cooperative kernel's grid barrier is made to wait for one arrival
+    that never comes (a test knob raises the expected count), with a short
+    poll limit: every CTA gives up, bit 30 of the error word is set, the
+    expand is skipped (y untouched), the shrink result is complete and the
+    barrier words are back to zero.  The next call on the same metadata
+    succeeds."""
+    import expand_gemm_gb300 as eg
+    inp = W.generate("decode")
+    w = inp.workload
+    T = w.num_tokens
+    x = dev_bf16(inp.x)
+    A = [dev_bf16(a) for a in inp.lora_a]
+    B = [dev_bf16(b) for b in inp.lora_b]
+    ids = dev_i32(inp.ids)
+    meta = eg.LoRAKernelMeta.make(w.max_loras, T, "cuda")
+    monkeypatch.setenv("LORA_PUNICA_COOP", "1")
+    monkeypatch.setenv("LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS", "1")
+    monkeypatch.setenv("LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES", "20000000")   # ~10 ms
+    y = dev_bf16(inp.y)
+    buf = dev_f32(inp.buf)
+    eg.lora_linear(ids, x, A, B, None, w.scale, buf, y, meta)
+    torch.cuda.synchronize()
+    assert int(meta.error_word.item()) & (1 << 30)
+    assert meta.grid_sync.cpu().tolist() == [0, 0]
+    np.testing.assert_array_equal(host_bits(y), inp.y)
+    ref_buf = oracle_mod.shrink(inp.x, inp.lora_a, inp.ids, w.scale, inp.buf)
+    assert_close(buf.cpu().numpy(), ref_buf, SHRINK_ATOL, SHRINK_RTOL, "buffer after timeout")
+
+    monkeypatch.delenv("LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS")
+    monkeypatch.delenv("LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES")
+    y = dev_bf16(inp.y)
+    buf = dev_f32(inp.buf)
+    eg.lora_linear(ids, x, A, B, None, w.scale, buf, y, meta)
+    torch.cuda.synchronize()
+    assert int(meta.error_word.item()) & (1 << 30) == 0
+    assert meta.grid_sync.cpu().tolist() == [0, 0]
+    assert_close(buf.cpu().numpy(), ref_buf, SHRINK_ATOL, SHRINK_RTOL, "buffer after recovery")
+    ref_y = oracle_mod.expand(ref_buf.astype(np.float32), inp.lora_b, inp.ids, inp.y, w.slices,
+                              0, True)
+    assert_close(bits_to_f64(host_bits(y)), ref_y, EXPAND_ATOL, EXPAND_RTOL, "y after recovery")
