@@ -37,15 +37,25 @@ METRIC = "LoRA shrink+expand tokens/s and effective HBM GB/s (% of roofline), 1 
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
-# the committed ncu summaries, keyed by kernel and the sha256 of the kernel
-# source they were taken on; a stale hash reports traffic as null.
+# the committed ncu summaries, keyed by (kernel, workload) and the hash of
+# the kernel's sources they were taken on; a stale hash reports null.
 NCU_TRAFFIC = {}
 
+# The source files each reported kernel is built from.
+KERNEL_SOURCES = {
+    "expand": ("lora_expand.cu", "lora_expand.cuh", "lora_common.cuh"),
+    "shrink": ("lora_shrink.cu", "lora_shrink_umma.cu", "lora_umma.cuh", "lora_common.cuh"),
+    "linear_coop": ("lora_linear_coop.cu", "lora_expand.cuh", "lora_common.cuh"),
+    "linear_fused": ("lora_fused.cu", "lora_common.cuh"),
+}
 
-def _src_hash(name: str) -> str:
-    p = os.path.join(ROOT, "expand_gemm_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+def _src_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "expand_gemm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def parse_args():
@@ -54,6 +64,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--workload", default="decode", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--num-tokens", type=int, default=None,
+                    help="a smaller case of the workload (profiling captures)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--kernel-seconds", type=float, default=0.5,
@@ -216,6 +228,9 @@ def run_ours(args, rank, world):
         dist.init_process_group("nccl", device_id=dev)
 
     w = W.WORKLOADS[args.workload]
+    if args.num_tokens is not None:
+        from dataclasses import replace
+        w = replace(w, num_tokens=args.num_tokens, n_decode=min(w.n_decode, args.num_tokens))
     inp = W.generate(w)
     ub = W.unique_bytes(w, inp.ids)
     props = torch.cuda.get_device_properties(dev)
@@ -356,17 +371,16 @@ def run_ours(args, rank, world):
     fused = (fused_path(w) and not emb) or coop
     if coop:
         # the whole step is one kernel: its bytes are the step's bytes
-        dominant, dom_bytes, dom_ms, src = ("linear_coop", step_bytes, k_step,
-                                            "lora_linear_coop.cu")
+        dominant, dom_bytes, dom_ms = "linear_coop", step_bytes, k_step
     elif fused:
-        dominant, dom_bytes, dom_ms, src = "linear_fused", step_bytes, k_step, "lora_fused.cu"
+        dominant, dom_bytes, dom_ms = "linear_fused", step_bytes, k_step
     else:
         dominant = "expand" if k_expand >= k_shrink else "shrink"
         dom_bytes, dom_ms = ub[dominant], kern[dominant]
-        src = {"shrink": "lora_shrink.cu", "expand": "lora_expand.cu"}[dominant]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     tr = NCU_TRAFFIC.get((dominant, args.workload))
-    traffic = tr[1] if (tr and tr[0] == _src_hash(src)) else None
+    traffic = tr[1] if (tr and tr[0] == _src_hash(dominant)
+                        and args.num_tokens is None) else None
     out = {
         "metric": METRIC,
         "value": value,
@@ -381,7 +395,9 @@ def run_ours(args, rank, world):
         "dtype": "bf16",
         "data": "synthetic (seeded numpy PCG64; no dataset or weights)",
         "config": {
-            "workload": "%s: %s" % (w.name, w.description),
+            "workload": "%s: %s%s" % (w.name, w.description,
+                                      "" if args.num_tokens is None else
+                                      " (this run: %d tokens)" % w.num_tokens),
             "num_tokens": T, "active_tokens": ub["t_active"], "distinct_loras": ub["distinct"],
             "hidden": w.hidden, "rank": w.rank, "max_loras": w.max_loras,
             "slices": list(w.slices), "bias": w.bias, "scale": w.scale,
@@ -516,6 +532,9 @@ def run_reference(args, rank, world):
     import oracle
     oracle.build()
     w = W.WORKLOADS[args.workload]
+    if args.num_tokens is not None:
+        from dataclasses import replace
+        w = replace(w, num_tokens=args.num_tokens, n_decode=min(w.n_decode, args.num_tokens))
     inp = W.generate(w)
     T = w.num_tokens
     sel = np.arange(min(T, 16))

@@ -70,7 +70,13 @@ struct ExpandTile {
     static constexpr int MI = WM / 16;
     static constexpr int NI = WN / 8;
     static constexpr int YCH = BN / 8;                 // 16-byte chunks per y row
-    static constexpr int Y_LD = BN * 2 + 16;           // padded shared y row (bytes)
+    // DIRECT epilogue (128-column chunks): each thread's accumulators cover 8
+    // contiguous columns (B rows stored permuted, see b_slot) and leave with
+    // 16-byte stores straight to global memory.  Otherwise (64-column chunks,
+    // rank 128, measured faster): the tile is rounded in place in shared
+    // memory and written back row by row.
+    static constexpr bool DIRECT = (BN == 128);
+    static constexpr int Y_LD = DIRECT ? BN * 2 : BN * 2 + 16;   // shared y row (bytes)
     static constexpr int Y_BYTES = EX_BM * Y_LD;
     static constexpr int B_BYTES = BN * RP * 2;
     static constexpr int BIAS_BYTES = BN * 2;                // bf16 bias chunk
@@ -85,7 +91,7 @@ struct ExpandTile {
     static constexpr int Y_PASSES = EX_BM / Y_RPP;
     static constexpr int B_RPP = EX_THREADS / CPR;
     static constexpr int B_PASSES = (BN + B_RPP - 1) / B_RPP;
-    static_assert(WN == 32 && MI >= 1, "warp tile");
+    static_assert(WN == 32 && NI == 4 && MI >= 1, "warp tile: 8 output columns per thread");
     static_assert(EX_THREADS % YCH == 0 && EX_BM % Y_RPP == 0, "y copy shape");
     static_assert(EX_THREADS % CPR == 0 && B_RPP % 8 == 0, "B copy shape (swizzle period)");
 };
@@ -103,6 +109,26 @@ inline size_t expand_smem_bytes(int kt, int nbins)
     default: t = ExpandTile<8>::BYTES; break;
     }
     return t + seg_tab_bytes(nbins);
+}
+
+// 16-byte piece `chunk` of shared y-tile row `row`: odd rows swap the two
+// halves of every 8-piece group, so the two rows a quarter-warp reads with
+// 16-byte loads fall in disjoint banks.
+__device__ __forceinline__ int ysw(int row, int chunk)
+{
+    return chunk ^ ((row & 1) << 2);
+}
+
+// Shared row of B row (output column) r of a chunk.  Within each 32-column
+// warp block, column q * 8 + 2n + e (q, n < 4, e < 2) goes to row
+// n * 8 + 2q + e: the MMA's n-tile n then reads, as its columns 2q + e, the
+// output columns q * 8 + 2n + e, so each thread's accumulators cover 8
+// contiguous columns.  The reads stay on 8 consecutive rows (conflict-free
+// under swz).
+__device__ __forceinline__ int b_slot(int r)
+{
+    const int l = r & 31;
+    return (r & ~31) | (((l >> 1) & 3) << 3) | ((l >> 3) << 1) | (l & 1);
 }
 
 // Host: checks the arguments of an expand call and fills `p` (the layout
@@ -182,11 +208,10 @@ __device__ __forceinline__ void expand_items(const ExpandArgs &p, SegTab tab,
 #pragma unroll
         for (int j = 0; j < Cfg::Y_PASSES; ++j) ytok[j] = s_tok[yr0 + j * Cfg::Y_RPP];
         uint16_t *const ybase = yslice + ycc * 8;
-        const uint32_t y_soff = yr0 * Cfg::Y_LD + ycc * 16;
+        const uint32_t y_soff = yr0 * Cfg::Y_LD + (Cfg::DIRECT ? ysw(yr0, ycc) : ycc) * 16;
         const int bcc = tid % CPR, br0 = tid / CPR;
         const bool b_kin = bcc * 8 < R;
         const uint16_t *brow = bslice + int64_t(br0) * R + bcc * 8;
-        const uint32_t b_soff = swz<CPR>(br0, bcc);
 
         auto load_chunk = [&](int slot, int c) {
             const int c0 = (c - p.chunk0[s]) * BN;
@@ -208,7 +233,7 @@ __device__ __forceinline__ void expand_items(const ExpandArgs &p, SegTab tab,
                 const int r = br0 + j * Cfg::B_RPP;
                 if (Cfg::B_PASSES * Cfg::B_RPP > BN && r >= BN) break;
                 const bool ok = b_kin && r < ncols;
-                cp_async16(sb + b_soff + j * Cfg::B_RPP * CPR * 16,
+                cp_async16(sb + swz<CPR>(Cfg::DIRECT ? b_slot(r) : r, bcc),
                            ok ? bc + int64_t(j) * Cfg::B_RPP * R : p.b[s], ok);
             }
             if (bias_row != nullptr && p.bias_vec && tid < BN / 8) {
@@ -283,6 +308,14 @@ __device__ __forceinline__ void expand_items(const ExpandArgs &p, SegTab tab,
             uint8_t *sy = smem + slot * Cfg::STAGE_BYTES;
             const uint32_t sb = ring + slot * Cfg::STAGE_BYTES + Cfg::Y_BYTES;
 
+            // This thread's output column for n-tile n, pair element e: in the
+            // DIRECT layout colw + 2n + e (8 contiguous ones), else the MMA's
+            // own n * 8 + 2 (lane % 4) + e.
+            const int colw = wn * Cfg::WN + (lane & 3) * 8;
+            auto out_col = [&](int n, int e) {
+                return Cfg::DIRECT ? colw + 2 * n + e : wn * Cfg::WN + n * 8 + 2 * (lane & 3) + e;
+            };
+
             // bias of this chunk: staged with the chunk when aligned, else read here
             float bv[NI][2];
             const uint16_t *sbias = reinterpret_cast<const uint16_t *>(
@@ -291,7 +324,7 @@ __device__ __forceinline__ void expand_items(const ExpandArgs &p, SegTab tab,
             for (int n = 0; n < NI; ++n)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int c = wn * Cfg::WN + n * 8 + 2 * (lane & 3) + h;
+                    const int c = out_col(n, h);
                     float b = 0.f;
                     if (bias_row != nullptr && c < ncols)
                         b = bf16_to_f32(p.bias_vec ? sbias[c] : bias_row[c0 + c]);
@@ -306,6 +339,9 @@ __device__ __forceinline__ void expand_items(const ExpandArgs &p, SegTab tab,
                 for (int n = 0; n < NI; ++n)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) acc[m][n][q] = bv[n][q & 1];
+            // B operand (DIRECT: shared row j of n-tile n holds the B row that
+            // b_slot maps there, so the thread that gets C columns 2q, 2q + 1
+            // of every n-tile holds the output columns colw .. colw + 7).
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk)
 #pragma unroll
@@ -322,7 +358,46 @@ __device__ __forceinline__ void expand_items(const ExpandArgs &p, SegTab tab,
                     }
                 }
 
-            if (p.vec) {
+            if (Cfg::DIRECT && p.vec) {
+                // per row: old y (one 16-byte shared load) + product + bias,
+                // rounded once, one 16-byte store straight to global memory
+                if (colw < ncols) {
+#pragma unroll
+                    for (int m = 0; m < MI; ++m)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int r = wm * Cfg::WM + m * 16 + (lane >> 2) + 8 * h;
+                            const int tok = s_tok[r];
+                            if (tok < 0) continue;
+                            float v[2 * NI];
+#pragma unroll
+                            for (int n = 0; n < NI; ++n) {
+                                v[2 * n] = acc[m][n][2 * h];
+                                v[2 * n + 1] = acc[m][n][2 * h + 1];
+                            }
+                            if (p.add_inputs) {
+                                const uint4 old = *reinterpret_cast<const uint4 *>(
+                                    sy + r * Cfg::Y_LD + ysw(r, colw >> 3) * 16);
+                                v[0] += bf16_lo(old.x);
+                                v[1] += bf16_hi(old.x);
+                                v[2] += bf16_lo(old.y);
+                                v[3] += bf16_hi(old.y);
+                                v[4] += bf16_lo(old.z);
+                                v[5] += bf16_hi(old.z);
+                                v[6] += bf16_lo(old.w);
+                                v[7] += bf16_hi(old.w);
+                            }
+                            uint4 out;
+                            out.x = pack_bf16x2(v[0], v[1]);
+                            out.y = pack_bf16x2(v[2], v[3]);
+                            out.z = pack_bf16x2(v[4], v[5]);
+                            out.w = pack_bf16x2(v[6], v[7]);
+                            *reinterpret_cast<uint4 *>(yslice + int64_t(tok) * p.y_ld + c0 + colw) =
+                                out;
+                        }
+                }
+            } else if (p.vec) {
+                // round in place in the shared tile, then whole rows out
 #pragma unroll
                 for (int m = 0; m < MI; ++m)
 #pragma unroll
@@ -330,8 +405,8 @@ __device__ __forceinline__ void expand_items(const ExpandArgs &p, SegTab tab,
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const int r = wm * Cfg::WM + m * 16 + (lane >> 2) + 8 * h;
-                            const int c = wn * Cfg::WN + n * 8 + 2 * (lane & 3);
-                            uint32_t *cell = reinterpret_cast<uint32_t *>(sy + r * Cfg::Y_LD + c * 2);
+                            uint32_t *cell = reinterpret_cast<uint32_t *>(
+                                sy + r * Cfg::Y_LD + out_col(n, 0) * 2);
                             float v0 = acc[m][n][2 * h];
                             float v1 = acc[m][n][2 * h + 1];
                             if (p.add_inputs) {
@@ -359,7 +434,7 @@ __device__ __forceinline__ void expand_items(const ExpandArgs &p, SegTab tab,
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const int r = wm * Cfg::WM + m * 16 + (lane >> 2) + 8 * (q >> 1);
-                            const int c = wn * Cfg::WN + n * 8 + 2 * (lane & 3) + (q & 1);
+                            const int c = out_col(n, q & 1);
                             const int tok = s_tok[r];
                             if (tok < 0 || c >= ncols) continue;
                             uint16_t *dst = yslice + int64_t(tok) * p.y_ld + c0 + c;
