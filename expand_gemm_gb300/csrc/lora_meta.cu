@@ -1,7 +1,8 @@
 // lora_meta.cu -- metadata step (page "vllm.lora.ops.triton_ops.
 // lora_kernel_metadata", LoRAKernelMeta._reset + prepare_tensors) as one
-// single-CTA kernel: per-warp bin histograms built with __match_any_sync,
-// a warp-shuffle scan over (bin, warp), and a stable counting-sort scatter.
+// single-CTA kernel: the id map staged in shared memory, per-warp bin
+// histograms built with __match_any_sync, a warp-shuffle scan over
+// (bin, warp), and a stable counting-sort scatter.
 //
 // Bins: bin 0 holds id -1 (and every invalid id), bin b > 0 holds id b - 1.
 // Token order inside a bin is preserved because (1) each warp owns one
@@ -15,6 +16,10 @@ namespace lora {
 
 constexpr int META_THREADS = 1024;
 constexpr int META_WARPS = META_THREADS / 32;
+// Batches up to this many tokens are first copied into shared memory with
+// one block-wide load (all of it in flight at once); both passes then read
+// shared memory.  Larger batches read the map from global memory.
+constexpr int META_STAGE_MAX = 16384;
 
 struct MetaArgs {
     const int32_t *map;
@@ -29,10 +34,11 @@ struct MetaArgs {
     int32_t *error_word;
 };
 
-size_t meta_smem_bytes(int max_loras)
+size_t meta_smem_bytes(int max_loras, int num_tokens)
 {
     const size_t nb = size_t(max_loras) + 1;
-    return (META_WARPS * nb + 3 * nb) * sizeof(int32_t);
+    const size_t staged = num_tokens <= META_STAGE_MAX ? size_t(num_tokens) : 0;
+    return (META_WARPS * nb + 3 * nb + staged) * sizeof(int32_t);
 }
 
 // Bin of one token; counts an invalid id into `bad`.
@@ -51,6 +57,7 @@ __global__ void __launch_bounds__(META_THREADS, 1) meta_prepare_kernel(MetaArgs 
     int32_t *tot = cnt + META_WARPS * nb;       // [nb] tokens per bin
     int32_t *base = tot + nb;                   // [nb] first sorted slot of the bin
     int32_t *pos = base + nb;                   // [nb] index among non-empty bins
+    int32_t *ids_s = pos + nb;                  // [T] the map, when staged
     __shared__ int32_t s_invalid, s_nactive;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -59,6 +66,10 @@ __global__ void __launch_bounds__(META_THREADS, 1) meta_prepare_kernel(MetaArgs 
     pdl_wait();
     pdl_launch_dependents();
 
+    const bool staged = T <= META_STAGE_MAX;
+    if (staged)
+        for (int t = tid; t < T; t += META_THREADS) ids_s[t] = a.map[t];
+    const int32_t *ids = staged ? ids_s : a.map;
     for (int i = tid; i < META_WARPS * nb; i += META_THREADS) cnt[i] = 0;
     if (tid == 0) s_invalid = 0;
     __syncthreads();
@@ -74,7 +85,7 @@ __global__ void __launch_bounds__(META_THREADS, 1) meta_prepare_kernel(MetaArgs 
     for (int g = t0; g < t1; g += 32) {
         const int t = g + lane;
         const bool has = t < t1;
-        const int b = has ? token_bin(a.map[t], a.max_loras, bad) : -1;
+        const int b = has ? token_bin(ids[t], a.max_loras, bad) : -1;
         const unsigned grp = __match_any_sync(0xffffffffu, b);
         if (has && lane == __ffs(grp) - 1) cnt[warp * nb + b] += __popc(grp);
     }
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(META_THREADS, 1) meta_prepare_kernel(MetaArgs 
     for (int g = t0; g < t1; g += 32) {
         const int t = g + lane;
         const bool has = t < t1;
-        const int32_t id = has ? a.map[t] : -1;
+        const int32_t id = has ? ids[t] : -1;
         const int b = has ? token_bin(id, a.max_loras, unused) : -1;
         const unsigned grp = __match_any_sync(0xffffffffu, b);
         const int rank = __popc(grp & ((1u << lane) - 1u));
@@ -175,9 +186,9 @@ int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return int(e);
-    const size_t smem = meta_smem_bytes(a.max_loras);
+    const size_t smem = meta_smem_bytes(a.max_loras, a.num_tokens);
     if (dev < 64 && configured_smem[dev] < int(smem)) {
-        const int want = int(meta_smem_bytes(LORA_MAX_LORAS));
+        const int want = int(meta_smem_bytes(LORA_MAX_LORAS, META_STAGE_MAX));
         e = cudaFuncSetAttribute(meta_prepare_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, want);
         if (e != cudaSuccess) return int(e);
