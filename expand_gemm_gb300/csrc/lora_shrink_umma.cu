@@ -3,7 +3,9 @@
 // "vllm.lora.punica_wrapper.punica_gpu", PunicaWrapperGPU.add_shrink:
 // y[s][t, :] += scale * x[t, :] @ A[s][id(t)]^T).
 //
-// One CTA per SM, persistent over tiles; warp-specialised:
+// One CTA per SM, persistent over (tile, hidden chunk) items: the hidden
+// dimension is split when there are too few whole tiles to fill the GPU
+// (see umma_kchunks).  Warp-specialised:
 //   warp 0      producer: per 64-wide hidden block, the tile's 128 x rows
 //               arrive by 2-D TMA: the tile's tokens (increasing, as the
 //               sort is stable) are cut into runs of consecutive tokens and
@@ -19,7 +21,8 @@
 //               a tile, to hand the accumulators to the epilogue.
 //   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (one token row
 //               per thread), buf[s][t, :] += scale * acc with float4
-//               read-modify-writes (every row has one owner: no atomics).
+//               read-modify-writes, or float4 atomic adds when the tile's
+//               hidden dimension is split over several CTAs.
 // x is read once per tile for all slices; the A block of a LoRA is shared in
 // L2 by the CTAs working on tiles of the same segment.
 //
@@ -40,6 +43,7 @@ constexpr int UM_MAX_STAGES = 8;
 constexpr int UM_SMEM_BUDGET = 200 * 1024;
 constexpr long long UM_TIMEOUT_CYCLES = 2000000000ll;
 constexpr int UM_ERROR_BIT = 1 << 30;
+constexpr int UM_MIN_BLOCKS = 8;      // shortest hidden chunk of a split item
 
 struct UmmaShrinkArgs {
     CUtensorMap map_x[UM_XMAPS];               // x: [T, H], box {64, 2^i rows}
@@ -65,6 +69,27 @@ struct UmmaShrinkArgs {
 struct UmmaLayout {
     int x_bytes, a_bytes, stage_bytes, ring_bytes, bar_off, misc_off, piece_off, tab_off, total;
 };
+
+// Split of the hidden dimension: the number of chunks (items per tile)
+// that minimises rounds x chunk length (+ a fixed cost of about two blocks
+// per item for the pipeline fill and the epilogue), with chunks of at least
+// UM_MIN_BLOCKS blocks.  Every CTA computes the same value.
+__device__ __forceinline__ int umma_kchunks(int tiles, int nk, int grid)
+{
+    int best = 1;
+    long long best_cost = (long long)((tiles + grid - 1) / grid) * (nk + 2);
+    for (int kc = 2; kc <= 16 && nk / kc >= UM_MIN_BLOCKS; ++kc) {
+        const int spc = (nk + kc - 1) / kc;
+        const int kce = (nk + spc - 1) / spc;
+        const long long rounds = ((long long)tiles * kce + grid - 1) / grid;
+        const long long cost = rounds * (spc + 2);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = kce;
+        }
+    }
+    return best;
+}
 
 __host__ __device__ inline UmmaLayout umma_layout(int S, int rp, int stages, int nbins)
 {
@@ -120,7 +145,13 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     // Full 128-token tiles only: a segment of c tokens contributes c / 128.
     const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
                                           p.nbins, UM_BM, tab, /*full_tiles_only=*/true);
-    if (total_tiles == 0 || int(blockIdx.x) >= total_tiles) return;
+    const int H = p.hidden, R = p.rank, T = p.num_tokens;
+    const int nk = (H + UM_BK - 1) / UM_BK;
+    const int kchunks = umma_kchunks(total_tiles, nk, int(gridDim.x));
+    const int spc = (nk + kchunks - 1) / kchunks;
+    const bool split = kchunks > 1;
+    const int total_items = total_tiles * kchunks;      // item = kc * total_tiles + tile
+    if (total_tiles == 0 || int(blockIdx.x) >= total_items) return;
 
     if (warp == UM_MMA_WARP) tmem_alloc(smem_addr(s_tmem), p.tmem_cols);
     tc_fence_before();
@@ -128,8 +159,6 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    const int H = p.hidden, R = p.rank, T = p.num_tokens;
-    const int nk = (H + UM_BK - 1) / UM_BK;
     const long long deadline = clock64() + UM_TIMEOUT_CYCLES;
 
     if (warp == 0) {
@@ -146,7 +175,9 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
         uint32_t phase = 0;
         int issued = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x) {
+            const int tile = item % total_tiles, kc = item / total_tiles;
+            const int kb0 = kc * spc, kb1 = min(nk, kb0 + spc);
             const int seg = find_segment(tab.tile, p.nbins, tile);
             const int id = tab.id[seg];
             const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * UM_BM;
@@ -166,7 +197,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
             }
             npieces = __shfl_sync(0xffffffffu, npieces, 0);
             __syncwarp();
-            for (int kb = 0; kb < nk; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 bool got = mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, s_abort, deadline);
                 if (__all_sync(0xffffffffu, got) == 0) {
                     ok = false;
@@ -207,13 +238,15 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x) {
+                const int kc = item / total_tiles;
+                const int kb0 = kc * spc, kb1 = min(nk, kb0 + spc);
                 if (!mbar_wait_bounded(bar_acc_empty, acc_phase ^ 1, s_abort, deadline)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_bounded(bar_full + 8 * stage, phase, s_abort, deadline)) {
                         ok = false;
                         break;
@@ -225,7 +258,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
                         const uint64_t adesc = umma_desc_sw128(sx + kk * 32);
                         for (int s = 0; s < S; ++s) {
                             const uint64_t bdesc = umma_desc_sw128(sx + L.x_bytes + s * L.a_bytes + kk * 32);
-                            umma_bf16(tmem + s * RP, adesc, bdesc, idesc, (kb | kk) != 0);
+                            umma_bf16(tmem + s * RP, adesc, bdesc, idesc, kb != kb0 || kk != 0);
                         }
                     }
                     umma_commit(bar_empty + 8 * stage);
@@ -250,7 +283,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         const int row = q * 32 + lane;          // token row inside the tile
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+            const int tile = item % total_tiles;
             const int seg = find_segment(tab.tile, p.nbins, tile);
             const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * UM_BM;
             const int tok = p.sorted[row0 + row];
@@ -266,12 +300,18 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
                     for (int j = 0; j < 16; j += 4) {
                         if (c + j < R) {
                             float4 *d4 = reinterpret_cast<float4 *>(dst + c + j);
-                            float4 o = *d4;
-                            o.x += p.scale * v[j];
-                            o.y += p.scale * v[j + 1];
-                            o.z += p.scale * v[j + 2];
-                            o.w += p.scale * v[j + 3];
-                            *d4 = o;
+                            const float4 a = make_float4(p.scale * v[j], p.scale * v[j + 1],
+                                                         p.scale * v[j + 2], p.scale * v[j + 3]);
+                            if (split) {
+                                atomicAdd(d4, a);
+                            } else {
+                                float4 o = *d4;
+                                o.x += a.x;
+                                o.y += a.y;
+                                o.z += a.z;
+                                o.w += a.w;
+                                *d4 = o;
+                            }
                         }
                     }
                 }
