@@ -39,7 +39,11 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # the committed ncu summaries, keyed by (kernel, workload) and the hash of
 # the kernel's sources they were taken on; a stale hash reports null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/expand_decode_ncu.md: reads 8.914 MB, writes 0 (the y writes
+    # stay in L2 past the end of the launch)
+    ("expand", "decode"): ("6be756206cd60265", 8914176),
+}
 
 # The source files each reported kernel is built from.
 KERNEL_SOURCES = {
