@@ -308,9 +308,13 @@ static int launch_shrink_mt(const ShrinkArgs &p, cudaStream_t stream)
     }
     const size_t used = shrink_smem_bytes(MT, p.nbins) +
                         (p.map != nullptr ? shrink_self_meta_bytes(p.nbins) : 0);
-    // In early mode (small batches inside lora_linear) at most three CTAs
-    // per SM, so that the expand that follows finds room to start loading.
-    if (p.early) grid = min(grid, 3 * device_sm_count());
+    // In early mode (small batches inside lora_linear) at most
+    // LORA_PUNICA_EARLY_SHRINK_CTAS CTAs per SM, so that one CTA of the
+    // expand that follows fits beside them and starts loading.  Two was
+    // measured best on 256-token q/k/v decode (14.9 us a step, against 15.3
+    // with one and 15.4 with three).
+    if (p.early)
+        grid = min(grid, max(1, env_int("LORA_PUNICA_EARLY_SHRINK_CTAS", 2)) * device_sm_count());
     e = launch_kernel(shrink_kernel<MT>, dim3(grid), dim3(SH_THREADS), used, stream, p);
     return int(e);
 }

@@ -50,7 +50,9 @@ def _check(ids: np.ndarray, L: int, oracle_mod, max_tokens=None):
     (0, 1, 1, 0.0), (1, 31, 3, 0.2), (2, 32, 4, 0.0), (3, 33, 4, 0.5),
     (4, 1000, 7, 0.1), (5, 1023, 16, 0.0), (6, 1025, 64, 0.3), (7, 4097, 2, 0.9),
     (8, 16384, 64, 0.2), (9, 65536, 1024, 0.05), (10, 70001, 300, 0.0),
-    (11, 5, 1024, 0.0)])
+    (11, 5, 1024, 0.0),
+    (12, 16384, 1024, 0.1),     # the largest batch the kernel stages in shared memory
+    (13, 16385, 1024, 0.1)])    # one past it: read from global memory
 def test_meta_random_maps(oracle_mod, seed, T, L, p_none):
     rng = np.random.default_rng(seed)
     ids = rng.integers(0, L, size=T).astype(np.int32)

@@ -266,3 +266,17 @@ def test_add_lora_linear_matches_oracle_composition(oracle_mod, name, T):
     buf = oracle_mod.shrink(inp.x, inp.lora_a, inp.ids, w.scale, inp.buf).astype(np.float32)
     ref = oracle_mod.expand(buf, inp.lora_b, inp.ids, inp.y, w.slices, 0, True, inp.lora_bias)
     assert_close(bits_to_f64(host_bits(y)), ref, EXPAND_ATOL, EXPAND_RTOL, "add_lora_linear")
+
+
+def test_shrink_expand_every_lora_of_the_largest_table(oracle_mod):
+    """max_loras = LORA_MAX_LORAS (1025 bins) with every id in use and ids
+    spread over the batch: the segment tables hold all bins."""
+    import expand_gemm_gb300 as eg
+    L = eg.LORA_MAX_LORAS
+    rng = np.random.default_rng(1024)
+    T = 3000
+    ids = rng.permutation(np.concatenate([np.arange(L), rng.integers(-1, L, T - L)]))
+    inp = _custom(T, 64, 16, L, [64, 24], seed=77, bias=True)
+    inp.ids[:] = ids.astype(np.int32)
+    _shrink_case(oracle_mod, inp, scale=0.5)
+    _expand_case(oracle_mod, inp)
