@@ -62,7 +62,7 @@ def _src_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
@@ -75,7 +75,7 @@ def parse_args():
     ap.add_argument("--kernel-seconds", type=float, default=0.5,
                     help="minimum timed seconds per kernel in the per-kernel loops")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def peaks():
@@ -176,6 +176,25 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(self.rows)}
+
+
+# ------------------------------------------------------ multi-rank host logic
+
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest `value` over all ranks (the timed region of the slowest
+    replica); the value itself when there is no process group."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every rank runs its own replica of the step, so
+    the job processes world x tokens per step in the slowest rank's time."""
+    return world * tokens_per_step * steps / (elapsed_ms / 1e3)
 
 
 # ------------------------------------------------------------ GPU arm
@@ -309,11 +328,7 @@ def run_ours(args, rank, world):
     wall = time.perf_counter() - t_wall
     if dist:
         dist.barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
 
     # ---- per-kernel timing: graphs of one kernel over the rotation
     def time_kernel(make, min_s):
@@ -362,7 +377,7 @@ def run_ours(args, rank, world):
 
     T = w.num_tokens
     ms_per_step = elapsed_ms / args.steps
-    value = world * T * args.steps / (elapsed_ms / 1e3)
+    value = job_tokens_per_s(world, T, args.steps, elapsed_ms)
     hbm, peak_src = peaks()
     kern = {"meta": k_meta, "shrink": k_shrink, "expand": k_expand,
             ("embedding_step" if emb else "lora_linear"): k_step}

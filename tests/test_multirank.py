@@ -1,0 +1,59 @@
+"""The N > 1 host logic of bench.py, on CPU with two gloo ranks: replicas
+only, so the only exchange is the max-over-ranks of the timed region, the
+job's value counts every replica, and the reference arm runs on rank 0
+alone (the other ranks exit without work)."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        elapsed = [12.5, 20.0][rank]
+        out[rank] = {"max": bench.max_over_ranks(elapsed, dist, "cpu"),
+                     "value": bench.job_tokens_per_s(world, 256, 10,
+                                                     bench.max_over_ranks(elapsed, dist, "cpu"))}
+        args = bench.parse_args(["--impl", "reference", "--workload", "tiny", "--steps", "3",
+                                 "--warmup", "3"])
+        res = bench.run_reference(args, rank, world)
+        out[rank] = dict(out[rank], ref=None if res is None else res["impl"])
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_max_time_and_aggregate_value():
+    world = 2
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world,
+                           start_method="spawn")
+        res = dict(out)
+    for r in range(world):
+        assert res[r]["max"] == 20.0                    # the slowest replica's time
+        assert res[r]["value"] == pytest.approx(2 * 256 * 10 / 0.020)
+        assert res[r]["ref"] == ("reference" if r == 0 else None)   # rank 0 alone
+
+
+def test_single_process_helpers():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5) == 3.5
+    assert bench.job_tokens_per_s(1, 256, 100, 10.0) == pytest.approx(256 * 100 / 0.010)
