@@ -281,10 +281,16 @@ int expand_early(const float *x, const lora_bf16_t *const *lora_b,
                  int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st,
                  const int32_t *map)
 {
-    const bool self_sort = map != nullptr && num_tokens <= EX_SELF_SORT_MAX_TOKENS &&
-                           meta->max_loras <= EX_SELF_SORT_MAX_LORAS;
+    // With `map` the caller asks the expand to sort the ids itself (its
+    // predecessor may be the kernel that writes the metadata).  When the
+    // batch is too large for that, it runs in plain mode: everything is read
+    // after the grid-dependency wait.
+    if (map != nullptr && (num_tokens > EX_SELF_SORT_MAX_TOKENS ||
+                           meta->max_loras > EX_SELF_SORT_MAX_LORAS))
+        return lora_expand_impl(x, 0, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
+                                num_tokens, 0, 1, meta, st, 0, nullptr);
     return lora_expand_impl(x, 0, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
-                            num_tokens, 0, 1, meta, st, 1, self_sort ? map : nullptr);
+                            num_tokens, 0, 1, meta, st, 1, map);
 }
 
 }  // namespace lora

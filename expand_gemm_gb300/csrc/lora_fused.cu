@@ -774,10 +774,16 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
     const int self_meta = lora::env_int("LORA_PUNICA_SELF_META", -1);
     int r = 0;
     bool early = false;
-    if (self_meta == 1) {
+    if (self_meta == 1 || self_meta == 2) {
+        // =2: the expand too sorts the ids itself and starts (sorting,
+        // fetching y and B) while the shrink runs; it reads nothing the
+        // shrink writes but the buffer, after its grid-dependency wait.
         r = lora::shrink_self_meta(token_lora_mapping, x, num_tokens, hidden, x_ld, lora_a,
-                                   num_slices, rank, buf, meta, scale, st, 0);
+                                   num_slices, rank, buf, meta, scale, st, self_meta == 2 ? 2 : 0);
         if (r < 0 || r > 1) return r;
+        if (r == 1 && self_meta == 2)
+            return lora::expand_early(buf, lora_b, lora_bias, slice_sizes, num_slices, rank, y,
+                                      y_ld, num_tokens, meta, st, token_lora_mapping);
     } else if (self_meta == -1) {
         r = lora_meta_prepare(token_lora_mapping, num_tokens, meta, stream);
         if (r != 0) return r;

@@ -60,6 +60,7 @@ struct ShrinkArgs {
     // nothing the metadata kernel writes; it lets its own dependents launch
     // only after that wait, which is what lora_linear's expand relies on.
     int32_t early;
+    int32_t leave_room;            // cap the grid like early mode (the next kernel starts early)
 };
 
 constexpr int SH_SELF_META_MAX_TOKENS = 512;
@@ -313,7 +314,7 @@ static int launch_shrink_mt(const ShrinkArgs &p, cudaStream_t stream)
     // expand that follows fits beside them and starts loading.  Two was
     // measured best on 256-token q/k/v decode (14.9 us a step, against 15.3
     // with one and 15.4 with three).
-    if (p.early)
+    if (p.early || p.leave_room)
         grid = min(grid, max(1, env_int("LORA_PUNICA_EARLY_SHRINK_CTAS", 2)) * device_sm_count());
     e = launch_kernel(shrink_kernel<MT>, dim3(grid), dim3(SH_THREADS), used, stream, p);
     return int(e);
@@ -366,6 +367,7 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
     p.map = nullptr;
     p.write_meta = 0;
     p.early = 0;
+    p.leave_room = 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -459,9 +461,12 @@ int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_token
     p.active_out = meta->active_lora_ids;
     p.no_lora_out = meta->no_lora_flag;
     p.error_out = meta->error_word;
-    // early: the metadata kernel writes the buffers; otherwise CTA 0 does
-    p.write_meta = early ? 0 : 1;
-    p.early = early ? 1 : 0;
+    // early == 1: the metadata kernel writes the buffers, and the loads start
+    // before the grid-dependency wait.  Otherwise CTA 0 writes them; with
+    // early == 2 the grid also leaves room for an early-starting expand.
+    p.write_meta = early == 1 ? 0 : 1;
+    p.early = early == 1 ? 1 : 0;
+    p.leave_room = early == 2 ? 1 : 0;
     int r;
     if (rank <= 16) r = launch_shrink_mt<1>(p, st);
     else if (rank <= 32) r = launch_shrink_mt<2>(p, st);

@@ -15,13 +15,15 @@ pytestmark = pytest.mark.gpu
 # grid barrier, expand); one cluster kernel; the metadata kernel, then
 # shrink and expand each loading before their grid-dependency wait; the
 # same with the expand sorting the ids itself; the shrink sorting the ids
-# itself and writing the metadata + expand; the plain metadata kernel +
+# itself and writing the metadata + expand (plain, or also sorting the ids
+# itself and starting early); the plain metadata kernel +
 # shrink + expand.  Batches a path does not take fall through to the next.
 PATHS = [pytest.param(("1", "0", "", ""), id="coop"),
          pytest.param(("0", "1", "", ""), id="fused"),
          pytest.param(("0", "0", "", ""), id="early"),
          pytest.param(("0", "0", "", "1"), id="early_self_sort"),
          pytest.param(("0", "0", "1", ""), id="two_kernels"),
+         pytest.param(("0", "0", "2", ""), id="two_kernels_self_sort"),
          pytest.param(("0", "0", "0", ""), id="three_kernels")]
 
 
