@@ -76,13 +76,14 @@ struct UmmaLayout {
 // UM_MIN_BLOCKS blocks.  Every CTA computes the same value.
 __device__ __forceinline__ int umma_kchunks(int tiles, int nk, int grid)
 {
+    // 32-bit arithmetic: tiles * 16 and nk are far below 2^31 (T < 2^21).
     int best = 1;
-    long long best_cost = (long long)((tiles + grid - 1) / grid) * (nk + 2);
+    int best_cost = ((tiles + grid - 1) / grid) * (nk + 2);
     for (int kc = 2; kc <= 16 && nk / kc >= UM_MIN_BLOCKS; ++kc) {
         const int spc = (nk + kc - 1) / kc;
         const int kce = (nk + spc - 1) / spc;
-        const long long rounds = ((long long)tiles * kce + grid - 1) / grid;
-        const long long cost = rounds * (spc + 2);
+        const int rounds = (tiles * kce + grid - 1) / grid;
+        const int cost = rounds * (spc + 2);
         if (cost < best_cost) {
             best_cost = cost;
             best = kce;
@@ -145,13 +146,14 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     // Full 128-token tiles only: a segment of c tokens contributes c / 128.
     const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
                                           p.nbins, UM_BM, tab, /*full_tiles_only=*/true);
+    if (total_tiles == 0) return;
     const int H = p.hidden, R = p.rank, T = p.num_tokens;
     const int nk = (H + UM_BK - 1) / UM_BK;
     const int kchunks = umma_kchunks(total_tiles, nk, int(gridDim.x));
     const int spc = (nk + kchunks - 1) / kchunks;
     const bool split = kchunks > 1;
     const int total_items = total_tiles * kchunks;      // item = kc * total_tiles + tile
-    if (total_tiles == 0 || int(blockIdx.x) >= total_items) return;
+    if (int(blockIdx.x) >= total_items) return;
 
     if (warp == UM_MMA_WARP) tmem_alloc(smem_addr(s_tmem), p.tmem_cols);
     tc_fence_before();
