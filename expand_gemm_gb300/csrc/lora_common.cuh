@@ -391,6 +391,7 @@ struct ShrinkLaunch {
     const int32_t *active;
     const int32_t *no_lora;
     int32_t *error_word;
+    int32_t partial;      // the tensor-core path takes partial tiles too
 };
 int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream);
 int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_tokens,

@@ -371,7 +371,7 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    // Tensor-core path for the whole 128-token tiles of long segments.  It
+    // Tensor-core path for the 128-token tiles of long segments.  It
     // pays where the contraction is dense enough to outrun mma.sync: a batch
     // large enough to hold long segments (LORA_PUNICA_UMMA_MIN_TOKENS,
     // default 1024) and at least LORA_PUNICA_UMMA_MIN_COLS output columns per
@@ -397,7 +397,12 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
         u.active = p.active;
         u.no_lora = p.no_lora;
         u.error_word = meta->error_word;
+        // LORA_PUNICA_UMMA_PARTIAL=1 (default): the tensor-core kernel takes
+        // the partial tile at the end of every segment too, and covers the
+        // whole batch; =0: whole tiles only, the remainders on mma.sync.
+        u.partial = lora::env_int("LORA_PUNICA_UMMA_PARTIAL", 1) ? 1 : 0;
         const int r = lora::launch_shrink_umma(u, st);
+        if (r == 1 && u.partial) return LORA_OK;
         if (r == 1) p.skip_rows = 128;
         else if (r != 0) return r;
     }

@@ -1,5 +1,6 @@
 // lora_shrink_umma.cu -- tensor-core (tcgen05 / TMEM) path of lora_shrink
-// for the full 128-token tiles of long LoRA segments (page
+// for the 128-token tiles of long LoRA segments, the partial last tile of
+// each segment included (page
 // "vllm.lora.punica_wrapper.punica_gpu", PunicaWrapperGPU.add_shrink:
 // y[s][t, :] += scale * x[t, :] @ A[s][id(t)]^T).
 //
@@ -64,6 +65,7 @@ struct UmmaShrinkArgs {
     const int32_t *no_lora;
     int32_t *error_word;
     int32_t nbins;
+    int32_t partial;                           // take partial tiles too (else whole ones only)
 };
 
 struct UmmaLayout {
@@ -143,9 +145,10 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
         for (int i = 0; i < UM_XMAPS; ++i) tma_prefetch_map(&p.map_x[i]);
     }
     const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + L.tab_off), p.nbins);
-    // Full 128-token tiles only: a segment of c tokens contributes c / 128.
+    // Every tile of every segment (partial), or the whole 128-token tiles
+    // only (a segment of c tokens then contributes c / 128).
     const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
-                                          p.nbins, UM_BM, tab, /*full_tiles_only=*/true);
+                                          p.nbins, UM_BM, tab, /*full_tiles_only=*/!p.partial);
     if (total_tiles == 0) return;
     const int H = p.hidden, R = p.rank, T = p.num_tokens;
     const int nk = (H + UM_BK - 1) / UM_BK;
@@ -172,7 +175,6 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
         // height, written at its row of the 128-byte-swizzled tile.  Long
         // prefill sequences make most tiles a single 128-row box.
         uint32_t *pieces = reinterpret_cast<uint32_t *>(smem + L.piece_off);
-        const uint32_t tx = uint32_t(L.x_bytes + S * L.a_bytes);
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
@@ -183,13 +185,18 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
             const int seg = find_segment(tab.tile, p.nbins, tile);
             const int id = tab.id[seg];
             const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * UM_BM;
+            // rows of this tile that belong to the segment (all 128 but in
+            // the last, partial tile of a segment); only they are loaded, and
+            // the stage's barrier expects exactly their bytes
+            const int nrows = min(UM_BM, tab.start[seg] + tab.count[seg] - row0);
+            const uint32_t tx = uint32_t(nrows * 128 + S * L.a_bytes);
             int npieces = 0;
             if (lane == 0) {
                 const int32_t *tk = p.sorted + row0;
                 int j = 0;
-                while (j < UM_BM) {
+                while (j < nrows) {
                     int lg = 7;
-                    while ((1 << lg) > UM_BM - j || (j & ((1 << lg) - 1)) != 0 ||
+                    while ((1 << lg) > nrows - j || (j & ((1 << lg) - 1)) != 0 ||
                            tk[j + (1 << lg) - 1] - tk[j] != (1 << lg) - 1)
                         --lg;
                     pieces[npieces++] = uint32_t(j) | (uint32_t(lg) << 8) |
@@ -289,18 +296,21 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
             const int tile = item % total_tiles;
             const int seg = find_segment(tab.tile, p.nbins, tile);
             const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * UM_BM;
-            const int tok = p.sorted[row0 + row];
+            // rows past the segment's end hold stale shared data: their
+            // accumulators are read (the load is warp-wide) but not stored
+            const int nrows = min(UM_BM, tab.start[seg] + tab.count[seg] - row0);
+            const int tok = row < nrows ? p.sorted[row0 + row] : -1;
             bool got = mbar_wait_bounded(bar_acc_full, acc_phase, s_abort, deadline);
             if (__all_sync(0xffffffffu, got) == 0) break;       // warp-uniform exit
             tc_fence_after();
             for (int s = 0; s < S; ++s) {
-                float *dst = p.y + (int64_t(s) * T + tok) * R;
+                float *dst = p.y + (int64_t(s) * T + max(tok, 0)) * R;
                 for (int c = 0; c < RP; c += 16) {
                     float v[16];
                     tmem_ld16(tmem + (uint32_t(q * 32) << 16) + uint32_t(s * RP + c), v);
 #pragma unroll
                     for (int j = 0; j < 16; j += 4) {
-                        if (c + j < R) {
+                        if (tok >= 0 && c + j < R) {
                             float4 *d4 = reinterpret_cast<float4 *>(dst + c + j);
                             const float4 a = make_float4(p.scale * v[j], p.scale * v[j + 1],
                                                          p.scale * v[j + 2], p.scale * v[j + 3]);
@@ -414,6 +424,7 @@ int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream)
     p.no_lora = a.no_lora;
     p.error_word = a.error_word;
     p.nbins = nbins;
+    p.partial = a.partial;
 
     static int configured[64] = {0};
     int dev = 0;
