@@ -40,9 +40,9 @@ FALLBACK_HBM_GBS = 6800.0
 # the committed ncu summaries, keyed by (kernel, workload) and the hash of
 # the kernel's sources they were taken on; a stale hash reports null.
 NCU_TRAFFIC = {
-    # profiles/expand_decode_ncu.md: reads 8.914 MB, writes 0 (the y writes
-    # stay in L2 past the end of the launch)
-    ("expand", "decode"): ("6be756206cd60265", 8914176),
+    # profiles/expand_decode_ncu.md: reads 8.915 MB (median of three
+    # launches), writes 0 (the y writes stay in L2 past the end of the launch)
+    ("expand", "decode"): ("2caa2c5021570068", 8914944),
 }
 
 # The source files each reported kernel is built from.
@@ -113,7 +113,9 @@ def fused_path(w) -> bool:
 
 
 def umma_shrink_path(w) -> bool:
-    """lora_shrink's rule for adding its tensor-core kernel."""
+    """lora_shrink's rule for taking its tensor-core kernel (which covers the
+    whole batch, or only the whole tiles with LORA_PUNICA_UMMA_PARTIAL=0, the
+    remainders then on the mma.sync kernel)."""
     return (w.num_tokens >= int(os.environ.get("LORA_PUNICA_UMMA_MIN_TOKENS", "1024"))
             and w.num_slices * w.rank >= int(os.environ.get("LORA_PUNICA_UMMA_MIN_COLS", "256"))
             and os.environ.get("LORA_PUNICA_UMMA", "1") != "0")
@@ -446,7 +448,8 @@ def run_ours(args, rank, world):
         },
         "hbm_frac_step": (step_bytes / (ms_per_step * 1e-3) / 1e9) / hbm,
         "gpu_launches": args.steps * (2 if emb else 1 if fused
-                                      else 3 + (1 if umma_shrink_path(w) else 0)),
+                                      else 3 + (1 if umma_shrink_path(w) and os.environ.get(
+                                          "LORA_PUNICA_UMMA_PARTIAL", "1") == "0" else 0)),
         "clocks": clocks.summary(),
         "e2e": e2e,
         "wall_s_timed": wall,
