@@ -14,8 +14,9 @@
 
 namespace lora {
 
-constexpr int META_THREADS = 1024;
-constexpr int META_WARPS = META_THREADS / 32;
+constexpr int META_THREADS = 1024;       // the largest block (big batches)
+constexpr int META_SMALL_THREADS = 256;  // batches of up to META_SMALL_MAX tokens
+constexpr int META_SMALL_MAX = 512;
 // Batches up to this many tokens are first copied into shared memory with
 // one block-wide load (all of it in flight at once); both passes then read
 // shared memory.  Larger batches read the map from global memory.
@@ -34,11 +35,11 @@ struct MetaArgs {
     int32_t *error_word;
 };
 
-size_t meta_smem_bytes(int max_loras, int num_tokens)
+size_t meta_smem_bytes(int warps, int max_loras, int num_tokens)
 {
     const size_t nb = size_t(max_loras) + 1;
     const size_t staged = num_tokens <= META_STAGE_MAX ? size_t(num_tokens) : 0;
-    return (META_WARPS * nb + 3 * nb + staged) * sizeof(int32_t);
+    return (size_t(warps) * nb + 3 * nb + staged) * sizeof(int32_t);
 }
 
 // Bin of one token; counts an invalid id into `bad`.
@@ -49,8 +50,10 @@ __device__ __forceinline__ int token_bin(int32_t id, int32_t max_loras, int &bad
     return 0;
 }
 
-__global__ void __launch_bounds__(META_THREADS, 1) meta_prepare_kernel(MetaArgs a)
+template <int NT>
+__global__ void __launch_bounds__(NT, 1) meta_prepare_kernel(MetaArgs a)
 {
+    constexpr int META_WARPS = NT / 32;
     extern __shared__ int32_t sm[];
     const int nb = a.max_loras + 1;
     int32_t *cnt = sm;                          // [META_WARPS][nb]: count, then offset
@@ -68,14 +71,14 @@ __global__ void __launch_bounds__(META_THREADS, 1) meta_prepare_kernel(MetaArgs 
 
     const bool staged = T <= META_STAGE_MAX;
     if (staged)
-        for (int t = tid; t < T; t += META_THREADS) ids_s[t] = a.map[t];
+        for (int t = tid; t < T; t += NT) ids_s[t] = a.map[t];
     const int32_t *ids = staged ? ids_s : a.map;
-    for (int i = tid; i < META_WARPS * nb; i += META_THREADS) cnt[i] = 0;
+    for (int i = tid; i < META_WARPS * nb; i += NT) cnt[i] = 0;
     if (tid == 0) s_invalid = 0;
     __syncthreads();
 
     // Each warp owns tokens [t0, t1), a multiple of 32 long (the last may be short).
-    const int per_warp = ((T + META_THREADS - 1) / META_THREADS) * 32;
+    const int per_warp = ((T + NT - 1) / NT) * 32;
     const int t0 = min(T, warp * per_warp);
     const int t1 = min(T, t0 + per_warp);
 
@@ -95,7 +98,7 @@ __global__ void __launch_bounds__(META_THREADS, 1) meta_prepare_kernel(MetaArgs 
     __syncthreads();
 
     // Per bin, exclusive scan over warps (warp order = token order).
-    for (int b = tid; b < nb; b += META_THREADS) {
+    for (int b = tid; b < nb; b += NT) {
         int run = 0;
         for (int w = 0; w < META_WARPS; ++w) {
             const int c = cnt[w * nb + b];
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(META_THREADS, 1) meta_prepare_kernel(MetaArgs 
     const int nact = no_lora ? 0 : s_nactive;
 
     // _reset values for every slot that no active id fills.
-    for (int k = tid; k < nb; k += META_THREADS) {
+    for (int k = tid; k < nb; k += NT) {
         if (k >= nact) {
             a.active[k] = -1;
             a.counts[k] = 0;
@@ -151,7 +154,7 @@ __global__ void __launch_bounds__(META_THREADS, 1) meta_prepare_kernel(MetaArgs 
     if (no_lora) return;                        // early exit: nothing else written
 
     // unique(sorted=True, return_counts=True) and cumsum into start_loc[1:].
-    for (int b = tid; b < nb; b += META_THREADS) {
+    for (int b = tid; b < nb; b += NT) {
         const int c = tot[b];
         if (c > 0) {
             const int k = pos[b];
@@ -182,19 +185,33 @@ __global__ void __launch_bounds__(META_THREADS, 1) meta_prepare_kernel(MetaArgs 
 
 int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
 {
-    static int configured_smem[64] = {0};
+    static int configured[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return int(e);
-    const size_t smem = meta_smem_bytes(a.max_loras, a.num_tokens);
-    if (dev < 64 && configured_smem[dev] < int(smem)) {
-        const int want = int(meta_smem_bytes(LORA_MAX_LORAS, META_STAGE_MAX));
-        e = cudaFuncSetAttribute(meta_prepare_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+    if (dev < 64 && configured[dev] == 0) {
+        e = cudaFuncSetAttribute(meta_prepare_kernel<META_THREADS>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(meta_smem_bytes(META_THREADS / 32, LORA_MAX_LORAS,
+                                                     META_STAGE_MAX)));
         if (e != cudaSuccess) return int(e);
-        configured_smem[dev] = want;
+        e = cudaFuncSetAttribute(meta_prepare_kernel<META_SMALL_THREADS>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(meta_smem_bytes(META_SMALL_THREADS / 32, LORA_MAX_LORAS,
+                                                     META_SMALL_MAX)));
+        if (e != cudaSuccess) return int(e);
+        configured[dev] = 1;
     }
-    return int(launch_kernel(meta_prepare_kernel, dim3(1), dim3(META_THREADS), smem, stream, a));
+    // Small batches on 8 warps (fewer warps to pass each barrier), the rest
+    // on 32.  LORA_PUNICA_META_SMALL=0 always takes 32 warps.
+    if (a.num_tokens <= META_SMALL_MAX && env_int("LORA_PUNICA_META_SMALL", 1)) {
+        const size_t smem = meta_smem_bytes(META_SMALL_THREADS / 32, a.max_loras, a.num_tokens);
+        return int(launch_kernel(meta_prepare_kernel<META_SMALL_THREADS>, dim3(1),
+                                 dim3(META_SMALL_THREADS), smem, stream, a));
+    }
+    const size_t smem = meta_smem_bytes(META_THREADS / 32, a.max_loras, a.num_tokens);
+    return int(launch_kernel(meta_prepare_kernel<META_THREADS>, dim3(1), dim3(META_THREADS), smem,
+                             stream, a));
 }
 
 }  // namespace lora
