@@ -321,7 +321,8 @@ def lora_linear(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_a_stacke
                 y: torch.Tensor, meta: LoRAKernelMeta) -> None:
     """Metadata + shrink + expand of one LoRA layer in one library call
     (PunicaWrapperGPU.update_metadata followed by add_lora_linear).  Small
-    batches run as one fused kernel; see include/lora_punica.h."""
+    batches run as one kernel, larger ones as three overlapping launches;
+    see include/lora_punica.h."""
     if not isinstance(buffer, torch.Tensor):
         raise TypeError("buffer must be a torch.Tensor (lora_linear_noalloc needs none)")
     a = _linear_args(token_lora_mapping, x, lora_a_stacked, lora_b_stacked, lora_bias_stacked,

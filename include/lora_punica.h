@@ -145,9 +145,12 @@ int lora_meta_prepare(const int32_t *token_lora_mapping, int32_t num_tokens,
  *               get a plain product).
  *   scale       multiplies the product before it is added.
  *
- * Accumulation is fp32 on the tensor cores; when the hidden dimension is
+ * Accumulation is fp32 on the tensor cores (mma.sync; tcgen05 with TMEM
+ * accumulators for batches of >= 1024 tokens with num_slices * rank >=
+ * 256, LORA_PUNICA_UMMA* in the environment); when the hidden dimension is
  * split across CTAs the partial sums are added with fp32 atomics, so the
- * rounding order is not fixed from run to run.
+ * rounding order is not fixed from run to run.  A bounded wait of the
+ * tcgen05 path that runs out sets bit 30 of meta->error_word.
  */
 int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidden,
                 int64_t x_ld, const lora_bf16_t *const *lora_a,
@@ -215,17 +218,24 @@ int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lora_b,
  * three calls; `buf` is accumulated into like lora_shrink's y, and every
  * metadata buffer of `meta` is written as lora_meta_prepare writes it.
  *
- * Small batches (by default at most 128 tokens; max_loras <= 256,
- * num_slices * padded rank <= 128, 16-byte-aligned rows, offsets and
- * widths) run as ONE kernel: a thread-block cluster per (LoRA segment,
- * 64-token tile) builds the metadata in shared memory, splits the shrink
- * over the hidden dimension, sums the rank-r partials through distributed
- * shared memory and expands its share of the output columns.  Other
- * batches run the three kernels in sequence.  Either way the results equal
- * the three calls' (the fused shrink sums its partials in a different
- * order).  Environment: LORA_PUNICA_FUSED=0 forces the three kernels,
- * LORA_PUNICA_FUSED=1 allows the fused kernel up to 512 tokens,
- * LORA_PUNICA_FUSED_MAX_TOKENS sets the default limit.
+ * How the layer runs (every form gives the three calls' results; the
+ * shrink's partial sums may be added in a different order):
+ *   - one cooperative kernel, by default when num_tokens * num_slices <=
+ *     256 (and num_tokens <= 512, max_loras <= 256, rank <= 64, 16-byte
+ *     aligned rows): every CTA sorts the ids in shared memory, the shrink
+ *     is spread over the grid, a grid barrier (meta->grid_sync; bounded,
+ *     bit 30 of the error word on expiry) separates it from the expand;
+ *   - one thread-block-cluster kernel for other batches of at most 128
+ *     tokens (max_loras <= 256, num_slices * padded rank <= 128);
+ *   - otherwise three kernels with programmatic dependent launch: the
+ *     metadata kernel, the shrink (sorting the ids itself and loading
+ *     before its dependency wait, for <= 512 tokens) and the expand
+ *     (fetching the metadata, y and B before its wait).
+ * Environment (read at each call): LORA_PUNICA_COOP=0/1 never / always
+ * (when the batch fits) the cooperative kernel; LORA_PUNICA_FUSED=0/1 and
+ * LORA_PUNICA_FUSED_MAX_TOKENS the cluster kernel; LORA_PUNICA_SELF_META=1
+ * two kernels (the shrink writes the metadata), =2 the same with the
+ * expand sorting the ids itself, =0 the plain three calls.
  */
 int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
                 const lora_bf16_t *x, int32_t hidden, int64_t x_ld,
