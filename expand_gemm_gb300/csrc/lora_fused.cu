@@ -187,8 +187,7 @@ __global__ void __launch_bounds__(FU_THREADS, 1) fused_kernel(FusedArgs p)
             if (id >= 0 && id < p.max_loras) b = id + 1;
             else { b = 0; if (id != -1) ++bad; }
         }
-        const unsigned grp = __match_any_sync(0xffffffffu, b);
-        if (has && lane == __ffs(grp) - 1) cnt[warp * nbins + b] += __popc(grp);
+        if (has) atomicAdd(&cnt[warp * nbins + b], 1);          // counts only
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);

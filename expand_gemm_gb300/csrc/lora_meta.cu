@@ -1,8 +1,9 @@
 // lora_meta.cu -- metadata step (page "vllm.lora.ops.triton_ops.
 // lora_kernel_metadata", LoRAKernelMeta._reset + prepare_tensors) as one
 // single-CTA kernel: the id map staged in shared memory, per-warp bin
-// histograms built with __match_any_sync, a warp-shuffle scan over
-// (bin, warp), and a stable counting-sort scatter.
+// histograms (shared-memory atomic adds), a warp-shuffle scan over
+// (bin, warp), and a stable counting-sort scatter (lanes of one bin ranked
+// with __match_any_sync).
 //
 // Bins: bin 0 holds id -1 (and every invalid id), bin b > 0 holds id b - 1.
 // Token order inside a bin is preserved because (1) each warp owns one
@@ -82,15 +83,16 @@ __global__ void __launch_bounds__(NT, 1) meta_prepare_kernel(MetaArgs a)
     const int t0 = min(T, warp * per_warp);
     const int t1 = min(T, t0 + per_warp);
 
-    // Pass 1: per-warp histogram.  Lanes holding the same bin form one
-    // __match_any_sync group; its lowest lane adds the group size.
+    // Pass 1: per-warp histogram, one shared-memory atomic add per token
+    // (counts only: pass 2 keeps the order).  Measured faster than grouping
+    // lanes with __match_any_sync, whose cost grows with the number of
+    // distinct ids in a warp.
     int bad = 0;
     for (int g = t0; g < t1; g += 32) {
         const int t = g + lane;
         const bool has = t < t1;
         const int b = has ? token_bin(ids[t], a.max_loras, bad) : -1;
-        const unsigned grp = __match_any_sync(0xffffffffu, b);
-        if (has && lane == __ffs(grp) - 1) cnt[warp * nb + b] += __popc(grp);
+        if (has) atomicAdd(&cnt[warp * nb + b], 1);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
