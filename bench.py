@@ -433,6 +433,9 @@ def run_ours(args, rank, world):
                          "one fused cluster kernel" if fused else "three kernels")),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
+        # the metric's other reading: tokens over the shrink and expand
+        # kernels' standalone times, metadata (once per forward) left out
+        "tokens_per_s_shrink_expand": T / ((k_shrink + k_expand) * 1e-3),
         "effective_gbps": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "step_unique_bytes": step_bytes,
         "kernels_us": {k: v * 1e3 for k, v in kern.items()},
