@@ -4,28 +4,29 @@
 // PunicaWrapperTPU._apply_bias):
 //   y[t, off_s + j] (+)= x[s][t, :] @ B[s][id(t)][j, :] + bias[s][id(t)][j]
 //
-// Work items are (token tile of 128 tokens of one LoRA segment, 128-column
+// Work items are (token tile of 128 tokens of one LoRA segment, 64-column
 // chunk of one slice), numbered chunk-fastest; one persistent CTA per SM
 // takes a contiguous, balanced range of them.  Ten warps, specialised:
 //   warp 0      producer, all TMA: per chunk one 2-D box of B[s][id] (two
 //               for rank 128) in the swizzled K-major layout UMMA reads; the
-//               tile's y rows as 2-D boxes over runs of consecutive tokens
-//               (power-of-two heights, two 64-column halves, 128-byte
-//               swizzle); the bias chunk as one 1-D bulk copy.
-//   warp 1      owns TMEM (two 128-column fp32 accumulators); lane 0 issues
-//               tcgen05.mma (M = 128 tokens, N = 128 columns, K = 16 steps
+//               tile's old y rows as 2-D boxes over runs of consecutive
+//               tokens (power-of-two heights, 128-byte swizzle; the runs are
+//               found once per tile from its token list staged in shared
+//               memory); the bias chunk as one 1-D bulk copy.
+//   warp 1      owns TMEM (two 64-column fp32 accumulators); lane 0 issues
+//               tcgen05.mma (M = 128 tokens, N = 64 columns, K = 16 steps
 //               over the rank) and commits.
 //   warps 2..9  epilogue, one token row per thread (its TMEM lane), two
 //               warps per lane quarter splitting the columns: at each new
 //               tile the fp32 x rows are rounded to bf16 into the A operand;
 //               per chunk the accumulators are read with tcgen05.ld, bias
-//               and old y added in fp32 and rounded once to bf16 in place in
-//               the swizzled y tile, and one thread sends the tile back with
-//               TMA stores over the same token runs.  A half-chunk that runs
-//               past the end of a slice is stored by its threads directly.
+//               and old y added in fp32, rounded once to bf16 and written
+//               with 16-byte stores straight to the thread's own y row.
 // The accumulators are double-buffered so the MMA of chunk i + 1 runs while
-// the epilogue drains chunk i; B, y and bias stream through a ring of stages
-// that is released once the TMA stores of a chunk have read it.
+// the epilogue drains chunk i.  B, old y and bias stream through a ring of
+// up to six stages; a stage is refilled once the MMA has read its B and
+// every epilogue warp its y and bias, so the loads run several chunks ahead
+// of the epilogue.  The epilogue warps never wait for one another.
 //
 // Used when y rows, offsets and slice widths are 16-byte aligned (the same
 // condition as the vector path of the mma.sync kernel).  Every mbarrier
@@ -37,11 +38,11 @@
 namespace lora {
 
 constexpr int XU_BM = 128;              // tokens per tile (UMMA M, TMEM lanes)
-constexpr int XU_BN = 128;              // columns per chunk (UMMA N)
+constexpr int XU_BN = 64;               // columns per chunk (UMMA N; one 128-byte y row)
 constexpr int XU_EPI_WARPS = 8;         // two per TMEM lane quarter (column halves)
 constexpr int XU_THREADS = 64 + 32 * XU_EPI_WARPS;
-constexpr int XU_MAX_STAGES = 4;
-constexpr int XU_SMEM_BUDGET = 200 * 1024;
+constexpr int XU_MAX_STAGES = 6;
+constexpr int XU_SMEM_BUDGET = 224 * 1024;
 constexpr int XU_YMAPS = 8;             // y box heights 1, 2, 4, ..., 128
 constexpr long long XU_TIMEOUT_CYCLES = 2000000000ll;
 constexpr int XU_ERROR_BIT = 1 << 30;
@@ -74,26 +75,25 @@ struct ExpandUmmaArgs {
 
 struct XuLayout {
     int a_bytes, b_bytes, y_off, bias_off, stage_bytes, ring_off, bar_off, misc_off, ppc_off,
-        epc_off, etok_off, tab_off, total;
+        ptok_off, tab_off, total;
 };
 
-// Stage: B tile | y tile (two 64-column halves of 128 rows x 128 bytes,
-// 128-byte swizzle) | bias chunk.
+// Stage: B tile | old y tile (128 rows x 128 bytes, 128-byte swizzle) |
+// bias chunk.
 __host__ __device__ inline XuLayout xu_layout(int rp, int stages, int nbins)
 {
     XuLayout l;
     l.a_bytes = XU_BM * rp * 2;
     l.b_bytes = XU_BN * rp * 2;
     l.y_off = l.b_bytes;
-    l.bias_off = l.y_off + 2 * XU_BM * 128;
+    l.bias_off = l.y_off + XU_BM * 128;
     l.stage_bytes = ((l.bias_off + XU_BN * 2) + 1023) & ~1023;
     l.ring_off = l.a_bytes;
     l.bar_off = l.ring_off + stages * l.stage_bytes;
     l.misc_off = l.bar_off + (2 * XU_MAX_STAGES + 6) * 8;
     l.ppc_off = l.misc_off + 16;                         // producer pieces [128]
-    l.epc_off = l.ppc_off + XU_BM * 4;                   // store pieces [128]
-    l.etok_off = l.epc_off + XU_BM * 4;                  // epilogue token rows [128]
-    l.tab_off = l.etok_off + XU_BM * 4;
+    l.ptok_off = l.ppc_off + XU_BM * 4;                  // producer's token list [128]
+    l.tab_off = l.ptok_off + XU_BM * 4;
     l.total = l.tab_off + int(seg_tab_bytes(nbins)) + 1024;
     return l;
 }
@@ -147,11 +147,6 @@ __device__ __forceinline__ int token_pieces(const int32_t *tk, int n, uint32_t *
     return np;
 }
 
-__device__ __forceinline__ void named_barrier(int id, int count)
-{
-    asm volatile("bar.sync %0, %1;\n" :: "r"(id), "r"(count) : "memory");
-}
-
 __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid_constant__ ExpandUmmaArgs p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -161,7 +156,7 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
     const XuLayout L = xu_layout(RP, STAGES, p.nbins);
     const uint32_t base = smem_addr(smem);
     const uint32_t bar_full = base + L.bar_off;                   // [STAGES] B + y + bias (TMA)
-    const uint32_t bar_empty = bar_full + 8 * XU_MAX_STAGES;      // [STAGES] MMA + stores read
+    const uint32_t bar_empty = bar_full + 8 * XU_MAX_STAGES;      // [STAGES] MMA + epilogue warps
     const uint32_t bar_acc_full = bar_empty + 8 * XU_MAX_STAGES;  // [2]
     const uint32_t bar_acc_empty = bar_acc_full + 16;             // [2]
     const uint32_t bar_x_ready = bar_acc_empty + 16;
@@ -169,8 +164,7 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L.misc_off);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L.misc_off + 4);
     uint32_t *s_ppieces = reinterpret_cast<uint32_t *>(smem + L.ppc_off);
-    uint32_t *s_epieces = reinterpret_cast<uint32_t *>(smem + L.epc_off);
-    int *s_etok = reinterpret_cast<int *>(smem + L.etok_off);
+    int32_t *s_ptok = reinterpret_cast<int32_t *>(smem + L.ptok_off);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -180,7 +174,7 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(bar_full + 8 * i, 1);
-            mbar_init(bar_empty + 8 * i, 2);
+            mbar_init(bar_empty + 8 * i, 1 + XU_EPI_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_acc_full + 8 * i, 1);
@@ -236,9 +230,14 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
             row_item(w, tile, s, cb, ce);
             tile_rows(tile, id, row0, nrows);
             int np = 0;
-            if (lane == 0) np = token_pieces(p.sorted + row0, nrows, s_ppieces);
-            np = __shfl_sync(0xffffffffu, np, 0);
-            __syncwarp();
+            if (p.add_inputs) {
+                // the tile's tokens in one coalesced read, then the runs
+                for (int i = lane; i < nrows; i += 32) s_ptok[i] = p.sorted[row0 + i];
+                __syncwarp();
+                if (lane == 0) np = token_pieces(s_ptok, nrows, s_ppieces);
+                np = __shfl_sync(0xffffffffu, np, 0);
+                __syncwarp();
+            }
             const int n_s = p.n[s];
             const uint16_t *bias_row = p.bias[s] ? p.bias[s] + int64_t(id) * n_s : nullptr;
             for (int c = cb; c < ce; ++c, ++g) {
@@ -256,7 +255,7 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
                 const bool with_bias = bias_row != nullptr && p.bias_vec;
                 if (lane == 0) {
                     const uint32_t tx = uint32_t(L.b_bytes) +
-                                        (p.add_inputs ? uint32_t(nrows) * 256u : 0u) +
+                                        (p.add_inputs ? uint32_t(nrows) * 128u : 0u) +
                                         (with_bias ? uint32_t(ncols) * 2u : 0u);
                     mbar_arrive_expect_tx(full, tx);
                 }
@@ -267,7 +266,6 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
                         const uint32_t pc = s_ppieces[i];
                         const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
                         tma_load_2d(st + L.y_off + r * 128, &p.map_y[lg], col, t0, full);
-                        tma_load_2d(st + L.y_off + XU_BM * 128 + r * 128, &p.map_y[lg], col + 64, t0, full);
                     }
                 }
                 if (lane == 0) {
@@ -330,24 +328,21 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
     } else {
         // ------------------------------------------ epilogue (8 warps)
         // Warp e = warp - 2: TMEM lane quarter q = warp % 4 (one token row per
-        // thread), column half hf = e / 4.  After an abort the warps keep
-        // walking the items (skipping work) so named barriers stay matched.
+        // thread), column half hf = e / 4 (32 of the chunk's 64 columns).
         const int e = warp - 2;
         const int q = warp & 3;
         const int hf = e >> 2;
         const int row = q * 32 + lane;
-        const int etid = tid - 64;                       // 0..255
-        const bool storer = (etid == 0);
-        int g = 0, items = 0, stores_open = 0, open_stage = 0;
+        int g = 0;
         bool ok = true;
-        for (int64_t w = w_begin; w < w_end; ++items) {
+        for (int64_t w = w_begin; ok && w < w_end;) {
             int tile, s, cb, ce, id, row0, nrows;
             row_item(w, tile, s, cb, ce);
             tile_rows(tile, id, row0, nrows);
             const int tok = (row < nrows) ? p.sorted[row0 + row] : -1;
-            named_barrier(2, 32 * XU_EPI_WARPS);         // previous item finished
-            if (hf == 0) s_etok[row] = tok;
-            // x row -> bf16 A operand row; each half converts half of the chunks
+            // x row -> bf16 A operand row; each half converts half of the
+            // 16-byte pieces.  A is free: this warp has seen the accumulator
+            // of the previous item's last chunk, committed after its MMAs.
             {
                 const float *xr = p.x + (int64_t(s) * p.num_tokens + (tok >= 0 ? tok : 0)) * R;
                 const int nch = RP / 8;
@@ -367,120 +362,64 @@ __global__ void __launch_bounds__(XU_THREADS, 1) expand_umma_kernel(const __grid
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_x_ready);
             }
-            named_barrier(2, 32 * XU_EPI_WARPS);         // s_etok visible
-            int np = 0;
-            if (storer) np = token_pieces(s_etok, nrows, s_epieces);
             const int n_s = p.n[s];
             const uint16_t *bias_row = p.bias[s] ? p.bias[s] + int64_t(id) * n_s : nullptr;
+            uint16_t *yrow = (tok >= 0) ? p.y + int64_t(tok) * p.y_ld + p.col0[s] : nullptr;
             for (int c = cb; c < ce; ++c, ++g) {
                 const int stage = g % STAGES, ab = g & 1;
-                if (ok) {
-                    bool got = mbar_wait_bounded(bar_acc_full + 8 * ab, uint32_t(g >> 1) & 1u, s_abort, deadline) &&
-                               mbar_wait_bounded(bar_full + 8 * stage, uint32_t(g / STAGES) & 1u, s_abort, deadline);
-                    ok = __all_sync(0xffffffffu, got) != 0;
+                const bool got =
+                    mbar_wait_bounded(bar_acc_full + 8 * ab, uint32_t(g >> 1) & 1u, s_abort, deadline) &&
+                    mbar_wait_bounded(bar_full + 8 * stage, uint32_t(g / STAGES) & 1u, s_abort, deadline);
+                if (__all_sync(0xffffffffu, got) == 0) {
+                    ok = false;
+                    break;
                 }
+                tc_fence_after();
                 const int c0 = (c - p.chunk0[s]) * XU_BN;
-                const int ncols = min(XU_BN, n_s - c0);
-                const int colg = p.col0[s] + c0;         // first column of the chunk in y
-                const bool half_full = (hf + 1) * 64 <= ncols;
-                if (ok) {
-                    tc_fence_after();
-                    uint8_t *ysub = smem + L.ring_off + stage * L.stage_bytes + L.y_off + hf * XU_BM * 128;
-                    const uint16_t *sbias = reinterpret_cast<const uint16_t *>(
-                        smem + L.ring_off + stage * L.stage_bytes + L.bias_off);
-                    uint32_t va[32], vb[32];
-                    const uint32_t ta = tmem + ab * XU_BN + hf * 64 + (uint32_t(q * 32) << 16);
-                    tmem_ld32_nowait(ta, va);
-                    tmem_ld32_nowait(ta + 32, vb);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);   // TMEM buffer free
-                    if (tok >= 0) {
+                const int ncols = min(XU_BN, n_s - c0);         // a multiple of 8
+                const uint8_t *ysm = smem + L.ring_off + stage * L.stage_bytes + L.y_off + row * 128;
+                const uint16_t *sbias = reinterpret_cast<const uint16_t *>(
+                    smem + L.ring_off + stage * L.stage_bytes + L.bias_off);
+                uint32_t va[32];
+                tmem_ld32_nowait(tmem + ab * XU_BN + hf * 32 + (uint32_t(q * 32) << 16), va);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);   // TMEM buffer free
+                if (yrow != nullptr) {
 #pragma unroll
-                        for (int j4 = 0; j4 < 4; ++j4) {
-                            const int cl = hf * 64 + j4 * 16;          // chunk column of this group
-                            if (cl >= ncols) continue;
-                            // 16-byte chunks 2*j4, 2*j4+1 of this row's 128-byte half row
-                            uint4 *p0 = reinterpret_cast<uint4 *>(ysub + row * 128 + (((2 * j4) ^ (row & 7)) << 4));
-                            uint4 *p1 = reinterpret_cast<uint4 *>(ysub + row * 128 + (((2 * j4 + 1) ^ (row & 7)) << 4));
-                            uint32_t yw[8], bw[8];
-                            if (p.add_inputs) {
-                                const uint4 y0 = *p0, y1 = *p1;
-                                yw[0] = y0.x; yw[1] = y0.y; yw[2] = y0.z; yw[3] = y0.w;
-                                yw[4] = y1.x; yw[5] = y1.y; yw[6] = y1.z; yw[7] = y1.w;
-                            } else {
-#pragma unroll
-                                for (int k = 0; k < 8; ++k) yw[k] = 0u;
-                            }
-                            if (bias_row != nullptr && p.bias_vec) {
-                                const uint4 b0 = reinterpret_cast<const uint4 *>(sbias + cl)[0];
-                                const uint4 b1 = reinterpret_cast<const uint4 *>(sbias + cl)[1];
-                                bw[0] = b0.x; bw[1] = b0.y; bw[2] = b0.z; bw[3] = b0.w;
-                                bw[4] = b1.x; bw[5] = b1.y; bw[6] = b1.z; bw[7] = b1.w;
-                            } else if (bias_row != nullptr) {
-#pragma unroll
-                                for (int k = 0; k < 8; ++k) {
-                                    const int cc = cl + 2 * k;
-                                    const uint32_t lo = cc < ncols ? bias_row[c0 + cc] : 0u;
-                                    const uint32_t hi = cc + 1 < ncols ? bias_row[c0 + cc + 1] : 0u;
-                                    bw[k] = lo | (hi << 16);
-                                }
-                            } else {
-#pragma unroll
-                                for (int k = 0; k < 8; ++k) bw[k] = 0u;
-                            }
-                            uint32_t o[8];
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                const uint32_t a = (j4 < 2) ? va[(j4 & 1) * 16 + 2 * k] : vb[(j4 & 1) * 16 + 2 * k];
-                                const uint32_t b = (j4 < 2) ? va[(j4 & 1) * 16 + 2 * k + 1] : vb[(j4 & 1) * 16 + 2 * k + 1];
-                                const float a0 = __uint_as_float(a) + bf16_lo(bw[k]) + bf16_lo(yw[k]);
-                                const float a1 = __uint_as_float(b) + bf16_hi(bw[k]) + bf16_hi(yw[k]);
-                                o[k] = pack_bf16x2(a0, a1);
-                            }
-                            const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]);
-                            const uint4 o1 = make_uint4(o[4], o[5], o[6], o[7]);
-                            if (half_full) {
-                                *p0 = o0;                              // leaves by TMA store
-                                *p1 = o1;
-                            } else {
-                                // a half that runs past the slice: store the valid columns here
-                                uint16_t *dst = p.y + int64_t(tok) * p.y_ld + colg + cl;
-                                *reinterpret_cast<uint4 *>(dst) = o0;
-                                if (cl + 8 < ncols) *reinterpret_cast<uint4 *>(dst + 8) = o1;
-                            }
+                    for (int j = 0; j < 4; ++j) {
+                        const int cl = hf * 32 + j * 8;                 // 8 columns, one 16-byte piece
+                        if (cl >= ncols) break;
+                        uint32_t yw[4] = {0u, 0u, 0u, 0u}, bw[4] = {0u, 0u, 0u, 0u};
+                        if (p.add_inputs) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(
+                                ysm + ((((hf * 4 + j) ^ (row & 7))) << 4));
+                            yw[0] = v.x; yw[1] = v.y; yw[2] = v.z; yw[3] = v.w;
                         }
-                    }
-                    fence_proxy_async_smem();
-                }
-                named_barrier(2, 32 * XU_EPI_WARPS);     // every row of the tile combined
-                if (storer) {
-                    if (ok) {
-                        const uint32_t ys = base + L.ring_off + stage * L.stage_bytes + L.y_off;
-                        for (int i = 0; i < np; ++i) {
-                            const uint32_t pc = s_epieces[i];
-                            const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
-                            for (int h = 0; h < 2; ++h)
-                                if ((h + 1) * 64 <= ncols)
-                                    tma_store_2d(&p.map_y[lg], colg + h * 64, t0, ys + h * XU_BM * 128 + r * 128);
+                        if (bias_row != nullptr && p.bias_vec) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(sbias + cl);
+                            bw[0] = v.x; bw[1] = v.y; bw[2] = v.z; bw[3] = v.w;
+                        } else if (bias_row != nullptr) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                bw[k] = uint32_t(bias_row[c0 + cl + 2 * k]) |
+                                        (uint32_t(bias_row[c0 + cl + 2 * k + 1]) << 16);
                         }
+                        uint32_t o[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float a0 = __uint_as_float(va[j * 8 + 2 * k]) + bf16_lo(bw[k]) + bf16_lo(yw[k]);
+                            const float a1 = __uint_as_float(va[j * 8 + 2 * k + 1]) + bf16_hi(bw[k]) + bf16_hi(yw[k]);
+                            o[k] = pack_bf16x2(a0, a1);
+                        }
+                        *reinterpret_cast<uint4 *>(yrow + c0 + cl) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
-                    bulk_commit_group();
-                    // the previous chunk's stores have read their tile: free that stage
-                    if (stores_open) {
-                        bulk_wait_group_read<1>();
-                        mbar_arrive(bar_empty + 8 * open_stage);
-                    }
-                    stores_open = 1;
-                    open_stage = stage;
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * stage);    // this warp is done with the stage
             }
             w += ce - cb;
-        }
-        if (storer) {
-            bulk_wait_group_all();
-            if (stores_open) mbar_arrive(bar_empty + 8 * open_stage);
         }
     }
 

@@ -229,7 +229,9 @@ def test_expand_long_segments(oracle_mod, monkeypatch, path):
     _expand_case(oracle_mod, inp, offset=8, y_extra=8)
 
 
-def test_expand_overwrite_mode(oracle_mod):
+@pytest.mark.parametrize("path", EXPAND_PATHS)
+def test_expand_overwrite_mode(oracle_mod, monkeypatch, path):
+    monkeypatch.setenv("LORA_PUNICA_EXPAND_UMMA", path)
     inp = _custom(333, 64, 32, 4, (256, 128), seed=22, bias=True)
     _expand_case(oracle_mod, inp, add_inputs=False, offset=8, y_extra=16)
     _expand_case(oracle_mod, inp, add_inputs=False, offset=3, y_extra=1)   # scalar path
