@@ -114,8 +114,13 @@ class LoRAKernelMeta:
                 self.active_lora_ids, self.no_lora_flag)
 
     def no_lora(self) -> bool:
-        """Host read of the flag (synchronises; the kernels never need it)."""
-        return bool(self.no_lora_flag.item())
+        """Host read of the flag through ``lora_meta_read_no_lora``
+        (synchronises the current stream; the kernels never need it)."""
+        out = ctypes.c_int32(-1)
+        st = _lib.load().lora_meta_read_no_lora(ctypes.byref(self.c), _stream_handle(self.device),
+                                               ctypes.byref(out))
+        _lib.check("lora_meta_read_no_lora", st)
+        return bool(out.value)
 
 
 def lora_meta_prepare(token_lora_mapping: torch.Tensor, meta: LoRAKernelMeta) -> None:

@@ -13,8 +13,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "liblora_punica.so")
 
 # Public entry points of include/lora_punica.h (checked by the test suite).
-EXPORTS = ("lora_meta_prepare", "lora_shrink", "lora_expand", "lora_expand_bf16",
-           "lora_linear", "lora_linear_noalloc", "lora_status_string", "lora_version")
+EXPORTS = ("lora_meta_prepare", "lora_meta_read_no_lora", "lora_shrink", "lora_expand",
+           "lora_expand_bf16", "lora_linear", "lora_linear_noalloc", "lora_status_string",
+           "lora_version")
 
 LORA_MAX_SLICES = 8
 LORA_MAX_LORAS = 1024
@@ -66,6 +67,9 @@ def load(path: str | None = None):
         lib = ctypes.CDLL(p)
         lib.lora_meta_prepare.argtypes = [_P, _I32, ctypes.POINTER(LoraMetaC), _P]
         lib.lora_meta_prepare.restype = ctypes.c_int
+        lib.lora_meta_read_no_lora.argtypes = [ctypes.POINTER(LoraMetaC), _P,
+                                               ctypes.POINTER(ctypes.c_int32)]
+        lib.lora_meta_read_no_lora.restype = ctypes.c_int
         lib.lora_shrink.argtypes = [_P, _I32, _I32, _I64, _P, _I32, _I32, _P,
                                     ctypes.POINTER(LoraMetaC), ctypes.c_float, _P]
         lib.lora_shrink.restype = ctypes.c_int

@@ -1,5 +1,5 @@
-// lora_api.cu -- library-wide C entry points (status names, version) and
-// the host helpers the launchers share.
+// lora_api.cu -- library-wide C entry points (status names, version, the
+// host read of the no-LoRA flag) and the host helpers the launchers share.
 #include <stdlib.h>
 
 #include "lora_common.cuh"
@@ -62,3 +62,19 @@ LORA_API const char *lora_status_string(int status)
 }
 
 LORA_API int lora_version(void) { return LORA_PUNICA_VERSION; }
+
+// Host copy of the flag, as LoRAKernelMeta.no_lora_flag_cpu on the page
+// "vllm.lora.ops.triton_ops.lora_kernel_metadata": one 4-byte copy ordered
+// after the metadata step on `stream`, then a synchronisation.
+LORA_API int lora_meta_read_no_lora(const lora_meta_t *meta, void *stream, int32_t *no_lora)
+{
+    if (meta == nullptr || meta->no_lora_flag == nullptr || no_lora == nullptr)
+        return LORA_ERR_NULL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, meta->no_lora_flag, sizeof(v), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return int(e);
+    *no_lora = v != 0 ? 1 : 0;
+    return LORA_OK;
+}

@@ -2,8 +2,8 @@
  * lora_punica.h -- C ABI of the GB300 (sm_103a) multi-LoRA shrink/expand
  * library (liblora_punica.so).
  *
- * The three entry points are the three steps of the Punica-style batched
- * LoRA apply described by vLLM's API pages:
+ * The three core entry points are the three steps of the Punica-style
+ * batched LoRA apply described by vLLM's API pages:
  *
  *   lora_meta_prepare  page "vllm.lora.ops.triton_ops.lora_kernel_metadata",
  *                      class LoRAKernelMeta, methods make / _reset /
@@ -124,6 +124,26 @@ typedef struct lora_meta {
  */
 int lora_meta_prepare(const int32_t *token_lora_mapping, int32_t num_tokens,
                       const lora_meta_t *meta, void *stream);
+
+/*
+ * lora_meta_read_no_lora -- the host copy of the no-LoRA flag (page
+ * "vllm.lora.ops.triton_ops.lora_kernel_metadata", LoRAKernelMeta field
+ * no_lora_flag_cpu, set by prepare_tensors).
+ *
+ *   meta      the metadata a preceding lora_meta_prepare on `stream` wrote;
+ *             only meta->no_lora_flag is read.
+ *   stream    the stream that call was ordered on.
+ *   no_lora   HOST int32, receives 1 when every id of that batch is -1 (or
+ *             it had no tokens), else 0.
+ *
+ * Copies the 4-byte device flag to the host and synchronises `stream`, so
+ * it cannot be captured in a CUDA graph.  No other call needs it: every
+ * kernel reads the device flag itself and returns early.
+ * Errors: LORA_ERR_NULL for a NULL meta, meta->no_lora_flag or no_lora (on
+ * the host, before any CUDA call); a positive cudaError_t if the copy or the
+ * synchronisation fails (then *no_lora is left unchanged).
+ */
+int lora_meta_read_no_lora(const lora_meta_t *meta, void *stream, int32_t *no_lora);
 
 /*
  * lora_shrink -- y[s][t, :] += scale * x[t, :] @ lora_a[s][id(t)]^T for

@@ -80,6 +80,15 @@ def test_meta_prepare_rejects_bad_arguments(lib):
     assert lib.lora_meta_prepare(0x1000, 1, ctypes.byref(_meta(max_loras=1025)), None) == -2
 
 
+def test_read_no_lora_rejects_null_arguments(lib):
+    out = ctypes.c_int32(7)
+    assert lib.lora_meta_read_no_lora(None, None, ctypes.byref(out)) == -1
+    assert lib.lora_meta_read_no_lora(ctypes.byref(_meta()), None, None) == -1
+    assert lib.lora_meta_read_no_lora(ctypes.byref(_meta(null_field="no_lora_flag")), None,
+                                      ctypes.byref(out)) == -1
+    assert out.value == 7
+
+
 def test_shrink_rejects_bad_arguments(lib):
     m = _meta()
     A = (ctypes.c_void_p * 2)(0x2000, 0x3000)

@@ -83,6 +83,18 @@ def test_meta_no_lora_and_empty(oracle_mod):
     assert g.no_lora()
 
 
+def test_meta_read_no_lora_follows_each_batch(oracle_mod):
+    """The host read (lora_meta_read_no_lora) sees the flag of the batch the
+    last prepare wrote, in stream order, with no explicit synchronisation."""
+    import expand_gemm_gb300 as eg
+    from gpu_helpers import dev_i32
+    meta = eg.LoRAKernelMeta.make(4, 64, "cuda")
+    for ids, want in (([-1] * 64, True), ([-1] * 63 + [2], False), ([], True),
+                      ([9, -1], True), ([0], False)):
+        meta.prepare_tensors(dev_i32(np.array(ids, np.int32)))
+        assert meta.no_lora() is want, ids
+
+
 def test_meta_invalid_ids_counted(oracle_mod):
     ids = np.array([0, 9, -1, 2, -7, 0, 3, 3, 1 << 30], np.int32)
     g = _check(ids, 3, oracle_mod)
