@@ -458,10 +458,9 @@ def run_ours(args, rank, world):
         "e2e": e2e,
         "wall_s_timed": wall,
     }
+    # the oracle's CPU baseline is timed at N = 1 only
     if not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline(w, inp, target_s=10.0)
-    elif world > 1:
-        out["cpu_baseline"] = cpu_baseline(w, inp, target_s=10.0) if rank == 0 else None
     if dist:
         dist.destroy_process_group()
     return out
