@@ -417,12 +417,7 @@ def run_ours(args, rank, world):
         "dtype": "bf16",
         "data": "synthetic (seeded numpy PCG64; no dataset or weights)",
         "config": {
-            "workload": "%s: %s%s" % (w.name, w.description,
-                                      "" if args.num_tokens is None else
-                                      " (this run: %d tokens)" % w.num_tokens),
-            "num_tokens": T, "active_tokens": ub["t_active"], "distinct_loras": ub["distinct"],
-            "hidden": w.hidden, "rank": w.rank, "max_loras": w.max_loras,
-            "slices": list(w.slices), "bias": w.bias, "scale": w.scale,
+            **workload_config(w, ub, args),
             "l2": "inputs larger than L2: %d resident input sets of %.1f MB rotated "
                   "(%.0f MB total, L2 %.0f MB)" % (n_sets, base.nbytes / 1e6,
                                                    n_sets * base.nbytes / 1e6, l2 / 1e6),
@@ -590,6 +585,18 @@ def cpu_baseline(w, inp, target_s=10.0):
                       "%d tokens in %.1f s" % (sel.size, T, w.name, done, el)}
 
 
+def workload_config(w, ub, args):
+    """The workload part of the line's config, shared by both arms."""
+    return {
+        "workload": "%s: %s%s" % (w.name, w.description,
+                                  "" if args.num_tokens is None else
+                                  " (this run: %d tokens)" % w.num_tokens),
+        "num_tokens": w.num_tokens, "active_tokens": ub["t_active"],
+        "distinct_loras": ub["distinct"], "hidden": w.hidden, "rank": w.rank,
+        "max_loras": w.max_loras, "slices": list(w.slices), "bias": w.bias, "scale": w.scale,
+    }
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -622,7 +629,7 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy PCG64)",
-        "config": {"workload": "%s: %s" % (w.name, w.description), "num_tokens": T,
+        "config": {**workload_config(w, W.unique_bytes(w, inp.ids), args),
                    "parallelism": "host cores (OpenMP)"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cores(),
                          "kind": "oracle", "sample": sample},
