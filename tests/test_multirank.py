@@ -1,7 +1,8 @@
-"""The N > 1 host logic of bench.py, on CPU with two gloo ranks: replicas
-only, so the only exchange is the max-over-ranks of the timed region, the
+"""The host logic of bench.py on CPU: with two gloo ranks (replicas
+only, so the only exchange is the max-over-ranks of the timed region), the
 job's value counts every replica, and the reference arm runs on rank 0
-alone (the other ranks exit without work)."""
+alone (the other ranks exit without work); in one process, the reference
+arm's line carries the same workload config as the GPU arm's."""
 import os
 import socket
 import sys
@@ -57,3 +58,25 @@ def test_single_process_helpers():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.job_tokens_per_s(1, 256, 100, 10.0) == pytest.approx(256 * 100 / 0.010)
+
+
+def test_reference_line_matches_the_contract():
+    """The reference arm times the oracle on the host on the same workload
+    config as the GPU arm, with zero host-device bytes in its e2e."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    args = bench.parse_args(["--impl", "reference", "--workload", "tiny", "--steps", "3",
+                             "--warmup", "3"])
+    res = bench.run_reference(args, 0, 1)
+    assert res["impl"] == "reference" and res["metric"] == bench.METRIC
+    assert res["unit"] == "tokens/s" and res["higher_is_better"] is True
+    assert res["steps"] == 3 and res["warmup"] == 3 and res["value"] > 0
+    w = W.WORKLOADS["tiny"]
+    want = bench.workload_config(w, W.unique_bytes(w, W.generate(w).ids), args)
+    assert {k: v for k, v in res["config"].items() if k != "parallelism"} == want
+    assert res["e2e"] == {"value": res["value"], "unit": "tokens/s",
+                          "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    cb = res["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == res["value"] and cb["cores"] >= 1
+    assert "tokens" in cb["sample"]
