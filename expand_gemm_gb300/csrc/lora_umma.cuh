@@ -1,6 +1,7 @@
 // lora_umma.cuh -- inline-PTX wrappers for the Blackwell (sm_100 family)
-// asynchronous path: mbarriers, TMA tensor loads (2-D tile and tile::gather4),
-// and tcgen05 (TMEM allocation, UMMA issue/commit, TMEM loads), plus the
+// asynchronous path: mbarriers, TMA loads (2-D tiles, with or without
+// cluster multicast, and 1-D bulk copies), cluster rank and barrier, and
+// tcgen05 (TMEM allocation, UMMA issue/commit, TMEM loads), plus the
 // shared-memory and instruction descriptors UMMA takes.
 //
 // Every wait is bounded: it gives up after `deadline` (a clock64 value) and
@@ -103,46 +104,6 @@ __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
-// Four rows (r0..r3, any order, out-of-range rows read as zero) of one box
-// width starting at column c0; the map's box is one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int c0, int r0,
-                                            int r1, int r2, int r3, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2),
-           "r"(r3), "r"(bar)
-        : "memory");
-}
-
-// 2-D tile store from shared memory (bulk-group completion); elements of
-// the box outside the tensor are not written.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int c1, uint32_t src)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];\n"
-        :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(src) : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group()
-{
-    asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
-}
-
-// Wait until at most N bulk groups are pending reading their shared source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;\n" :: "n"(N) : "memory");
-}
-
-// Wait until every bulk group has completed (global writes performed).
-__device__ __forceinline__ void bulk_wait_group_all()
-{
-    asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
 }
 
 // 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
