@@ -43,7 +43,7 @@ E2E_GRAPH_STEPS = 16
 NCU_TRAFFIC = {
     # profiles/expand_decode_ncu.md: reads 8.915 MB (median of three
     # launches), writes 0 (the y writes stay in L2 past the end of the launch)
-    ("expand", "decode"): ("90b7d3f56e6aec76", 8914688),
+    ("expand", "decode"): ("9798a146a5d17271", 8914688),
 }
 
 # The source files each reported kernel is built from.

@@ -48,6 +48,26 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
             return;
         total_tiles = segments_from_sort(tot, base, p.nbins, EX_BM, tab);
         tokens = srt;
+    } else if (p.num_tokens <= EX_TOKLIST_MAX) {
+        // Small batches: the whole sorted token list is loaded together with
+        // the segment table (the loads are in flight while the table is
+        // read), then kept in shared memory, so no item waits on a token load.
+        int pre[EX_TOKLIST_MAX / EX_THREADS];
+#pragma unroll
+        for (int j = 0; j < EX_TOKLIST_MAX / EX_THREADS; ++j) {
+            const int i = threadIdx.x + j * EX_THREADS;
+            pre[j] = (i < p.num_tokens) ? p.sorted[i] : 0;
+        }
+        total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc, p.nbins, EX_BM,
+                                    tab);
+        int *s_list = reinterpret_cast<int *>(sA + Cfg::A_BYTES + seg_tab_bytes(p.nbins));
+#pragma unroll
+        for (int j = 0; j < EX_TOKLIST_MAX / EX_THREADS; ++j) {
+            const int i = threadIdx.x + j * EX_THREADS;
+            if (i < p.num_tokens) s_list[i] = pre[j];
+        }
+        __syncthreads();
+        tokens = s_list;
     } else {
         total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc, p.nbins, EX_BM,
                                     tab);
@@ -86,7 +106,9 @@ static int launch_expand_kt(const ExpandArgs &p, cudaStream_t stream)
         if (dev < 64) grid_cache[dev] = grid;
     }
     const size_t used = expand_smem_bytes(KT, p.nbins) +
-                        (p.map != nullptr ? expand_self_sort_bytes(p.nbins) : 0);
+                        (p.map != nullptr ? expand_self_sort_bytes(p.nbins)
+                         : p.num_tokens <= EX_TOKLIST_MAX ? size_t(p.num_tokens) * sizeof(int)
+                                                          : 0);
     e = launch_kernel(expand_kernel<KT>, dim3(grid), dim3(EX_THREADS), used, stream, p);
     return int(e);
 }

@@ -51,6 +51,9 @@ struct ExpandArgs {
 };
 
 constexpr int EX_SELF_SORT_MAX_TOKENS = 512;
+// Batches of up to this many tokens keep the whole sorted token list in
+// shared memory (4 bytes a token; within the self-sort area's size).
+constexpr int EX_TOKLIST_MAX = 1024;
 constexpr int EX_SELF_SORT_MAX_LORAS = 256;
 
 inline size_t expand_self_sort_bytes(int nbins)
