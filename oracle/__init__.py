@@ -42,37 +42,55 @@ _I64 = ctypes.c_int64
 _I32 = ctypes.c_int32
 
 
+def compile_source(src: str, out: str) -> str:
+    """Compile an oracle C source into a shared library with the flags
+    :func:`build` uses (the mutation tests build altered copies this way)."""
+    tmp = out + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-std=gnu11", "-O2", "-fopenmp", "-ffp-contract=off",
+           "-fPIC", "-shared", "-Wall", "-o", tmp, src]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
     """Compile ``lora_oracle.c`` into ``liblora_oracle.so`` beside it."""
     stale = (not os.path.exists(_LIB_PATH)
              or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
     if force or stale:
-        tmp = _LIB_PATH + ".tmp%d" % os.getpid()
-        cmd = ["gcc", "-std=gnu11", "-O2", "-fopenmp", "-ffp-contract=off",
-               "-fPIC", "-shared", "-Wall", "-o", tmp, _SRC]
-        subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB_PATH)
+        compile_source(_SRC, _LIB_PATH)
     return _LIB_PATH
+
+
+def _bind(lib):
+    lib.oracle_bf16_to_f64.argtypes = [_P, _I64, _P]
+    lib.oracle_bf16_to_f64.restype = None
+    lib.oracle_meta_prepare.argtypes = [_P, _I64, _I32, _P, _P, _P, _P, _P, _P]
+    lib.oracle_meta_prepare.restype = _I64
+    lib.oracle_shrink.argtypes = [_P, _I64, _I64, _I64, _P, _I32, _I32, _I32, _P,
+                                  ctypes.c_double, _P, _P]
+    lib.oracle_shrink.restype = None
+    lib.oracle_expand.argtypes = [_P, _I64, _I32, _P, _P, _P, _I32, _I32, _P, _P, _I64,
+                                  _I64, _I32, _P]
+    lib.oracle_expand.restype = None
+    return lib
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            lib.oracle_bf16_to_f64.argtypes = [_P, _I64, _P]
-            lib.oracle_bf16_to_f64.restype = None
-            lib.oracle_meta_prepare.argtypes = [_P, _I64, _I32, _P, _P, _P, _P,
-                                                _P, _P]
-            lib.oracle_meta_prepare.restype = _I64
-            lib.oracle_shrink.argtypes = [_P, _I64, _I64, _I64, _P, _I32, _I32,
-                                          _I32, _P, ctypes.c_double, _P, _P]
-            lib.oracle_shrink.restype = None
-            lib.oracle_expand.argtypes = [_P, _I64, _I32, _P, _P, _P, _I32,
-                                          _I32, _P, _P, _I64, _I64, _I32, _P]
-            lib.oracle_expand.restype = None
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+def load_library(path: str) -> None:
+    """Bind this module to another build of the oracle source, such as a
+    copy with a planted mistake (the mutation tests do this in a child
+    process, to check that the pins catch the mistake)."""
+    global _lib
+    with _lock:
+        _lib = _bind(ctypes.CDLL(os.path.abspath(path)))
 
 
 def _ptr(a: np.ndarray) -> int:

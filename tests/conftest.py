@@ -17,4 +17,9 @@ def pytest_configure(config):
 def oracle_mod():
     import oracle
     oracle.build()
+    # tests/test_oracle_mutants.py runs the pins in a child process against
+    # a build of the oracle with a planted mistake
+    mutant = os.environ.get("ORACLE_MUTANT_LIB")
+    if mutant:
+        oracle.load_library(mutant)
     return oracle
