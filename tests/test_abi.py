@@ -153,3 +153,52 @@ def test_linear_noalloc_rejects_sizes_above_its_buffer(lib):
     assert call(8, S=0) == -5
     assert call(8, S=2, r=12) == -4
     assert call(-1) == -2
+
+
+def test_expand_bf16_rejects_bad_arguments(lib):
+    """Same host checks as lora_expand, on a bf16 input."""
+    m = _meta()
+    B = (ctypes.c_void_p * 2)(0x2000, 0x3000)
+    sizes = (ctypes.c_int32 * 2)(64, 32)
+    ok = dict(x=0x4000, B=B, sizes=sizes, S=2, r=16, y=0x5000, ld=96, T=8, off=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.lora_expand_bf16(a["x"], a["B"], None, a["sizes"], a["S"], a["r"], a["y"],
+                                    a["ld"], a["T"], a["off"], 1, ctypes.byref(m), None)
+    assert call(S=0) == -5
+    assert call(S=9) == -5
+    assert call(r=20) == -4
+    assert call(ld=95) == -7
+    assert call(off=-1) == -2
+    assert call(T=17) == -6
+    assert call(sizes=(ctypes.c_int32 * 2)(64, -1)) == -2
+    assert call(B=(ctypes.c_void_p * 2)(0, 0x3000)) == -1
+    assert call(x=0x4002) == -3
+    assert call(T=0) == 0
+
+
+def test_linear_rejects_bad_arguments(lib):
+    """lora_linear's own checks, all on the host before any CUDA call."""
+    m = _meta()
+    A = (ctypes.c_void_p * 2)(0x2000, 0x3000)
+    B = (ctypes.c_void_p * 2)(0x6000, 0x7000)
+    sizes = (ctypes.c_int32 * 2)(64, 64)
+    ok = dict(meta=ctypes.byref(m), A=A, B=B, sizes=sizes, S=2, r=16, T=8, H=64, x_ld=64)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.lora_linear(0x1000, a["T"], 0x4000, a["H"], a["x_ld"], a["A"], a["B"], None,
+                               a["sizes"], a["S"], a["r"], 1.0, 0x8000, 0x5000, 128, a["meta"],
+                               None)
+    assert call(meta=None) == -1
+    assert call(A=None) == -1
+    assert call(B=None) == -1
+    assert call(sizes=None) == -1
+    assert call(S=0) == -5
+    assert call(S=9) == -5
+    assert call(r=12) == -4
+    assert call(r=136) == -4
+    assert call(T=-1) == -2
+    assert call(x_ld=32) == -2
+    assert call(T=17) == -6
