@@ -9,7 +9,8 @@ is no CPU fallback: without the built library every call raises.
 Names follow vLLM's API pages:
 
 * :class:`LoRAKernelMeta` -- page ``vllm.lora.ops.triton_ops.lora_kernel_metadata``
-  (``make``, ``prepare_tensors``, ``meta_args``).
+  (``make``, ``prepare_tensors``, ``meta_args``; ``no_lora`` is the host copy of
+  the flag, the page's ``no_lora_flag_cpu``).
 * :func:`lora_shrink`, :func:`lora_expand`, :func:`add_lora_linear`,
   :func:`add_lora_embedding`, :func:`add_lora_logits` -- page
   ``vllm.lora.punica_wrapper.punica_gpu`` (``PunicaWrapperGPU.add_shrink``,
@@ -55,6 +56,17 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
 
 
+def _same_device(meta: "LoRAKernelMeta", named) -> None:
+    """Every tensor of ``named`` ((name, tensor or None) pairs) must be on
+    the GPU that holds the metadata: the kernels take raw pointers, so a
+    tensor on another device would be read through the wrong address space."""
+    dev = meta.no_lora_flag.get_device()
+    for name, t in named:
+        if t is not None and t.get_device() != dev:
+            raise ValueError("%s is on cuda:%d, the metadata on cuda:%d"
+                             % (name, t.get_device(), dev))
+
+
 def _ptr_array(tensors) -> ctypes.Array:
     arr = (ctypes.c_void_p * len(tensors))()
     for i, t in enumerate(tensors):
@@ -67,13 +79,16 @@ class LoRAKernelMeta:
 
     Buffers are int32 device tensors allocated once by :meth:`make`; the
     no-LoRA flag lives on the device (the kernels read it there, so no host
-    sync is needed); ``error_word`` counts ids outside ``[-1, max_loras)``
-    seen by the last :meth:`prepare_tensors`.
+    sync is needed; :meth:`no_lora` copies it to the host on request);
+    ``error_word`` counts ids outside ``[-1, max_loras)`` seen by the last
+    :meth:`prepare_tensors`.
     """
 
     def __init__(self, max_loras: int, max_num_tokens: int, device):
         if not 1 <= max_loras <= LORA_MAX_LORAS:
             raise ValueError("max_loras must be in [1, %d]" % LORA_MAX_LORAS)
+        if max_num_tokens < 0:
+            raise ValueError("max_num_tokens must be >= 0")
         dev = torch.device(device)
         i32 = dict(dtype=torch.int32, device=dev)
         self.max_loras = int(max_loras)
@@ -128,6 +143,7 @@ def lora_meta_prepare(token_lora_mapping: torch.Tensor, meta: LoRAKernelMeta) ->
     _need(m, "token_lora_mapping", torch.int32)
     if m.dim() != 1 or not m.is_contiguous():
         raise ValueError("token_lora_mapping must be a contiguous 1-D tensor")
+    _same_device(meta, [("token_lora_mapping", m)])
     st = _lib.load().lora_meta_prepare(m.data_ptr() if m.numel() else None, m.numel(),
                                       ctypes.byref(meta.c), _stream_handle(meta.device))
     _lib.check("lora_meta_prepare", st)
@@ -166,6 +182,8 @@ def lora_shrink(x: torch.Tensor, lora_a_stacked, y: torch.Tensor,
         raise ValueError("lora_a_stacked has %d LoRAs, metadata expects %d" % (L, meta.max_loras))
     if tuple(y.shape) != (len(A), T, r) or not y.is_contiguous():
         raise ValueError("y must be a contiguous fp32 [%d, %d, %d] tensor" % (len(A), T, r))
+    _same_device(meta, [("x", x), ("y", y)] +
+                 [("lora_a_stacked[%d]" % i, a) for i, a in enumerate(A)])
     st = _lib.load().lora_shrink(x2.data_ptr(), T, H, x2.stride(0), _ptr_array(A), len(A), r,
                                  y.data_ptr(), ctypes.byref(meta.c), float(scale),
                                  _stream_handle(x.device))
@@ -211,6 +229,10 @@ def lora_expand(x: torch.Tensor, lora_b_stacked, y: torch.Tensor,
                 raise ValueError("lora_bias_stacked[%d] must be [%d, %d]" % (i, L, n))
             bl.append(bb)
         bias_arr = _ptr_array(bl)
+    biases = () if lora_bias_stacked is None else lora_bias_stacked
+    _same_device(meta, [("x", x), ("y", y)] +
+                 [("lora_b_stacked[%d]" % i, b) for i, b in enumerate(B)] +
+                 [("lora_bias_stacked[%d]" % i, b) for i, b in enumerate(biases)])
     size_arr = (ctypes.c_int32 * S)(*sizes)
     fn = "lora_expand_bf16" if x.dtype == torch.bfloat16 else "lora_expand"
     st = getattr(_lib.load(), fn)(x.data_ptr(), _ptr_array(B), bias_arr, size_arr, S, r,
@@ -295,8 +317,8 @@ def _linear_args(token_lora_mapping, x, lora_a_stacked, lora_b_stacked, lora_bia
     if Ha != H or any(a.shape != A[0].shape for a in A):
         raise ValueError("lora_a_stacked shapes must all be [L, r, %d]" % H)
     for i, b in enumerate(B):
-        if b.size(2) != r:
-            raise ValueError("lora_b_stacked[%d] must be [L, n, %d]" % (i, r))
+        if b.size(0) != B[0].size(0) or b.size(2) != r:
+            raise ValueError("lora_b_stacked[%d] must be [%d, n, %d]" % (i, B[0].size(0), r))
     if buffer is not None:
         _need(buffer, "buffer", torch.float32)
         if tuple(buffer.shape) != (len(A), T, r) or not buffer.is_contiguous():
@@ -314,7 +336,12 @@ def _linear_args(token_lora_mapping, x, lora_a_stacked, lora_b_stacked, lora_bia
                     raise ValueError("lora_bias_stacked[%d] must be [L, %d]" % (i, n))
         bias_arr = _ptr_array(list(lora_bias_stacked))
     size_arr = (ctypes.c_int32 * len(B))(*sizes)
-    return dict(L=L, nb=B[0].size(0),
+    named = ([("token_lora_mapping", m), ("x", x), ("y", y), ("buffer", buffer)] +
+             [("lora_a_stacked[%d]" % i, a) for i, a in enumerate(A)] +
+             [("lora_b_stacked[%d]" % i, b) for i, b in enumerate(B)] +
+             [("lora_bias_stacked[%d]" % i, b)
+              for i, b in enumerate(() if lora_bias_stacked is None else lora_bias_stacked)])
+    return dict(L=L, nb=B[0].size(0), named=named,
                 head=(m.data_ptr(), T, x2.data_ptr(), H, x2.stride(0), _ptr_array(A),
                       _ptr_array(B), bias_arr, size_arr, len(B), r),
                 buf=None if buffer is None else buffer.data_ptr(),
@@ -334,6 +361,7 @@ def lora_linear(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_a_stacke
                      buffer, y)
     if a["L"] < meta.max_loras or a["nb"] < meta.max_loras:
         raise ValueError("weights hold fewer LoRAs than the metadata expects")
+    _same_device(meta, a["named"])
     st = _lib.load().lora_linear(*a["head"], float(scale), a["buf"], *a["tail"],
                                  ctypes.byref(meta.c), _stream_handle(x.device))
     _lib.check("lora_linear", st)
@@ -351,6 +379,7 @@ def lora_linear_noalloc(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_
                      None, y)
     if a["L"] < meta.max_loras or a["nb"] < meta.max_loras:
         raise ValueError("weights hold fewer LoRAs than the metadata expects")
+    _same_device(meta, a["named"])
     st = _lib.load().lora_linear_noalloc(*a["head"], float(scale), *a["tail"],
                                          ctypes.byref(meta.c), _stream_handle(x.device))
     _lib.check("lora_linear_noalloc", st)
