@@ -540,13 +540,6 @@ def run_e2e(args, inp, w, dev, eg, stream, step):
 
 # ------------------------------------------------------ oracle (CPU) arm
 
-def _cores():
-    try:
-        return len(os.sched_getaffinity(0))
-    except AttributeError:
-        return os.cpu_count() or 1
-
-
 def _oracle_step(oracle, w, inp, sel):
     """One oracle pass: metadata on the whole map, shrink + expand (expand of
     the bf16 input for an embedding workload) on tokens sel."""
@@ -580,7 +573,8 @@ def cpu_baseline(w, inp, target_s=10.0):
         el = time.perf_counter() - t0
         if el >= target_s:
             break
-    return {"value": done / el, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+    return {"value": done / el, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
             "sample": "%d of %d tokens of the %s batch per pass (metadata on the full map), "
                       "%d tokens in %.1f s" % (sel.size, T, w.name, done, el)}
 
@@ -631,7 +625,7 @@ def run_reference(args, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy PCG64)",
         "config": {**workload_config(w, W.unique_bytes(w, inp.ids), args),
                    "parallelism": "host cores (OpenMP)"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cores(),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

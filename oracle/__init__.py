@@ -73,6 +73,8 @@ def _bind(lib):
     lib.oracle_expand.argtypes = [_P, _I64, _I32, _P, _P, _P, _I32, _I32, _P, _P, _I64,
                                   _I64, _I32, _P]
     lib.oracle_expand.restype = None
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = ctypes.c_int
     return lib
 
 
@@ -104,6 +106,12 @@ def _ptr_array(arrays):
     for i, a in enumerate(arrays):
         arr[i] = None if a is None else _ptr(a)
     return arr
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops run on (OMP_NUM_THREADS, else the
+    cores this process may use)."""
+    return int(_load().oracle_num_threads())
 
 
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:

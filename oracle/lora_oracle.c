@@ -34,9 +34,16 @@
  *     other rows are left untouched in both modes.
  *   - bias columns are shifted by offset_start like the product.
  */
+#include <omp.h>
 #include <stdint.h>
 #include <stddef.h>
 #include <string.h>
+
+/* Threads the OpenMP loops below run on (reported with CPU timings). */
+int oracle_num_threads(void)
+{
+    return omp_get_max_threads();
+}
 
 /* bf16 is the upper 16 bits of an IEEE-754 binary32: widening is exact. */
 static double bf16_to_f64(uint16_t b)
