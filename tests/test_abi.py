@@ -202,3 +202,33 @@ def test_linear_rejects_bad_arguments(lib):
     assert call(T=-1) == -2
     assert call(x_ld=32) == -2
     assert call(T=17) == -6
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """A C99 program (no C++, no CUDA headers) includes the header, links
+    the library and calls entry points that need no GPU."""
+    import shutil
+    import subprocess
+    from expand_gemm_gb300 import _lib
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not found")
+    src = tmp_path / "consumer.c"
+    src.write_text(
+        '#include <stdio.h>\n'
+        '#include "lora_punica.h"\n'
+        'int main(void)\n'
+        '{\n'
+        '    lora_meta_t m = {0};\n'
+        '    int32_t out = 7;\n'
+        '    printf("%d %s %d %d\\n", lora_version(), lora_status_string(LORA_ERR_RANK),\n'
+        '           lora_meta_read_no_lora(&m, NULL, &out), out);\n'
+        '    return 0;\n'
+        '}\n')
+    exe = tmp_path / "consumer"
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-L", libdir, "-llora_punica",
+                    "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    assert out[0] == "1" and out[-2:] == ["-1", "7"]
+    assert " ".join(out[1:-2]) == lib.lora_status_string(-4).decode()
