@@ -67,6 +67,15 @@ def _same_device(meta: "LoRAKernelMeta", named) -> None:
                              % (name, t.get_device(), dev))
 
 
+def _call(fn: str, device: torch.device, *args) -> None:
+    """Calls library entry point `fn` with `device` current (the library
+    looks up per-device state for the current device), then raises on a
+    non-zero status."""
+    with torch.cuda.device(device):
+        st = getattr(_lib.load(), fn)(*args)
+    _lib.check(fn, st)
+
+
 def _ptr_array(tensors) -> ctypes.Array:
     arr = (ctypes.c_void_p * len(tensors))()
     for i, t in enumerate(tensors):
@@ -132,9 +141,8 @@ class LoRAKernelMeta:
         """Host read of the flag through ``lora_meta_read_no_lora``
         (synchronises the current stream; the kernels never need it)."""
         out = ctypes.c_int32(-1)
-        st = _lib.load().lora_meta_read_no_lora(ctypes.byref(self.c), _stream_handle(self.device),
-                                               ctypes.byref(out))
-        _lib.check("lora_meta_read_no_lora", st)
+        _call("lora_meta_read_no_lora", self.device, ctypes.byref(self.c),
+              _stream_handle(self.device), ctypes.byref(out))
         return bool(out.value)
 
 
@@ -144,9 +152,8 @@ def lora_meta_prepare(token_lora_mapping: torch.Tensor, meta: LoRAKernelMeta) ->
     if m.dim() != 1 or not m.is_contiguous():
         raise ValueError("token_lora_mapping must be a contiguous 1-D tensor")
     _same_device(meta, [("token_lora_mapping", m)])
-    st = _lib.load().lora_meta_prepare(m.data_ptr() if m.numel() else None, m.numel(),
-                                      ctypes.byref(meta.c), _stream_handle(meta.device))
-    _lib.check("lora_meta_prepare", st)
+    _call("lora_meta_prepare", meta.device, m.data_ptr() if m.numel() else None, m.numel(),
+          ctypes.byref(meta.c), _stream_handle(meta.device))
 
 
 def _weights(ws: Sequence[torch.Tensor], name: str):
@@ -184,10 +191,8 @@ def lora_shrink(x: torch.Tensor, lora_a_stacked, y: torch.Tensor,
         raise ValueError("y must be a contiguous fp32 [%d, %d, %d] tensor" % (len(A), T, r))
     _same_device(meta, [("x", x), ("y", y)] +
                  [("lora_a_stacked[%d]" % i, a) for i, a in enumerate(A)])
-    st = _lib.load().lora_shrink(x2.data_ptr(), T, H, x2.stride(0), _ptr_array(A), len(A), r,
-                                 y.data_ptr(), ctypes.byref(meta.c), float(scale),
-                                 _stream_handle(x.device))
-    _lib.check("lora_shrink", st)
+    _call("lora_shrink", x.device, x2.data_ptr(), T, H, x2.stride(0), _ptr_array(A), len(A), r,
+          y.data_ptr(), ctypes.byref(meta.c), float(scale), _stream_handle(x.device))
 
 
 def lora_expand(x: torch.Tensor, lora_b_stacked, y: torch.Tensor,
@@ -235,11 +240,9 @@ def lora_expand(x: torch.Tensor, lora_b_stacked, y: torch.Tensor,
                  [("lora_bias_stacked[%d]" % i, b) for i, b in enumerate(biases)])
     size_arr = (ctypes.c_int32 * S)(*sizes)
     fn = "lora_expand_bf16" if x.dtype == torch.bfloat16 else "lora_expand"
-    st = getattr(_lib.load(), fn)(x.data_ptr(), _ptr_array(B), bias_arr, size_arr, S, r,
-                                  y2.data_ptr(), y2.stride(0), T, int(offset_start),
-                                  1 if add_inputs else 0, ctypes.byref(meta.c),
-                                  _stream_handle(x.device))
-    _lib.check(fn, st)
+    _call(fn, x.device, x.data_ptr(), _ptr_array(B), bias_arr, size_arr, S, r,
+          y2.data_ptr(), y2.stride(0), T, int(offset_start), 1 if add_inputs else 0,
+          ctypes.byref(meta.c), _stream_handle(x.device))
 
 
 def add_lora_embedding(y: torch.Tensor, x: torch.Tensor, lora_b_stacked,
@@ -362,9 +365,8 @@ def lora_linear(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_a_stacke
     if a["L"] < meta.max_loras or a["nb"] < meta.max_loras:
         raise ValueError("weights hold fewer LoRAs than the metadata expects")
     _same_device(meta, a["named"])
-    st = _lib.load().lora_linear(*a["head"], float(scale), a["buf"], *a["tail"],
-                                 ctypes.byref(meta.c), _stream_handle(x.device))
-    _lib.check("lora_linear", st)
+    _call("lora_linear", x.device, *a["head"], float(scale), a["buf"], *a["tail"],
+          ctypes.byref(meta.c), _stream_handle(x.device))
 
 
 def lora_linear_noalloc(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_a_stacked,
@@ -380,6 +382,5 @@ def lora_linear_noalloc(token_lora_mapping: torch.Tensor, x: torch.Tensor, lora_
     if a["L"] < meta.max_loras or a["nb"] < meta.max_loras:
         raise ValueError("weights hold fewer LoRAs than the metadata expects")
     _same_device(meta, a["named"])
-    st = _lib.load().lora_linear_noalloc(*a["head"], float(scale), *a["tail"],
-                                         ctypes.byref(meta.c), _stream_handle(x.device))
-    _lib.check("lora_linear_noalloc", st)
+    _call("lora_linear_noalloc", x.device, *a["head"], float(scale), *a["tail"],
+          ctypes.byref(meta.c), _stream_handle(x.device))

@@ -29,10 +29,18 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_tok[EX_BM];
 
-    if (!p.early) {
-        pdl_wait();
-        pdl_launch_dependents();
-    }
+    // In early mode every CTA still passes the grid-dependency wait before it
+    // exits (no tile, no item, or the no-LoRA batch), so the kernel completes
+    // only after everything before it in the stream has.
+    bool waited = false;
+    auto wait_once = [&]() {
+        if (!waited) {
+            pdl_wait();
+            pdl_launch_dependents();
+            waited = true;
+        }
+    };
+    if (!p.early) wait_once();
 
     uint8_t *sA = smem + EX_STAGES * Cfg::STAGE_BYTES;
     const SegTab tab = seg_tab(reinterpret_cast<int *>(sA + Cfg::A_BYTES), p.nbins);
@@ -44,8 +52,10 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
         int *srt = pos + p.nbins, *ids = srt + EX_SELF_SORT_MAX_TOKENS;
         int *misc = ids + EX_SELF_SORT_MAX_TOKENS;
         if (block_sort_ids<EX_THREADS / 32>(p.map, p.num_tokens, p.nbins - 1, cnt, tot, base,
-                                            pos, srt, misc, ids))
+                                            pos, srt, misc, ids)) {
+            wait_once();
             return;
+        }
         total_tiles = segments_from_sort(tot, base, p.nbins, EX_BM, tab);
         tokens = srt;
     } else if (p.num_tokens <= EX_TOKLIST_MAX) {
@@ -72,16 +82,17 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
         total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc, p.nbins, EX_BM,
                                     tab);
     }
-    if (total_tiles == 0) return;
+    if (total_tiles == 0) {
+        wait_once();
+        return;
+    }
     // early mode: the grid-dependency wait sits right before the first read
     // of the shrink output
     expand_items<KT>(p, tab, tokens, total_tiles, smem, s_tok, [&]() {
-        if (p.early) {
-            pdl_wait();
-            pdl_launch_dependents();
-        }
+        wait_once();
         return true;
     });
+    wait_once();                              // a CTA that had no item
 }
 
 template <int KT>

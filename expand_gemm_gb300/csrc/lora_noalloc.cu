@@ -19,13 +19,17 @@
 // that overlap on the GPU (other streams, other threads) race on it and must
 // be serialised by the caller.  Each call clears the part it uses before the
 // shrink accumulates into it.
+#include <atomic>
+
 #include "lora_common.cuh"
 
 namespace lora {
 
 static __device__ __align__(256) float g_noalloc_buf[LORA_NOALLOC_MAX_FLOATS];
 
-static float *noalloc_ptr[64] = {nullptr};
+// Per-device address of g_noalloc_buf (host threads may race to fill an
+// entry; they all store the same value).
+static std::atomic<float *> noalloc_ptr[64];
 
 }  // namespace lora
 
@@ -48,14 +52,23 @@ LORA_API int lora_linear_noalloc(const int32_t *token_lora_mapping, int32_t num_
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return int(e);
     if (dev < 0 || dev >= 64) return LORA_ERR_DEVICE;
-    if (lora::noalloc_ptr[dev] == nullptr) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The array is looked up for the current device, so the stream must
+    // belong to it (a stream of another GPU would be handed this GPU's array).
+    if (st != nullptr) {
+        int sdev = -1;
+        e = cudaStreamGetDevice(st, &sdev);
+        if (e != cudaSuccess) return int(e);
+        if (sdev != dev) return LORA_ERR_DEVICE;
+    }
+    float *buf = lora::noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (buf == nullptr) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, lora::g_noalloc_buf);
         if (e != cudaSuccess) return int(e);
-        lora::noalloc_ptr[dev] = static_cast<float *>(p);
+        buf = static_cast<float *>(p);
+        lora::noalloc_ptr[dev].store(buf, std::memory_order_release);
     }
-    float *buf = lora::noalloc_ptr[dev];
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (floats > 0) {
         e = cudaMemsetAsync(buf, 0, size_t(floats) * sizeof(float), st);
         if (e != cudaSuccess) return int(e);

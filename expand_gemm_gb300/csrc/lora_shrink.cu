@@ -103,11 +103,18 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
     __shared__ int s_tok[SH_BN];
 
     bool waited = false;
-    if (!p.early) {
-        pdl_wait();
-        pdl_launch_dependents();
-        waited = true;
-    }
+    // Every CTA passes the grid-dependency wait before it exits, whichever
+    // way it leaves: a kernel's completion then implies the completion of
+    // everything before it in the stream, which the expand that follows (it
+    // reads the metadata before its own wait) relies on.
+    auto wait_once = [&]() {
+        if (!waited) {
+            pdl_wait();
+            pdl_launch_dependents();
+            waited = true;
+        }
+    };
+    if (!p.early) wait_once();
 
     const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + Cfg::RING_BYTES), p.nbins);
     const int32_t *tokens = p.sorted;
@@ -123,14 +130,20 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
             write_meta(p.map, p.num_tokens, p.nbins - 1, nl, tot, base, pos, srt, misc,
                        p.mapping_copy, p.sorted_out, p.counts_out, p.start_out, p.active_out,
                        p.no_lora_out, p.error_out);
-        if (nl) return;
+        if (nl) {
+            wait_once();
+            return;
+        }
         total_tiles = segments_from_sort(tot, base, p.nbins, SH_BN, tab);
         tokens = srt;
     } else {
         total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
                                     p.nbins, SH_BN, tab, false, p.skip_rows);
     }
-    if (total_tiles == 0) return;
+    if (total_tiles == 0) {
+        wait_once();
+        return;
+    }
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = p.num_slices, H = p.hidden, T = p.num_tokens, R = p.rank;
@@ -213,11 +226,7 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
             cp_async_commit();
         }
 
-        if (!waited) {                        // y (the buffer) is written from here on
-            pdl_wait();
-            pdl_launch_dependents();
-            waited = true;
-        }
+        wait_once();                          // y (the buffer) is written from here on
         for (int ks = 0; ks < k_steps; ++ks) {
             cp_async_wait<SH_STAGES - 2>();
             __syncthreads();
@@ -284,6 +293,7 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
         }
         __syncthreads();
     }
+    wait_once();                              // a CTA that had no item
 }
 
 template <int MT>

@@ -49,7 +49,6 @@ constexpr int UM_MIN_BLOCKS = 8;      // shortest hidden chunk of a split item
 struct UmmaShrinkArgs {
     CUtensorMap map_x[UM_XMAPS];               // x: [T, H], box {64, 2^i rows}
     CUtensorMap map_a[LORA_MAX_SLICES];        // A[s]: [L * r, H], box {64, RP}
-    CUtensorMap map_ah[LORA_MAX_SLICES];       // the same, box {64, RP / 2} (cluster form)
     float *y;
     float scale;
     int32_t num_tokens;
@@ -70,8 +69,7 @@ struct UmmaShrinkArgs {
 };
 
 struct UmmaLayout {
-    int x_bytes, a_bytes, stage_bytes, ring_bytes, bar_off, misc_off, piece_off, tab_off,
-        pair_off, total;
+    int x_bytes, a_bytes, stage_bytes, ring_bytes, bar_off, misc_off, piece_off, tab_off, total;
 };
 
 // Split of the hidden dimension: the number of chunks (items per tile)
@@ -107,8 +105,7 @@ __host__ __device__ inline UmmaLayout umma_layout(int S, int rp, int stages, int
     l.misc_off = l.bar_off + (2 * UM_MAX_STAGES + 3) * 8; // tmem base, abort flag
     l.piece_off = l.misc_off + 16;                      // [UM_BM] (row, token, log2 rows)
     l.tab_off = l.piece_off + UM_BM * 4;
-    l.pair_off = l.tab_off + int(seg_tab_bytes(nbins));  // [nbins + 1] tile pairs before k
-    l.total = l.pair_off + (nbins + 1) * 4 + 1024;        // + alignment slack
+    l.total = l.tab_off + int(seg_tab_bytes(nbins)) + 1024;   // + alignment slack
     return l;
 }
 
@@ -346,292 +343,6 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
 }
 
 
-// ---------------------------------------------------------- cluster form
-//
-// (Opt-in, see launch_shrink_umma.)  The same work by clusters of two CTAs (one per SM, each with its own
-// TMEM accumulators and epilogue) that take two tiles of the same LoRA
-// segment over the same hidden chunk at once.  The A block of a stage is
-// the same for both, so each CTA loads half of every slice's A rows with a
-// multicast TMA into the stage of both CTAs: per 64-wide hidden block an SM
-// moves 128 x rows + S * RP / 2 A rows instead of 128 + S * RP, which is
-// what bounds the single-CTA form (the TMA engine's rate for 128-byte rows).
-//   - full[stage] of a CTA expects its own x bytes plus all A bytes (half
-//     from each CTA's multicast);
-//   - empty[stage] of a CTA counts two arrivals: the UMMA commits of both
-//     CTAs are multicast to both, so neither refills a stage (which writes
-//     into the partner too) before both have consumed it;
-//   - a segment with an odd number of tiles leaves the second CTA of its
-//     last pair without a tile: it loads and signals like its partner but
-//     issues no UMMA and has no epilogue for that item;
-//   - the cluster synchronises after the barrier set-up and before exit,
-//     so no multicast write or remote arrival reaches an exited CTA.  Every
-//     other wait is bounded as in the single-CTA form.
-__global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_mc_kernel(const __grid_constant__ UmmaShrinkArgs p)
-{
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int S = p.num_slices, RP = p.rp, STAGES = p.stages, HALF = RP / 2;
-    const UmmaLayout L = umma_layout(S, RP, STAGES, p.nbins);
-    const uint32_t base = smem_addr(smem);
-    const uint32_t bar_full = base + L.bar_off;
-    const uint32_t bar_empty = bar_full + 8 * UM_MAX_STAGES;
-    const uint32_t bar_acc_full = bar_empty + 8 * UM_MAX_STAGES;
-    const uint32_t bar_acc_empty = bar_acc_full + 8;
-    const uint32_t bar_drain = bar_acc_empty + 8;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L.misc_off);
-    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L.misc_off + 4);
-    int *ppair = reinterpret_cast<int *>(smem + L.pair_off);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rank = int(cluster_rank());                 // 0 or 1
-    const uint16_t both = 0x3;
-
-    pdl_wait();
-    pdl_launch_dependents();
-
-    if (tid == 0) {
-        for (int i = 0; i < STAGES; ++i) {
-            mbar_init(bar_full + 8 * i, 1);
-            mbar_init(bar_empty + 8 * i, 2);              // both CTAs' UMMA commits
-        }
-        mbar_init(bar_acc_full, 1);
-        mbar_init(bar_acc_empty, 4);
-        mbar_init(bar_drain, 1);
-        mbar_fence_init();
-        *s_abort = 0;
-        for (int s = 0; s < S; ++s) tma_prefetch_map(&p.map_ah[s]);
-        for (int i = 0; i < UM_XMAPS; ++i) tma_prefetch_map(&p.map_x[i]);
-    }
-    cluster_sync();                                       // barriers ready in both CTAs
-
-    const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + L.tab_off), p.nbins);
-    const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
-                                          p.nbins, UM_BM, tab, /*full_tiles_only=*/!p.partial);
-    if (total_tiles == 0) return;                         // the same in both CTAs
-    // pairs of tiles per segment (an odd last tile is a pair of its own)
-    if (tid < 32) {
-        int carry = 0;
-        for (int b0 = 0; b0 < p.nbins; b0 += 32) {
-            const int k = b0 + lane;
-            const int n = (k < p.nbins) ? (tab.tile[k + 1] - tab.tile[k] + 1) / 2 : 0;
-            int v = n;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += u;
-            }
-            if (k < p.nbins) ppair[k] = carry + v - n;
-            carry += __shfl_sync(0xffffffffu, v, 31);
-        }
-        if (lane == 0) ppair[p.nbins] = carry;
-    }
-    __syncthreads();
-    const int total_pairs = ppair[p.nbins];
-    const int H = p.hidden, R = p.rank, T = p.num_tokens;
-    const int nk = (H + UM_BK - 1) / UM_BK;
-    const int nclusters = int(gridDim.x) / 2, cid = int(blockIdx.x) / 2;
-    const int kchunks = umma_kchunks(total_pairs, nk, nclusters);
-    const int spc = (nk + kchunks - 1) / kchunks;
-    const bool split = kchunks > 1;
-    const int total_items = total_pairs * kchunks;        // item = kc * total_pairs + pair
-    if (cid >= total_items) return;                       // the same in both CTAs
-
-    // This CTA's tile of a pair: segment, first row, rows (0: no tile).
-    auto my_tile = [&](int pair, int &seg, int &row0, int &nrows) {
-        seg = find_segment(ppair, p.nbins, pair);
-        const int t = 2 * (pair - ppair[seg]) + rank;
-        const int ntl = tab.tile[seg + 1] - tab.tile[seg];
-        row0 = tab.start[seg] + t * UM_BM;
-        nrows = (t < ntl) ? min(UM_BM, tab.start[seg] + tab.count[seg] - row0) : 0;
-    };
-
-    if (warp == UM_MMA_WARP) tmem_alloc(smem_addr(s_tmem), p.tmem_cols);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *s_tmem;
-
-    const long long deadline = clock64() + UM_TIMEOUT_CYCLES;
-
-    if (warp == 0) {
-        // ------------------------------------------------------ producer
-        uint32_t *pieces = reinterpret_cast<uint32_t *>(smem + L.piece_off);
-        int stage = 0;
-        uint32_t phase = 0;
-        int issued = 0;
-        bool ok = true;
-        for (int item = cid; ok && item < total_items; item += nclusters) {
-            const int pair = item % total_pairs, kc = item / total_pairs;
-            const int kb0 = kc * spc, kb1 = min(nk, kb0 + spc);
-            int seg, row0, nrows;
-            my_tile(pair, seg, row0, nrows);
-            const int id = tab.id[seg];
-            const uint32_t tx = uint32_t(nrows * 128 + S * L.a_bytes);
-            int npieces = 0;
-            if (lane == 0) {
-                const int32_t *tk = p.sorted + row0;
-                int j = 0;
-                while (j < nrows) {
-                    int lg = 7;
-                    while ((1 << lg) > nrows - j || (j & ((1 << lg) - 1)) != 0 ||
-                           tk[j + (1 << lg) - 1] - tk[j] != (1 << lg) - 1)
-                        --lg;
-                    pieces[npieces++] = uint32_t(j) | (uint32_t(lg) << 8) |
-                                        (uint32_t(tk[j]) << 11);
-                    j += 1 << lg;
-                }
-            }
-            npieces = __shfl_sync(0xffffffffu, npieces, 0);
-            __syncwarp();
-            for (int kb = kb0; kb < kb1; ++kb) {
-                bool got = mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, s_abort, deadline);
-                if (__all_sync(0xffffffffu, got) == 0) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t sx = base + stage * L.stage_bytes;
-                const uint32_t full = bar_full + 8 * stage;
-                if (lane == 0) mbar_arrive_expect_tx(full, tx);
-                __syncwarp();
-                for (int i = lane; i < npieces; i += 32) {
-                    const uint32_t pc = pieces[i];
-                    const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
-                    tma_load_2d(sx + r * 128, &p.map_x[lg], kb * UM_BK, t0, full);
-                }
-                if (lane == 0) {
-                    for (int s = 0; s < S; ++s)
-                        tma_load_2d_mc(sx + L.x_bytes + s * L.a_bytes + rank * HALF * 128,
-                                       &p.map_ah[s], kb * UM_BK, id * R + rank * HALF, full, both);
-                }
-                ++issued;
-                if (++stage == STAGES) { stage = 0; phase ^= 1; }
-            }
-        }
-        if (lane == 0) {
-            // Every fill landed, and both CTAs' commits for it arrived here
-            // (the partner's commits are remote arrivals on this CTA's
-            // barriers: they must land before this CTA may exit).
-            const long long drain_deadline = clock64() + UM_TIMEOUT_CYCLES;
-            for (int i = max(0, issued - STAGES); i < issued; ++i) {
-                const uint32_t ph = uint32_t(i / STAGES) & 1u;
-                while (!mbar_try_wait(bar_full + 8 * (i % STAGES), ph) &&
-                       clock64() < drain_deadline) {
-                }
-                while (!mbar_try_wait(bar_empty + 8 * (i % STAGES), ph) &&
-                       clock64() < drain_deadline) {
-                }
-            }
-        }
-    } else if (warp == UM_MMA_WARP) {
-        // ------------------------------------------------------ MMA issue
-        if (lane == 0) {
-            const uint32_t idesc = umma_idesc_bf16(UM_BM, RP);
-            int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
-            bool ok = true;
-            for (int item = cid; ok && item < total_items; item += nclusters) {
-                const int pair = item % total_pairs, kc = item / total_pairs;
-                const int kb0 = kc * spc, kb1 = min(nk, kb0 + spc);
-                int seg, row0, nrows;
-                my_tile(pair, seg, row0, nrows);
-                const bool mine = nrows > 0;
-                if (mine) {
-                    if (!mbar_wait_bounded(bar_acc_empty, acc_phase ^ 1, s_abort, deadline)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_bounded(bar_full + 8 * stage, phase, s_abort, deadline)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (mine) {
-                        const uint32_t sx = base + stage * L.stage_bytes;
-#pragma unroll
-                        for (int kk = 0; kk < UM_BK / 16; ++kk) {
-                            const uint64_t adesc = umma_desc_sw128(sx + kk * 32);
-                            for (int s = 0; s < S; ++s) {
-                                const uint64_t bdesc =
-                                    umma_desc_sw128(sx + L.x_bytes + s * L.a_bytes + kk * 32);
-                                umma_bf16(tmem + s * RP, adesc, bdesc, idesc, kb != kb0 || kk != 0);
-                            }
-                        }
-                    }
-                    umma_commit_mc(bar_empty + 8 * stage, both);   // consumed here and there
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
-                }
-                if (!ok) break;
-                if (mine) {
-                    umma_commit(bar_acc_full);
-                    acc_phase ^= 1;
-                }
-            }
-            if (!ok || *s_abort) {
-                umma_commit(bar_drain);
-                const long long drain_deadline = clock64() + UM_TIMEOUT_CYCLES;
-                while (!mbar_try_wait(bar_drain, 0) && clock64() < drain_deadline) {
-                }
-            }
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------------ epilogue
-        const int q = warp & 3;
-        const int row = q * 32 + lane;
-        uint32_t acc_phase = 0;
-        for (int item = cid; item < total_items; item += nclusters) {
-            const int pair = item % total_pairs;
-            int seg, row0, nrows;
-            my_tile(pair, seg, row0, nrows);
-            if (nrows == 0) continue;                     // no tile of this CTA in the pair
-            const int tok = row < nrows ? p.sorted[row0 + row] : -1;
-            bool got = mbar_wait_bounded(bar_acc_full, acc_phase, s_abort, deadline);
-            if (__all_sync(0xffffffffu, got) == 0) break;
-            tc_fence_after();
-            for (int s = 0; s < S; ++s) {
-                float *dst = p.y + (int64_t(s) * T + max(tok, 0)) * R;
-                for (int c = 0; c < RP; c += 16) {
-                    float v[16];
-                    tmem_ld16(tmem + (uint32_t(q * 32) << 16) + uint32_t(s * RP + c), v);
-#pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        if (tok >= 0 && c + j < R) {
-                            float4 *d4 = reinterpret_cast<float4 *>(dst + c + j);
-                            const float4 a = make_float4(p.scale * v[j], p.scale * v[j + 1],
-                                                         p.scale * v[j + 2], p.scale * v[j + 3]);
-                            if (split) {
-                                atomicAdd(d4, a);
-                            } else {
-                                float4 o = *d4;
-                                o.x += a.x;
-                                o.y += a.y;
-                                o.z += a.z;
-                                o.w += a.w;
-                                *d4 = o;
-                            }
-                        }
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acc_empty);
-            acc_phase ^= 1;
-        }
-    }
-
-    if (tid == 0 && *s_abort) atomicOr(p.error_word, UM_ERROR_BIT);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == UM_MMA_WARP) tmem_dealloc(tmem, p.tmem_cols);
-    cluster_sync();                                       // no more traffic to this CTA
-}
-
 // ------------------------------------------------------------------ host
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -694,17 +405,9 @@ int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream)
         if (!encode_2d(&p.map_x[i], a.x, uint64_t(a.num_tokens), uint64_t(a.hidden),
                        uint64_t(a.x_ld), 1u << i))
             return 0;
-    // Cluster form (two CTAs share each A block by multicast): opt-in with
-    // LORA_PUNICA_UMMA_MC=1.  Measured slower on the large workload (rank
-    // 128, three slices: 190 us against 152 us), where only three 64 KB
-    // stages fit and each refill waits for both SMs' commits.
-    const bool mc = env_int("LORA_PUNICA_UMMA_MC", 0) != 0 && device_sm_count() >= 2;
     for (int s = 0; s < S; ++s) {
         if (!encode_2d(&p.map_a[s], a.a[s], uint64_t(a.max_loras) * a.rank, uint64_t(a.hidden),
                        uint64_t(a.hidden), uint32_t(rp)))
-            return 0;
-        if (mc && !encode_2d(&p.map_ah[s], a.a[s], uint64_t(a.max_loras) * a.rank,
-                             uint64_t(a.hidden), uint64_t(a.hidden), uint32_t(rp / 2)))
             return 0;
     }
     p.y = a.y;
@@ -733,32 +436,10 @@ int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream)
         e = cudaFuncSetAttribute(shrink_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  227 * 1024);
         if (e != cudaSuccess) return int(e);
-        e = cudaFuncSetAttribute(shrink_umma_mc_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return int(e);
         configured[dev] = 1;
     }
-    if (!mc) {
-        const int grid = device_sm_count();
-        e = launch_kernel(shrink_umma_kernel, dim3(grid), dim3(UM_THREADS), size_t(L.total),
-                          stream, p);
-        return e == cudaSuccess ? 1 : int(e);
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((device_sm_count() / 2) * 2);
-    cfg.blockDim = dim3(UM_THREADS);
-    cfg.dynamicSmemBytes = size_t(L.total);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, shrink_umma_mc_kernel, p);
+    const int grid = device_sm_count();
+    e = launch_kernel(shrink_umma_kernel, dim3(grid), dim3(UM_THREADS), size_t(L.total), stream, p);
     return e == cudaSuccess ? 1 : int(e);
 }
 

@@ -1,7 +1,6 @@
 // lora_umma.cuh -- inline-PTX wrappers for the Blackwell (sm_100 family)
-// asynchronous path: mbarriers, TMA loads (2-D tiles, with or without
-// cluster multicast, and 1-D bulk copies), cluster rank and barrier, and
-// tcgen05 (TMEM allocation, UMMA issue/commit, TMEM loads), plus the
+// asynchronous path: mbarriers, TMA loads (2-D tiles and 1-D bulk
+// copies) and tcgen05 (TMEM allocation, UMMA issue/commit, TMEM loads), plus the
 // shared-memory and instruction descriptors UMMA takes.
 //
 // Every wait is bounded: it gives up after `deadline` (a clock64 value) and
@@ -77,35 +76,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// The same tile load delivered to every CTA of the cluster named in `mask`
-// (same shared offset and mbarrier offset in each; each of those mbarriers
-// is credited with the bytes its CTA receives).
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, int c0,
-                                               int c1, uint32_t bar, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;\n"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
-        : "memory");
-}
-
-// ---------------------------------------------------------------- cluster
-
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-    return r;
-}
-
-// Every thread of every CTA of the cluster (release / acquire).
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n"
-                 "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
 // 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint32_t bytes,
                                              uint32_t bar)
@@ -163,15 +133,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
                  :: "r"(bar) : "memory");
-}
-
-// Arrive on `bar` (the same shared offset) in every CTA of `mask` once every
-// UMMA issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster"
-                 ".multicast::cluster.b64 [%0], %1;\n"
-                 :: "r"(bar), "h"(mask) : "memory");
 }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane.

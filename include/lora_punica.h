@@ -29,6 +29,9 @@
  *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t passed
  *     as void*; NULL is the legacy default stream).  Nothing is
  *     synchronised and nothing is read back to the host.
+ *   - The device that owns `stream` and every tensor of a call must be the
+ *     calling thread's current CUDA device (per-device launch settings are
+ *     looked up for the current device).
  *   - Return value: 0 on success; a negative LORA_ERR_* code when an
  *     argument is rejected on the host (nothing is launched); a positive
  *     cudaError_t when a launch fails.  lora_status_string() names both.
@@ -281,9 +284,11 @@ int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
  * is called.
  *
  * The first call on a device looks up the array's device address (with that
- * device current); make it before any stream capture.  All calls on a
- * device share the array: calls that may overlap on the GPU (other streams
- * or threads) race on it and must be serialised by the caller.
+ * device current); make it before any stream capture.  `stream` must belong
+ * to the current device, else LORA_ERR_DEVICE is returned before anything
+ * runs.  All calls on a device share the array: calls that may overlap on
+ * the GPU (other streams or threads) race on it and must be serialised by
+ * the caller.
  */
 int lora_linear_noalloc(const int32_t *token_lora_mapping, int32_t num_tokens,
                         const lora_bf16_t *x, int32_t hidden, int64_t x_ld,

@@ -180,3 +180,51 @@ def test_coop_barrier_timeout_reports_and_recovers(oracle_mod, monkeypatch):
     ref_y = oracle_mod.expand(ref_buf.astype(np.float32), inp.lora_b, inp.ids, inp.y, w.slices,
                               0, True)
     assert_close(bits_to_f64(host_bits(y)), ref_y, EXPAND_ATOL, EXPAND_RTOL, "y after recovery")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("name,T", [("decode", None), ("mlp", 512), ("prefill", 2048)])
+def test_linear_alternating_no_lora_batches(oracle_mod, monkeypatch, path, name, T):
+    """Calls with a mixed id map (with bias) and all -1 calls alternate on one
+    metadata struct, back to back in one stream.  After every all -1 call, y
+    and the buffer are bit-identical to what they were before it: no kernel
+    of that call may act on the metadata of the mixed call before it (early
+    mode fetches the metadata before its grid-dependency wait, so every
+    kernel of the chain must pass its wait before it exits).  Every mixed
+    call is checked against the oracle."""
+    import expand_gemm_gb300 as eg
+    _set_path(monkeypatch, path)
+    w0 = W.generate(name, num_tokens=T).workload
+    from dataclasses import replace
+    w = replace(w0, bias=True, scale=0.9)
+    inp = W.generate(w)
+    T = w.num_tokens
+    x = dev_bf16(inp.x)
+    A = [dev_bf16(a) for a in inp.lora_a]
+    B = [dev_bf16(b) for b in inp.lora_b]
+    bias = [dev_bf16(b) for b in inp.lora_bias]
+    ids_mixed = dev_i32(inp.ids)
+    ids_none = dev_i32(np.full(T, -1, np.int32))
+    meta = eg.LoRAKernelMeta.make(w.max_loras, T, "cuda")
+    y = dev_bf16(inp.y)
+    buf = torch.zeros(inp.buf.shape, dtype=torch.float32, device="cuda")
+    ref_buf = oracle_mod.shrink(inp.x, inp.lora_a, inp.ids, w.scale, inp.buf)
+    for it in range(3):
+        y_before = host_bits(y)
+        buf.zero_()
+        eg.lora_linear(ids_mixed, x, A, B, bias, w.scale, buf, y, meta)
+        eg.lora_linear(ids_none, x, A, B, bias, w.scale, buf, y, meta)
+        y_after_none = host_bits(y)
+        buf_after_none = buf.cpu().numpy()
+        assert int(meta.no_lora_flag.item()) == 1
+        assert int(meta.error_word.item()) == 0
+        ref_y = oracle_mod.expand(ref_buf.astype(np.float32), inp.lora_b, inp.ids, y_before,
+                                  w.slices, 0, True, inp.lora_bias)
+        assert_close(buf_after_none, ref_buf, SHRINK_ATOL, SHRINK_RTOL, "buffer, round %d" % it)
+        assert_close(bits_to_f64(y_after_none), ref_y, EXPAND_ATOL, EXPAND_RTOL,
+                     "y, round %d" % it)
+        # the all -1 call itself changed nothing: run it twice more and compare bits
+        eg.lora_linear(ids_none, x, A, B, bias, w.scale, buf, y, meta)
+        eg.lora_linear(ids_none, x, A, B, bias, w.scale, buf, y, meta)
+        np.testing.assert_array_equal(host_bits(y), y_after_none)
+        np.testing.assert_array_equal(buf.cpu().numpy(), buf_after_none)

@@ -94,17 +94,14 @@ def test_shrink_shapes(oracle_mod, T, H, r, L, S):
     (1500, 192, 128, 3, 3),     # rank 128, three slices: 384 TMEM columns
     (1100, 128, 24, 2, 2),      # padded rank 24 -> 32
 ])
-@pytest.mark.parametrize("umma,partial,mc", [("0", "1", "1"), ("1", "1", "1"), ("1", "0", "1"),
-                                             ("1", "1", "0"), ("1", "0", "0")])
-def test_shrink_long_segments(oracle_mod, monkeypatch, umma, partial, mc, T, H, r, L, S):
+@pytest.mark.parametrize("umma,partial", [("0", "1"), ("1", "1"), ("1", "0")])
+def test_shrink_long_segments(oracle_mod, monkeypatch, umma, partial, T, H, r, L, S):
     """Long sequences per LoRA: with the tensor-core path forced on it takes
     every tile, the partial last tile of each segment included (partial=1),
     or the whole 128-token tiles with the remainders on mma.sync
-    (partial=0), as two-CTA clusters sharing the A blocks (mc=1) or one CTA
-    per tile (mc=0); with it off, mma.sync covers everything."""
+    (partial=0); with it off, mma.sync covers everything."""
     monkeypatch.setenv("LORA_PUNICA_UMMA", umma)
     monkeypatch.setenv("LORA_PUNICA_UMMA_PARTIAL", partial)
-    monkeypatch.setenv("LORA_PUNICA_UMMA_MC", mc)
     monkeypatch.setenv("LORA_PUNICA_UMMA_MIN_COLS", "0")
     monkeypatch.setenv("LORA_PUNICA_UMMA_MIN_TOKENS", "0")
     w = W.Workload("long", T + r, T, H, r, L, tuple([16] * S), "zipf_seq", p_none=0.1,
