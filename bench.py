@@ -1,17 +1,26 @@
 """Benchmark of the multi-LoRA path (metadata + shrink + expand) on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...     # the fp64 CPU oracle, timed
 
 One step = one pass of the whole path over one batch: metadata, shrink and
 expand through the C ABI (lora_linear), or metadata and the expand of a
-bf16 input for the embedding workload, on inputs already resident in HBM.  Input sets (ids, x, A, B, bias, y, buffer) are replicated until
-they total at least 4x the L2 cache, and consecutive steps rotate through
-them, so every step reads from HBM.  Steps are captured in CUDA graphs (one
-graph per rotation), warm-up steps run first, and exactly K steps are timed
-with CUDA events between a barrier + synchronize on both sides.  Rank 0
-prints one JSON line.  N > 1 (torchrun) runs independent replicas, one per
-GPU, and reports the aggregate over ranks with the max time over ranks.
+bf16 input for the embedding workload, on inputs already resident in HBM.
+Input sets (ids, x, A, B, bias, y, buffer) are replicated until they total
+at least 4x the L2 cache, and consecutive steps rotate through them, so
+every step reads from HBM.  Steps are captured in CUDA graphs (one graph per
+rotation).
+
+With no --workload the headline is the large workload (16384 tokens,
+hidden 8192, rank 128, three slices: the largest configuration): W warm-up
+steps, then exactly K steps timed with CUDA events between a barrier +
+synchronize on both sides, clocks sampled meanwhile; then the end-to-end
+figure through the public API with host copies, and each kernel alone.
+Every other workload of the layer (tiny, decode, prefill, mlp, the all -1
+batch) is then timed the same way, step and kernels, and reported under
+per_workload.  Rank 0 prints one JSON line.  N > 1 (torchrun) runs
+independent replicas, one per GPU, and reports the aggregate over ranks
+with the max time over ranks.
 """
 from __future__ import annotations
 
@@ -35,15 +44,13 @@ import workloads as W  # noqa: E402
 
 METRIC = "LoRA shrink+expand tokens/s and effective HBM GB/s (% of roofline), 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
-E2E_GRAPH_STEPS = 16
+E2E_GRAPH_STEPS = 8
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
-# the committed ncu summaries, keyed by (kernel, workload) and the hash of
-# the kernel's sources they were taken on; a stale hash reports null.
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum of an
+# ncu capture of the bench command), keyed by (kernel, workload), with the
+# hash of the kernel's sources the capture was taken on; a stale hash
+# reports null.
 NCU_TRAFFIC = {
-    # profiles/expand_decode_ncu.md: reads 8.915 MB (median of three
-    # launches), writes 0 (the y writes stay in L2 past the end of the launch)
-    ("expand", "decode"): ("9798a146a5d17271", 8914688),
 }
 
 # The source files each reported kernel is built from.
@@ -63,19 +70,28 @@ def _src_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+HEADLINE = "large"
+# Workloads of one LoRA layer timed by a default run: the headline first,
+# then the rest (each reported under per_workload).
+LAYER_WORKLOADS = ["large", "tiny", "decode", "prefill", "mlp", "none"]
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
-    ap.add_argument("--workload", default="decode", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=None, choices=sorted(W.WORKLOADS),
+                    help="time this workload alone (default: the large workload as the "
+                         "headline, then every other workload of the layer)")
     ap.add_argument("--num-tokens", type=int, default=None,
                     help="a smaller case of the workload (profiling captures)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--kernel-seconds", type=float, default=0.5,
+    ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--kernel-seconds", type=float, default=0.25,
                     help="minimum timed seconds per kernel in the per-kernel loops")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args(argv)
 
 
@@ -240,6 +256,215 @@ class DeviceSet:
         return c
 
 
+def _workload(name, args):
+    w = W.WORKLOADS[name]
+    if args.num_tokens is not None:
+        from dataclasses import replace
+        w = replace(w, num_tokens=args.num_tokens, n_decode=min(w.n_decode, args.num_tokens))
+    return w
+
+
+class Measured:
+    """One workload measured on the GPU: the step timed over a rotation of
+    resident input sets, then each kernel alone."""
+
+    def __init__(self, name, args, dev, eg, stream, props, dist, headline, clocks):
+        import torch
+        w = _workload(name, args)
+        inp = W.generate(w)
+        ub = W.unique_bytes(w, inp.ids)
+        l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+        base = DeviceSet(inp, dev, eg)
+        n_sets = max(2, -(-4 * l2 // base.nbytes))
+        sets = [base] + [base.clone(eg) for _ in range(n_sets - 1)]
+        emb = w.kind == "embedding"
+
+        def step(s: DeviceSet):
+            if emb:
+                # metadata + expand of the looked-up bf16 rows (embedding LoRA)
+                s.meta.prepare_tensors(s.ids)
+                eg.add_lora_embedding(s.y, s.x, s.B[0], s.meta, w.add_inputs)
+            else:
+                # metadata + shrink + expand of one layer (or of the logits):
+                # one C-ABI call (one kernel for small batches, three otherwise)
+                eg.lora_linear(s.ids, s.x, s.A, s.B, s.bias, w.scale, s.buf, s.y, s.meta)
+
+        # eager pass first: configures kernels (smem attributes, occupancy) before capture
+        with torch.cuda.stream(stream):
+            for s in sets:
+                step(s)
+        torch.cuda.synchronize(dev)
+
+        def capture(fn_list):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for fn in fn_list:
+                    fn()
+            return g
+
+        def graphs_for(n_steps, make):
+            """Graphs covering exactly n_steps steps: full rotations + a tail."""
+            rot = capture([make(s) for s in sets])
+            tail_n = n_steps % n_sets
+            tail = capture([make(s) for s in sets[:tail_n]]) if tail_n else None
+            return [rot] * (n_steps // n_sets) + ([tail] if tail else [])
+
+        def mk_step(s):
+            return lambda: step(s)
+
+        def time_kernel(make, min_s):
+            """ms per call of make(s)'s work: graphs of one rotation, replayed
+            (after at least three warm-up calls) until min_s seconds pass."""
+            g = capture([make(s) for s in sets])
+            with torch.cuda.stream(stream):
+                for _ in range(-(-3 // n_sets)):
+                    g.replay()
+            torch.cuda.synchronize(dev)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            reps = 1
+            while True:
+                with torch.cuda.stream(stream):
+                    a.record(stream)
+                    for _ in range(reps):
+                        g.replay()
+                    b.record(stream)
+                torch.cuda.synchronize(dev)
+                ms = a.elapsed_time(b)
+                if ms >= min_s * 1e3 or reps >= 1 << 16:
+                    return ms / (reps * n_sets)
+                reps *= 2 if ms <= 0 else max(2, min(16, int(min_s * 1e3 / ms) + 1))
+
+        self.elapsed_ms = None
+        self.wall = None
+        if headline:
+            # exactly K timed steps after W warm-up steps, barrier + synchronize
+            # on both sides, clocks sampled meanwhile
+            warm = graphs_for(args.warmup, mk_step)
+            timed = graphs_for(args.steps, mk_step)
+            with torch.cuda.stream(stream):
+                for g in warm:
+                    g.replay()
+            torch.cuda.synchronize(dev)
+            clocks.start()
+            time.sleep(0.3)
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            if dist:
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            t_wall = time.perf_counter()
+            with torch.cuda.stream(stream):
+                ev0.record(stream)
+                for g in timed:
+                    g.replay()
+                ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            self.wall = time.perf_counter() - t_wall
+            if dist:
+                dist.barrier()
+            self.elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
+
+        ks = args.kernel_seconds
+        k_step = time_kernel(mk_step, ks)
+        k_meta = time_kernel(lambda s: (lambda: s.meta.prepare_tensors(s.ids)), ks)
+        if emb:
+            k_shrink = 0.0
+            k_expand = time_kernel(lambda s: (lambda: eg.lora_expand(
+                s.x.unsqueeze(0), s.B, s.y, s.meta, w.offset_start, w.add_inputs, s.bias)), ks)
+        else:
+            k_shrink = time_kernel(lambda s: (lambda: eg.lora_shrink(s.x, s.A, s.buf, s.meta,
+                                                                     w.scale)), ks)
+            k_expand = time_kernel(lambda s: (lambda: eg.lora_expand(
+                s.buf, s.B, s.y, s.meta, w.offset_start, w.add_inputs, s.bias)), ks)
+        if headline:
+            clocks.stop()
+        self.w, self.inp, self.ub, self.emb, self.step = w, inp, ub, emb, step
+        self.n_sets, self.set_bytes, self.l2 = n_sets, base.nbytes, l2
+        self.k = {"meta": k_meta, "shrink": k_shrink, "expand": k_expand, "step": k_step}
+        self.coop = coop_path(w) and not emb
+        self.fused = (fused_path(w) and not emb) or self.coop
+        self.launches_per_step = (2 if emb else 1 if self.fused else 3 + (
+            1 if umma_shrink_path(w) and os.environ.get("LORA_PUNICA_UMMA_PARTIAL", "1") == "0"
+            else 0))
+        del sets, base
+        torch.cuda.synchronize(dev)
+
+    def path(self):
+        if self.emb:
+            return "metadata + expand of a bf16 input (add_lora_embedding): two kernels"
+        return "lora_linear (metadata + shrink + expand): %s" % (
+            "one cooperative kernel" if self.coop else
+            "one fused cluster kernel" if self.fused else "three kernels")
+
+    def summary(self, args, step_ms=None):
+        """The workload's figures: the step and each kernel, with the
+        dominant kernel's roofline.  step_ms: the step time to report (the
+        exact-K timed region for the headline; else the per-kernel loop's)."""
+        w, ub, k = self.w, self.ub, self.k
+        step_ms = k["step"] if step_ms is None else step_ms
+        hbm, peak_src = peaks()
+        step_bytes = ub["shrink"] + ub["expand"]
+        if self.coop:
+            # the whole step is one kernel: its bytes are the step's bytes
+            dominant, dom_bytes, dom_ms = "linear_coop", step_bytes, k["step"]
+        elif self.fused:
+            dominant, dom_bytes, dom_ms = "linear_fused", step_bytes, k["step"]
+        else:
+            dominant = "expand" if k["expand"] >= k["shrink"] else "shrink"
+            dom_bytes, dom_ms = ub[dominant], k[dominant]
+        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+        tr = NCU_TRAFFIC.get((dominant, w.name))
+        traffic = tr[1] if (tr and tr[0] == _src_hash(dominant)
+                            and args.num_tokens is None) else None
+        kern_us = {"meta": k["meta"] * 1e3, "shrink": k["shrink"] * 1e3,
+                   "expand": k["expand"] * 1e3,
+                   ("embedding_step" if self.emb else "lora_linear"): k["step"] * 1e3}
+        if self.emb:
+            del kern_us["shrink"]
+        step_gbps = step_bytes / (step_ms * 1e-3) / 1e9
+        return {
+            "workload": w.name,
+            "step": self.path(),
+            "num_tokens": w.num_tokens, "active_tokens": ub["t_active"],
+            "distinct_loras": ub["distinct"],
+            "step_us": step_ms * 1e3,
+            "tokens_per_s": w.num_tokens / (step_ms * 1e-3),
+            "step_unique_bytes": step_bytes,
+            "step_gbps": step_gbps,
+            "step_frac": step_gbps / hbm,
+            # the metric's other reading: tokens over the shrink and expand
+            # kernels' standalone times, metadata (once per forward) left out
+            "tokens_per_s_shrink_expand": (w.num_tokens / ((k["shrink"] + k["expand"]) * 1e-3)
+                                           if k["shrink"] + k["expand"] > 0 else None),
+            "kernels_us": kern_us,
+            "kernels_gbps": {
+                "shrink": (ub["shrink"] / (k["shrink"] * 1e-3) / 1e9
+                           if k["shrink"] and ub["shrink"] else None),
+                "expand": ub["expand"] / (k["expand"] * 1e-3) / 1e9 if ub["expand"] else None},
+            "kernels_frac": {
+                "shrink": (ub["shrink"] / (k["shrink"] * 1e-3) / 1e9 / hbm
+                           if k["shrink"] and ub["shrink"] else None),
+                "expand": (ub["expand"] / (k["expand"] * 1e-3) / 1e9 / hbm
+                           if ub["expand"] else None)},
+            "roofline": {
+                "bound": "hbm", "kernel": "lora_" + dominant,
+                "note": ("single kernel: algorithmic bytes of shrink + expand per launch"
+                         if self.fused else "the step's longest kernel"),
+                "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": dom_bytes,
+                "launch_us": dom_ms * 1e3,
+                "peak_source": peak_src + " (of measured)" if "measured" in peak_src
+                else peak_src,
+            },
+            "l2": "inputs larger than L2: %d resident input sets of %.1f MB rotated "
+                  "(%.0f MB total, L2 %.0f MB)" % (self.n_sets, self.set_bytes / 1e6,
+                                                   self.n_sets * self.set_bytes / 1e6,
+                                                   self.l2 / 1e6),
+        }
+
+
 def run_ours(args, rank, world):
     import torch
     import expand_gemm_gb300 as eg
@@ -252,126 +477,24 @@ def run_ours(args, rank, world):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-
-    w = W.WORKLOADS[args.workload]
-    if args.num_tokens is not None:
-        from dataclasses import replace
-        w = replace(w, num_tokens=args.num_tokens, n_decode=min(w.n_decode, args.num_tokens))
-    inp = W.generate(w)
-    ub = W.unique_bytes(w, inp.ids)
     props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
-
-    base = DeviceSet(inp, dev, eg)
-    n_sets = max(2, -(-4 * l2 // base.nbytes))
-    sets = [base] + [base.clone(eg) for _ in range(n_sets - 1)]
-
-    emb = w.kind == "embedding"
-
-    def step(s: DeviceSet):
-        if emb:
-            # metadata + expand of the looked-up bf16 rows (embedding LoRA)
-            s.meta.prepare_tensors(s.ids)
-            eg.add_lora_embedding(s.y, s.x, s.B[0], s.meta, w.add_inputs)
-        else:
-            # metadata + shrink + expand of one layer (or of the logits): one
-            # C-ABI call (fused into a single kernel for small batches, three
-            # kernels otherwise)
-            eg.lora_linear(s.ids, s.x, s.A, s.B, s.bias, w.scale, s.buf, s.y, s.meta)
-
-    stream = torch.cuda.Stream(dev)
-    # eager pass first: configures kernels (smem attributes, occupancy) before capture
-    with torch.cuda.stream(stream):
-        for s in sets:
-            step(s)
-    torch.cuda.synchronize(dev)
-
-    def capture(fn_list):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for fn in fn_list:
-                fn()
-        return g
-
-    def graphs_for(n_steps, make):
-        """Graphs covering exactly n_steps steps: full rotations + a tail."""
-        rot = capture([make(s) for s in sets])
-        tail_n = n_steps % n_sets
-        tail = capture([make(s) for s in sets[:tail_n]]) if tail_n else None
-        return [rot] * (n_steps // n_sets) + ([tail] if tail else [])
-
-    def mk_step(s):
-        return lambda: step(s)
-
-    warm = graphs_for(args.warmup, mk_step)
-    timed = graphs_for(args.steps, mk_step)
     gpu_uuid = getattr(props, "uuid", None)
     gpu_uuid = ("GPU-" + str(gpu_uuid)) if gpu_uuid is not None else None
     clocks = ClockSampler(gpu_uuid)
+    stream = torch.cuda.Stream(dev)
 
-    with torch.cuda.stream(stream):
-        for g in warm:
-            g.replay()
-    torch.cuda.synchronize(dev)
-
-    clocks.start()
-    time.sleep(0.3)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    t_wall = time.perf_counter()
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for g in timed:
-            g.replay()
-        ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    wall = time.perf_counter() - t_wall
-    if dist:
-        dist.barrier()
-    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
-
-    # ---- per-kernel timing: graphs of one kernel over the rotation
-    def time_kernel(make, min_s):
-        g = capture([make(s) for s in sets])
-        with torch.cuda.stream(stream):
-            g.replay()
-        torch.cuda.synchronize(dev)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        reps = 1
-        while True:
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                for _ in range(reps):
-                    g.replay()
-                b.record(stream)
-            torch.cuda.synchronize(dev)
-            ms = a.elapsed_time(b)
-            if ms >= min_s * 1e3 or reps >= 1 << 16:
-                return ms / (reps * n_sets)
-            reps *= 2 if ms <= 0 else max(2, min(16, int(min_s * 1e3 / ms) + 1))
-
-    k_step = time_kernel(mk_step, args.kernel_seconds)
-    k_meta = time_kernel(lambda s: (lambda: s.meta.prepare_tensors(s.ids)), args.kernel_seconds)
-    if emb:
-        k_shrink = 0.0
-        k_expand = time_kernel(lambda s: (lambda: eg.lora_expand(
-            s.x.unsqueeze(0), s.B, s.y, s.meta, w.offset_start, w.add_inputs, s.bias)),
-            args.kernel_seconds)
-    else:
-        k_shrink = time_kernel(lambda s: (lambda: eg.lora_shrink(s.x, s.A, s.buf, s.meta,
-                                                                 w.scale)),
-                               args.kernel_seconds)
-        k_expand = time_kernel(lambda s: (lambda: eg.lora_expand(
-            s.buf, s.B, s.y, s.meta, w.offset_start, w.add_inputs, s.bias)),
-            args.kernel_seconds)
-    clocks.stop()
-
+    names = [args.workload] if args.workload else LAYER_WORKLOADS
+    head = Measured(names[0], args, dev, eg, stream, props, dist, True, clocks)
+    w, inp = head.w, head.inp
     # ---- end to end through the public API, host buffers, copies timed
-    e2e = run_e2e(args, inp, w, dev, eg, stream, step)
+    e2e = None if args.no_e2e else run_e2e(args, inp, w, dev, eg, stream, head.step)
+    torch.cuda.empty_cache()
+    per = {}
+    for name in names[1:]:
+        m = Measured(name, args, dev, eg, stream, props, None, False, clocks)
+        per[name] = m.summary(args)
+        del m
+        torch.cuda.empty_cache()
 
     if rank != 0:
         if dist:
@@ -379,30 +502,10 @@ def run_ours(args, rank, world):
         return None
 
     T = w.num_tokens
-    ms_per_step = elapsed_ms / args.steps
-    value = job_tokens_per_s(world, T, args.steps, elapsed_ms)
-    hbm, peak_src = peaks()
-    kern = {"meta": k_meta, "shrink": k_shrink, "expand": k_expand,
-            ("embedding_step" if emb else "lora_linear"): k_step}
-    if emb:
-        del kern["shrink"]
-    shrink_gbs = ub["shrink"] / (k_shrink * 1e-3) / 1e9 if k_shrink else None
-    expand_gbs = ub["expand"] / (k_expand * 1e-3) / 1e9
-    step_bytes = ub["shrink"] + ub["expand"]
-    coop = coop_path(w) and not emb
-    fused = (fused_path(w) and not emb) or coop
-    if coop:
-        # the whole step is one kernel: its bytes are the step's bytes
-        dominant, dom_bytes, dom_ms = "linear_coop", step_bytes, k_step
-    elif fused:
-        dominant, dom_bytes, dom_ms = "linear_fused", step_bytes, k_step
-    else:
-        dominant = "expand" if k_expand >= k_shrink else "shrink"
-        dom_bytes, dom_ms = ub[dominant], kern[dominant]
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    tr = NCU_TRAFFIC.get((dominant, args.workload))
-    traffic = tr[1] if (tr and tr[0] == _src_hash(dominant)
-                        and args.num_tokens is None) else None
+    ms_per_step = head.elapsed_ms / args.steps
+    value = job_tokens_per_s(world, T, args.steps, head.elapsed_ms)
+    hs = head.summary(args, step_ms=ms_per_step)
+    per = {names[0]: hs, **per}
     out = {
         "metric": METRIC,
         "value": value,
@@ -417,41 +520,24 @@ def run_ours(args, rank, world):
         "dtype": "bf16",
         "data": "synthetic (seeded numpy PCG64; no dataset or weights)",
         "config": {
-            **workload_config(w, ub, args),
-            "l2": "inputs larger than L2: %d resident input sets of %.1f MB rotated "
-                  "(%.0f MB total, L2 %.0f MB)" % (n_sets, base.nbytes / 1e6,
-                                                   n_sets * base.nbytes / 1e6, l2 / 1e6),
+            **workload_config(w, head.ub, args),
+            "l2": hs["l2"],
             "timing": "CUDA graphs of one rotation of steps, CUDA events on the launch stream",
-            "step": ("metadata + expand of a bf16 input (add_lora_embedding): two kernels"
-                     if emb else "lora_linear (metadata + shrink + expand): %s" % (
-                         "one cooperative kernel" if coop else
-                         "one fused cluster kernel" if fused else "three kernels")),
+            "step": head.path(),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
-        # the metric's other reading: tokens over the shrink and expand
-        # kernels' standalone times, metadata (once per forward) left out
-        "tokens_per_s_shrink_expand": T / ((k_shrink + k_expand) * 1e-3),
-        "effective_gbps": step_bytes / (ms_per_step * 1e-3) / 1e9,
-        "step_unique_bytes": step_bytes,
-        "kernels_us": {k: v * 1e3 for k, v in kern.items()},
-        "kernels_gbps": {"shrink": shrink_gbs, "expand": expand_gbs},
-        "roofline": {
-            "bound": "hbm", "kernel": "lora_" + dominant,
-            "note": ("single kernel: algorithmic bytes of shrink + expand per launch"
-                     if fused else "the step's longest kernel"),
-            "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-            "traffic": traffic,
-            "algorithmic_bytes_per_launch": dom_bytes,
-            "launch_us": dom_ms * 1e3,
-            "peak_source": peak_src + " (of measured)" if "measured" in peak_src else peak_src,
-        },
-        "hbm_frac_step": (step_bytes / (ms_per_step * 1e-3) / 1e9) / hbm,
-        "gpu_launches": args.steps * (2 if emb else 1 if fused
-                                      else 3 + (1 if umma_shrink_path(w) and os.environ.get(
-                                          "LORA_PUNICA_UMMA_PARTIAL", "1") == "0" else 0)),
+        "tokens_per_s_shrink_expand": hs["tokens_per_s_shrink_expand"],
+        "effective_gbps": hs["step_gbps"],
+        "step_unique_bytes": hs["step_unique_bytes"],
+        "hbm_frac_step": hs["step_frac"],
+        "kernels_us": hs["kernels_us"],
+        "kernels_gbps": hs["kernels_gbps"],
+        "roofline": hs["roofline"],
+        "gpu_launches": args.steps * head.launches_per_step,
         "clocks": clocks.summary(),
         "e2e": e2e,
-        "wall_s_timed": wall,
+        "wall_s_timed": head.wall,
+        "per_workload": per,
     }
     # the oracle's CPU baseline is timed at N = 1 only
     if not args.no_cpu_baseline and world == 1:
@@ -596,10 +682,7 @@ def run_reference(args, rank, world):
         return None
     import oracle
     oracle.build()
-    w = W.WORKLOADS[args.workload]
-    if args.num_tokens is not None:
-        from dataclasses import replace
-        w = replace(w, num_tokens=args.num_tokens, n_decode=min(w.n_decode, args.num_tokens))
+    w = _workload(args.workload or HEADLINE, args)
     inp = W.generate(w)
     T = w.num_tokens
     sel = np.arange(min(T, 16))
