@@ -30,7 +30,7 @@ from ._lib import (LoraError, LORA_MAX_LORAS, LORA_MAX_RANK, LORA_MAX_SLICES,  #
 
 __all__ = ["LoRAKernelMeta", "lora_meta_prepare", "lora_shrink", "lora_expand",
            "lora_linear", "lora_linear_noalloc", "add_lora_linear", "add_lora_embedding",
-           "add_lora_logits", "LoraError", "library", "build"]
+           "add_lora_logits", "reload_options", "LoraError", "library", "build"]
 
 
 def library():
@@ -41,6 +41,12 @@ def library():
 def build(force: bool = False) -> str:
     from .build import build as _build
     return _build(force=force)
+
+
+def reload_options() -> None:
+    """Re-read the LORA_PUNICA_* tuning variables (the library reads them
+    once, at its first call): ``lora_reload_options``."""
+    _lib.load().lora_reload_options()
 
 
 def _stream_handle(device: torch.device) -> int:

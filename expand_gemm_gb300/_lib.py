@@ -14,8 +14,8 @@ LIB_PATH = os.path.join(PKG, "liblora_punica.so")
 
 # Public entry points of include/lora_punica.h (checked by the test suite).
 EXPORTS = ("lora_meta_prepare", "lora_meta_read_no_lora", "lora_shrink", "lora_expand",
-           "lora_expand_bf16", "lora_linear", "lora_linear_noalloc", "lora_status_string",
-           "lora_version")
+           "lora_expand_bf16", "lora_linear", "lora_linear_noalloc", "lora_reload_options",
+           "lora_status_string", "lora_version")
 
 LORA_MAX_SLICES = 8
 LORA_MAX_LORAS = 1024
@@ -85,6 +85,8 @@ def load(path: str | None = None):
                                             _I32, ctypes.c_float, _P, _I64,
                                             ctypes.POINTER(LoraMetaC), _P]
         lib.lora_linear_noalloc.restype = ctypes.c_int
+        lib.lora_reload_options.argtypes = []
+        lib.lora_reload_options.restype = None
         lib.lora_status_string.argtypes = [ctypes.c_int]
         lib.lora_status_string.restype = ctypes.c_char_p
         lib.lora_version.argtypes = []

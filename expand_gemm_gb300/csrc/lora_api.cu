@@ -2,7 +2,10 @@
 // host read of the no-LoRA flag) and the host helpers the launchers share.
 #include <stdlib.h>
 
+#include <mutex>
+
 #include "lora_common.cuh"
+#include "lora_umma.cuh"
 
 namespace lora {
 
@@ -19,25 +22,76 @@ int device_sm_count()
     return n;
 }
 
-// Programmatic dependent launch is on unless LORA_PUNICA_PDL=0 is set in
-// the environment (read once).
-bool pdl_enabled()
-{
-    static int cached = -1;
-    if (cached < 0) {
-        const char *v = getenv("LORA_PUNICA_PDL");
-        cached = (v != nullptr && v[0] == '0') ? 0 : 1;
-    }
-    return cached == 1;
-}
-
-// Integer tuning knob from the environment (read at every call; the
-// callers cache what they need).
-int env_int(const char *name, int fallback)
+static int env_int(const char *name, int fallback)
 {
     const char *v = getenv(name);
     if (v == nullptr || *v == 0) return fallback;
     return atoi(v);
+}
+
+static Knobs read_knobs()
+{
+    Knobs k;
+    k.pdl = env_int("LORA_PUNICA_PDL", 1);
+    k.coop = env_int("LORA_PUNICA_COOP", -1);
+    k.fused = env_int("LORA_PUNICA_FUSED", -1);
+    k.fused_max_tokens = env_int("LORA_PUNICA_FUSED_MAX_TOKENS", 128);
+    k.self_meta = env_int("LORA_PUNICA_SELF_META", -1);
+    k.umma = env_int("LORA_PUNICA_UMMA", 1);
+    k.umma_min_tokens = env_int("LORA_PUNICA_UMMA_MIN_TOKENS", 1024);
+    k.umma_min_cols = env_int("LORA_PUNICA_UMMA_MIN_COLS", 256);
+    k.umma_partial = env_int("LORA_PUNICA_UMMA_PARTIAL", 1);
+    k.early_shrink_ctas = env_int("LORA_PUNICA_EARLY_SHRINK_CTAS", 2);
+    k.expand_tc = env_int("LORA_PUNICA_EXPAND_TC", 0);
+    k.expand_tc_min_rank = env_int("LORA_PUNICA_EXPAND_TC_MIN_RANK", 64);
+    k.meta_small = env_int("LORA_PUNICA_META_SMALL", 1);
+    k.coop_test_extra = env_int("LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS", 0);
+    k.coop_test_timeout = env_int("LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES", 0);
+    return k;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+bool encode_tile_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols,
+                     uint64_t row_stride, uint32_t box_cols, uint32_t box_rows,
+                     CUtensorMapSwizzle swizzle)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_stride * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static Knobs g_knobs;
+static std::once_flag g_knobs_once;
+
+const Knobs &knobs()
+{
+    std::call_once(g_knobs_once, [] { g_knobs = read_knobs(); });
+    return g_knobs;
 }
 
 }  // namespace lora
@@ -77,4 +131,12 @@ LORA_API int lora_meta_read_no_lora(const lora_meta_t *meta, void *stream, int32
     if (e != cudaSuccess) return int(e);
     *no_lora = v != 0 ? 1 : 0;
     return LORA_OK;
+}
+
+// Re-reads the LORA_PUNICA_* tuning variables (otherwise read once, at the
+// first call).  Not to be called while another thread calls the library.
+LORA_API void lora_reload_options(void)
+{
+    lora::knobs();
+    lora::g_knobs = lora::read_knobs();
 }

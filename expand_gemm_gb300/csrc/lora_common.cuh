@@ -369,8 +369,31 @@ __device__ __forceinline__ int find_segment(const int *s_tile, int nbins, int ti
 // Host-side launch helpers (lora_api.cu).
 namespace lora {
 int device_sm_count();
-bool pdl_enabled();
-int env_int(const char *name, int fallback);
+
+// Tuning knobs: the LORA_PUNICA_* environment variables, read once (at the
+// first library call) into this process-wide struct; lora_reload_options()
+// reads them again.  No call reads the environment after that.
+struct Knobs {
+    int pdl;                  // LORA_PUNICA_PDL: programmatic dependent launch (1)
+    int coop;                 // LORA_PUNICA_COOP: single cooperative kernel (-1 auto, 0, 1)
+    int fused;                // LORA_PUNICA_FUSED: cluster kernel (-1 auto, 0, 1)
+    int fused_max_tokens;     // LORA_PUNICA_FUSED_MAX_TOKENS (128)
+    int self_meta;            // LORA_PUNICA_SELF_META (-1 early mode, 0 three calls, 1 two kernels)
+    int umma;                 // LORA_PUNICA_UMMA: tcgen05 shrink (1)
+    int umma_min_tokens;      // LORA_PUNICA_UMMA_MIN_TOKENS (1024)
+    int umma_min_cols;        // LORA_PUNICA_UMMA_MIN_COLS (256)
+    int umma_partial;         // LORA_PUNICA_UMMA_PARTIAL (1)
+    int early_shrink_ctas;    // LORA_PUNICA_EARLY_SHRINK_CTAS (2)
+    int expand_tc;            // LORA_PUNICA_EXPAND_TC: tcgen05 expand (0 off, -1 ranks >= min, 1 all)
+    int expand_tc_min_rank;   // LORA_PUNICA_EXPAND_TC_MIN_RANK (64)
+    int meta_small;           // LORA_PUNICA_META_SMALL (1)
+    int coop_test_extra;      // LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS (0, tests only)
+    int coop_test_timeout;    // LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES (0, tests only)
+};
+const Knobs &knobs();
+inline bool pdl_enabled() { return knobs().pdl != 0; }
+inline int knob_expand_tc() { return knobs().expand_tc; }
+inline int knob_expand_tc_min_rank() { return knobs().expand_tc_min_rank; }
 
 // Host-side description of one lora_shrink call, shared by its two paths.
 struct ShrinkLaunch {
@@ -400,8 +423,7 @@ int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_token
 int expand_early(const float *x, const lora_bf16_t *const *lora_b,
                  const lora_bf16_t *const *lora_bias, const int32_t *slice_sizes,
                  int32_t num_slices, int32_t rank, lora_bf16_t *y, int64_t y_ld,
-                 int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st,
-                 const int32_t *map);
+                 int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st);
 // lora_linear as one cooperative kernel (small batches).  Returns 1 when
 // launched, 0 when the batch or its layout does not fit that path.
 int linear_coop(const int32_t *map, int32_t num_tokens, const lora_bf16_t *x, int32_t hidden,
@@ -413,7 +435,9 @@ int linear_coop(const int32_t *map, int32_t num_tokens, const lora_bf16_t *x, in
 
 // Host-side description of one lora_expand call for its tensor-core path.
 struct ExpandLaunch {
-    const float *x;
+    const void *x;                 // fp32, or bf16 when x_bf16
+    int32_t x_bf16;
+    int32_t early;                 // lora_linear's early mode
     const uint16_t *b[LORA_MAX_SLICES];
     const uint16_t *bias[LORA_MAX_SLICES];
     int32_t n[LORA_MAX_SLICES];
@@ -434,7 +458,7 @@ struct ExpandLaunch {
     const int32_t *no_lora;
     int32_t *error_word;
 };
-int launch_expand_umma(const ExpandLaunch &a, cudaStream_t stream);
+int launch_expand_tc(const ExpandLaunch &a, cudaStream_t stream);
 
 // Launch with the programmatic-stream-serialization attribute (when
 // enabled), so the kernel may start while its predecessor drains; the

@@ -46,19 +46,7 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
     const SegTab tab = seg_tab(reinterpret_cast<int *>(sA + Cfg::A_BYTES), p.nbins);
     const int32_t *tokens = p.sorted;
     int total_tiles;
-    if (p.map != nullptr) {
-        int *mm = reinterpret_cast<int *>(sA + Cfg::A_BYTES + seg_tab_bytes(p.nbins));
-        int *cnt = mm, *tot = cnt + 8 * p.nbins, *base = tot + p.nbins, *pos = base + p.nbins;
-        int *srt = pos + p.nbins, *ids = srt + EX_SELF_SORT_MAX_TOKENS;
-        int *misc = ids + EX_SELF_SORT_MAX_TOKENS;
-        if (block_sort_ids<EX_THREADS / 32>(p.map, p.num_tokens, p.nbins - 1, cnt, tot, base,
-                                            pos, srt, misc, ids)) {
-            wait_once();
-            return;
-        }
-        total_tiles = segments_from_sort(tot, base, p.nbins, EX_BM, tab);
-        tokens = srt;
-    } else if (p.num_tokens <= EX_TOKLIST_MAX) {
+    if (p.num_tokens <= EX_TOKLIST_MAX) {
         // Small batches: the whole sorted token list is loaded together with
         // the segment table (the loads are in flight while the table is
         // read), then kept in shared memory, so no item waits on a token load.
@@ -102,8 +90,7 @@ static int launch_expand_kt(const ExpandArgs &p, cudaStream_t stream)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return int(e);
-    const size_t smem = expand_smem_bytes(KT, LORA_MAX_LORAS + 1) +
-                        expand_self_sort_bytes(EX_SELF_SORT_MAX_LORAS + 1);
+    const size_t smem = expand_smem_bytes(KT, LORA_MAX_LORAS + 1) + EX_TOKLIST_MAX * sizeof(int);
     int grid = (dev < 64) ? grid_cache[dev] : 0;
     if (grid == 0) {
         e = cudaFuncSetAttribute(expand_kernel<KT>,
@@ -117,9 +104,7 @@ static int launch_expand_kt(const ExpandArgs &p, cudaStream_t stream)
         if (dev < 64) grid_cache[dev] = grid;
     }
     const size_t used = expand_smem_bytes(KT, p.nbins) +
-                        (p.map != nullptr ? expand_self_sort_bytes(p.nbins)
-                         : p.num_tokens <= EX_TOKLIST_MAX ? size_t(p.num_tokens) * sizeof(int)
-                                                          : 0);
+                        (p.num_tokens <= EX_TOKLIST_MAX ? size_t(p.num_tokens) * sizeof(int) : 0);
     e = launch_kernel(expand_kernel<KT>, dim3(grid), dim3(EX_THREADS), used, stream, p);
     return int(e);
 }
@@ -140,8 +125,7 @@ static int lora_expand_impl(const void *x, int x_bf16, const lora_bf16_t *const 
                             const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
                             lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
                             int32_t offset_start, int32_t add_inputs,
-                            const lora_meta_t *meta, cudaStream_t stream, int early,
-                            const int32_t *map);
+                            const lora_meta_t *meta, cudaStream_t stream, int early);
 }  // namespace lora
 
 LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
@@ -153,7 +137,7 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
 {
     return lora::lora_expand_impl(x, 0, lora_b, lora_bias, slice_sizes, num_slices, rank, y,
                                   y_ld, num_tokens, offset_start, add_inputs, meta,
-                                  static_cast<cudaStream_t>(stream), 0, nullptr);
+                                  static_cast<cudaStream_t>(stream), 0);
 }
 
 // The same product over a bf16 input, which the MMA takes as it is (page
@@ -168,7 +152,7 @@ LORA_API int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lo
 {
     return lora::lora_expand_impl(x, 1, lora_b, lora_bias, slice_sizes, num_slices, rank, y,
                                   y_ld, num_tokens, offset_start, add_inputs, meta,
-                                  static_cast<cudaStream_t>(stream), 0, nullptr);
+                                  static_cast<cudaStream_t>(stream), 0);
 }
 
 int lora::expand_setup(ExpandArgs &p, const void *x, int x_bf16,
@@ -237,7 +221,6 @@ int lora::expand_setup(ExpandArgs &p, const void *x, int x_bf16,
     p.no_lora = meta->no_lora_flag;
     p.nbins = meta->max_loras + 1;
     p.early = 0;
-    p.map = nullptr;
     return LORA_OK;
 }
 
@@ -246,8 +229,7 @@ static int lora::lora_expand_impl(const void *x, int x_bf16, const lora_bf16_t *
                                   const int32_t *slice_sizes, int32_t num_slices, int32_t rank,
                                   lora_bf16_t *y, int64_t y_ld, int32_t num_tokens,
                                   int32_t offset_start, int32_t add_inputs,
-                                  const lora_meta_t *meta, cudaStream_t stream, int early,
-                                  const int32_t *map)
+                                  const lora_meta_t *meta, cudaStream_t stream, int early)
 {
     lora::ExpandArgs p;
     const int r = lora::expand_setup(p, x, x_bf16, lora_b, lora_bias, slice_sizes, num_slices,
@@ -255,7 +237,6 @@ static int lora::lora_expand_impl(const void *x, int x_bf16, const lora_bf16_t *
     if (r == 1) return LORA_OK;              // nothing to do
     if (r != LORA_OK) return r;
     p.early = early;
-    p.map = map;
     return lora::expand_dispatch(p, meta, stream);
 }
 
@@ -267,14 +248,19 @@ int expand_dispatch(ExpandArgs &p, const lora_meta_t *meta, cudaStream_t st)
     lora_bf16_t *y = p.y;
     const int64_t y_ld = p.y_ld;
 
-    // Tensor-core path (tcgen05, TMEM accumulators, TMA for B and for y over
-    // runs of consecutive tokens) for 16-byte-aligned outputs.  Opt-in with
-    // LORA_PUNICA_EXPAND_UMMA=1: on these workloads it was measured slower
-    // than the mma.sync kernel (a TMA box per scattered token row costs far
-    // more than the cp.async gather), so the default stays on mma.sync.
-    if (lora::env_int("LORA_PUNICA_EXPAND_UMMA", 0) && p.vec && !p.x_bf16) {
+    // Tensor-core path (tcgen05, TMEM accumulators; lora_expand_tc.cu) for
+    // 16-byte-aligned outputs.  Opt-in: measured slower than the mma.sync
+    // kernel on every workload (large 232 against 219 us, prefill 49 against
+    // 37), its per-chunk chain of copies, hand-offs and epilogue being
+    // longer than the mma.sync kernel's.  LORA_PUNICA_EXPAND_TC=1 takes it at
+    // every rank, =-1 at ranks of at least LORA_PUNICA_EXPAND_TC_MIN_RANK.
+    const int tc_mode = lora::knob_expand_tc();
+    if (tc_mode != 0 && p.vec &&
+        (tc_mode == 1 || rank >= lora::knob_expand_tc_min_rank())) {
         lora::ExpandLaunch u;
-        u.x = static_cast<const float *>(p.x);
+        u.x = p.x;
+        u.x_bf16 = p.x_bf16;
+        u.early = p.early;
         for (int s = 0; s < LORA_MAX_SLICES; ++s) {
             u.b[s] = p.b[s];
             u.bias[s] = p.bias[s];
@@ -296,7 +282,7 @@ int expand_dispatch(ExpandArgs &p, const lora_meta_t *meta, cudaStream_t st)
         u.active = p.active;
         u.no_lora = p.no_lora;
         u.error_word = meta->error_word;
-        const int r = lora::launch_expand_umma(u, st);
+        const int r = lora::launch_expand_tc(u, st);
         if (r == 1) return LORA_OK;
         if (r != 0) return r;
     }
@@ -311,19 +297,10 @@ int expand_dispatch(ExpandArgs &p, const lora_meta_t *meta, cudaStream_t st)
 int expand_early(const float *x, const lora_bf16_t *const *lora_b,
                  const lora_bf16_t *const *lora_bias, const int32_t *slice_sizes,
                  int32_t num_slices, int32_t rank, lora_bf16_t *y, int64_t y_ld,
-                 int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st,
-                 const int32_t *map)
+                 int32_t num_tokens, const lora_meta_t *meta, cudaStream_t st)
 {
-    // With `map` the caller asks the expand to sort the ids itself (its
-    // predecessor may be the kernel that writes the metadata).  When the
-    // batch is too large for that, it runs in plain mode: everything is read
-    // after the grid-dependency wait.
-    if (map != nullptr && (num_tokens > EX_SELF_SORT_MAX_TOKENS ||
-                           meta->max_loras > EX_SELF_SORT_MAX_LORAS))
-        return lora_expand_impl(x, 0, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
-                                num_tokens, 0, 1, meta, st, 0, nullptr);
     return lora_expand_impl(x, 0, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
-                            num_tokens, 0, 1, meta, st, 1, map);
+                            num_tokens, 0, 1, meta, st, 1);
 }
 
 }  // namespace lora

@@ -43,23 +43,11 @@ struct ExpandArgs {
     // kernel and everything before it in the stream have completed, and the
     // shrink writes neither the metadata, y, B nor bias.
     int32_t early;
-    // With `map` (early mode, small batches) every CTA sorts the id map
-    // itself instead of reading the segment table and token list: one round
-    // trip instead of two.  The result is the metadata the metadata kernel
-    // writes, so the two agree.
-    const int32_t *map;
 };
 
-constexpr int EX_SELF_SORT_MAX_TOKENS = 512;
 // Batches of up to this many tokens keep the whole sorted token list in
-// shared memory (4 bytes a token; within the self-sort area's size).
+// shared memory (4 bytes a token).
 constexpr int EX_TOKLIST_MAX = 1024;
-constexpr int EX_SELF_SORT_MAX_LORAS = 256;
-
-inline size_t expand_self_sort_bytes(int nbins)
-{
-    return size_t(8 * nbins + 3 * nbins + 2 * EX_SELF_SORT_MAX_TOKENS + 4) * sizeof(int);
-}
 
 template <int KT>
 struct ExpandTile {

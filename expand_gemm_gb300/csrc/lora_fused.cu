@@ -682,7 +682,8 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
     // where the shrink phase and the barrier cost more than the launches
     // they replace.  LORA_PUNICA_COOP=1 takes it for every batch that fits
     // (up to 512 tokens), LORA_PUNICA_COOP=0 never.
-    const int coop_mode = lora::env_int("LORA_PUNICA_COOP", -1);
+    const lora::Knobs &kn = lora::knobs();
+    const int coop_mode = kn.coop;
     if (coop_mode == 1 ||
         (coop_mode != 0 && int64_t(num_tokens) * num_slices <= 256)) {
         const int r = lora::linear_coop(token_lora_mapping, num_tokens, x, hidden, x_ld, lora_a,
@@ -699,9 +700,8 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
     // shared-memory reductions made it slower than the three kernels, on 64
     // tokens faster.  LORA_PUNICA_FUSED=1 takes it up to 512 tokens,
     // LORA_PUNICA_FUSED=0 never.
-    const int fused_mode = lora::env_int("LORA_PUNICA_FUSED", -1);
-    const int fused_max = fused_mode == 1 ? lora::FU_TMAX
-                        : lora::env_int("LORA_PUNICA_FUSED_MAX_TOKENS", 128);
+    const int fused_mode = kn.fused;
+    const int fused_max = fused_mode == 1 ? lora::FU_TMAX : kn.fused_max_tokens;
     bool fused = fused_mode != 0 && num_tokens > 0 && num_tokens <= fused_max &&
                  token_lora_mapping != nullptr && x != nullptr && buf != nullptr && y != nullptr &&
                  hidden > 0 && hidden % 8 == 0 && x_ld % 8 == 0 && y_ld % 8 == 0 &&
@@ -764,25 +764,19 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
             if (r != 0) return r;
         }
     }
-    // Small batches: the metadata kernel, then the shrink in early mode
-    // (it sorts the ids itself and starts its loads while the metadata
-    // kernel runs), then the expand in early mode (it fetches the metadata,
-    // y and B while the shrink runs).  LORA_PUNICA_SELF_META=1 instead drops
-    // the metadata kernel (the shrink writes the metadata); =0 runs the
-    // plain three calls.
-    const int self_meta = lora::env_int("LORA_PUNICA_SELF_META", -1);
+    // The metadata kernel, then the shrink in early mode (for batches of up
+    // to 512 tokens it sorts the ids itself and starts its loads while the
+    // metadata kernel runs), then the expand in early mode (it fetches the
+    // metadata, y and B while the shrink runs).  LORA_PUNICA_SELF_META=1
+    // instead drops the metadata kernel (the shrink writes the metadata);
+    // =0 runs the plain three calls.
+    const int self_meta = kn.self_meta;
     int r = 0;
     bool early = false;
-    if (self_meta == 1 || self_meta == 2) {
-        // =2: the expand too sorts the ids itself and starts (sorting,
-        // fetching y and B) while the shrink runs; it reads nothing the
-        // shrink writes but the buffer, after its grid-dependency wait.
+    if (self_meta == 1) {
         r = lora::shrink_self_meta(token_lora_mapping, x, num_tokens, hidden, x_ld, lora_a,
-                                   num_slices, rank, buf, meta, scale, st, self_meta == 2 ? 2 : 0);
+                                   num_slices, rank, buf, meta, scale, st, 0);
         if (r < 0 || r > 1) return r;
-        if (r == 1 && self_meta == 2)
-            return lora::expand_early(buf, lora_b, lora_bias, slice_sizes, num_slices, rank, y,
-                                      y_ld, num_tokens, meta, st, token_lora_mapping);
     } else if (self_meta == -1) {
         r = lora_meta_prepare(token_lora_mapping, num_tokens, meta, stream);
         if (r != 0) return r;
@@ -805,14 +799,8 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
         if (r != 0) return r;
     }
     if (early)
-        // The expand reads the segment table and token list the metadata
-        // kernel wrote (two round trips); sorting the ids in every expand
-        // CTA was measured slower on decode batches, so it is opt-in
-        // (LORA_PUNICA_EXPAND_SELF_SORT=1).
         return lora::expand_early(buf, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld,
-                                  num_tokens, meta, st,
-                                  lora::env_int("LORA_PUNICA_EXPAND_SELF_SORT", 0)
-                                      ? token_lora_mapping : nullptr);
+                                  num_tokens, meta, st);
     return lora_expand(buf, lora_b, lora_bias, slice_sizes, num_slices, rank, y, y_ld, num_tokens,
                        0, 1, meta, stream);
 }

@@ -282,8 +282,8 @@ int launch_linear_coop(CoopArgs &p, cudaStream_t st)
         grid_cache[dev][ti] = grid;
     }
     if (grid < 0) return 0;
-    p.expect = uint32_t(grid) + uint32_t(max(0, env_int("LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS", 0)));
-    const long long tmo = env_int("LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES", 0);
+    p.expect = uint32_t(grid) + uint32_t(max(0, knobs().coop_test_extra));
+    const long long tmo = knobs().coop_test_timeout;
     p.timeout = (tmo > 0) ? tmo : CO_TIMEOUT_CYCLES;
 
     cudaLaunchConfig_t cfg = {};

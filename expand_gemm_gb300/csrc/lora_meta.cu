@@ -206,7 +206,7 @@ int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
     }
     // Small batches on 8 warps (fewer warps to pass each barrier), the rest
     // on 32.  LORA_PUNICA_META_SMALL=0 always takes 32 warps.
-    if (a.num_tokens <= META_SMALL_MAX && env_int("LORA_PUNICA_META_SMALL", 1)) {
+    if (a.num_tokens <= META_SMALL_MAX && knobs().meta_small) {
         const size_t smem = meta_smem_bytes(META_SMALL_THREADS / 32, a.max_loras, a.num_tokens);
         return int(launch_kernel(meta_prepare_kernel<META_SMALL_THREADS>, dim3(1),
                                  dim3(META_SMALL_THREADS), smem, stream, a));

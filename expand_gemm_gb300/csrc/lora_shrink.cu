@@ -60,7 +60,6 @@ struct ShrinkArgs {
     // nothing the metadata kernel writes; it lets its own dependents launch
     // only after that wait, which is what lora_linear's expand relies on.
     int32_t early;
-    int32_t leave_room;            // cap the grid like early mode (the next kernel starts early)
 };
 
 constexpr int SH_SELF_META_MAX_TOKENS = 512;
@@ -324,8 +323,8 @@ static int launch_shrink_mt(const ShrinkArgs &p, cudaStream_t stream)
     // expand that follows fits beside them and starts loading.  Two was
     // measured best on 256-token q/k/v decode (14.9 us a step, against 15.3
     // with one and 15.4 with three).
-    if (p.early || p.leave_room)
-        grid = min(grid, max(1, env_int("LORA_PUNICA_EARLY_SHRINK_CTAS", 2)) * device_sm_count());
+    if (p.early)
+        grid = min(grid, max(1, knobs().early_shrink_ctas) * device_sm_count());
     e = launch_kernel(shrink_kernel<MT>, dim3(grid), dim3(SH_THREADS), used, stream, p);
     return int(e);
 }
@@ -377,7 +376,6 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
     p.map = nullptr;
     p.write_meta = 0;
     p.early = 0;
-    p.leave_room = 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -387,9 +385,10 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
     // default 1024) and at least LORA_PUNICA_UMMA_MIN_COLS output columns per
     // token over all slices (num_slices * rank, default 256).
     // LORA_PUNICA_UMMA=0 turns it off.  The variables are read at each call.
-    const int umma_on = lora::env_int("LORA_PUNICA_UMMA", 1);
-    const int umma_min_tokens = lora::env_int("LORA_PUNICA_UMMA_MIN_TOKENS", 1024);
-    const int umma_min_cols = lora::env_int("LORA_PUNICA_UMMA_MIN_COLS", 256);
+    const lora::Knobs &kn = lora::knobs();
+    const int umma_on = kn.umma;
+    const int umma_min_tokens = kn.umma_min_tokens;
+    const int umma_min_cols = kn.umma_min_cols;
     if (umma_on && num_tokens >= umma_min_tokens && num_slices * rank >= umma_min_cols &&
         meta->error_word != nullptr) {
         u.x = x;
@@ -410,7 +409,7 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
         // LORA_PUNICA_UMMA_PARTIAL=1 (default): the tensor-core kernel takes
         // the partial tile at the end of every segment too, and covers the
         // whole batch; =0: whole tiles only, the remainders on mma.sync.
-        u.partial = lora::env_int("LORA_PUNICA_UMMA_PARTIAL", 1) ? 1 : 0;
+        u.partial = kn.umma_partial ? 1 : 0;
         const int r = lora::launch_shrink_umma(u, st);
         if (r == 1 && u.partial) return LORA_OK;
         if (r == 1) p.skip_rows = 128;
@@ -477,11 +476,9 @@ int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_token
     p.no_lora_out = meta->no_lora_flag;
     p.error_out = meta->error_word;
     // early == 1: the metadata kernel writes the buffers, and the loads start
-    // before the grid-dependency wait.  Otherwise CTA 0 writes them; with
-    // early == 2 the grid also leaves room for an early-starting expand.
+    // before the grid-dependency wait.  Otherwise CTA 0 writes them.
     p.write_meta = early == 1 ? 0 : 1;
     p.early = early == 1 ? 1 : 0;
-    p.leave_room = early == 2 ? 1 : 0;
     int r;
     if (rank <= 16) r = launch_shrink_mt<1>(p, st);
     else if (rank <= 32) r = launch_shrink_mt<2>(p, st);

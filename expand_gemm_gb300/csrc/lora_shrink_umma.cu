@@ -345,42 +345,6 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
 
 // ------------------------------------------------------------------ host
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// 2-D bf16 map over rows x cols (row stride in elements), 128-byte swizzle.
-static bool encode_2d(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols,
-                      uint64_t row_stride, uint32_t box_rows)
-{
-    EncodeTiledFn fn = encode_fn();
-    if (fn == nullptr) return false;
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {row_stride * 2};
-    const cuuint32_t box[2] = {uint32_t(UM_BK), box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Launches the UMMA path if the shapes allow it; returns 1 if launched, 0
 // if not applicable (caller then covers every row with the mma.sync path),
 // or a negative value / cudaError_t on failure.
@@ -402,12 +366,12 @@ int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream)
 
     static UmmaShrinkArgs p;      // large (>1 KB): keep off the stack
     for (int i = 0; i < UM_XMAPS; ++i)
-        if (!encode_2d(&p.map_x[i], a.x, uint64_t(a.num_tokens), uint64_t(a.hidden),
-                       uint64_t(a.x_ld), 1u << i))
+        if (!encode_tile_map(&p.map_x[i], a.x, uint64_t(a.num_tokens), uint64_t(a.hidden),
+                             uint64_t(a.x_ld), UM_BK, 1u << i, CU_TENSOR_MAP_SWIZZLE_128B))
             return 0;
     for (int s = 0; s < S; ++s) {
-        if (!encode_2d(&p.map_a[s], a.a[s], uint64_t(a.max_loras) * a.rank, uint64_t(a.hidden),
-                       uint64_t(a.hidden), uint32_t(rp)))
+        if (!encode_tile_map(&p.map_a[s], a.a[s], uint64_t(a.max_loras) * a.rank, uint64_t(a.hidden),
+                             uint64_t(a.hidden), UM_BK, uint32_t(rp), CU_TENSOR_MAP_SWIZZLE_128B))
             return 0;
     }
     p.y = a.y;

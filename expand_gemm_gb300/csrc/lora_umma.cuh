@@ -197,4 +197,11 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n)
          | (uint32_t(m >> 4) << 24);         // M / 16            [24, 29)
 }
 
+// Host: encodes a 2-D bf16 tensor map over `rows` rows of `cols` elements
+// (row stride in elements) with box {box_cols, box_rows} and the given
+// swizzle; false if the driver entry point is missing or rejects it.
+bool encode_tile_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols,
+                     uint64_t row_stride, uint32_t box_cols, uint32_t box_rows,
+                     CUtensorMapSwizzle swizzle);
+
 }  // namespace lora

@@ -201,9 +201,13 @@ int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidden,
  *   add_inputs   nonzero: add to y; zero: overwrite the slice columns.
  *
  * x is rounded to bf16 for the tensor cores (as the Triton kernel does when
- * it casts its input to the weight type); products accumulate in fp32; y,
- * the bias and the product are summed in fp32 and rounded to bf16 once
- * (round to nearest even).  Output: deterministic.
+ * it casts its input to the weight type); products accumulate in fp32
+ * (mma.sync; an opt-in tcgen05 path with TMEM accumulators when y's rows,
+ * offsets and slice widths are 16-byte aligned, LORA_PUNICA_EXPAND_TC* in
+ * the environment); y, the bias and the product are summed in fp32 and
+ * rounded to bf16 once (round to nearest even).  Output: deterministic.  A
+ * bounded wait of the tcgen05 path that runs out sets bit 30 of
+ * meta->error_word.
  */
 int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
                 const lora_bf16_t *const *lora_bias,
@@ -254,11 +258,11 @@ int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lora_b,
  *     metadata kernel, the shrink (sorting the ids itself and loading
  *     before its dependency wait, for <= 512 tokens) and the expand
  *     (fetching the metadata, y and B before its wait).
- * Environment (read at each call): LORA_PUNICA_COOP=0/1 never / always
- * (when the batch fits) the cooperative kernel; LORA_PUNICA_FUSED=0/1 and
- * LORA_PUNICA_FUSED_MAX_TOKENS the cluster kernel; LORA_PUNICA_SELF_META=1
- * two kernels (the shrink writes the metadata), =2 the same with the
- * expand sorting the ids itself, =0 the plain three calls.
+ * Environment (read once, see lora_reload_options): LORA_PUNICA_COOP=0/1
+ * never / always (when the batch fits) the cooperative kernel;
+ * LORA_PUNICA_FUSED=0/1 and LORA_PUNICA_FUSED_MAX_TOKENS the cluster
+ * kernel; LORA_PUNICA_SELF_META=1 two kernels (the shrink writes the
+ * metadata), =0 the plain three calls.
  */
 int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
                 const lora_bf16_t *x, int32_t hidden, int64_t x_ld,
@@ -296,6 +300,17 @@ int lora_linear_noalloc(const int32_t *token_lora_mapping, int32_t num_tokens,
                         const lora_bf16_t *const *lora_bias, const int32_t *slice_sizes,
                         int32_t num_slices, int32_t rank, float scale, lora_bf16_t *y,
                         int64_t y_ld, const lora_meta_t *meta, void *stream);
+
+/*
+ * lora_reload_options -- re-reads the library's tuning variables
+ * (LORA_PUNICA_*: which of lora_linear's launch paths a batch takes, which
+ * batches the tensor-core kernels take, programmatic dependent launch).
+ * The library reads them once, at its first call; no later call reads the
+ * environment unless this is called.  It must not run while another thread
+ * is inside the library.  The pages have no counterpart: this is a control
+ * of this library's own launch choices.
+ */
+void lora_reload_options(void);
 
 /* Human-readable name of a status (negative LORA_ERR_* or cudaError_t). */
 const char *lora_status_string(int status);

@@ -23,3 +23,23 @@ def oracle_mod():
     if mutant:
         oracle.load_library(mutant)
     return oracle
+
+
+@pytest.fixture
+def knob(monkeypatch):
+    """Sets LORA_PUNICA_* tuning variables for one test: knob(NAME=value,
+    ...) (None removes one).  The library reads its tuning variables once,
+    so each call makes it read them again, and so does the end of the test
+    after the environment is restored."""
+    import expand_gemm_gb300 as eg
+
+    def set_(**kv):
+        for k, v in kv.items():
+            if v is None:
+                monkeypatch.delenv(k, raising=False)
+            else:
+                monkeypatch.setenv(k, str(v))
+        eg.reload_options()
+    yield set_
+    monkeypatch.undo()
+    eg.reload_options()

@@ -10,28 +10,21 @@ from gpu_helpers import (EXPAND_ATOL, EXPAND_RTOL, SHRINK_ATOL, SHRINK_RTOL, ass
 
 pytestmark = pytest.mark.gpu
 
-# (LORA_PUNICA_COOP, LORA_PUNICA_FUSED, LORA_PUNICA_SELF_META,
-#  LORA_PUNICA_EXPAND_SELF_SORT): one cooperative kernel (metadata, shrink,
-# grid barrier, expand); one cluster kernel; the metadata kernel, then
-# shrink and expand each loading before their grid-dependency wait; the
-# same with the expand sorting the ids itself; the shrink sorting the ids
-# itself and writing the metadata + expand (plain, or also sorting the ids
-# itself and starting early); the plain metadata kernel +
-# shrink + expand.  Batches a path does not take fall through to the next.
-PATHS = [pytest.param(("1", "0", "", ""), id="coop"),
-         pytest.param(("0", "1", "", ""), id="fused"),
-         pytest.param(("0", "0", "", ""), id="early"),
-         pytest.param(("0", "0", "", "1"), id="early_self_sort"),
-         pytest.param(("0", "0", "1", ""), id="two_kernels"),
-         pytest.param(("0", "0", "2", ""), id="two_kernels_self_sort"),
-         pytest.param(("0", "0", "0", ""), id="three_kernels")]
+# (LORA_PUNICA_COOP, LORA_PUNICA_FUSED, LORA_PUNICA_SELF_META): one
+# cooperative kernel (metadata, shrink, grid barrier, expand); one cluster
+# kernel; the metadata kernel, then shrink and expand each loading before
+# their grid-dependency wait; the shrink sorting the ids itself and writing
+# the metadata, then the expand; the plain metadata kernel + shrink +
+# expand.  Batches a path does not take fall through to the next.
+PATHS = [pytest.param(("1", "0", None), id="coop"),
+         pytest.param(("0", "1", None), id="fused"),
+         pytest.param(("0", "0", None), id="early"),
+         pytest.param(("0", "0", "1"), id="two_kernels"),
+         pytest.param(("0", "0", "0"), id="three_kernels")]
 
 
-def _set_path(monkeypatch, path):
-    monkeypatch.setenv("LORA_PUNICA_COOP", path[0])
-    monkeypatch.setenv("LORA_PUNICA_FUSED", path[1])
-    monkeypatch.setenv("LORA_PUNICA_SELF_META", path[2])
-    monkeypatch.setenv("LORA_PUNICA_EXPAND_SELF_SORT", path[3])
+def _set_path(knob, path):
+    knob(LORA_PUNICA_COOP=path[0], LORA_PUNICA_FUSED=path[1], LORA_PUNICA_SELF_META=path[2])
 
 
 def _check_linear(oracle_mod, inp, ids=None, buf0=None, L=None):
@@ -78,8 +71,8 @@ def _check_linear(oracle_mod, inp, ids=None, buf0=None, L=None):
 
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("mlp", 200)])
-def test_linear_workloads(oracle_mod, monkeypatch, path, name, T):
-    _set_path(monkeypatch, path)
+def test_linear_workloads(oracle_mod, knob, path, name, T):
+    _set_path(knob, path)
     _check_linear(oracle_mod, W.generate(name, num_tokens=T))
 
 
@@ -93,8 +86,8 @@ def test_linear_workloads(oracle_mod, monkeypatch, path, name, T):
     (513, 256, 16, 3, (128,), False, "uniform"),           # one past it: three kernels
     (200, 256, 16, 300, (64,), False, "uniform"),          # many LoRAs: three kernels
 ])
-def test_linear_shapes(oracle_mod, monkeypatch, path, T, H, r, L, slices, bias, ids):
-    _set_path(monkeypatch, path)
+def test_linear_shapes(oracle_mod, knob, path, T, H, r, L, slices, bias, ids):
+    _set_path(knob, path)
     w = W.Workload("lin", T + H + r, T, H, r, L, slices, ids, p_none=0.2, seq_len=(20, 90),
                    bias=bias, scale=0.8)
     inp = W.generate(w)
@@ -103,8 +96,8 @@ def test_linear_shapes(oracle_mod, monkeypatch, path, T, H, r, L, slices, bias, 
 
 
 @pytest.mark.parametrize("path", PATHS)
-def test_linear_no_lora_and_invalid_ids(oracle_mod, monkeypatch, path):
-    _set_path(monkeypatch, path)
+def test_linear_no_lora_and_invalid_ids(oracle_mod, knob, path):
+    _set_path(knob, path)
     inp = W.generate("decode")
     _check_linear(oracle_mod, inp, ids=np.full(256, -1, np.int32))
     ids = inp.ids.copy()
@@ -139,7 +132,7 @@ def test_linear_repeated_calls_accumulate(oracle_mod):
     assert_close(bits_to_f64(host_bits(y)), y2, 2 * EXPAND_ATOL, 2 * EXPAND_RTOL, "y after two calls")
 
 
-def test_coop_barrier_timeout_reports_and_recovers(oracle_mod, monkeypatch):
+def test_coop_barrier_timeout_reports_and_recovers(oracle_mod, knob):
     """The cooperative kernel's grid barrier is made to wait for one arrival
     that never comes (a test knob raises the expected count), with a short
     poll limit: every CTA gives up, bit 30 of the error word is set, the
@@ -155,9 +148,8 @@ def test_coop_barrier_timeout_reports_and_recovers(oracle_mod, monkeypatch):
     B = [dev_bf16(b) for b in inp.lora_b]
     ids = dev_i32(inp.ids)
     meta = eg.LoRAKernelMeta.make(w.max_loras, T, "cuda")
-    monkeypatch.setenv("LORA_PUNICA_COOP", "1")
-    monkeypatch.setenv("LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS", "1")
-    monkeypatch.setenv("LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES", "20000000")   # ~10 ms
+    knob(LORA_PUNICA_COOP=1, LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS=1,
+         LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES=20000000)   # ~10 ms
     y = dev_bf16(inp.y)
     buf = dev_f32(inp.buf)
     eg.lora_linear(ids, x, A, B, None, w.scale, buf, y, meta)
@@ -168,8 +160,7 @@ def test_coop_barrier_timeout_reports_and_recovers(oracle_mod, monkeypatch):
     ref_buf = oracle_mod.shrink(inp.x, inp.lora_a, inp.ids, w.scale, inp.buf)
     assert_close(buf.cpu().numpy(), ref_buf, SHRINK_ATOL, SHRINK_RTOL, "buffer after timeout")
 
-    monkeypatch.delenv("LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS")
-    monkeypatch.delenv("LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES")
+    knob(LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS=None, LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES=None)
     y = dev_bf16(inp.y)
     buf = dev_f32(inp.buf)
     eg.lora_linear(ids, x, A, B, None, w.scale, buf, y, meta)
@@ -184,7 +175,7 @@ def test_coop_barrier_timeout_reports_and_recovers(oracle_mod, monkeypatch):
 
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name,T", [("decode", None), ("mlp", 512), ("prefill", 2048)])
-def test_linear_alternating_no_lora_batches(oracle_mod, monkeypatch, path, name, T):
+def test_linear_alternating_no_lora_batches(oracle_mod, knob, path, name, T):
     """Calls with a mixed id map (with bias) and all -1 calls alternate on one
     metadata struct, back to back in one stream.  After every all -1 call, y
     and the buffer are bit-identical to what they were before it: no kernel
@@ -193,7 +184,7 @@ def test_linear_alternating_no_lora_batches(oracle_mod, monkeypatch, path, name,
     kernel of the chain must pass its wait before it exits).  Every mixed
     call is checked against the oracle."""
     import expand_gemm_gb300 as eg
-    _set_path(monkeypatch, path)
+    _set_path(knob, path)
     w0 = W.generate(name, num_tokens=T).workload
     from dataclasses import replace
     w = replace(w0, bias=True, scale=0.9)

@@ -95,15 +95,13 @@ def test_shrink_shapes(oracle_mod, T, H, r, L, S):
     (1100, 128, 24, 2, 2),      # padded rank 24 -> 32
 ])
 @pytest.mark.parametrize("umma,partial", [("0", "1"), ("1", "1"), ("1", "0")])
-def test_shrink_long_segments(oracle_mod, monkeypatch, umma, partial, T, H, r, L, S):
+def test_shrink_long_segments(oracle_mod, knob, umma, partial, T, H, r, L, S):
     """Long sequences per LoRA: with the tensor-core path forced on it takes
     every tile, the partial last tile of each segment included (partial=1),
     or the whole 128-token tiles with the remainders on mma.sync
     (partial=0); with it off, mma.sync covers everything."""
-    monkeypatch.setenv("LORA_PUNICA_UMMA", umma)
-    monkeypatch.setenv("LORA_PUNICA_UMMA_PARTIAL", partial)
-    monkeypatch.setenv("LORA_PUNICA_UMMA_MIN_COLS", "0")
-    monkeypatch.setenv("LORA_PUNICA_UMMA_MIN_TOKENS", "0")
+    knob(LORA_PUNICA_UMMA=umma, LORA_PUNICA_UMMA_PARTIAL=partial, LORA_PUNICA_UMMA_MIN_COLS=0,
+         LORA_PUNICA_UMMA_MIN_TOKENS=0)
     w = W.Workload("long", T + r, T, H, r, L, tuple([16] * S), "zipf_seq", p_none=0.1,
                    seq_len=(200, 900), scale=0.75)
     inp = W.generate(w)
@@ -189,8 +187,8 @@ EXPAND_PATHS = [pytest.param("1", id="tcgen05"), pytest.param("0", id="mma_sync"
 @pytest.mark.parametrize("path", EXPAND_PATHS)
 @pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("prefill", 1536),
                                     ("mlp", 512), ("large", 384)])
-def test_expand_workloads_reduced(oracle_mod, monkeypatch, path, name, T):
-    monkeypatch.setenv("LORA_PUNICA_EXPAND_UMMA", path)
+def test_expand_workloads_reduced(oracle_mod, knob, path, name, T):
+    knob(LORA_PUNICA_EXPAND_TC=path)
     inp = W.generate(name, num_tokens=T)
     _expand_case(oracle_mod, inp)
 
@@ -203,8 +201,8 @@ def test_expand_workloads_reduced(oracle_mod, monkeypatch, path, name, T):
     (50, 32, 5, (16,) * 8, 0, 0),         # eight slices
 ])
 @pytest.mark.parametrize("path", EXPAND_PATHS)
-def test_expand_shapes(oracle_mod, monkeypatch, path, T, r, L, slices, offset, y_extra):
-    monkeypatch.setenv("LORA_PUNICA_EXPAND_UMMA", path)
+def test_expand_shapes(oracle_mod, knob, path, T, r, L, slices, offset, y_extra):
+    knob(LORA_PUNICA_EXPAND_TC=path)
     rng_bias = [True, False][T % 2]
     inp = _custom(T, 64, r, L, slices, seed=T + r, bias=rng_bias)
     _expand_case(oracle_mod, inp, offset=offset, y_extra=y_extra)
@@ -217,9 +215,9 @@ def test_expand_unaligned_scalar_path(oracle_mod, slices, offset):
 
 
 @pytest.mark.parametrize("path", EXPAND_PATHS)
-def test_expand_long_segments(oracle_mod, monkeypatch, path):
+def test_expand_long_segments(oracle_mod, knob, path):
     """Sequences of hundreds of tokens per LoRA: many full 128-token tiles."""
-    monkeypatch.setenv("LORA_PUNICA_EXPAND_UMMA", path)
+    knob(LORA_PUNICA_EXPAND_TC=path)
     w = W.Workload("longx", 31, 2500, 64, 64, 5, (384, 136, 8), "zipf_seq", p_none=0.2,
                    seq_len=(150, 700), bias=True)
     inp = W.generate(w)
@@ -227,8 +225,8 @@ def test_expand_long_segments(oracle_mod, monkeypatch, path):
 
 
 @pytest.mark.parametrize("path", EXPAND_PATHS)
-def test_expand_overwrite_mode(oracle_mod, monkeypatch, path):
-    monkeypatch.setenv("LORA_PUNICA_EXPAND_UMMA", path)
+def test_expand_overwrite_mode(oracle_mod, knob, path):
+    knob(LORA_PUNICA_EXPAND_TC=path)
     inp = _custom(333, 64, 32, 4, (256, 128), seed=22, bias=True)
     _expand_case(oracle_mod, inp, add_inputs=False, offset=8, y_extra=16)
     _expand_case(oracle_mod, inp, add_inputs=False, offset=3, y_extra=1)   # scalar path
