@@ -1,9 +1,18 @@
 // lora_meta.cu -- metadata step (page "vllm.lora.ops.triton_ops.
-// lora_kernel_metadata", LoRAKernelMeta._reset + prepare_tensors) as one
-// single-CTA kernel: the id map staged in shared memory, per-warp bin
-// histograms (shared-memory atomic adds), a warp-shuffle scan over
-// (bin, warp), and a stable counting-sort scatter (lanes of one bin ranked
-// with __match_any_sync).
+// lora_kernel_metadata", LoRAKernelMeta._reset + prepare_tensors): a
+// stable counting sort by LoRA id.  Per-warp bin histograms (shared-memory
+// atomic adds), a warp-shuffle scan over (bin, warp), and a stable scatter
+// (lanes of one bin ranked with __match_any_sync).
+//
+// Two kernels compute it:
+//   - meta_prepare_kernel: one CTA, the id map staged in shared memory;
+//     batches of up to META_MULTI_MIN tokens.
+//   - meta_multi_kernel: one CTA per run of META_MULTI_CHUNK tokens.  Every
+//     CTA counts the whole map itself (one coalesced load and one vote per
+//     32 tokens; the map is read from L2), keeping apart the tokens before
+//     its run, those of its run (per warp) and those after it.  That gives
+//     it the bin totals and its own start inside every bin without any
+//     exchange between CTAs, and it scatters the tokens of its run.
 //
 // Bins: bin 0 holds id -1 (and every invalid id), bin b > 0 holds id b - 1.
 // Token order inside a bin is preserved because (1) each warp owns one
@@ -22,6 +31,10 @@ constexpr int META_SMALL_MAX = 512;
 // one block-wide load (all of it in flight at once); both passes then read
 // shared memory.  Larger batches read the map from global memory.
 constexpr int META_STAGE_MAX = 16384;
+// Batches above this many tokens take the multi-CTA kernel.
+constexpr int META_MULTI_MIN = 2048;
+constexpr int META_MULTI_THREADS = 1024;
+constexpr int META_MULTI_CHUNK = 1024;   // tokens per CTA: one 32-token group per warp
 
 struct MetaArgs {
     const int32_t *map;
@@ -49,6 +62,34 @@ __device__ __forceinline__ int token_bin(int32_t id, int32_t max_loras, int &bad
     if (id >= 0 && id < max_loras) return id + 1;
     if (id != -1) ++bad;
     return 0;
+}
+
+// Pass 1 for one 32-token group: adds the group's tokens to this warp's bin
+// counts.  A group whose tokens all fall in one bin (runs of one sequence,
+// the all -1 batch) takes one add instead of 32 conflicting ones.
+__device__ __forceinline__ void count_group(int32_t *cnt_w, int b, bool has, int lane)
+{
+    const int b0 = __shfl_sync(0xffffffffu, b, 0);
+    if (__all_sync(0xffffffffu, has && b == b0)) {
+        if (lane == 0) atomicAdd(&cnt_w[b0], 32);
+    } else if (has) {
+        atomicAdd(&cnt_w[b], 1);
+    }
+}
+
+// Pass 2 for one 32-token group: each token's rank among the group's tokens
+// of its bin, and the number of those tokens (returned to rank 0 of each
+// bin).  Lane order is token order, so the ranks keep the sort stable.
+__device__ __forceinline__ int rank_in_group(int b, bool has, int lane, int &group_count)
+{
+    const int b0 = __shfl_sync(0xffffffffu, b, 0);
+    if (__all_sync(0xffffffffu, has && b == b0)) {
+        group_count = 32;
+        return lane;
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, b);
+    group_count = __popc(grp);
+    return __popc(grp & ((1u << lane) - 1u));
 }
 
 template <int NT>
@@ -83,16 +124,17 @@ __global__ void __launch_bounds__(NT, 1) meta_prepare_kernel(MetaArgs a)
     const int t0 = min(T, warp * per_warp);
     const int t1 = min(T, t0 + per_warp);
 
-    // Pass 1: per-warp histogram, one shared-memory atomic add per token
-    // (counts only: pass 2 keeps the order).  Measured faster than grouping
-    // lanes with __match_any_sync, whose cost grows with the number of
-    // distinct ids in a warp.
+    // Pass 1: per-warp histogram, one shared-memory atomic add per token,
+    // or one per group of 32 tokens of one bin (counts only: pass 2 keeps
+    // the order).  Per-token adds were measured faster than grouping lanes
+    // with __match_any_sync, whose cost grows with the number of distinct
+    // ids in a warp.
     int bad = 0;
     for (int g = t0; g < t1; g += 32) {
         const int t = g + lane;
         const bool has = t < t1;
         const int b = has ? token_bin(ids[t], a.max_loras, bad) : -1;
-        if (has) atomicAdd(&cnt[warp * nb + b], 1);
+        count_group(cnt + warp * nb, b, has, lane);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
@@ -173,16 +215,156 @@ __global__ void __launch_bounds__(NT, 1) meta_prepare_kernel(MetaArgs a)
         const bool has = t < t1;
         const int32_t id = has ? ids[t] : -1;
         const int b = has ? token_bin(id, a.max_loras, unused) : -1;
-        const unsigned grp = __match_any_sync(0xffffffffu, b);
-        const int rank = __popc(grp & ((1u << lane) - 1u));
+        int n = 0;
+        const int rank = rank_in_group(b, has, lane, n);
         if (has) {
             a.sorted[base[b] + cnt[warp * nb + b] + rank] = t;
             a.mapping_copy[t] = id;
         }
         __syncwarp();
-        if (has && rank == 0) cnt[warp * nb + b] += __popc(grp);
+        if (has && rank == 0) cnt[warp * nb + b] += n;
         __syncwarp();
     }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) meta_multi_kernel(MetaArgs a)
+{
+    constexpr int NW = NT / 32;
+    static_assert(NW * 32 == META_MULTI_CHUNK, "one 32-token group per warp in the CTA's run");
+    extern __shared__ int32_t sm[];
+    const int nb = a.max_loras + 1;
+    int32_t *own = sm;                          // [NW][nb]: run counts per warp, then offsets
+    int32_t *bef = own + NW * nb;               // [nb] tokens before the run
+    int32_t *aft = bef + nb;                    // [nb] tokens after the run
+    int32_t *tot = aft + nb;                    // [nb] all tokens
+    int32_t *base = tot + nb;                   // [nb] first sorted slot of the bin
+    int32_t *pos = base + nb;                   // [nb] index among non-empty bins
+    __shared__ int32_t s_invalid, s_nactive;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = a.num_tokens, cta = int(blockIdx.x);
+    const int g_run = cta * NW;                 // first 32-token group of the run
+    const int ngroups = (T + 31) / 32;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    for (int i = tid; i < (NW + 2) * nb; i += NT) sm[i] = 0;
+    if (tid == 0) s_invalid = 0;
+    __syncthreads();
+
+    // Pass 1 over the whole map: the run's group of this warp into own[warp],
+    // every other group into bef or aft (groups dealt round-robin to warps).
+    // Sixteen groups' ids are loaded at once so their latencies overlap.
+    constexpr int U = 16;
+    int bad = 0;
+    for (int g0 = warp; g0 < ngroups; g0 += NW * U) {
+        int32_t idv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int t = (g0 + u * NW) * 32 + lane;
+            idv[u] = (t < T) ? a.map[t] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int gi = g0 + u * NW;             // the same in every lane
+            if (gi >= ngroups) break;
+            const int t = gi * 32 + lane;
+            const bool has = t < T;
+            const int b = has ? token_bin(idv[u], a.max_loras, bad) : -1;
+            int32_t *dst = (gi < g_run) ? bef : (gi >= g_run + NW) ? aft
+                                                                   : own + (gi - g_run) * nb;
+            count_group(dst, b, has, lane);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if (lane == 0 && bad) atomicAdd(&s_invalid, bad);
+    __syncthreads();
+    // Per bin: the run's warps scanned in token order, and the totals.
+    for (int b = tid; b < nb; b += NT) {
+        int run = 0;
+        for (int w = 0; w < NW; ++w) {
+            const int c = own[w * nb + b];
+            own[w * nb + b] = run;
+            run += c;
+        }
+        tot[b] = bef[b] + run + aft[b];
+    }
+    __syncthreads();
+    // Exclusive scans over bins: first sorted slot, rank among the non-empty
+    // bins (torch.unique(sorted=True) order).
+    if (warp == 0) {
+        int carry_t = 0, carry_p = 0;
+        for (int b0 = 0; b0 < nb; b0 += 32) {
+            const int b = b0 + lane;
+            const int v = (b < nb) ? tot[b] : 0;
+            const int f = v > 0 ? 1 : 0;
+            int iv = v, jf = f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, iv, o);
+                const int w = __shfl_up_sync(0xffffffffu, jf, o);
+                if (lane >= o) { iv += u; jf += w; }
+            }
+            if (b < nb) {
+                base[b] = carry_t + iv - v;
+                pos[b] = carry_p + jf - f;
+            }
+            carry_t += __shfl_sync(0xffffffffu, iv, 31);
+            carry_p += __shfl_sync(0xffffffffu, jf, 31);
+        }
+        if (lane == 0) s_nactive = carry_p;
+    }
+    __syncthreads();
+
+    const bool no_lora = (tot[0] == T);
+    const int nact = no_lora ? 0 : s_nactive;
+    if (cta == 0) {
+        for (int k = tid; k < nb; k += NT) {
+            if (k >= nact) {
+                a.active[k] = -1;
+                a.counts[k] = 0;
+                a.start_loc[k + 1] = 0;
+            }
+        }
+        if (tid == 0) {
+            a.start_loc[0] = 0;
+            *a.no_lora = no_lora ? 1 : 0;
+            *a.error_word = s_invalid;
+        }
+        if (!no_lora) {
+            for (int b = tid; b < nb; b += NT) {
+                const int c = tot[b];
+                if (c > 0) {
+                    const int k = pos[b];
+                    a.active[k] = b - 1;
+                    a.counts[k] = c;
+                    a.start_loc[k + 1] = base[b] + c;
+                }
+            }
+        }
+    }
+    if (no_lora) return;                        // early exit: nothing else written
+    // Pass 2: stable scatter of this warp's group of the run + mapping copy.
+    const int t = (g_run + warp) * 32 + lane;
+    const bool has = t < T;
+    int unused = 0;
+    const int32_t id = has ? a.map[t] : -1;
+    const int b = has ? token_bin(id, a.max_loras, unused) : -1;
+    int n = 0;
+    const int rank = rank_in_group(b, has, lane, n);
+    if (has) {
+        a.sorted[base[b] + bef[b] + own[warp * nb + b] + rank] = t;
+        a.mapping_copy[t] = id;
+    }
+}
+
+size_t meta_multi_smem_bytes(int max_loras)
+{
+    const size_t nb = size_t(max_loras) + 1;
+    return (size_t(META_MULTI_THREADS / 32) * nb + 5 * nb) * sizeof(int32_t);
 }
 
 int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
@@ -202,7 +384,19 @@ int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
                                  int(meta_smem_bytes(META_SMALL_THREADS / 32, LORA_MAX_LORAS,
                                                      META_SMALL_MAX)));
         if (e != cudaSuccess) return int(e);
+        e = cudaFuncSetAttribute(meta_multi_kernel<META_MULTI_THREADS>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(meta_multi_smem_bytes(LORA_MAX_LORAS)));
+        if (e != cudaSuccess) return int(e);
         configured[dev] = 1;
+    }
+    // Batches above META_MULTI_MIN tokens on one CTA per 1024 tokens
+    // (LORA_PUNICA_META_MULTI=0 turns it off).
+    if (a.num_tokens > META_MULTI_MIN && knobs().meta_multi) {
+        const int grid = (a.num_tokens + META_MULTI_CHUNK - 1) / META_MULTI_CHUNK;
+        return int(launch_kernel(meta_multi_kernel<META_MULTI_THREADS>, dim3(grid),
+                                 dim3(META_MULTI_THREADS), meta_multi_smem_bytes(a.max_loras),
+                                 stream, a));
     }
     // Small batches on 8 warps (fewer warps to pass each barrier), the rest
     // on 32.  LORA_PUNICA_META_SMALL=0 always takes 32 warps.

@@ -127,3 +127,27 @@ def test_meta_reuse_across_batches(oracle_mod):
         if not o.no_lora_flag[0]:
             np.testing.assert_array_equal(meta.token_indices_sorted_by_lora_ids[:T].cpu().numpy(),
                                           o.token_indices_sorted_by_lora_ids[:T])
+
+
+def _maps(T, L, seed):
+    """A per-token map with invalid ids, a run-ordered (sequence) map and
+    the all -1 map, each of T tokens over L LoRAs."""
+    rng = np.random.default_rng(seed)
+    per_token = rng.integers(-1, L, size=T).astype(np.int32)
+    per_token[rng.random(T) < 0.01] = L + 3                      # invalid
+    per_token[rng.random(T) < 0.01] = -7                         # invalid
+    runs = np.repeat(rng.integers(-1, L, size=T // 100 + 1), 100)[:T].astype(np.int32)
+    return [per_token, runs, np.full(T, -1, np.int32)]
+
+
+@pytest.mark.parametrize("multi", ["0", "1"])
+@pytest.mark.parametrize("T,L", [(2048, 8), (2049, 8), (4096, 64), (16384, 64), (20000, 1024),
+                                 (70001, 300)])
+def test_meta_single_and_multi_cta(oracle_mod, knob, multi, T, L):
+    """The single-CTA kernel and the multi-CTA kernel (one CTA per 512
+    tokens, each counting the whole map itself; batches above 2048 tokens)
+    give the oracle's metadata bit for bit, on per-token maps with invalid
+    ids, run-ordered maps and the all -1 map."""
+    knob(LORA_PUNICA_META_MULTI=multi)
+    for ids in _maps(T, L, seed=T + L):
+        _check(ids, L, oracle_mod)
