@@ -7,13 +7,18 @@
 // One CTA per SM, persistent over (tile, hidden chunk) items: the hidden
 // dimension is split when there are too few whole tiles to fill the GPU
 // (see umma_kchunks).  Warp-specialised:
-//   warp 0      producer: per 64-wide hidden block, the tile's 128 x rows
+//   warp 0      x producer: per 64-wide hidden block, the tile's 128 x rows
 //               arrive by 2-D TMA: the tile's tokens (increasing, as the
 //               sort is stable) are cut into runs of consecutive tokens and
 //               each run into power-of-two pieces, one TMA box per piece
-//               (a long prefill sequence makes the tile one 128-row box);
-//               one more 2-D TMA box per slice brings the r rows of
-//               A[s][id].  All complete on the stage's mbarrier.
+//               (a long prefill sequence makes the tile one 128-row box).
+//   warps 6..8  A producers: one 2-D TMA box per slice brings the r rows of
+//               A[s][id], slice s issued by warp 6 + s % 3.  Each producer
+//               arrives on the stage's mbarrier with the bytes it loads, so
+//               a stage completes when all of them have landed.  One thread
+//               issuing every box was measured to hold the kernel at its TMA
+//               issue rate (on this GPU about 1000 cycles of latency per box
+//               for each issuing thread); several issuers overlap them.
 //               (Per-row TMA tile::gather4 and an LSU cp.async gather were
 //               both measured slower: they stay near 30 GB/s per SM.)
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (M = 128 tokens,
@@ -37,8 +42,10 @@ namespace lora {
 
 constexpr int UM_BM = 128;            // tokens per tile = UMMA M
 constexpr int UM_BK = 64;             // hidden per stage (one 128-byte swizzle atom)
-constexpr int UM_MMA_WARP = 1;        // warp 0: TMA producer; warp 1: TMEM owner, UMMA issue
-constexpr int UM_THREADS = 192;       // + warps 2..5: epilogue
+constexpr int UM_MMA_WARP = 1;        // warp 0: x producer; warp 1: TMEM owner, UMMA issue
+constexpr int UM_APROD0 = 6;          // warps 2..5: epilogue; warps 6..8: A producers
+constexpr int UM_APRODS = 3;
+constexpr int UM_THREADS = 32 * (UM_APROD0 + UM_APRODS);
 constexpr int UM_XMAPS = 8;           // x box heights 1, 2, 4, ..., 128
 constexpr int UM_MAX_STAGES = 8;
 constexpr int UM_SMEM_BUDGET = 200 * 1024;
@@ -133,7 +140,9 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
 
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(bar_full + 8 * i, 1);       // the producer's expect_tx arrival
+            // one expect_tx arrival from the x producer and one from each A
+            // producer that has a slice
+            mbar_init(bar_full + 8 * i, 1 + min(S, UM_APRODS));
             mbar_init(bar_empty + 8 * i, 1);
         }
         mbar_init(bar_acc_full, 1);
@@ -189,7 +198,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
             // the last, partial tile of a segment); only they are loaded, and
             // the stage's barrier expects exactly their bytes
             const int nrows = min(UM_BM, tab.start[seg] + tab.count[seg] - row0);
-            const uint32_t tx = uint32_t(nrows * 128 + S * L.a_bytes);
+            const uint32_t tx = uint32_t(nrows * 128);
             int npieces = 0;
             if (lane == 0) {
                 const int32_t *tk = p.sorted + row0;
@@ -221,11 +230,6 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
                     const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
                     tma_load_2d(sx + r * 128, &p.map_x[lg], kb * UM_BK, t0, full);
                 }
-                if (lane == 0) {
-                    for (int s = 0; s < S; ++s)
-                        tma_load_2d(sx + L.x_bytes + s * L.a_bytes, &p.map_a[s], kb * UM_BK,
-                                    id * R, full);
-                }
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
@@ -240,6 +244,48 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
                 }
             }
         }
+    } else if (warp >= UM_APROD0) {
+        // ------------------------------------------------------ A producers
+        // Producer j loads the A blocks of slices j, j + 3, ... into every
+        // stage, in the same stage order as the x producer.
+        const int j = warp - UM_APROD0;
+        if (j < S && lane == 0) {
+            int nsl = 0;
+            for (int s = j; s < S; s += UM_APRODS) ++nsl;
+            const uint32_t tx = uint32_t(nsl * L.a_bytes);
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x) {
+                const int tile = item % total_tiles, kc = item / total_tiles;
+                const int kb0 = kc * spc, kb1 = min(nk, kb0 + spc);
+                const int id = tab.id[find_segment(tab.tile, p.nbins, tile)];
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, s_abort, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sx = base + stage * L.stage_bytes;
+                    const uint32_t full = bar_full + 8 * stage;
+                    mbar_arrive_expect_tx(full, tx);
+                    for (int s = j; s < S; s += UM_APRODS)
+                        tma_load_2d(sx + L.x_bytes + s * L.a_bytes, &p.map_a[s], kb * UM_BK,
+                                    id * R, full);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            // Every issued fill must land before the CTA may exit.
+            const long long drain_deadline = clock64() + UM_TIMEOUT_CYCLES;
+            for (int i = max(0, issued - STAGES); i < issued; ++i) {
+                const uint32_t ph = uint32_t(i / STAGES) & 1u;
+                while (!mbar_try_wait(bar_full + 8 * (i % STAGES), ph) &&
+                       clock64() < drain_deadline) {
+                }
+            }
+        }
+        __syncwarp();
     } else if (warp == UM_MMA_WARP) {
         // ------------------------------------------------------ MMA issue
         if (lane == 0) {
