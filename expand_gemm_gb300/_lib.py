@@ -54,12 +54,14 @@ _I64 = ctypes.c_int64
 
 
 def load(path: str | None = None):
-    """Load (once) and return the CUDA library; raise if it is not built."""
+    """Load (once) and return the CUDA library; raise if it is not built.
+    ``LORA_PUNICA_LIBRARY`` in the environment names another build of it
+    (the debug-checks build) to load instead."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        p = path or LIB_PATH
+        p = path or os.environ.get("LORA_PUNICA_LIBRARY") or LIB_PATH
         if not os.path.exists(p):
             raise RuntimeError(
                 "liblora_punica.so is not built (expected at %s); run "

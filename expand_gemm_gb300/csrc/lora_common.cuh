@@ -107,6 +107,39 @@ __device__ __forceinline__ void pdl_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
+// ------------------------------------------------------- debug checks
+//
+// A build with LORA_PUNICA_DEBUG_CHECKS defined checks every LoRA id, token
+// index and segment bound a kernel takes from the metadata before it
+// indexes x, y, A, B or the buffer with it.  A value out of range sets bit
+// 29 of the metadata error word and the access is skipped (the token or
+// segment is treated as having no LoRA); nothing traps.  The normal build
+// compiles the checks away.
+#ifdef LORA_PUNICA_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+constexpr int LORA_DEBUG_BIT = 1 << 29;
+
+__device__ __forceinline__ void debug_flag(int32_t *err)
+{
+    if (err != nullptr) atomicOr(err, LORA_DEBUG_BIT);
+}
+
+// A token index read from the sorted list: itself, or -1 (no LoRA) when a
+// debug build finds it outside [0, T).
+__device__ __forceinline__ int checked_token(int tok, int T, int32_t *err)
+{
+    if constexpr (kDebugChecks) {
+        if (tok >= T || tok < -1) {
+            debug_flag(err);
+            return -1;
+        }
+    }
+    return tok;
+}
+
 // ----------------------------------------------------------- schedule
 //
 // Segment table held in shared memory (4 * nbins + 2 ints):
@@ -141,16 +174,28 @@ __host__ __device__ constexpr size_t seg_tab_bytes(int nbins)
 //   skip_rows:       when nonzero, the first (count / skip_rows) * skip_rows
 //                    tokens of every segment are left out (another kernel
 //                    covers them) and only the rest is tiled.
+//   num_tokens, err: a debug build drops (and reports in err) segments
+//                    whose id is outside [-1, nbins - 1) or whose tokens
+//                    leave [0, num_tokens).
 __device__ __forceinline__ int load_segments(const int32_t *no_lora, const int32_t *active,
                                              const int32_t *counts, const int32_t *start_loc,
                                              int nbins, int tile_rows, SegTab t,
-                                             bool full_tiles_only = false, int skip_rows = 0)
+                                             bool full_tiles_only = false, int skip_rows = 0,
+                                             int num_tokens = 0, int32_t *err = nullptr)
 {
     int *s_flag = t.count + nbins;
     for (int k = threadIdx.x; k < nbins; k += blockDim.x) {
-        const int id = active[k];
+        int id = active[k];
         int c = counts[k];
         int st = start_loc[k];
+        if constexpr (kDebugChecks) {
+            if (id < -1 || id >= nbins - 1 ||
+                (id >= 0 && c > 0 && (st < 0 || c > num_tokens || st > num_tokens - c))) {
+                debug_flag(err);
+                id = -1;
+                c = 0;
+            }
+        }
         if (skip_rows > 0) {
             const int skip = (c / skip_rows) * skip_rows;
             st += skip;

@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
             pre[j] = (i < p.num_tokens) ? p.sorted[i] : 0;
         }
         total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc, p.nbins, EX_BM,
-                                    tab);
+                                    tab, false, 0, p.num_tokens, p.error_word);
         int *s_list = reinterpret_cast<int *>(sA + Cfg::A_BYTES + seg_tab_bytes(p.nbins));
 #pragma unroll
         for (int j = 0; j < EX_TOKLIST_MAX / EX_THREADS; ++j) {
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
         tokens = s_list;
     } else {
         total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc, p.nbins, EX_BM,
-                                    tab);
+                                    tab, false, 0, p.num_tokens, p.error_word);
     }
     if (total_tiles == 0) {
         wait_once();
@@ -219,6 +219,7 @@ int lora::expand_setup(ExpandArgs &p, const void *x, int x_bf16,
     p.start_loc = meta->lora_token_start_loc;
     p.active = meta->active_lora_ids;
     p.no_lora = meta->no_lora_flag;
+    p.error_word = meta->error_word;
     p.nbins = meta->max_loras + 1;
     p.early = 0;
     return LORA_OK;

@@ -34,6 +34,7 @@ struct ExpandArgs {
     const int32_t *start_loc;
     const int32_t *active;
     const int32_t *no_lora;
+    int32_t *error_word;                 // debug checks report here
     int32_t nbins;
     // Early mode (set only by lora_linear, whose preceding kernel is its own
     // shrink): the segment table, the token list and the y / B / bias loads
@@ -189,7 +190,8 @@ __device__ __forceinline__ void expand_items(const ExpandArgs &p, SegTab tab,
         const uint16_t *bias_row = p.bias[s] ? p.bias[s] + int64_t(id) * n_s : nullptr;
         uint16_t *yslice = p.y + p.col0[s];
 
-        if (tid < EX_BM) s_tok[tid] = (tid < nrows) ? tokens[row0 + tid] : -1;
+        if (tid < EX_BM)
+            s_tok[tid] = (tid < nrows) ? checked_token(tokens[row0 + tid], T, p.error_word) : -1;
         __syncthreads();
 
         // This thread's y rows for the whole tile (piece ycc of rows

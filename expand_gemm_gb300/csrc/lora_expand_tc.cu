@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
     }
     const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + C::TAB_OFF), p.nbins);
     const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc, p.nbins,
-                                          TC_BM, tab);
+                                          TC_BM, tab, false, 0, p.num_tokens, p.error_word);
     const int S = p.num_slices;
     const int nchunks = p.chunk0[S];
     const int64_t total = int64_t(total_tiles) * nchunks;
@@ -300,7 +300,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
 #pragma unroll
                 for (int i = 0; i < 32 / RPI; ++i) {
                     const int r = q * 32 + i * RPI + lane / TC_WPC;
-                    ltok[i] = (r < nrows) ? p.sorted[row0 + r] : -1;
+                    ltok[i] = (r < nrows) ? checked_token(p.sorted[row0 + r], T, p.error_word)
+                                          : -1;
                 }
             }
             const uint32_t st = base + C::RING_OFF + slot * C::SLOT_BYTES;
@@ -342,7 +343,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                 c_id = tab.id[seg];
                 const int row0 = tab.start[seg] + (ct - tab.tile[seg]) * TC_BM;
                 const int nrows = min(TC_BM, tab.start[seg] + tab.count[seg] - row0);
-                ctok = (my_row < nrows) ? p.sorted[row0 + my_row] : -1;
+                ctok = (my_row < nrows) ? checked_token(p.sorted[row0 + my_row], T, p.error_word)
+                                        : -1;
             }
         };
         // this warp's rows of x (slice s), rounded to bf16, into the A operand

@@ -41,6 +41,7 @@ struct ShrinkArgs {
     const int32_t *active;
     const int32_t *no_lora;
     int32_t nbins;                 // max_loras + 1
+    int32_t *error_word;           // debug checks report here
     int32_t skip_rows;             // rows per segment left to the tensor-core path
     // Self-built metadata (small batches, lora_linear): every CTA sorts the
     // raw id map in shared memory; CTA 0 also writes the metadata buffers.
@@ -137,7 +138,8 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
         tokens = srt;
     } else {
         total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
-                                    p.nbins, SH_BN, tab, false, p.skip_rows);
+                                    p.nbins, SH_BN, tab, false, p.skip_rows, p.num_tokens,
+                                    p.error_word);
     }
     if (total_tiles == 0) {
         wait_once();
@@ -173,7 +175,8 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
         const int id = tab.id[seg];
         const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * SH_BN;
         const int nrows = min(SH_BN, tab.start[seg] + tab.count[seg] - row0);
-        if (tid < SH_BN) s_tok[tid] = (tid < nrows) ? tokens[row0 + tid] : -1;
+        if (tid < SH_BN)
+            s_tok[tid] = (tid < nrows) ? checked_token(tokens[row0 + tid], T, p.error_word) : -1;
         __syncthreads();
 
         const int k_first = kc * steps_per_chunk;
@@ -372,6 +375,7 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
     p.active = meta->active_lora_ids;
     p.no_lora = meta->no_lora_flag;
     p.nbins = meta->max_loras + 1;
+    p.error_word = meta->error_word;
     p.skip_rows = 0;
     p.map = nullptr;
     p.write_meta = 0;
@@ -466,6 +470,7 @@ int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_token
     p.active = nullptr;
     p.no_lora = nullptr;
     p.nbins = meta->max_loras + 1;
+    p.error_word = meta->error_word;
     p.skip_rows = 0;
     p.map = map;
     p.mapping_copy = meta->token_lora_mapping;

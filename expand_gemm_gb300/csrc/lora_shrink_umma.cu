@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     // Every tile of every segment (partial), or the whole 128-token tiles
     // only (a segment of c tokens then contributes c / 128).
     const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc,
-                                          p.nbins, UM_BM, tab, /*full_tiles_only=*/!p.partial);
+                                          p.nbins, UM_BM, tab, /*full_tiles_only=*/!p.partial, 0,
+                                          p.num_tokens, p.error_word);
     if (total_tiles == 0) return;
     const int H = p.hidden, R = p.rank, T = p.num_tokens;
     const int nk = (H + UM_BK - 1) / UM_BK;
@@ -345,7 +346,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
             // rows past the segment's end hold stale shared data: their
             // accumulators are read (the load is warp-wide) but not stored
             const int nrows = min(UM_BM, tab.start[seg] + tab.count[seg] - row0);
-            const int tok = row < nrows ? p.sorted[row0 + row] : -1;
+            const int tok =
+                row < nrows ? checked_token(p.sorted[row0 + row], T, p.error_word) : -1;
             bool got = mbar_wait_bounded(bar_acc_full, acc_phase, s_abort, deadline);
             if (__all_sync(0xffffffffu, got) == 0) break;       // warp-uniform exit
             tc_fence_after();
