@@ -8,34 +8,36 @@
 // slice), numbered chunk-fastest; one persistent CTA per SM takes a
 // contiguous, balanced range of them, so it walks the chunks of one tile
 // with the tile's x rows (the MMA's A operand) resident in shared memory.
+// Chunks stream through a ring of DEPTH slots, each holding the chunk's B
+// tile (swizzled K-major, as UMMA reads it) and its old y rows.
 //
-// Seventeen warps:
+// Thirteen warps, one job each:
 //   warp 0       owns TMEM (two 64-column fp32 accumulators); lane 0 issues
 //                tcgen05.mma (M = 128 tokens, N = 64 columns, K = 16 steps
-//                over the rank) and commits each chunk's accumulator.
-//   warps 1..16  workers.  Worker (q, h) = (warp % 4, (warp - 1) / 4) owns
-//                the tile rows of TMEM lane quarter q and the h-th 16 columns
-//                of every chunk.  It streams, DEPTH - 1 chunks ahead, its 32
-//                rows x 16 columns of old y and one sixteenth of the chunk's
-//                B tile with coalesced 16-byte cp.async into a ring of DEPTH
-//                slots (B in the swizzled K-major layout UMMA reads), and
-//                hands each chunk's B to the MMA two chunks ahead (through an
-//                mbarrier, after a proxy fence), so the MMA of chunk g + 1
-//                runs while the workers finish chunk g.  Per chunk it reads
-//                its accumulators with tcgen05.ld (one token row per thread),
-//                adds bias and old y in fp32, rounds once to bf16 into the
-//                slot and writes its rows back with coalesced 16-byte stores
-//                (16 rows x 32 bytes per instruction).  When the next chunk
-//                opens a new tile or slice, the workers round its x rows to
+//                over the rank) and commits each chunk's accumulator and
+//                the release of its slot's B.
+//   warps 1..4   loaders.  They fill slots with coalesced 16-byte cp.async
+//                (four whole 128-byte lines per instruction): the chunk's
+//                128 old y rows and its B tile.  Up to DEPTH - 1 chunks are
+//                in flight; as each one lands, the loaders fence it for the
+//                tensor core and signal the slot's mbarrier.
+//   warps 5..12  epilogue.  Warp (q, h) = (warp % 4, (warp - 5) / 4) owns
+//                the tile rows of TMEM lane quarter q and column half h.
+//                Per chunk it reads its accumulators with tcgen05.ld (one
+//                token row per thread), adds bias and old y in fp32, rounds
+//                once to bf16 into the slot and writes its rows back with
+//                coalesced 16-byte stores (8 rows x 64 bytes per
+//                instruction), then releases the slot.  When the next chunk
+//                opens a new tile or slice, it rounds that item's x rows to
 //                bf16 into the A operand right after reading the current
-//                accumulator.  Four workers per lane quarter keep four warps
-//                on every scheduler to hide the latency of each one's chain.
+//                accumulator.
+// Splitting loading from the epilogue keeps each warp on one latency chain:
+// a version in which every warp did both ran at half the rate.
 //
 // The ring is fed by the load/store units, not TMA: measured on this GPU,
 // a TMA box costs about 1000 cycles of latency per issuing thread and the
 // engine tops out near 50 bytes per clock per SM, and the old y rows of a
-// tile cut into several boxes wherever its token runs break; a TMA-fed
-// version of this kernel ran at a quarter of the HBM rate.
+// tile cut into several boxes wherever its token runs break.
 //
 // Every mbarrier wait is bounded (about one second); on expiry the kernel
 // sets bit 30 of the metadata error word, drains its copies and MMAs, frees
@@ -47,11 +49,11 @@ namespace lora {
 
 constexpr int TC_BM = 128;                    // tokens per tile (UMMA M, TMEM lanes)
 constexpr int TC_BN = 64;                     // columns per chunk (UMMA N)
-constexpr int TC_WORKERS = 16;                // four per TMEM lane quarter
-constexpr int TC_WG = TC_WORKERS / 4;          // workers sharing a lane quarter
-constexpr int TC_WCOLS = TC_BN / TC_WG;        // chunk columns per worker (16)
-constexpr int TC_WPC = TC_WCOLS / 8;           // 16-byte pieces per row and worker (2)
-constexpr int TC_THREADS = 32 * (1 + TC_WORKERS);
+constexpr int TC_LOADERS = 4;
+constexpr int TC_EPI = 8;
+constexpr int TC_EPI0 = 1 + TC_LOADERS;       // first epilogue warp
+constexpr int TC_THREADS = 32 * (TC_EPI0 + TC_EPI);
+constexpr int TC_LT = 32 * TC_LOADERS;        // loader threads
 constexpr long long TC_TIMEOUT_CYCLES = 2000000000ll;
 constexpr int TC_ERROR_BIT = 1 << 30;
 
@@ -91,10 +93,11 @@ struct TcCfg {
     static constexpr int DEPTH = (KT >= 8) ? 5 : 8;
     static constexpr int RING_OFF = A_BYTES;
     static constexpr int BAR_OFF = RING_OFF + DEPTH * SLOT_BYTES;
-    static constexpr int MISC_OFF = BAR_OFF + (DEPTH + 6) * 8;
+    static constexpr int MISC_OFF = BAR_OFF + (2 * DEPTH + 6) * 8;
     static constexpr int TAB_OFF = MISC_OFF + 16;
+    static constexpr int Y_PER_T = TC_BM * 8 / TC_LT;      // y pieces per loader thread (8)
+    static constexpr int B_PER_T = (TC_BN * CPR + TC_LT - 1) / TC_LT;
     static_assert(SLOT_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1024-byte aligned operands");
-    static_assert(DEPTH >= 4, "loads three chunks ahead of the MMA hand-off");
 };
 
 template <int KT>
@@ -177,10 +180,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t base = smem_addr(smem);
-    const uint32_t bar_bfull = base + C::BAR_OFF;          // [DEPTH]: 8 worker arrivals
-    const uint32_t bar_accf = bar_bfull + 8 * DEPTH;       // [2]: MMA commit
-    const uint32_t bar_acce = bar_accf + 16;               // [2]: 8 worker arrivals
-    const uint32_t bar_x = bar_acce + 16;                  // A operand ready: 8 arrivals
+    const uint32_t bar_full = base + C::BAR_OFF;           // [DEPTH]: 4 loader warps
+    const uint32_t bar_empty = bar_full + 8 * DEPTH;       // [DEPTH]: MMA + 8 epilogue warps
+    const uint32_t bar_accf = bar_empty + 8 * DEPTH;       // [2]: MMA commit
+    const uint32_t bar_acce = bar_accf + 16;               // [2]: 8 epilogue warps
+    const uint32_t bar_x = bar_acce + 16;                  // A operand ready: 8 epilogue warps
     const uint32_t bar_drain = bar_x + 8;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
@@ -201,12 +205,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
     if (!p.early) wait_once();
 
     if (tid == 0) {
-        for (int i = 0; i < DEPTH; ++i) mbar_init(bar_bfull + 8 * i, TC_WORKERS);
+        for (int i = 0; i < DEPTH; ++i) {
+            mbar_init(bar_full + 8 * i, TC_LOADERS);
+            mbar_init(bar_empty + 8 * i, 1 + TC_EPI);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_accf + 8 * i, 1);
-            mbar_init(bar_acce + 8 * i, TC_WORKERS);
+            mbar_init(bar_acce + 8 * i, TC_EPI);
         }
-        mbar_init(bar_x, TC_WORKERS);
+        mbar_init(bar_x, TC_EPI);
         mbar_init(bar_drain, 1);
         mbar_fence_init();
         *s_abort = 0;
@@ -250,7 +257,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                     ++items;
                 }
                 const int slot = g % DEPTH, ab = g & 1;
-                if (!mbar_wait_bounded(bar_bfull + 8 * slot, uint32_t(g / DEPTH) & 1u, s_abort,
+                if (!mbar_wait_bounded(bar_full + 8 * slot, uint32_t(g / DEPTH) & 1u, s_abort,
                                        deadline) ||
                     !mbar_wait_bounded(bar_acce + 8 * ab, (uint32_t(g >> 1) & 1u) ^ 1u, s_abort,
                                        deadline)) {
@@ -263,6 +270,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                 for (int kk = 0; kk < KT; ++kk)
                     umma_bf16(tmem + ab * TC_BN, tc_kmajor_desc(RP, TC_BM, a_tile, kk),
                               tc_kmajor_desc(RP, TC_BN, bt, kk), idesc, kk != 0);
+                umma_commit(bar_empty + 8 * slot);           // B read
                 umma_commit(bar_accf + 8 * ab);
             }
             // After an abort, wait (bounded) for every MMA issued so far
@@ -275,66 +283,83 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
             }
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------ workers
-        const int wi = warp - 1, q = warp & 3, h = wi >> 2;   // h: column share of the chunk
-        const int my_row = q * 32 + lane;                  // epilogue row (TMEM lane)
-        constexpr int RPI = 32 / TC_WPC;                   // rows per copy instruction (16)
+    } else if (warp < TC_EPI0) {
+        // ------------------------------------------------------ loaders
+        const int lt = tid - 32;                           // 0 .. TC_LT - 1
         const uint16_t *const ydummy = p.y;
-
-        // load cursor: DEPTH - 1 chunks ahead of the consume cursor
-        int64_t wl = w_begin;
-        TcCursor kl;
-        kl.start(p, w_begin, nchunks);
-        int lt = -1, l_id = 0;
-        int ltok[TC_WPC];                                  // rows q*32 + i*RPI + lane/TC_WPC
-        auto issue = [&](int slot) {
-            const TcCursor &k = kl;
-            const int kc0 = k.c0(p), kncols = min(TC_BN, p.n[k.s] - kc0);
-            if (k.tile != lt) {
-                lt = k.tile;
-                const int seg = find_segment(tab.tile, p.nbins, lt);
+        int cur_tile = -1, l_id = 0;
+        int ltok[C::Y_PER_T];                              // rows i * 16 + lt / 8
+        int issued = 0, signalled = 0;
+        bool ok = true;
+        // Hands the oldest chunk in flight to the MMA and the epilogue.
+        auto signal_oldest = [&]() {
+            fence_proxy_async_smem();                      // B is read by the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_full + 8 * (signalled % DEPTH));
+            ++signalled;
+        };
+        TcCursor k;
+        k.start(p, w_begin, nchunks);
+        for (int64_t w = w_begin; w < w_end; ++w, k.next(p, nchunks)) {
+            const int g = issued, slot = g % DEPTH;
+            const bool got = mbar_wait_bounded(bar_empty + 8 * slot,
+                                               (uint32_t(g / DEPTH) & 1u) ^ 1u, s_abort, deadline);
+            if (__all_sync(0xffffffffu, got) == 0) {
+                ok = false;
+                break;
+            }
+            if (k.tile != cur_tile) {
+                cur_tile = k.tile;
+                const int seg = find_segment(tab.tile, p.nbins, cur_tile);
                 l_id = tab.id[seg];
-                const int row0 = tab.start[seg] + (lt - tab.tile[seg]) * TC_BM;
+                const int row0 = tab.start[seg] + (cur_tile - tab.tile[seg]) * TC_BM;
                 const int nrows = min(TC_BM, tab.start[seg] + tab.count[seg] - row0);
 #pragma unroll
-                for (int i = 0; i < 32 / RPI; ++i) {
-                    const int r = q * 32 + i * RPI + lane / TC_WPC;
+                for (int i = 0; i < C::Y_PER_T; ++i) {
+                    const int r = i * (TC_LT / 8) + lt / 8;
                     ltok[i] = (r < nrows) ? checked_token(p.sorted[row0 + r], T, p.error_word)
                                           : -1;
                 }
             }
+            const int c0 = k.c0(p), ncols = min(TC_BN, p.n[k.s] - c0);
             const uint32_t st = base + C::RING_OFF + slot * C::SLOT_BYTES;
             if (p.add_inputs) {
-                const int piece = TC_WPC * h + lane % TC_WPC;
-                const bool cin = piece * 8 < kncols;
-                const uint16_t *ycol = p.y + p.col0[k.s] + kc0 + piece * 8;
+                const int piece = lt % 8;
+                const bool cin = piece * 8 < ncols;
+                const uint16_t *ycol = p.y + p.col0[k.s] + c0 + piece * 8;
 #pragma unroll
-                for (int i = 0; i < 32 / RPI; ++i) {
-                    const int r = q * 32 + i * RPI + lane / TC_WPC;
-                    const bool ok = cin && ltok[i] >= 0;
+                for (int i = 0; i < C::Y_PER_T; ++i) {
+                    const int r = i * (TC_LT / 8) + lt / 8;
+                    const bool ld = cin && ltok[i] >= 0;
                     cp_async16(st + C::B_BYTES + r * 128 + ((piece ^ (r & 7)) << 4),
-                               ok ? ycol + int64_t(ltok[i]) * p.y_ld : ydummy, ok);
+                               ld ? ycol + int64_t(ltok[i]) * p.y_ld : ydummy, ld);
                 }
             }
-            // this warp's share of B: rows wi * BRW .. wi * BRW + BRW - 1 of the chunk
             const int n_s = p.n[k.s];
-            const uint16_t *brows = p.b[k.s] + (int64_t(l_id) * n_s + kc0) * R;
-            constexpr int BRW = TC_BN / TC_WORKERS;          // 4 rows
+            const uint16_t *brows = p.b[k.s] + (int64_t(l_id) * n_s + c0) * R;
 #pragma unroll
-            for (int j0 = 0; j0 < BRW * CPR; j0 += 32) {
-                const int j = j0 + lane;
-                if (BRW * CPR % 32 != 0 && j >= BRW * CPR) break;
-                const int r = wi * BRW + j / CPR, c = j % CPR;
-                const bool ok = r < kncols && c * 8 < R;
+            for (int i = 0; i < C::B_PER_T; ++i) {
+                const int j = i * TC_LT + lt;
+                if (TC_BN * CPR % TC_LT != 0 && j >= TC_BN * CPR) break;
+                const int r = j / CPR, c = j % CPR;
+                const bool ld = r < ncols && c * 8 < R;
                 cp_async16(st + tc_kmajor_off(RP, TC_BN, r, c),
-                           ok ? brows + int64_t(r) * R + c * 8 : p.b[k.s], ok);
+                           ld ? brows + int64_t(r) * R + c * 8 : p.b[k.s], ld);
             }
-            ++wl;
-            kl.next(p, nchunks);
-        };
-
-        // consume cursor
+            cp_async_commit();
+            ++issued;
+            if (issued - signalled == DEPTH - 1) {         // the oldest must land now
+                cp_async_wait<DEPTH - 2>();
+                signal_oldest();
+            }
+        }
+        cp_async_wait<0>();
+        if (ok)
+            while (signalled < issued) signal_oldest();
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int ew = warp - TC_EPI0, q = warp & 3, h = ew >> 2;
+        const int my_row = q * 32 + lane;                  // TMEM lane
         int ct = -1, c_id = 0, ctok = -1;
         auto tile_rows = [&](int tile) {
             if (tile != ct) {
@@ -352,7 +377,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
             wait_once();                                   // x is the shrink output
             const int64_t xrow = (int64_t(s) * T + (ctok >= 0 ? ctok : 0)) * R;
 #pragma unroll
-            for (int c = h; c < CPR; c += TC_WG) {
+            for (int c = h * (CPR / 2); c < (h + 1) * (CPR / 2); ++c) {
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
                 if (ctok >= 0 && c * 8 < R) {
                     if (p.x_bf16) {
@@ -375,24 +400,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
             if (lane == 0) mbar_arrive(bar_x);
         };
 
-        // prologue: chunks 0 .. DEPTH - 2 in flight; chunks 0 and 1 handed
-        // to the MMA; the first item's A operand
-#pragma unroll 1
-        for (int i = 0; i < DEPTH - 1; ++i) {
-            if (wl < w_end) issue(i);
-            cp_async_commit();
-        }
-        cp_async_wait<DEPTH - 2>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_bfull);
-        if (w_begin + 1 < w_end) {
-            cp_async_wait<DEPTH - 3>();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_bfull + 8);
-        }
-        TcCursor k;                                        // consume cursor
+        TcCursor k;
         k.start(p, w_begin, nchunks);
         tile_rows(k.tile);
         convert_x(k.s);
@@ -400,57 +408,47 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
         int g = 0;
 #pragma unroll 1
         for (int64_t w = w_begin; w < w_end; ++w, ++g) {
-            // 1. the loads of chunk g + DEPTH - 1 (its slot held chunk g - 1,
-            //    whose accumulator this warp has already read: the MMA is
-            //    done with its B, and this warp with its y)
-            if (wl < w_end) issue((g + DEPTH - 1) % DEPTH);
-            cp_async_commit();
-            // 2. chunk g + 2 landed: hand its B to the MMA
-            if (w + 2 < w_end) {
-                cp_async_wait<DEPTH - 3>();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_bfull + 8 * ((g + 2) % DEPTH));
-            }
             tile_rows(k.tile);
             const int kc0 = k.c0(p), kncols = min(TC_BN, p.n[k.s] - kc0), ks = k.s;
             // bias of this warp's 32 columns, fetched before the waits
-            uint4 bpre[TC_WPC];
+            uint4 bpre[4];
             const uint16_t *bias_row = p.bias[ks] ? p.bias[ks] + int64_t(c_id) * p.n[ks] + kc0
                                                   : nullptr;
 #pragma unroll
-            for (int j = 0; j < TC_WPC; ++j) {
-                const int piece = TC_WPC * h + j;
+            for (int j = 0; j < 4; ++j) {
+                const int piece = 4 * h + j;
                 bpre[j] = make_uint4(0u, 0u, 0u, 0u);
                 if (bias_row != nullptr && p.bias_vec && piece * 8 < kncols)
                     bpre[j] = __ldg(reinterpret_cast<const uint4 *>(bias_row + piece * 8));
             }
-            // 3. the accumulator of chunk g
             const int ab = g & 1, slot = g % DEPTH;
-            const bool got = mbar_wait_bounded(bar_accf + 8 * ab, uint32_t(g >> 1) & 1u, s_abort,
-                                               deadline);
+            bool got = mbar_wait_bounded(bar_accf + 8 * ab, uint32_t(g >> 1) & 1u, s_abort,
+                                         deadline);
+            got = got && mbar_wait_bounded(bar_full + 8 * slot, uint32_t(g / DEPTH) & 1u, s_abort,
+                                           deadline);
             if (__all_sync(0xffffffffu, got) == 0) break;
             tc_fence_after();
-            float va[TC_WCOLS];
-            tmem_ld16(tmem + (uint32_t(q * 32) << 16) + uint32_t(ab * TC_BN + h * TC_WCOLS), va);
+            uint32_t va[32];
+            tmem_ld32_nowait(tmem + (uint32_t(q * 32) << 16) + uint32_t(ab * TC_BN + h * 32), va);
+            tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
             const int tok_g = ctok;
-            // 4. the next chunk opens a new tile or slice: its A operand now
-            //    (the MMA of chunk g is done; that of chunk g + 1 waits for it)
+            // the next chunk opens a new tile or slice: its A operand now (the
+            // MMA of chunk g is done; that of chunk g + 1 waits for it)
             k.next(p, nchunks);
             if (w + 1 < w_end && k.first) {
                 tile_rows(k.tile);
                 convert_x(k.s);
             }
-            // 5. + bias + old y, rounded once, back into the slot (own row)
+            // + bias + old y, rounded once, back into the slot (own row)
             uint8_t *yt = smem + C::RING_OFF + slot * C::SLOT_BYTES + C::B_BYTES;
             if (tok_g >= 0) {
-                uint4 yv[TC_WPC];
+                uint4 yv[4];
 #pragma unroll
-                for (int j = 0; j < TC_WPC; ++j) {
-                    const int piece = TC_WPC * h + j;
+                for (int j = 0; j < 4; ++j) {
+                    const int piece = 4 * h + j;
                     yv[j] = make_uint4(0u, 0u, 0u, 0u);
                     if (p.add_inputs)
                         yv[j] = *reinterpret_cast<const uint4 *>(
@@ -458,8 +456,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                 }
                 if (bias_row != nullptr && !p.bias_vec) {
 #pragma unroll
-                    for (int j = 0; j < TC_WPC; ++j) {
-                        const int piece = TC_WPC * h + j;
+                    for (int j = 0; j < 4; ++j) {
+                        const int piece = 4 * h + j;
                         if (piece * 8 < kncols) {
                             const uint16_t *bq = bias_row + piece * 8;
                             bpre[j].x = uint32_t(bq[0]) | (uint32_t(bq[1]) << 16);
@@ -470,15 +468,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                     }
                 }
 #pragma unroll
-                for (int j = 0; j < TC_WPC; ++j) {
-                    const int piece = TC_WPC * h + j;
+                for (int j = 0; j < 4; ++j) {
+                    const int piece = 4 * h + j;
                     const uint32_t yw[4] = {yv[j].x, yv[j].y, yv[j].z, yv[j].w};
                     const uint32_t bw[4] = {bpre[j].x, bpre[j].y, bpre[j].z, bpre[j].w};
                     uint32_t o[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float a0 = va[j * 8 + 2 * e] + bf16_lo(bw[e]) + bf16_lo(yw[e]);
-                        const float a1 = va[j * 8 + 2 * e + 1] + bf16_hi(bw[e]) + bf16_hi(yw[e]);
+                        const float a0 = __uint_as_float(va[j * 8 + 2 * e]) + bf16_lo(bw[e]) +
+                                         bf16_lo(yw[e]);
+                        const float a1 = __uint_as_float(va[j * 8 + 2 * e + 1]) + bf16_hi(bw[e]) +
+                                         bf16_hi(yw[e]);
                         o[e] = pack_bf16x2(a0, a1);
                     }
                     // columns past the slice are never stored
@@ -487,28 +487,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                 }
             }
             __syncwarp();
-            // 6. this warp's rows out: 16 rows x 32 bytes per store instruction
+            // this warp's rows out: 8 rows x 64 bytes per store instruction
             {
-                const int piece = TC_WPC * h + lane % TC_WPC;
+                const int piece = 4 * h + (lane & 3);
                 const bool cin = piece * 8 < kncols;
                 uint16_t *ycol = p.y + p.col0[ks] + kc0 + piece * 8;
-                int tok[32 / RPI];
-                uint4 v[32 / RPI];
+                int tok[4];
+                uint4 v[4];
 #pragma unroll
-                for (int i = 0; i < 32 / RPI; ++i) {
-                    const int rl = i * RPI + lane / TC_WPC;
+                for (int i = 0; i < 4; ++i) {
+                    const int rl = i * 8 + (lane >> 2);
                     const int r = q * 32 + rl;
                     tok[i] = __shfl_sync(0xffffffffu, tok_g, rl);
                     v[i] = *reinterpret_cast<const uint4 *>(yt + r * 128 + ((piece ^ (r & 7)) << 4));
                 }
 #pragma unroll
-                for (int i = 0; i < 32 / RPI; ++i)
+                for (int i = 0; i < 4; ++i)
                     if (cin && tok[i] >= 0)
                         *reinterpret_cast<uint4 *>(ycol + int64_t(tok[i]) * p.y_ld) = v[i];
             }
             __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);   // this warp is done with the slot
         }
-        cp_async_wait<0>();                                // no copy lands after exit
     }
 
     wait_once();
