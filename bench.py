@@ -59,7 +59,8 @@ NCU_TRAFFIC = {
 
 # The source files each reported kernel is built from.
 KERNEL_SOURCES = {
-    "expand": ("lora_expand.cu", "lora_expand.cuh", "lora_common.cuh"),
+    "expand": ("lora_expand.cu", "lora_expand.cuh", "lora_expand_tc.cu", "lora_umma.cuh",
+               "lora_common.cuh"),
     "shrink": ("lora_shrink.cu", "lora_shrink_umma.cu", "lora_umma.cuh", "lora_common.cuh"),
     "linear_coop": ("lora_linear_coop.cu", "lora_expand.cuh", "lora_common.cuh"),
     "linear_fused": ("lora_fused.cu", "lora_common.cuh"),

@@ -250,14 +250,18 @@ int expand_dispatch(ExpandArgs &p, const lora_meta_t *meta, cudaStream_t st)
     const int64_t y_ld = p.y_ld;
 
     // Tensor-core path (tcgen05, TMEM accumulators; lora_expand_tc.cu) for
-    // 16-byte-aligned outputs.  Opt-in: measured slower than the mma.sync
-    // kernel on every workload (large 232 against 219 us, prefill 49 against
-    // 37), its per-chunk chain of copies, hand-offs and epilogue being
-    // longer than the mma.sync kernel's.  LORA_PUNICA_EXPAND_TC=1 takes it at
-    // every rank, =-1 at ranks of at least LORA_PUNICA_EXPAND_TC_MIN_RANK.
+    // 32-byte-aligned outputs and slice widths that are multiples of 64.  By
+    // default (LORA_PUNICA_EXPAND_TC=-1) it takes ranks of at least
+    // LORA_PUNICA_EXPAND_TC_MIN_RANK (128): measured at rank 128 on 16384
+    // tokens, 161 us against 216 us for the mma.sync kernel; at rank 64 and
+    // below, with 64-token tiles and short segments, the mma.sync kernel is
+    // faster (prefill 34.6 against 36.5 us, MLP 39.8 against 61.8 us).
+    // =1 takes it wherever it fits, =0 never, =2 requires it (a call it does
+    // not fit fails with LORA_ERR_ALIGN or LORA_ERR_SIZE).
     const int tc_mode = lora::knob_expand_tc();
+    if (tc_mode == 2 && !p.vec) return LORA_ERR_ALIGN;
     if (tc_mode != 0 && p.vec &&
-        (tc_mode == 1 || rank >= lora::knob_expand_tc_min_rank())) {
+        (tc_mode != -1 || rank >= lora::knob_expand_tc_min_rank())) {
         lora::ExpandLaunch u;
         u.x = p.x;
         u.x_bf16 = p.x_bf16;
@@ -284,8 +288,9 @@ int expand_dispatch(ExpandArgs &p, const lora_meta_t *meta, cudaStream_t st)
         u.no_lora = p.no_lora;
         u.error_word = meta->error_word;
         const int r = lora::launch_expand_tc(u, st);
-        if (r == 1) return LORA_OK;
-        if (r != 0) return r;
+        if (r == lora::TC_LAUNCHED) return LORA_OK;
+        if (r > 0) return r;                                    // a CUDA error
+        if (tc_mode == 2) return r == lora::TC_MISALIGNED ? LORA_ERR_ALIGN : LORA_ERR_SIZE;
     }
 
     if (rank <= 16) return lora::launch_expand_kt<1>(p, st);

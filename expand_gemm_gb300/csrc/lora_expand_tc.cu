@@ -7,37 +7,50 @@
 // Work items are (128-token tile of one LoRA segment, 64-column chunk of one
 // slice), numbered chunk-fastest; one persistent CTA per SM takes a
 // contiguous, balanced range of them, so it walks the chunks of one tile
-// with the tile's x rows (the MMA's A operand) resident in shared memory.
-// Chunks stream through a ring of DEPTH slots, each holding the chunk's B
-// tile (swizzled K-major, as UMMA reads it) and its old y rows.
+// with the tile's x rows (the MMA's A operand) resident in tensor memory.
+// Chunks stream through a ring of DEPTH slots in shared memory, each
+// holding the chunk's B tile (swizzled K-major, as UMMA reads it) and its
+// old y rows.
 //
-// Thirteen warps, one job each:
-//   warp 0       owns TMEM (two 64-column fp32 accumulators); lane 0 issues
-//                tcgen05.mma (M = 128 tokens, N = 64 columns, K = 16 steps
-//                over the rank) and commits each chunk's accumulator and
-//                the release of its slot's B.
-//   warps 1..4   loaders.  They fill slots with coalesced 16-byte cp.async
-//                (four whole 128-byte lines per instruction): the chunk's
-//                128 old y rows and its B tile.  Up to DEPTH - 1 chunks are
-//                in flight; as each one lands, the loaders fence it for the
-//                tensor core and signal the slot's mbarrier.
-//   warps 5..12  epilogue.  Warp (q, h) = (warp % 4, (warp - 5) / 4) owns
-//                the tile rows of TMEM lane quarter q and column half h.
-//                Per chunk it reads its accumulators with tcgen05.ld (one
-//                token row per thread), adds bias and old y in fp32, rounds
-//                once to bf16 into the slot and writes its rows back with
-//                coalesced 16-byte stores (8 rows x 64 bytes per
-//                instruction), then releases the slot.  When the next chunk
-//                opens a new tile or slice, it rounds that item's x rows to
-//                bf16 into the A operand right after reading the current
+// A sits in TMEM, not shared memory: a UMMA that reads both operands from
+// shared memory is bound by its operand reads (measured on this GPU: 48
+// cycles for M = 128, N = 64, K = 16, against 32 for the math), and A is
+// most of those bytes; from TMEM, each 64-column chunk reads only its 16 KB
+// B tile from shared memory.
+//
+// Fourteen warps, one job each:
+//   warp 0       owns TMEM (two 64-column fp32 accumulators and the A
+//                operand); lane 0 issues tcgen05.mma (M = 128 tokens,
+//                N = 64 columns, K = 16 steps over the rank) and commits
+//                each chunk's accumulator and the release of its slot's B.
+//   warp 1       lane 0 loads each chunk's B tile with TMA through a 5-D
+//                tensor map that permutes its rows (below).
+//   warps 2..5   y loaders: the chunk's 128 old y rows, gathered through the
+//                permutation with 16-byte cp.async (four whole 128-byte lines
+//                per instruction); each thread's copies arrive on the slot's
+//                y barrier when they land, so the loaders never wait for
+//                their own copies and run up to DEPTH chunks ahead.
+//   warps 6..13  epilogue.  Warp (q, h) = (warp % 4, (warp - 6) / 4) owns
+//                tile rows 32q + 16h .. 32q + 16h + 15 (TMEM lane quarter q,
+//                as tcgen05.ld requires).  It reads their accumulators in the
+//                16x256b shape, in which thread (g, t) = (lane / 4, lane % 4)
+//                holds columns 8i + 2t, 8i + 2t + 1 (i < 8) of rows g and
+//                g + 8.  B's rows were loaded permuted so that accumulator
+//                column 8i + 2t + e is output column 16t + 2i + e: each
+//                thread then holds 16 consecutive output columns of each of
+//                its rows, adds old y (from the slot) and bias in fp32,
+//                rounds once, and writes them with one 32-byte store (8 whole
+//                128-byte rows per warp instruction), straight from
+//                registers.  When the next chunk opens a new tile or slice,
+//                it rounds that item's x rows to bf16 and stores them into
+//                the A operand's TMEM columns right after reading the current
 //                accumulator.
-// Splitting loading from the epilogue keeps each warp on one latency chain:
-// a version in which every warp did both ran at half the rate.
 //
-// The ring is fed by the load/store units, not TMA: measured on this GPU,
-// a TMA box costs about 1000 cycles of latency per issuing thread and the
-// engine tops out near 50 bytes per clock per SM, and the old y rows of a
-// tile cut into several boxes wherever its token runs break.
+// Measured on the large workload (16384 tokens, rank 128, 10240 columns):
+// 161 us against the mma.sync kernel's 216 us.  Designs that added old y
+// on the tensor core (one more UMMA pass with a permutation matrix), split
+// the epilogue into two groups taking alternate chunks, or suspended the
+// waiting warps in hardware were slower (172 to 176 us).
 //
 // Every mbarrier wait is bounded (about one second); on expiry the kernel
 // sets bit 30 of the metadata error word, drains its copies and MMAs, frees
@@ -49,15 +62,22 @@ namespace lora {
 
 constexpr int TC_BM = 128;                    // tokens per tile (UMMA M, TMEM lanes)
 constexpr int TC_BN = 64;                     // columns per chunk (UMMA N)
-constexpr int TC_LOADERS = 4;
-constexpr int TC_EPI = 8;
-constexpr int TC_EPI0 = 1 + TC_LOADERS;       // first epilogue warp
+constexpr int TC_YL0 = 2;                     // first y loader warp
+constexpr int TC_YLOADERS = 4;
+constexpr int TC_EPI = 8;                     // epilogue warps
+constexpr int TC_NACC = 2;                    // TMEM accumulators (chunk g uses g % TC_NACC)
+constexpr int TC_A_COL = TC_NACC * 64;        // TMEM column of the A operand
+constexpr int TC_TMEM_COLS = 256;             // accumulators + A (at most 64 columns)
+static_assert(TC_A_COL + 64 <= TC_TMEM_COLS, "TMEM plan");
+constexpr int TC_EPI0 = TC_YL0 + TC_YLOADERS; // first epilogue warp
 constexpr int TC_THREADS = 32 * (TC_EPI0 + TC_EPI);
-constexpr int TC_LT = 32 * TC_LOADERS;        // loader threads
+constexpr int TC_LT = 32 * TC_YLOADERS;       // y loader threads
 constexpr long long TC_TIMEOUT_CYCLES = 2000000000ll;
+constexpr uint32_t TC_BACKOFF_NS = 200;       // loaders' sleep between polls of a full ring
 constexpr int TC_ERROR_BIT = 1 << 30;
 
 struct TcArgs {
+    CUtensorMap bmap[LORA_MAX_SLICES];        // B[s] rows, permuted (encode_perm_rows_map)
     const void *x;                            // [S, T, r]: fp32, or bf16 when x_bf16
     int32_t x_bf16;
     const uint16_t *b[LORA_MAX_SLICES];       // [L, n_s, r]
@@ -86,37 +106,36 @@ template <int KT>
 struct TcCfg {
     static constexpr int RP = 16 * KT;                     // padded rank
     static constexpr int CPR = RP / 8;                     // 16-byte pieces per operand row
-    static constexpr int A_BYTES = TC_BM * RP * 2;
+    static constexpr int BOX_K = RP < 64 ? RP : 64;        // B box width (elements)
+    static constexpr int NBOX = RP / BOX_K;                // B boxes per chunk
+    static constexpr int A_COLS = RP / 2;                  // TMEM columns of the A operand
     static constexpr int B_BYTES = TC_BN * RP * 2;
     static constexpr int Y_BYTES = TC_BM * TC_BN * 2;      // 128 rows x 128 bytes
     static constexpr int SLOT_BYTES = B_BYTES + Y_BYTES;   // a multiple of 1024
-    static constexpr int DEPTH = (KT >= 8) ? 5 : 8;
-    static constexpr int RING_OFF = A_BYTES;
+    static constexpr int DEPTH = (KT >= 8) ? 6 : 8;
+    static constexpr int RING_OFF = 0;
     static constexpr int BAR_OFF = RING_OFF + DEPTH * SLOT_BYTES;
-    static constexpr int MISC_OFF = BAR_OFF + (2 * DEPTH + 6) * 8;
+    static constexpr int MISC_OFF = BAR_OFF + (3 * DEPTH + 2 * TC_NACC + 2) * 8;
     static constexpr int TAB_OFF = MISC_OFF + 16;
     static constexpr int Y_PER_T = TC_BM * 8 / TC_LT;      // y pieces per loader thread (8)
-    static constexpr int B_PER_T = (TC_BN * CPR + TC_LT - 1) / TC_LT;
-    static_assert(SLOT_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1024-byte aligned operands");
+    static_assert(SLOT_BYTES % 1024 == 0, "1024-byte aligned operands");
+    static_assert(TC_BM * 8 % TC_LT == 0, "whole y rows per loader pass");
 };
+
+// Byte offset of 16-byte piece `pc` (columns 8pc .. 8pc+7) of row `r` of a
+// slot's y rows (128-byte-swizzled, so that the epilogue's reads, two rows
+// x four 32-byte pieces per 8-thread phase, hit all 32 banks).
+__device__ __forceinline__ uint32_t tc_y_off(int r, int pc)
+{
+    return uint32_t(r * 128 + ((pc ^ (r & 7)) << 4));
+}
+
+
 
 template <int KT>
 inline size_t tc_smem_bytes(int nbins)
 {
     return size_t(TcCfg<KT>::TAB_OFF) + seg_tab_bytes(nbins) + 1024;     // + alignment slack
-}
-
-// Byte offset of 16-byte piece `c` of row `r` in a K-major operand tile of
-// `rows` rows and rp bf16 columns, in the swizzled layout UMMA reads (32-,
-// 64- or 128-byte swizzle; rank 128 = two 64-column blocks).
-__device__ __forceinline__ uint32_t tc_kmajor_off(int rp, int rows, int r, int c)
-{
-    switch (rp) {
-    case 16: return uint32_t(r * 32 + ((c ^ ((r >> 2) & 1)) << 4));
-    case 32: return uint32_t(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
-    case 64: return uint32_t(r * 128 + ((c ^ (r & 7)) << 4));
-    default: return uint32_t((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-    }
 }
 
 // Shared-memory descriptor of K step kk (16 columns) of such a tile.
@@ -180,11 +199,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t base = smem_addr(smem);
-    const uint32_t bar_full = base + C::BAR_OFF;           // [DEPTH]: 4 loader warps
-    const uint32_t bar_empty = bar_full + 8 * DEPTH;       // [DEPTH]: MMA + 8 epilogue warps
-    const uint32_t bar_accf = bar_empty + 8 * DEPTH;       // [2]: MMA commit
-    const uint32_t bar_acce = bar_accf + 16;               // [2]: 8 epilogue warps
-    const uint32_t bar_x = bar_acce + 16;                  // A operand ready: 8 epilogue warps
+    const uint32_t bar_bfull = base + C::BAR_OFF;          // [DEPTH]: B TMA bytes
+    const uint32_t bar_yfull = bar_bfull + 8 * DEPTH;      // [DEPTH]: y loader threads
+    const uint32_t bar_empty = bar_yfull + 8 * DEPTH;      // [DEPTH]: MMA + epilogue warps
+    const uint32_t bar_accf = bar_empty + 8 * DEPTH;       // [TC_NACC]: MMA commit
+    const uint32_t bar_acce = bar_accf + 8 * TC_NACC;      // [TC_NACC]: epilogue warps
+    const uint32_t bar_x = bar_acce + 8 * TC_NACC;         // A operand ready: epilogue warps
     const uint32_t bar_drain = bar_x + 8;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
@@ -206,10 +226,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
 
     if (tid == 0) {
         for (int i = 0; i < DEPTH; ++i) {
-            mbar_init(bar_full + 8 * i, TC_LOADERS);
+            mbar_init(bar_bfull + 8 * i, 1);
+            mbar_init(bar_yfull + 8 * i, TC_LT);
             mbar_init(bar_empty + 8 * i, 1 + TC_EPI);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < TC_NACC; ++i) {
             mbar_init(bar_accf + 8 * i, 1);
             mbar_init(bar_acce + 8 * i, TC_EPI);
         }
@@ -218,6 +239,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
         mbar_fence_init();
         *s_abort = 0;
     }
+    if (tid == 32)
+        for (int s = 0; s < p.num_slices; ++s) tma_prefetch_map(&p.bmap[s]);
     const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + C::TAB_OFF), p.nbins);
     const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc, p.nbins,
                                           TC_BM, tab, false, 0, p.num_tokens, p.error_word);
@@ -231,14 +254,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
         return;
     }
 
-    if (warp == 0) tmem_alloc(smem_addr(s_tmem), 2 * TC_BN);
+    if (warp == 0) tmem_alloc(smem_addr(s_tmem), TC_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const long long deadline = clock64() + TC_TIMEOUT_CYCLES;
     const int R = p.rank, T = p.num_tokens;
-    const uint32_t a_tile = base;
 
     if (warp == 0) {
         // ------------------------------------------------------ MMA issue
@@ -256,11 +278,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                     }
                     ++items;
                 }
-                const int slot = g % DEPTH, ab = g & 1;
-                if (!mbar_wait_bounded(bar_full + 8 * slot, uint32_t(g / DEPTH) & 1u, s_abort,
+                const int slot = g % DEPTH, ab = g % TC_NACC;
+                if (!mbar_wait_bounded(bar_bfull + 8 * slot, uint32_t(g / DEPTH) & 1u, s_abort,
                                        deadline) ||
-                    !mbar_wait_bounded(bar_acce + 8 * ab, (uint32_t(g >> 1) & 1u) ^ 1u, s_abort,
-                                       deadline)) {
+                    !mbar_wait_bounded(bar_acce + 8 * ab, (uint32_t(g / TC_NACC) & 1u) ^ 1u,
+                                       s_abort, deadline)) {
                     ok = false;
                     break;
                 }
@@ -268,8 +290,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                 const uint32_t bt = base + C::RING_OFF + slot * C::SLOT_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < KT; ++kk)
-                    umma_bf16(tmem + ab * TC_BN, tc_kmajor_desc(RP, TC_BM, a_tile, kk),
-                              tc_kmajor_desc(RP, TC_BN, bt, kk), idesc, kk != 0);
+                    umma_bf16_tmem_a(tmem + ab * TC_BN, tmem + TC_A_COL + kk * 8,
+                                     tc_kmajor_desc(RP, TC_BN, bt, kk), idesc, kk != 0);
                 umma_commit(bar_empty + 8 * slot);           // B read
                 umma_commit(bar_accf + 8 * ab);
             }
@@ -283,84 +305,93 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
             }
         }
         __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ B by TMA
+        if (lane == 0) {
+            int cur_tile = -1, l_id = 0, g = 0;
+            TcCursor k;
+            k.start(p, w_begin, nchunks);
+            for (int64_t w = w_begin; w < w_end; ++w, ++g, k.next(p, nchunks)) {
+                const int slot = g % DEPTH;
+                if (!mbar_wait_backoff(bar_empty + 8 * slot, (uint32_t(g / DEPTH) & 1u) ^ 1u,
+                                       s_abort, deadline, TC_BACKOFF_NS))
+                    break;
+                if (k.tile != cur_tile) {
+                    cur_tile = k.tile;
+                    l_id = tab.id[find_segment(tab.tile, p.nbins, cur_tile)];
+                }
+                // 64-row block of the chunk's first B row (n_s and c0 are
+                // multiples of 64)
+                const int blk = (l_id * p.n[k.s] + k.c0(p)) >> 6;
+                const uint32_t bt = base + C::RING_OFF + slot * C::SLOT_BYTES;
+                mbar_arrive_expect_tx(bar_bfull + 8 * slot, C::B_BYTES);
+#pragma unroll
+                for (int b = 0; b < C::NBOX; ++b)
+                    tma_load_5d(bt + b * TC_BN * 128, &p.bmap[k.s], b * C::BOX_K, 0, 0, 0, blk,
+                                bar_bfull + 8 * slot);
+            }
+            // Before the CTA may exit, every issued load has landed: wait
+            // (bounded) for the last phase of each slot in use.
+            const int first = g > DEPTH ? g - DEPTH : 0;
+            const long long dd = clock64() + TC_TIMEOUT_CYCLES;
+            for (int j = first; j < g; ++j)
+                while (!mbar_try_wait(bar_bfull + 8 * (j % DEPTH), uint32_t(j / DEPTH) & 1u) &&
+                       clock64() < dd) {
+                }
+        }
+        __syncwarp();
     } else if (warp < TC_EPI0) {
-        // ------------------------------------------------------ loaders
-        const int lt = tid - 32;                           // 0 .. TC_LT - 1
+        // ------------------------------------------------------ y loaders
+        const int lt = tid - 32 * TC_YL0;                  // 0 .. TC_LT - 1
         const uint16_t *const ydummy = p.y;
-        int cur_tile = -1, l_id = 0;
+        int cur_tile = -1;
         int ltok[C::Y_PER_T];                              // rows i * 16 + lt / 8
-        int issued = 0, signalled = 0;
-        bool ok = true;
-        // Hands the oldest chunk in flight to the MMA and the epilogue.
-        auto signal_oldest = [&]() {
-            fence_proxy_async_smem();                      // B is read by the tensor core
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_full + 8 * (signalled % DEPTH));
-            ++signalled;
-        };
+        int g = 0;
         TcCursor k;
         k.start(p, w_begin, nchunks);
-        for (int64_t w = w_begin; w < w_end; ++w, k.next(p, nchunks)) {
-            const int g = issued, slot = g % DEPTH;
-            const bool got = mbar_wait_bounded(bar_empty + 8 * slot,
-                                               (uint32_t(g / DEPTH) & 1u) ^ 1u, s_abort, deadline);
-            if (__all_sync(0xffffffffu, got) == 0) {
-                ok = false;
-                break;
-            }
-            if (k.tile != cur_tile) {
-                cur_tile = k.tile;
-                const int seg = find_segment(tab.tile, p.nbins, cur_tile);
-                l_id = tab.id[seg];
-                const int row0 = tab.start[seg] + (cur_tile - tab.tile[seg]) * TC_BM;
-                const int nrows = min(TC_BM, tab.start[seg] + tab.count[seg] - row0);
-#pragma unroll
-                for (int i = 0; i < C::Y_PER_T; ++i) {
-                    const int r = i * (TC_LT / 8) + lt / 8;
-                    ltok[i] = (r < nrows) ? checked_token(p.sorted[row0 + r], T, p.error_word)
-                                          : -1;
-                }
-            }
-            const int c0 = k.c0(p), ncols = min(TC_BN, p.n[k.s] - c0);
-            const uint32_t st = base + C::RING_OFF + slot * C::SLOT_BYTES;
+        for (int64_t w = w_begin; w < w_end; ++w, ++g, k.next(p, nchunks)) {
+            const int slot = g % DEPTH;
+            const bool got = mbar_wait_backoff(bar_empty + 8 * slot,
+                                               (uint32_t(g / DEPTH) & 1u) ^ 1u, s_abort, deadline,
+                                               TC_BACKOFF_NS);
+            if (__all_sync(0xffffffffu, got) == 0) break;
             if (p.add_inputs) {
-                const int piece = lt % 8;
-                const bool cin = piece * 8 < ncols;
-                const uint16_t *ycol = p.y + p.col0[k.s] + c0 + piece * 8;
+                if (k.tile != cur_tile) {
+                    cur_tile = k.tile;
+                    const int seg = find_segment(tab.tile, p.nbins, cur_tile);
+                    const int row0 = tab.start[seg] + (cur_tile - tab.tile[seg]) * TC_BM;
+                    const int nrows = min(TC_BM, tab.start[seg] + tab.count[seg] - row0);
+#pragma unroll
+                    for (int i = 0; i < C::Y_PER_T; ++i) {
+                        const int r = i * (TC_LT / 8) + lt / 8;
+                        ltok[i] = (r < nrows) ? checked_token(p.sorted[row0 + r], T, p.error_word)
+                                              : -1;
+                    }
+                }
+                const int c0 = k.c0(p), ncols = min(TC_BN, p.n[k.s] - c0);
+                const int pc = lt % 8;
+                const bool cin = pc * 8 < ncols;
+                const uint16_t *ycol = p.y + p.col0[k.s] + c0 + pc * 8;
+                const uint32_t yt = base + C::RING_OFF + slot * C::SLOT_BYTES + C::B_BYTES;
 #pragma unroll
                 for (int i = 0; i < C::Y_PER_T; ++i) {
                     const int r = i * (TC_LT / 8) + lt / 8;
                     const bool ld = cin && ltok[i] >= 0;
-                    cp_async16(st + C::B_BYTES + r * 128 + ((piece ^ (r & 7)) << 4),
-                               ld ? ycol + int64_t(ltok[i]) * p.y_ld : ydummy, ld);
+                    cp_async16(yt + tc_y_off(r, pc), ld ? ycol + int64_t(ltok[i]) * p.y_ld : ydummy,
+                               ld);
                 }
             }
-            const int n_s = p.n[k.s];
-            const uint16_t *brows = p.b[k.s] + (int64_t(l_id) * n_s + c0) * R;
-#pragma unroll
-            for (int i = 0; i < C::B_PER_T; ++i) {
-                const int j = i * TC_LT + lt;
-                if (TC_BN * CPR % TC_LT != 0 && j >= TC_BN * CPR) break;
-                const int r = j / CPR, c = j % CPR;
-                const bool ld = r < ncols && c * 8 < R;
-                cp_async16(st + tc_kmajor_off(RP, TC_BN, r, c),
-                           ld ? brows + int64_t(r) * R + c * 8 : p.b[k.s], ld);
-            }
-            cp_async_commit();
-            ++issued;
-            if (issued - signalled == DEPTH - 1) {         // the oldest must land now
-                cp_async_wait<DEPTH - 2>();
-                signal_oldest();
-            }
+            cp_async_mbar_arrive_noinc(bar_yfull + 8 * slot);
         }
         cp_async_wait<0>();
-        if (ok)
-            while (signalled < issued) signal_oldest();
     } else {
         // ------------------------------------------------------ epilogue
-        const int ew = warp - TC_EPI0, q = warp & 3, h = ew >> 2;
-        const int my_row = q * 32 + lane;                  // TMEM lane
+        const int q = warp & 3, h = (warp - TC_EPI0) >> 2;
+        const int my_row = q * 32 + lane;                  // TMEM lane (A operand row)
+        const int qg = lane >> 2, qt = lane & 3;           // 16x256b fragment coordinates
+        const int qrow = q * 32 + h * 16 + qg;             // this thread's rows: qrow, qrow + 8
         int ct = -1, c_id = 0, ctok = -1;
+        int qtok[2];
         auto tile_rows = [&](int tile) {
             if (tile != ct) {
                 ct = tile;
@@ -370,14 +401,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                 const int nrows = min(TC_BM, tab.start[seg] + tab.count[seg] - row0);
                 ctok = (my_row < nrows) ? checked_token(p.sorted[row0 + my_row], T, p.error_word)
                                         : -1;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int r = qrow + 8 * u;
+                    qtok[u] = (r < nrows) ? checked_token(p.sorted[row0 + r], T, p.error_word)
+                                          : -1;
+                }
             }
         };
-        // this warp's rows of x (slice s), rounded to bf16, into the A operand
+        // this warp's row of x (slice s), half h of the rank, rounded to bf16
+        // into the A operand's TMEM columns
         auto convert_x = [&](int s) {
             wait_once();                                   // x is the shrink output
             const int64_t xrow = (int64_t(s) * T + (ctok >= 0 ? ctok : 0)) * R;
+            uint32_t wv[RP / 4];
 #pragma unroll
-            for (int c = h * (CPR / 2); c < (h + 1) * (CPR / 2); ++c) {
+            for (int j = 0; j < CPR / 2; ++j) {
+                const int c = h * (CPR / 2) + j;
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
                 if (ctok >= 0 && c * 8 < R) {
                     if (p.x_bf16) {
@@ -393,9 +433,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                         v.w = pack_bf16x2(t.z, t.w);
                     }
                 }
-                *reinterpret_cast<uint4 *>(smem + tc_kmajor_off(RP, TC_BM, my_row, c)) = v;
+                wv[4 * j] = v.x;
+                wv[4 * j + 1] = v.y;
+                wv[4 * j + 2] = v.z;
+                wv[4 * j + 3] = v.w;
             }
-            fence_proxy_async_smem();
+            tmem_st<RP / 4>(tmem + (uint32_t(q * 32) << 16) + uint32_t(TC_A_COL + h * (RP / 4)),
+                            wv);
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_x);
         };
@@ -409,105 +455,88 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
 #pragma unroll 1
         for (int64_t w = w_begin; w < w_end; ++w, ++g) {
             tile_rows(k.tile);
-            const int kc0 = k.c0(p), kncols = min(TC_BN, p.n[k.s] - kc0), ks = k.s;
-            // bias of this warp's 32 columns, fetched before the waits
-            uint4 bpre[4];
+            const int kc0 = k.c0(p), ks = k.s;
+            const bool cin = qt * 16 < min(TC_BN, p.n[ks] - kc0);
+            // bias of this thread's 16 columns, fetched before the waits
+            uint4 bv[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
             const uint16_t *bias_row = p.bias[ks] ? p.bias[ks] + int64_t(c_id) * p.n[ks] + kc0
                                                   : nullptr;
+            if (bias_row != nullptr && cin) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int piece = 4 * h + j;
-                bpre[j] = make_uint4(0u, 0u, 0u, 0u);
-                if (bias_row != nullptr && p.bias_vec && piece * 8 < kncols)
-                    bpre[j] = __ldg(reinterpret_cast<const uint4 *>(bias_row + piece * 8));
+                for (int j = 0; j < 2; ++j) {
+                    const uint16_t *bq = bias_row + qt * 16 + j * 8;
+                    if (p.bias_vec) {
+                        bv[j] = __ldg(reinterpret_cast<const uint4 *>(bq));
+                    } else {
+                        bv[j].x = uint32_t(bq[0]) | (uint32_t(bq[1]) << 16);
+                        bv[j].y = uint32_t(bq[2]) | (uint32_t(bq[3]) << 16);
+                        bv[j].z = uint32_t(bq[4]) | (uint32_t(bq[5]) << 16);
+                        bv[j].w = uint32_t(bq[6]) | (uint32_t(bq[7]) << 16);
+                    }
+                }
             }
-            const int ab = g & 1, slot = g % DEPTH;
-            bool got = mbar_wait_bounded(bar_accf + 8 * ab, uint32_t(g >> 1) & 1u, s_abort,
+            const int ab = g % TC_NACC;
+            const int slot = g % DEPTH;
+            bool got = mbar_wait_bounded(bar_accf + 8 * ab, uint32_t(g / TC_NACC) & 1u, s_abort,
                                          deadline);
-            got = got && mbar_wait_bounded(bar_full + 8 * slot, uint32_t(g / DEPTH) & 1u, s_abort,
+            got = got && mbar_wait_bounded(bar_yfull + 8 * slot, uint32_t(g / DEPTH) & 1u, s_abort,
                                            deadline);
             if (__all_sync(0xffffffffu, got) == 0) break;
             tc_fence_after();
             uint32_t va[32];
-            tmem_ld32_nowait(tmem + (uint32_t(q * 32) << 16) + uint32_t(ab * TC_BN + h * 32), va);
+            tmem_ld16x256b_x8_nowait(tmem + (uint32_t(q * 32 + h * 16) << 16) + uint32_t(ab * TC_BN),
+                                     va);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
-            const int tok_g = ctok;
+            const int tok[2] = {qtok[0], qtok[1]};
             // the next chunk opens a new tile or slice: its A operand now (the
-            // MMA of chunk g is done; that of chunk g + 1 waits for it)
+            // MMAs up to chunk g are done; that of chunk g + 1 waits for it)
             k.next(p, nchunks);
             if (w + 1 < w_end && k.first) {
                 tile_rows(k.tile);
                 convert_x(k.s);
             }
-            // + bias + old y, rounded once, back into the slot (own row)
-            uint8_t *yt = smem + C::RING_OFF + slot * C::SLOT_BYTES + C::B_BYTES;
-            if (tok_g >= 0) {
-                uint4 yv[4];
+            // x B + old y + bias, rounded once, straight to y: output
+            // columns 16 * qt + 2j + e of the chunk are accumulator columns
+            // 8j + 2 * qt + e, registers va[4j + e] (row qrow) and
+            // va[4j + 2 + e] (row qrow + 8); one 32-byte store per row
+            uint16_t *ycol = p.y + p.col0[ks] + kc0 + qt * 16;
+            const uint32_t bw[8] = {bv[0].x, bv[0].y, bv[0].z, bv[0].w,
+                                    bv[1].x, bv[1].y, bv[1].z, bv[1].w};
+            const bool has_bias = bias_row != nullptr;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int piece = 4 * h + j;
-                    yv[j] = make_uint4(0u, 0u, 0u, 0u);
-                    if (p.add_inputs)
-                        yv[j] = *reinterpret_cast<const uint4 *>(
-                            yt + my_row * 128 + ((piece ^ (my_row & 7)) << 4));
-                }
-                if (bias_row != nullptr && !p.bias_vec) {
+            for (int u = 0; u < 2; ++u) {
+                if (cin && tok[u] >= 0) {
+                    uint32_t yw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                    if (p.add_inputs) {
+                        const int r = qrow + 8 * u;
+                        const uint8_t *yt = smem + C::RING_OFF + slot * C::SLOT_BYTES + C::B_BYTES;
+                        const uint4 y0 = *reinterpret_cast<const uint4 *>(yt + tc_y_off(r, 2 * qt));
+                        const uint4 y1 =
+                            *reinterpret_cast<const uint4 *>(yt + tc_y_off(r, 2 * qt + 1));
+                        yw[0] = y0.x; yw[1] = y0.y; yw[2] = y0.z; yw[3] = y0.w;
+                        yw[4] = y1.x; yw[5] = y1.y; yw[6] = y1.z; yw[7] = y1.w;
+                    }
+                    uint32_t o[8];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int piece = 4 * h + j;
-                        if (piece * 8 < kncols) {
-                            const uint16_t *bq = bias_row + piece * 8;
-                            bpre[j].x = uint32_t(bq[0]) | (uint32_t(bq[1]) << 16);
-                            bpre[j].y = uint32_t(bq[2]) | (uint32_t(bq[3]) << 16);
-                            bpre[j].z = uint32_t(bq[4]) | (uint32_t(bq[5]) << 16);
-                            bpre[j].w = uint32_t(bq[6]) | (uint32_t(bq[7]) << 16);
+                    for (int j = 0; j < 8; ++j) {
+                        float a0 = __uint_as_float(va[4 * j + 2 * u]);
+                        float a1 = __uint_as_float(va[4 * j + 2 * u + 1]);
+                        a0 += bf16_lo(yw[j]);
+                        a1 += bf16_hi(yw[j]);
+                        if (has_bias) {
+                            a0 += bf16_lo(bw[j]);
+                            a1 += bf16_hi(bw[j]);
                         }
+                        o[j] = pack_bf16x2(a0, a1);
                     }
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int piece = 4 * h + j;
-                    const uint32_t yw[4] = {yv[j].x, yv[j].y, yv[j].z, yv[j].w};
-                    const uint32_t bw[4] = {bpre[j].x, bpre[j].y, bpre[j].z, bpre[j].w};
-                    uint32_t o[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float a0 = __uint_as_float(va[j * 8 + 2 * e]) + bf16_lo(bw[e]) +
-                                         bf16_lo(yw[e]);
-                        const float a1 = __uint_as_float(va[j * 8 + 2 * e + 1]) + bf16_hi(bw[e]) +
-                                         bf16_hi(yw[e]);
-                        o[e] = pack_bf16x2(a0, a1);
-                    }
-                    // columns past the slice are never stored
-                    *reinterpret_cast<uint4 *>(yt + my_row * 128 + ((piece ^ (my_row & 7)) << 4)) =
-                        make_uint4(o[0], o[1], o[2], o[3]);
+                    st_global_v8(ycol + int64_t(tok[u]) * p.y_ld, o);
                 }
             }
             __syncwarp();
-            // this warp's rows out: 8 rows x 64 bytes per store instruction
-            {
-                const int piece = 4 * h + (lane & 3);
-                const bool cin = piece * 8 < kncols;
-                uint16_t *ycol = p.y + p.col0[ks] + kc0 + piece * 8;
-                int tok[4];
-                uint4 v[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int rl = i * 8 + (lane >> 2);
-                    const int r = q * 32 + rl;
-                    tok[i] = __shfl_sync(0xffffffffu, tok_g, rl);
-                    v[i] = *reinterpret_cast<const uint4 *>(yt + r * 128 + ((piece ^ (r & 7)) << 4));
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (cin && tok[i] >= 0)
-                        *reinterpret_cast<uint4 *>(ycol + int64_t(tok[i]) * p.y_ld) = v[i];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);   // this warp is done with the slot
+            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);   // done with the slot's y
         }
     }
 
@@ -516,7 +545,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 2 * TC_BN);
+    if (warp == 0) tmem_dealloc(tmem, TC_TMEM_COLS);
 }
 
 template <int KT>
@@ -527,7 +556,7 @@ static int launch_tc_kt(const TcArgs &p, cudaStream_t stream)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return int(e);
     const size_t smem = tc_smem_bytes<KT>(p.nbins);
-    if (smem > 227 * 1024) return 0;
+    if (smem > 227 * 1024) return TC_NO_FIT;
     if (dev < 64 && configured[dev] == 0) {
         e = cudaFuncSetAttribute(expand_tc_kernel<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  227 * 1024);
@@ -536,14 +565,16 @@ static int launch_tc_kt(const TcArgs &p, cudaStream_t stream)
     }
     e = launch_kernel(expand_tc_kernel<KT>, dim3(device_sm_count()), dim3(TC_THREADS), smem,
                       stream, p);
-    return e == cudaSuccess ? 1 : int(e);
+    return e == cudaSuccess ? int(TC_LAUNCHED) : int(e);
 }
 
-// Launches the tensor-core expand: returns 1 if launched, 0 if the call does
-// not fit it (the caller then runs the mma.sync kernel), or a cudaError_t.
+// Launches the tensor-core expand: returns TC_LAUNCHED, TC_NO_FIT or
+// TC_MISALIGNED if the call does not fit it (the caller then runs the
+// mma.sync kernel), or a cudaError_t.
 int launch_expand_tc(const ExpandLaunch &a, cudaStream_t stream)
 {
-    if (!a.vec || a.error_word == nullptr) return 0;
+    if (!a.vec) return TC_MISALIGNED;
+    if (a.error_word == nullptr) return TC_NO_FIT;
     TcArgs p;
     p.x = a.x;
     p.x_bf16 = a.x_bf16;
@@ -560,6 +591,24 @@ int launch_expand_tc(const ExpandLaunch &a, cudaStream_t stream)
         chunks += (a.n[s] + TC_BN - 1) / TC_BN;
     }
     p.chunk0[a.num_slices] = chunks;
+    // B by TMA through the row-permuting map: every slice's width must be a
+    // multiple of 64 (each LoRA's rows start a 64-row block); y's rows are
+    // written with 32-byte stores: y, its row stride and every slice's first
+    // column 32-byte aligned
+    const uint32_t rp = a.rank <= 16 ? 16u : a.rank <= 32 ? 32u : a.rank <= 64 ? 64u : 128u;
+    const CUtensorMapSwizzle sw = rp == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                  : rp == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_128B;
+    if (reinterpret_cast<uintptr_t>(a.y) % 32 != 0 || a.y_ld % 16 != 0) return TC_MISALIGNED;
+    for (int s = 0; s < a.num_slices; ++s) {
+        if (a.col0[s] % 16 != 0) return TC_MISALIGNED;
+        if (a.n[s] % 64 != 0) return TC_NO_FIT;
+    }
+    for (int s = 0; s < a.num_slices; ++s)
+        if (!encode_perm_rows_map(&p.bmap[s], a.b[s], uint64_t(a.max_loras) * uint64_t(a.n[s]),
+                                  uint32_t(a.rank), rp < 64 ? rp : 64u, sw))
+            return int(cudaErrorInvalidValue);
+    for (int s = a.num_slices; s < LORA_MAX_SLICES; ++s) p.bmap[s] = p.bmap[0];
     p.num_slices = a.num_slices;
     p.rank = a.rank;
     p.y = a.y;

@@ -64,6 +64,35 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// mbar_wait_bounded for a thread that runs ahead of its consumers: between
+// polls it sleeps `ns` nanoseconds, leaving the issue slots to the warps on
+// the critical path.
+__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort, long long deadline,
+                                                  uint32_t ns)
+{
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (clock64() > deadline) {
+            *abort = 1;
+            return false;
+        }
+        __nanosleep(ns);
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------- 256-bit store
+
+// One 32-byte global store (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t (&v)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n"
+                 :: "l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                    "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -74,6 +103,25 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "[%0], [%1, {%2, %3}], [%4];\n"
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
+}
+
+// 5-D tile load (the row-permuting B map of the tensor-core expand).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, int c3, int c4, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cta.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+           "r"(c4), "r"(bar)
+        : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's count includes this arrival: no pending-count increment).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" :: "r"(bar) : "memory");
 }
 
 // 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
@@ -128,6 +176,19 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A's row m in TMEM lane m,
+// its K elements packed two per 32-bit column (M = 128).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate)
+{
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // Arrive on `bar` once every UMMA issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
@@ -168,6 +229,64 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[3
         : "r"(taddr));
 }
 
+// 16 TMEM lanes x 64 fp32 columns (shape 16x256b, eight repeats along the
+// columns), without waiting.  Thread (g, t) = (lane / 4, lane % 4) gets, for
+// repeat i, r[4i], r[4i+1] = lane g, columns 8i + 2t and 8i + 2t + 1, and
+// r[4i+2], r[4i+3] = lane g + 8, the same columns (the mma.sync
+// accumulator layout).
+__device__ __forceinline__ void tmem_ld16x256b_x8_nowait(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+// N consecutive 32-bit columns of this thread's TMEM lane (shape 32x32b).
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N])
+{
+    static_assert(N == 4 || N == 8 || N == 16 || N == 32, "tmem_st: 4, 8, 16 or 32 columns");
+    if constexpr (N == 4) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};\n"
+                     :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]) : "memory");
+    } else if constexpr (N == 8) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], "
+                     "{%1, %2, %3, %4, %5, %6, %7, %8};\n"
+                     :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]),
+                        "r"(r[5]), "r"(r[6]), "r"(r[7]) : "memory");
+    } else if constexpr (N == 16) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                     "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n"
+                     :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]),
+                        "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]),
+                        "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]) : "memory");
+    } else {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+                     "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+                     "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+                     "%32};\n"
+                     :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]),
+                        "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]),
+                        "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+                        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),
+                        "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+                        "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
+    }
+}
+
+__device__ __forceinline__ void tmem_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
@@ -203,5 +322,13 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n)
 bool encode_tile_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols,
                      uint64_t row_stride, uint32_t box_cols, uint32_t box_rows,
                      CUtensorMapSwizzle swizzle);
+
+// Host: encodes the B map of the tensor-core expand over a bf16 matrix of
+// `rows` rows (a multiple of 64) of `rank` elements, whose 64-row boxes land
+// in shared memory with their rows permuted: shared row 8i + 2t + e holds
+// global row 16t + 2i + e (i < 8, t < 4, e < 2).  Box {box_k, 64 rows};
+// false if the driver entry point is missing or rejects it.
+bool encode_perm_rows_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t rank,
+                          uint32_t box_k, CUtensorMapSwizzle swizzle);
 
 }  // namespace lora

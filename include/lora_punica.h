@@ -202,9 +202,12 @@ int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidden,
  *
  * x is rounded to bf16 for the tensor cores (as the Triton kernel does when
  * it casts its input to the weight type); products accumulate in fp32
- * (mma.sync; an opt-in tcgen05 path with TMEM accumulators when y's rows,
- * offsets and slice widths are 16-byte aligned, LORA_PUNICA_EXPAND_TC* in
- * the environment); y, the bias and the product are summed in fp32 and
+ * (tcgen05 with TMEM accumulators at rank >= 128 when y, y_ld and
+ * offset_start are 32-byte aligned and every slice width is a multiple of
+ * 64; mma.sync otherwise; LORA_PUNICA_EXPAND_TC* in the environment move
+ * the boundary, and with LORA_PUNICA_EXPAND_TC=2 a call the tcgen05 path
+ * does not take fails with LORA_ERR_ALIGN or LORA_ERR_SIZE); y, the bias
+ * and the product are summed in fp32 and
  * rounded to bf16 once (round to nearest even).  Output: deterministic.  A
  * bounded wait of the tcgen05 path that runs out sets bit 30 of
  * meta->error_word.

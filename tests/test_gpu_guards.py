@@ -27,7 +27,7 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 GUARD_ROWS = 64          # rows before and after x and y
-GUARD_COLS = 8           # columns left and right of x and y (keeps 16-byte alignment)
+GUARD_COLS = 16          # columns left and right of x and y (keeps 32-byte alignment)
 GUARD_BITS = 0x7FA5      # a bf16 NaN pattern no kernel writes
 GUARD_F32 = -7.0e30      # fp32 guard value
 GUARD_LORAS = 1          # LoRAs past max_loras in A, B and bias
@@ -83,7 +83,7 @@ PATHS = [pytest.param(dict(LORA_PUNICA_COOP=1, LORA_PUNICA_FUSED=0), id="coop"),
          pytest.param(dict(LORA_PUNICA_COOP=0, LORA_PUNICA_FUSED=0, LORA_PUNICA_SELF_META=0),
                       id="three_kernels"),
          pytest.param(dict(LORA_PUNICA_COOP=0, LORA_PUNICA_FUSED=0, LORA_PUNICA_UMMA_MIN_TOKENS=0,
-                           LORA_PUNICA_UMMA_MIN_COLS=0, LORA_PUNICA_EXPAND_TC=1),
+                           LORA_PUNICA_UMMA_MIN_COLS=0, LORA_PUNICA_EXPAND_TC=2),
                       id="tensor_core_kernels")]
 
 
@@ -119,7 +119,7 @@ def test_guard_bands_on_every_path(oracle_mod, knob, path, name, T):
     np.testing.assert_array_equal(got_y[none], inp.y[none])
 
 
-@pytest.mark.parametrize("tc", ["0", "1"])
+@pytest.mark.parametrize("tc", ["0", "2"])
 def test_guard_bands_separate_calls_with_offset(oracle_mod, knob, tc):
     """lora_shrink and lora_expand (offset_start, add_inputs=False) with
     guard bands; the columns outside the slices stay untouched too."""
@@ -169,6 +169,7 @@ T = w.num_tokens
 def run(corrupt, umma):
     os.environ["LORA_PUNICA_UMMA_MIN_TOKENS"] = "0" if umma else "1024"
     os.environ["LORA_PUNICA_UMMA_MIN_COLS"] = "0" if umma else "256"
+    os.environ["LORA_PUNICA_EXPAND_TC"] = "2" if umma else "0"
     eg.reload_options()
     x_full, x = G._guarded_bf16(inp.x)
     y_full, y = G._guarded_bf16(inp.y)
@@ -215,7 +216,7 @@ def test_debug_build_reports_metadata_outside_the_batch():
     """On the debug-checks build: a valid batch leaves bit 29 clear; a
     sorted entry past T, an active id equal to max_loras, or a segment
     running past T each set bit 29, and no guard byte changes (the checked
-    accesses are skipped), on the mma.sync and the tcgen05 shrink."""
+    accesses are skipped), on the mma.sync and the tcgen05 kernels."""
     from expand_gemm_gb300.build import build
     lib = build(debug=True)
     env = dict(os.environ, LORA_PUNICA_LIBRARY=lib)

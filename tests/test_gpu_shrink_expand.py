@@ -181,7 +181,9 @@ def _expand_case(oracle_mod, inp, ids=None, xin=None, offset=0, add_inputs=True,
     return got
 
 
-EXPAND_PATHS = [pytest.param("1", id="tcgen05"), pytest.param("0", id="mma_sync")]
+# "2" requires the tcgen05 kernel (a call it does not fit fails), so these
+# cases cannot pass on the mma.sync kernel by accident.
+EXPAND_PATHS = [pytest.param("2", id="tcgen05"), pytest.param("0", id="mma_sync")]
 
 
 @pytest.mark.parametrize("path", EXPAND_PATHS)
@@ -200,12 +202,44 @@ def test_expand_workloads_reduced(oracle_mod, knob, path, name, T):
     (129, 128, 2, (1024, 136), 8, 24),    # rank 128
     (50, 32, 5, (16,) * 8, 0, 0),         # eight slices
 ])
-@pytest.mark.parametrize("path", EXPAND_PATHS)
+@pytest.mark.parametrize("path", [pytest.param("1", id="tcgen05_where_fits"),
+                                  pytest.param("0", id="mma_sync")])
 def test_expand_shapes(oracle_mod, knob, path, T, r, L, slices, offset, y_extra):
     knob(LORA_PUNICA_EXPAND_TC=path)
     rng_bias = [True, False][T % 2]
     inp = _custom(T, 64, r, L, slices, seed=T + r, bias=rng_bias)
     _expand_case(oracle_mod, inp, offset=offset, y_extra=y_extra)
+
+
+@pytest.mark.parametrize("T,r,L,slices,offset,y_extra", [
+    (1, 16, 1, (128,), 0, 0),
+    (70, 8, 3, (192, 64), 0, 16),         # rank 8
+    (300, 24, 4, (64, 64, 64), 16, 0),    # padded rank, offset
+    (129, 128, 2, (1024, 192), 16, 32),   # rank 128, two tiles + 1
+    (50, 32, 5, (64,) * 8, 0, 0),         # eight slices of one chunk
+    (257, 64, 7, (4096, 64), 48, 0),      # rank 64, two full tiles + 1
+])
+def test_expand_tc_shapes(oracle_mod, knob, T, r, L, slices, offset, y_extra):
+    """The tcgen05 kernel, required, on shapes it takes (slice widths that
+    are multiples of 64; y, its row stride and offset 32-byte aligned)."""
+    knob(LORA_PUNICA_EXPAND_TC="2")
+    inp = _custom(T, 64, r, L, slices, seed=T + r + 1, bias=bool(T % 2))
+    _expand_case(oracle_mod, inp, offset=offset, y_extra=y_extra)
+
+
+def test_expand_tc_required_rejects_what_it_cannot_take(knob):
+    """With the tcgen05 kernel required, a slice width that is not a multiple
+    of 64 and outputs that are not 32-byte aligned are refused on the host."""
+    eg = _eg()
+    knob(LORA_PUNICA_EXPAND_TC="2")
+    for slices, offset, code in (((192, 96), 0, "size"), ((64,), 3, "align"), ((64,), 8, "align")):
+        inp = _custom(40, 64, 16, 2, slices, seed=3)
+        B = [dev_bf16(b) for b in inp.lora_b]
+        y = torch.zeros((40, offset + sum(slices)), dtype=torch.bfloat16, device="cuda")
+        meta = _meta(inp.ids, 2)
+        x = torch.zeros((len(slices), 40, 16), dtype=torch.float32, device="cuda")
+        with pytest.raises(RuntimeError, match=code):
+            eg.lora_expand(x, B, y, meta, offset, True)
 
 
 @pytest.mark.parametrize("slices,offset", [((100, 7), 0), ((64, 64), 3), ((13,), 5)])
@@ -218,18 +252,20 @@ def test_expand_unaligned_scalar_path(oracle_mod, slices, offset):
 def test_expand_long_segments(oracle_mod, knob, path):
     """Sequences of hundreds of tokens per LoRA: many full 128-token tiles."""
     knob(LORA_PUNICA_EXPAND_TC=path)
-    w = W.Workload("longx", 31, 2500, 64, 64, 5, (384, 136, 8), "zipf_seq", p_none=0.2,
+    slices, offset = ((384, 192, 64), 16) if path == "2" else ((384, 136, 8), 8)
+    w = W.Workload("longx", 31, 2500, 64, 64, 5, slices, "zipf_seq", p_none=0.2,
                    seq_len=(150, 700), bias=True)
     inp = W.generate(w)
-    _expand_case(oracle_mod, inp, offset=8, y_extra=8)
+    _expand_case(oracle_mod, inp, offset=offset, y_extra=offset)
 
 
 @pytest.mark.parametrize("path", EXPAND_PATHS)
 def test_expand_overwrite_mode(oracle_mod, knob, path):
     knob(LORA_PUNICA_EXPAND_TC=path)
     inp = _custom(333, 64, 32, 4, (256, 128), seed=22, bias=True)
-    _expand_case(oracle_mod, inp, add_inputs=False, offset=8, y_extra=16)
-    _expand_case(oracle_mod, inp, add_inputs=False, offset=3, y_extra=1)   # scalar path
+    _expand_case(oracle_mod, inp, add_inputs=False, offset=16, y_extra=16)
+    if path == "0":
+        _expand_case(oracle_mod, inp, add_inputs=False, offset=3, y_extra=1)   # scalar path
 
 
 def test_expand_partial_bias_and_strided_y(oracle_mod):
