@@ -43,7 +43,7 @@ static Knobs read_knobs()
     k.umma_partial = env_int("LORA_PUNICA_UMMA_PARTIAL", 1);
     k.early_shrink_ctas = env_int("LORA_PUNICA_EARLY_SHRINK_CTAS", 2);
     k.expand_tc = env_int("LORA_PUNICA_EXPAND_TC", -1);
-    k.expand_tc_min_rank = env_int("LORA_PUNICA_EXPAND_TC_MIN_RANK", 128);
+    k.expand_tc_min_rank = env_int("LORA_PUNICA_EXPAND_TC_MIN_RANK", 64);
     k.meta_small = env_int("LORA_PUNICA_META_SMALL", 1);
     k.meta_multi = env_int("LORA_PUNICA_META_MULTI", 1);
     k.coop_test_extra = env_int("LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS", 0);
@@ -87,7 +87,7 @@ bool encode_tile_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t co
 }
 
 bool encode_perm_rows_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t rank,
-                          uint32_t box_k, CUtensorMapSwizzle swizzle)
+                          uint32_t box_k, uint32_t blocks, CUtensorMapSwizzle swizzle)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr || rows % 64 != 0) return false;
@@ -97,7 +97,7 @@ bool encode_perm_rows_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint32
     const cuuint64_t row = uint64_t(rank) * 2;
     const cuuint64_t dims[5] = {rank, 2, 4, 8, rows / 64};
     const cuuint64_t strides[4] = {row, 16 * row, 2 * row, 64 * row};
-    const cuuint32_t box[5] = {box_k, 2, 4, 8, 1};
+    const cuuint32_t box[5] = {box_k, 2, 4, 8, blocks};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(ptr), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -430,7 +430,7 @@ struct Knobs {
     int umma_partial;         // LORA_PUNICA_UMMA_PARTIAL (1)
     int early_shrink_ctas;    // LORA_PUNICA_EARLY_SHRINK_CTAS (2)
     int expand_tc;            // LORA_PUNICA_EXPAND_TC: tcgen05 expand (0 off, -1 ranks >= min, 1 where it fits, 2 required)
-    int expand_tc_min_rank;   // LORA_PUNICA_EXPAND_TC_MIN_RANK (128)
+    int expand_tc_min_rank;   // LORA_PUNICA_EXPAND_TC_MIN_RANK (64)
     int meta_small;           // LORA_PUNICA_META_SMALL (1)
     int meta_multi;           // LORA_PUNICA_META_MULTI: multi-CTA metadata kernel (1)
     int coop_test_extra;      // LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS (0, tests only)

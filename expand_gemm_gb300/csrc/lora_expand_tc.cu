@@ -4,8 +4,8 @@
 // PunicaWrapperTPU._apply_bias):
 //   y[t, off_s + j] (+)= x[s][t, :] @ B[s][id(t)][j, :] + bias[s][id(t)][j]
 //
-// Work items are (128-token tile of one LoRA segment, 64-column chunk of one
-// slice), numbered chunk-fastest; one persistent CTA per SM takes a
+// Work items are (128-token tile of one LoRA segment, 128-column chunk of
+// one slice), numbered chunk-fastest; one persistent CTA per SM takes a
 // contiguous, balanced range of them, so it walks the chunks of one tile
 // with the tile's x rows (the MMA's A operand) resident in tensor memory.
 // Chunks stream through a ring of DEPTH slots in shared memory, each
@@ -15,13 +15,13 @@
 // A sits in TMEM, not shared memory: a UMMA that reads both operands from
 // shared memory is bound by its operand reads (measured on this GPU: 48
 // cycles for M = 128, N = 64, K = 16, against 32 for the math), and A is
-// most of those bytes; from TMEM, each 64-column chunk reads only its 16 KB
-// B tile from shared memory.
+// a large share of those bytes; from TMEM, each chunk reads only its B tile
+// from shared memory.
 //
 // Fourteen warps, one job each:
-//   warp 0       owns TMEM (two 64-column fp32 accumulators and the A
+//   warp 0       owns TMEM (two 128-column fp32 accumulators and the A
 //                operand); lane 0 issues tcgen05.mma (M = 128 tokens,
-//                N = 64 columns, K = 16 steps over the rank) and commits
+//                N = 128 columns, K = 16 steps over the rank) and commits
 //                each chunk's accumulator and the release of its slot's B.
 //   warp 1       lane 0 loads each chunk's B tile with TMA through a 5-D
 //                tensor map that permutes its rows (below).
@@ -32,10 +32,11 @@
 //                their own copies and run up to DEPTH chunks ahead.
 //   warps 6..13  epilogue.  Warp (q, h) = (warp % 4, (warp - 6) / 4) owns
 //                tile rows 32q + 16h .. 32q + 16h + 15 (TMEM lane quarter q,
-//                as tcgen05.ld requires).  It reads their accumulators in the
-//                16x256b shape, in which thread (g, t) = (lane / 4, lane % 4)
-//                holds columns 8i + 2t, 8i + 2t + 1 (i < 8) of rows g and
-//                g + 8.  B's rows were loaded permuted so that accumulator
+//                as tcgen05.ld requires).  It reads their accumulators one
+//                64-column half at a time in the 16x256b shape, in which
+//                thread (g, t) = (lane / 4, lane % 4) holds columns 8i + 2t,
+//                8i + 2t + 1 (i < 8) of rows g and g + 8.  B's rows were
+//                loaded permuted so that, in each 64-column half, accumulator
 //                column 8i + 2t + e is output column 16t + 2i + e: each
 //                thread then holds 16 consecutive output columns of each of
 //                its rows, adds old y (from the slot) and bias in fp32,
@@ -47,10 +48,10 @@
 //                accumulator.
 //
 // Measured on the large workload (16384 tokens, rank 128, 10240 columns):
-// 161 us against the mma.sync kernel's 216 us.  Designs that added old y
-// on the tensor core (one more UMMA pass with a permutation matrix), split
-// the epilogue into two groups taking alternate chunks, or suspended the
-// waiting warps in hardware were slower (172 to 176 us).
+// 132 us against the mma.sync kernel's 216 us (149 us with 64-column
+// chunks).  Designs that added old y on the tensor core (one more UMMA pass
+// with a permutation matrix), split the epilogue into two groups taking
+// alternate chunks, or suspended the waiting warps in hardware were slower.
 //
 // Every mbarrier wait is bounded (about one second); on expiry the kernel
 // sets bit 30 of the metadata error word, drains its copies and MMAs, frees
@@ -61,14 +62,15 @@
 namespace lora {
 
 constexpr int TC_BM = 128;                    // tokens per tile (UMMA M, TMEM lanes)
-constexpr int TC_BN = 64;                     // columns per chunk (UMMA N)
+constexpr int TC_BN = 128;                    // columns per chunk (UMMA N)
+constexpr int TC_HALVES = TC_BN / 64;         // 64-column blocks per chunk
 constexpr int TC_YL0 = 2;                     // first y loader warp
 constexpr int TC_YLOADERS = 4;
 constexpr int TC_EPI = 8;                     // epilogue warps
 constexpr int TC_NACC = 2;                    // TMEM accumulators (chunk g uses g % TC_NACC)
-constexpr int TC_A_COL = TC_NACC * 64;        // TMEM column of the A operand
-constexpr int TC_TMEM_COLS = 256;             // accumulators + A (at most 64 columns)
-static_assert(TC_A_COL + 64 <= TC_TMEM_COLS, "TMEM plan");
+constexpr int TC_A_COL = TC_NACC * TC_BN;    // TMEM column of the A operand
+constexpr int TC_TMEM_COLS = TC_A_COL + 64 <= 256 ? 256 : 512;   // accumulators + A
+static_assert(TC_BN == 64 || TC_BN == 128, "chunk width");
 constexpr int TC_EPI0 = TC_YL0 + TC_YLOADERS; // first epilogue warp
 constexpr int TC_THREADS = 32 * (TC_EPI0 + TC_EPI);
 constexpr int TC_LT = 32 * TC_YLOADERS;       // y loader threads
@@ -84,7 +86,7 @@ struct TcArgs {
     const uint16_t *bias[LORA_MAX_SLICES];    // [L, n_s] or null
     int32_t n[LORA_MAX_SLICES];
     int32_t col0[LORA_MAX_SLICES];
-    int32_t chunk0[LORA_MAX_SLICES + 1];      // first 64-column chunk of each slice
+    int32_t chunk0[LORA_MAX_SLICES + 1];      // first chunk of each slice
     int32_t num_slices;
     int32_t rank;
     uint16_t *y;
@@ -110,16 +112,17 @@ struct TcCfg {
     static constexpr int NBOX = RP / BOX_K;                // B boxes per chunk
     static constexpr int A_COLS = RP / 2;                  // TMEM columns of the A operand
     static constexpr int B_BYTES = TC_BN * RP * 2;
-    static constexpr int Y_BYTES = TC_BM * TC_BN * 2;      // 128 rows x 128 bytes
+    static constexpr int Y_BYTES = TC_BM * TC_BN * 2;      // 128 rows x TC_BN columns
     static constexpr int SLOT_BYTES = B_BYTES + Y_BYTES;   // a multiple of 1024
-    static constexpr int DEPTH = (KT >= 8) ? 6 : 8;
+    static constexpr int DEPTH = 196608 / SLOT_BYTES < 8 ? 196608 / SLOT_BYTES : 8;
     static constexpr int RING_OFF = 0;
     static constexpr int BAR_OFF = RING_OFF + DEPTH * SLOT_BYTES;
     static constexpr int MISC_OFF = BAR_OFF + (3 * DEPTH + 2 * TC_NACC + 2) * 8;
     static constexpr int TAB_OFF = MISC_OFF + 16;
-    static constexpr int Y_PER_T = TC_BM * 8 / TC_LT;      // y pieces per loader thread (8)
+    static constexpr int PPR = TC_BN / 8;                  // 16-byte y pieces per row
+    static constexpr int Y_PER_T = TC_BM * PPR / TC_LT;    // y pieces per loader thread
     static_assert(SLOT_BYTES % 1024 == 0, "1024-byte aligned operands");
-    static_assert(TC_BM * 8 % TC_LT == 0, "whole y rows per loader pass");
+    static_assert(TC_LT % PPR == 0, "whole y rows per loader pass");
 };
 
 // Byte offset of 16-byte piece `pc` (columns 8pc .. 8pc+7) of row `r` of a
@@ -127,7 +130,7 @@ struct TcCfg {
 // x four 32-byte pieces per 8-thread phase, hit all 32 banks).
 __device__ __forceinline__ uint32_t tc_y_off(int r, int pc)
 {
-    return uint32_t(r * 128 + ((pc ^ (r & 7)) << 4));
+    return uint32_t((pc >> 3) * (TC_BM * 128) + r * 128 + (((pc & 7) ^ (r & 7)) << 4));
 }
 
 
@@ -345,7 +348,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
         const int lt = tid - 32 * TC_YL0;                  // 0 .. TC_LT - 1
         const uint16_t *const ydummy = p.y;
         int cur_tile = -1;
-        int ltok[C::Y_PER_T];                              // rows i * 16 + lt / 8
+        int ltok[C::Y_PER_T];                              // rows i * (TC_LT / PPR) + lt / PPR
         int g = 0;
         TcCursor k;
         k.start(p, w_begin, nchunks);
@@ -363,19 +366,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                     const int nrows = min(TC_BM, tab.start[seg] + tab.count[seg] - row0);
 #pragma unroll
                     for (int i = 0; i < C::Y_PER_T; ++i) {
-                        const int r = i * (TC_LT / 8) + lt / 8;
+                        const int r = i * (TC_LT / C::PPR) + lt / C::PPR;
                         ltok[i] = (r < nrows) ? checked_token(p.sorted[row0 + r], T, p.error_word)
                                               : -1;
                     }
                 }
                 const int c0 = k.c0(p), ncols = min(TC_BN, p.n[k.s] - c0);
-                const int pc = lt % 8;
+                const int pc = lt % C::PPR;
                 const bool cin = pc * 8 < ncols;
                 const uint16_t *ycol = p.y + p.col0[k.s] + c0 + pc * 8;
                 const uint32_t yt = base + C::RING_OFF + slot * C::SLOT_BYTES + C::B_BYTES;
 #pragma unroll
                 for (int i = 0; i < C::Y_PER_T; ++i) {
-                    const int r = i * (TC_LT / 8) + lt / 8;
+                    const int r = i * (TC_LT / C::PPR) + lt / C::PPR;
                     const bool ld = cin && ltok[i] >= 0;
                     cp_async16(yt + tc_y_off(r, pc), ld ? ycol + int64_t(ltok[i]) * p.y_ld : ydummy,
                                ld);
@@ -456,25 +459,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
         for (int64_t w = w_begin; w < w_end; ++w, ++g) {
             tile_rows(k.tile);
             const int kc0 = k.c0(p), ks = k.s;
-            const bool cin = qt * 16 < min(TC_BN, p.n[ks] - kc0);
-            // bias of this thread's 16 columns, fetched before the waits
-            uint4 bv[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+            const int ncols = min(TC_BN, p.n[ks] - kc0);
             const uint16_t *bias_row = p.bias[ks] ? p.bias[ks] + int64_t(c_id) * p.n[ks] + kc0
                                                   : nullptr;
-            if (bias_row != nullptr && cin) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint16_t *bq = bias_row + qt * 16 + j * 8;
-                    if (p.bias_vec) {
-                        bv[j] = __ldg(reinterpret_cast<const uint4 *>(bq));
-                    } else {
-                        bv[j].x = uint32_t(bq[0]) | (uint32_t(bq[1]) << 16);
-                        bv[j].y = uint32_t(bq[2]) | (uint32_t(bq[3]) << 16);
-                        bv[j].z = uint32_t(bq[4]) | (uint32_t(bq[5]) << 16);
-                        bv[j].w = uint32_t(bq[6]) | (uint32_t(bq[7]) << 16);
-                    }
-                }
-            }
             const int ab = g % TC_NACC;
             const int slot = g % DEPTH;
             bool got = mbar_wait_bounded(bar_accf + 8 * ab, uint32_t(g / TC_NACC) & 1u, s_abort,
@@ -483,56 +470,85 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                                            deadline);
             if (__all_sync(0xffffffffu, got) == 0) break;
             tc_fence_after();
-            uint32_t va[32];
-            tmem_ld16x256b_x8_nowait(tmem + (uint32_t(q * 32 + h * 16) << 16) + uint32_t(ab * TC_BN),
-                                     va);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
             const int tok[2] = {qtok[0], qtok[1]};
-            // the next chunk opens a new tile or slice: its A operand now (the
-            // MMAs up to chunk g are done; that of chunk g + 1 waits for it)
-            k.next(p, nchunks);
-            if (w + 1 < w_end && k.first) {
-                tile_rows(k.tile);
-                convert_x(k.s);
-            }
-            // x B + old y + bias, rounded once, straight to y: output
-            // columns 16 * qt + 2j + e of the chunk are accumulator columns
-            // 8j + 2 * qt + e, registers va[4j + e] (row qrow) and
-            // va[4j + 2 + e] (row qrow + 8); one 32-byte store per row
-            uint16_t *ycol = p.y + p.col0[ks] + kc0 + qt * 16;
-            const uint32_t bw[8] = {bv[0].x, bv[0].y, bv[0].z, bv[0].w,
-                                    bv[1].x, bv[1].y, bv[1].z, bv[1].w};
-            const bool has_bias = bias_row != nullptr;
+            const uint8_t *yt = smem + C::RING_OFF + slot * C::SLOT_BYTES + C::B_BYTES;
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                if (cin && tok[u] >= 0) {
-                    uint32_t yw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                    if (p.add_inputs) {
-                        const int r = qrow + 8 * u;
-                        const uint8_t *yt = smem + C::RING_OFF + slot * C::SLOT_BYTES + C::B_BYTES;
-                        const uint4 y0 = *reinterpret_cast<const uint4 *>(yt + tc_y_off(r, 2 * qt));
-                        const uint4 y1 =
-                            *reinterpret_cast<const uint4 *>(yt + tc_y_off(r, 2 * qt + 1));
-                        yw[0] = y0.x; yw[1] = y0.y; yw[2] = y0.z; yw[3] = y0.w;
-                        yw[4] = y1.x; yw[5] = y1.y; yw[6] = y1.z; yw[7] = y1.w;
+            for (int hf = 0; hf < TC_HALVES; ++hf) {
+                uint32_t va[32];
+                tmem_ld16x256b_x8_nowait(tmem + (uint32_t(q * 32 + h * 16) << 16) +
+                                             uint32_t(ab * TC_BN + hf * 64),
+                                         va);
+                tmem_wait_ld();
+                if (hf == TC_HALVES - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
+                    // the next chunk opens a new tile or slice: its A operand
+                    // now (the MMAs up to chunk g are done; that of chunk g + 1
+                    // waits for it)
+                    k.next(p, nchunks);
+                    if (w + 1 < w_end && k.first) {
+                        tile_rows(k.tile);
+                        convert_x(k.s);
                     }
-                    uint32_t o[8];
+                }
+                // x B + old y + bias, rounded once, straight to y: output
+                // columns 64 hf + 16 qt + 2j + e of the chunk are accumulator
+                // columns 64 hf + 8j + 2 qt + e, registers va[4j + e] (row
+                // qrow) and va[4j + 2 + e] (row qrow + 8); one 32-byte store
+                // per row
+                const int cb = hf * 64 + qt * 16;
+                const bool cin = cb < ncols;
+                uint32_t bw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                const bool has_bias = bias_row != nullptr;
+                if (has_bias && cin) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float a0 = __uint_as_float(va[4 * j + 2 * u]);
-                        float a1 = __uint_as_float(va[4 * j + 2 * u + 1]);
-                        a0 += bf16_lo(yw[j]);
-                        a1 += bf16_hi(yw[j]);
-                        if (has_bias) {
-                            a0 += bf16_lo(bw[j]);
-                            a1 += bf16_hi(bw[j]);
+                    for (int j = 0; j < 2; ++j) {
+                        const uint16_t *bq = bias_row + cb + j * 8;
+                        uint4 v;
+                        if (p.bias_vec) {
+                            v = __ldg(reinterpret_cast<const uint4 *>(bq));
+                        } else {
+                            v.x = uint32_t(bq[0]) | (uint32_t(bq[1]) << 16);
+                            v.y = uint32_t(bq[2]) | (uint32_t(bq[3]) << 16);
+                            v.z = uint32_t(bq[4]) | (uint32_t(bq[5]) << 16);
+                            v.w = uint32_t(bq[6]) | (uint32_t(bq[7]) << 16);
                         }
-                        o[j] = pack_bf16x2(a0, a1);
+                        bw[4 * j] = v.x;
+                        bw[4 * j + 1] = v.y;
+                        bw[4 * j + 2] = v.z;
+                        bw[4 * j + 3] = v.w;
                     }
-                    st_global_v8(ycol + int64_t(tok[u]) * p.y_ld, o);
+                }
+                uint16_t *ycol = p.y + p.col0[ks] + kc0 + cb;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (cin && tok[u] >= 0) {
+                        uint32_t yw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                        if (p.add_inputs) {
+                            const int r = qrow + 8 * u;
+                            const uint4 y0 = *reinterpret_cast<const uint4 *>(
+                                yt + tc_y_off(r, hf * 8 + 2 * qt));
+                            const uint4 y1 = *reinterpret_cast<const uint4 *>(
+                                yt + tc_y_off(r, hf * 8 + 2 * qt + 1));
+                            yw[0] = y0.x; yw[1] = y0.y; yw[2] = y0.z; yw[3] = y0.w;
+                            yw[4] = y1.x; yw[5] = y1.y; yw[6] = y1.z; yw[7] = y1.w;
+                        }
+                        uint32_t o[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            float a0 = __uint_as_float(va[4 * j + 2 * u]);
+                            float a1 = __uint_as_float(va[4 * j + 2 * u + 1]);
+                            a0 += bf16_lo(yw[j]);
+                            a1 += bf16_hi(yw[j]);
+                            if (has_bias) {
+                                a0 += bf16_lo(bw[j]);
+                                a1 += bf16_hi(bw[j]);
+                            }
+                            o[j] = pack_bf16x2(a0, a1);
+                        }
+                        st_global_v8(ycol + int64_t(tok[u]) * p.y_ld, o);
+                    }
                 }
             }
             __syncwarp();
@@ -606,7 +622,7 @@ int launch_expand_tc(const ExpandLaunch &a, cudaStream_t stream)
     }
     for (int s = 0; s < a.num_slices; ++s)
         if (!encode_perm_rows_map(&p.bmap[s], a.b[s], uint64_t(a.max_loras) * uint64_t(a.n[s]),
-                                  uint32_t(a.rank), rp < 64 ? rp : 64u, sw))
+                                  uint32_t(a.rank), rp < 64 ? rp : 64u, uint32_t(TC_HALVES), sw))
             return int(cudaErrorInvalidValue);
     for (int s = a.num_slices; s < LORA_MAX_SLICES; ++s) p.bmap[s] = p.bmap[0];
     p.num_slices = a.num_slices;

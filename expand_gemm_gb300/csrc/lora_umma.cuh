@@ -324,11 +324,12 @@ bool encode_tile_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t co
                      CUtensorMapSwizzle swizzle);
 
 // Host: encodes the B map of the tensor-core expand over a bf16 matrix of
-// `rows` rows (a multiple of 64) of `rank` elements, whose 64-row boxes land
-// in shared memory with their rows permuted: shared row 8i + 2t + e holds
-// global row 16t + 2i + e (i < 8, t < 4, e < 2).  Box {box_k, 64 rows};
-// false if the driver entry point is missing or rejects it.
+// `rows` rows (a multiple of 64) of `rank` elements, whose boxes of
+// `blocks` 64-row blocks land in shared memory with the rows of each block
+// permuted: shared row 8i + 2t + e holds global row 16t + 2i + e (i < 8,
+// t < 4, e < 2).  Box {box_k, 64 * blocks rows}; false if the driver entry
+// point is missing or rejects it.
 bool encode_perm_rows_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t rank,
-                          uint32_t box_k, CUtensorMapSwizzle swizzle);
+                          uint32_t box_k, uint32_t blocks, CUtensorMapSwizzle swizzle);
 
 }  // namespace lora

@@ -202,7 +202,7 @@ int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidden,
  *
  * x is rounded to bf16 for the tensor cores (as the Triton kernel does when
  * it casts its input to the weight type); products accumulate in fp32
- * (tcgen05 with TMEM accumulators at rank >= 128 when y, y_ld and
+ * (tcgen05 with TMEM accumulators at rank >= 64 when y, y_ld and
  * offset_start are 32-byte aligned and every slice width is a multiple of
  * 64; mma.sync otherwise; LORA_PUNICA_EXPAND_TC* in the environment move
  * the boundary, and with LORA_PUNICA_EXPAND_TC=2 a call the tcgen05 path
