@@ -290,7 +290,12 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     } else if (warp == UM_MMA_WARP) {
         // ------------------------------------------------------ MMA issue
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc_bf16(UM_BM, RP);
+            // Consecutive slices share one UMMA of N = G * RP <= 256 (their
+            // A blocks and TMEM columns are adjacent): x is read from shared
+            // memory once per group instead of once per slice.
+            const int G = 256 / RP < S ? 256 / RP : S;
+            const uint32_t idesc_g = umma_idesc_bf16(UM_BM, G * RP);
+            const uint32_t idesc_r = umma_idesc_bf16(UM_BM, (S % G == 0 ? G : S % G) * RP);
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
@@ -312,9 +317,10 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
 #pragma unroll
                     for (int kk = 0; kk < UM_BK / 16; ++kk) {
                         const uint64_t adesc = umma_desc_sw128(sx + kk * 32);
-                        for (int s = 0; s < S; ++s) {
+                        for (int s = 0; s < S; s += G) {
                             const uint64_t bdesc = umma_desc_sw128(sx + L.x_bytes + s * L.a_bytes + kk * 32);
-                            umma_bf16(tmem + s * RP, adesc, bdesc, idesc, kb != kb0 || kk != 0);
+                            umma_bf16(tmem + s * RP, adesc, bdesc, s + G <= S ? idesc_g : idesc_r,
+                                      kb != kb0 || kk != 0);
                         }
                     }
                     umma_commit(bar_empty + 8 * stage);
