@@ -428,6 +428,7 @@ struct Knobs {
     int umma_min_tokens;      // LORA_PUNICA_UMMA_MIN_TOKENS (1024)
     int umma_min_cols;        // LORA_PUNICA_UMMA_MIN_COLS (256)
     int umma_partial;         // LORA_PUNICA_UMMA_PARTIAL (1)
+    int umma_pair;            // LORA_PUNICA_UMMA_PAIR: CTA-pair (M = 256) tensor-core shrink
     int early_shrink_ctas;    // LORA_PUNICA_EARLY_SHRINK_CTAS (2)
     int expand_tc;            // LORA_PUNICA_EXPAND_TC: tcgen05 expand (0 off, -1 ranks >= min, 1 where it fits, 2 required)
     int expand_tc_min_rank;   // LORA_PUNICA_EXPAND_TC_MIN_RANK (64)
@@ -462,6 +463,7 @@ struct ShrinkLaunch {
     int32_t partial;      // the tensor-core path takes partial tiles too
 };
 int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream);
+int launch_shrink_pair(const ShrinkLaunch &a, cudaStream_t stream);
 int shrink_self_meta(const int32_t *map, const lora_bf16_t *x, int32_t num_tokens,
                      int32_t hidden, int64_t x_ld, const lora_bf16_t *const *lora_a,
                      int32_t num_slices, int32_t rank, float *y, const lora_meta_t *meta,

@@ -6,7 +6,7 @@
 //
 // One CTA per SM, persistent over (tile, hidden chunk) items: the hidden
 // dimension is split when there are too few whole tiles to fill the GPU
-// (see umma_kchunks).  Warp-specialised:
+// (see shrink_kchunks).  Warp-specialised:
 //   warp 0      x producer: per 64-wide hidden block, the tile's 128 x rows
 //               arrive by 2-D TMA: the tile's tokens (increasing, as the
 //               sort is stable) are cut into runs of consecutive tokens and
@@ -79,28 +79,6 @@ struct UmmaLayout {
     int x_bytes, a_bytes, stage_bytes, ring_bytes, bar_off, misc_off, piece_off, tab_off, total;
 };
 
-// Split of the hidden dimension: the number of chunks (items per tile)
-// that minimises rounds x chunk length (+ a fixed cost of about two blocks
-// per item for the pipeline fill and the epilogue), with chunks of at least
-// UM_MIN_BLOCKS blocks.  Every CTA computes the same value.
-__device__ __forceinline__ int umma_kchunks(int tiles, int nk, int grid)
-{
-    // 32-bit arithmetic: tiles * 16 and nk are far below 2^31 (T < 2^21).
-    int best = 1;
-    int best_cost = ((tiles + grid - 1) / grid) * (nk + 2);
-    for (int kc = 2; kc <= 16 && nk / kc >= UM_MIN_BLOCKS; ++kc) {
-        const int spc = (nk + kc - 1) / kc;
-        const int kce = (nk + spc - 1) / spc;
-        const int rounds = (tiles * kce + grid - 1) / grid;
-        const int cost = rounds * (spc + 2);
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = kce;
-        }
-    }
-    return best;
-}
-
 __host__ __device__ inline UmmaLayout umma_layout(int S, int rp, int stages, int nbins)
 {
     UmmaLayout l;
@@ -162,7 +140,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     if (total_tiles == 0) return;
     const int H = p.hidden, R = p.rank, T = p.num_tokens;
     const int nk = (H + UM_BK - 1) / UM_BK;
-    const int kchunks = umma_kchunks(total_tiles, nk, int(gridDim.x));
+    const int kchunks = shrink_kchunks(total_tiles, nk, int(gridDim.x), UM_MIN_BLOCKS);
     const int spc = (nk + kchunks - 1) / kchunks;
     const bool split = kchunks > 1;
     const int total_items = total_tiles * kchunks;      // item = kc * total_tiles + tile
@@ -404,6 +382,11 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
 // or a negative value / cudaError_t on failure.
 int launch_shrink_umma(const ShrinkLaunch &a, cudaStream_t stream)
 {
+    // The CTA-pair kernel (lora_shrink_pair.cu) is opt-in: measured slower.
+    if (knobs().umma_pair != 0) {
+        const int r = launch_shrink_pair(a, stream);
+        if (r != 0) return r;
+    }
     int rp = 16;
     while (rp < a.rank) rp <<= 1;
     const int S = a.num_slices;

@@ -82,6 +82,103 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
     return true;
 }
 
+// ---------------------------------------------------------------- CTA pairs
+// A cluster of two CTAs on neighbouring SMs driving one tcgen05 MMA with
+// M = 256 (cta_group::2): each CTA holds half of A's rows and half of B's
+// rows in its own shared memory and its 128 rows of D in its own TMEM.
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of `smem_addr` (a local shared address) in
+// CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+
+// Arrive (release, cluster scope) on an mbarrier of another CTA of the
+// cluster, given its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n"
+                 :: "r"(cluster_addr) : "memory");
+}
+
+// Every thread of every CTA of the cluster; memory operations before it are
+// visible to every thread after it.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// TMEM allocation shared by the CTA pair: one warp of each CTA executes it.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n"
+                 :: "r"(dst_smem), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n"
+                 :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem, both CTAs] (+)= A[smem desc, both CTAs] * B[smem desc, both CTAs]^T
+// with M = 256: issued by one thread of the even CTA of the pair.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Arrive on the mbarrier at shared::cluster address `bar` (this CTA's or
+// its peer's) once every pair UMMA issued so far by this thread has
+// completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+                 :: "r"(bar) : "memory");
+}
+
+// ---------------------------------------------------------------- shrink work split
+
+// Split of the hidden dimension of the tensor-core shrinks: the number of
+// chunks (items per tile) that minimises rounds x chunk length (+ a fixed
+// cost of about two blocks per item for the pipeline fill and the
+// epilogue), with chunks of at least `min_blocks` blocks, for `grid`
+// workers.  Every CTA computes the same value.
+__device__ __forceinline__ int shrink_kchunks(int tiles, int nk, int grid, int min_blocks)
+{
+    // 32-bit arithmetic: tiles * 16 and nk are far below 2^31 (T < 2^21).
+    int best = 1;
+    int best_cost = ((tiles + grid - 1) / grid) * (nk + 2);
+    for (int kc = 2; kc <= 16 && nk / kc >= min_blocks; ++kc) {
+        const int spc = (nk + kc - 1) / kc;
+        const int kce = (nk + spc - 1) / spc;
+        const int rounds = (tiles * kce + grid - 1) / grid;
+        const int cost = rounds * (spc + 2);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = kce;
+        }
+    }
+    return best;
+}
+
 // ---------------------------------------------------------------- 256-bit store
 
 // One 32-byte global store (the address must be 32-byte aligned).
@@ -91,6 +188,35 @@ __device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t (&v)[8])
                  :: "l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
                     "r"(v[6]), "r"(v[7])
                  : "memory");
+}
+
+// As mbar_try_wait / mbar_wait_bounded, with cluster-scope acquire: for
+// barriers that threads or tensor cores of another CTA of the cluster
+// arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                          volatile int *abort, long long deadline)
+{
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((i & 63) == 63) {
+            if (*abort) return false;
+            if (clock64() > deadline) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
 }
 
 // ---------------------------------------------------------------- TMA

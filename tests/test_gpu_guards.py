@@ -84,7 +84,10 @@ PATHS = [pytest.param(dict(LORA_PUNICA_COOP=1, LORA_PUNICA_FUSED=0), id="coop"),
                       id="three_kernels"),
          pytest.param(dict(LORA_PUNICA_COOP=0, LORA_PUNICA_FUSED=0, LORA_PUNICA_UMMA_MIN_TOKENS=0,
                            LORA_PUNICA_UMMA_MIN_COLS=0, LORA_PUNICA_EXPAND_TC=2),
-                      id="tensor_core_kernels")]
+                      id="tensor_core_kernels"),
+         pytest.param(dict(LORA_PUNICA_COOP=0, LORA_PUNICA_FUSED=0, LORA_PUNICA_UMMA_MIN_TOKENS=0,
+                           LORA_PUNICA_UMMA_MIN_COLS=0, LORA_PUNICA_UMMA_PAIR=1),
+                      id="cta_pair_shrink")]
 
 
 @pytest.mark.parametrize("path", PATHS)

@@ -94,14 +94,17 @@ def test_shrink_shapes(oracle_mod, T, H, r, L, S):
     (1500, 192, 128, 3, 3),     # rank 128, three slices: 384 TMEM columns
     (1100, 128, 24, 2, 2),      # padded rank 24 -> 32
 ])
-@pytest.mark.parametrize("umma,partial", [("0", "1"), ("1", "1"), ("1", "0")])
-def test_shrink_long_segments(oracle_mod, knob, umma, partial, T, H, r, L, S):
+@pytest.mark.parametrize("umma,partial,pair", [("0", "1", "0"), ("1", "1", "0"), ("1", "0", "0"),
+                                               ("1", "1", "1")])
+def test_shrink_long_segments(oracle_mod, knob, umma, partial, pair, T, H, r, L, S):
     """Long sequences per LoRA: with the tensor-core path forced on it takes
     every tile, the partial last tile of each segment included (partial=1),
     or the whole 128-token tiles with the remainders on mma.sync
-    (partial=0); with it off, mma.sync covers everything."""
+    (partial=0); with it off, mma.sync covers everything.  pair=1 runs the
+    CTA-pair kernel (256-token tiles, M = 256) where the padded rank is 64
+    or 128, the single-CTA kernel elsewhere."""
     knob(LORA_PUNICA_UMMA=umma, LORA_PUNICA_UMMA_PARTIAL=partial, LORA_PUNICA_UMMA_MIN_COLS=0,
-         LORA_PUNICA_UMMA_MIN_TOKENS=0)
+         LORA_PUNICA_UMMA_MIN_TOKENS=0, LORA_PUNICA_UMMA_PAIR=pair)
     w = W.Workload("long", T + r, T, H, r, L, tuple([16] * S), "zipf_seq", p_none=0.1,
                    seq_len=(200, 900), scale=0.75)
     inp = W.generate(w)
