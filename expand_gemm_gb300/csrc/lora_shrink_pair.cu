@@ -20,7 +20,7 @@
 // 1700 cycles to issue one stage's eight UMMAs, against 1050), and the
 // relay of each odd-CTA stage to the even CTA (a cluster-scope release
 // arrive) at about 1300 cycles; the hidden split that balances 256-token
-// tiles over 76 pairs also multiplies the epilogue's atomics.
+// tiles over 76 pairs also multiplies the epilogues.
 //
 // Slices are grouped as in the single-CTA kernel: a group of G consecutive
 // slices is one UMMA of N = G * RP.  In the M = 256 form each CTA holds N/2
@@ -40,8 +40,8 @@
 //               In the odd CTA lane 0 relays "stage landed" to the even CTA.
 //   warps 2..5  epilogue: tcgen05.ld of the CTA's own 128 TMEM lanes (one
 //               token row per thread), buf += scale * acc (float4
-//               read-modify-writes, or atomics when the hidden dimension is
-//               split); then they release the accumulators to the even CTA.
+//               reductions); then they release the accumulators to the even
+//               CTA.
 //
 // Every mbarrier wait is bounded (about one second); on expiry a CTA sets
 // bit 30 of the metadata error word, stops issuing, waits (bounded) for its
@@ -166,7 +166,6 @@ __global__ void __launch_bounds__(PR_THREADS, 1) shrink_pair_kernel(const __grid
     const int nk = (H + PR_BK - 1) / PR_BK;
     const int kchunks = shrink_kchunks(total_tiles, nk, nclusters, PR_MIN_BLOCKS);
     const int spc = (nk + kchunks - 1) / kchunks;
-    const bool split = kchunks > 1;
     const int total_items = total_tiles * kchunks;      // item = kc * total_tiles + tile
     if (cluster >= total_items) return;
 
@@ -403,31 +402,8 @@ __global__ void __launch_bounds__(PR_THREADS, 1) shrink_pair_kernel(const __grid
             const bool got = mbar_wait_bounded_cluster(bar_acc_full, acc_phase, s_abort, deadline);
             if (__all_sync(0xffffffffu, got) == 0) break;       // warp-uniform exit
             tc_fence_after();
-            for (int s = 0; s < p.num_slices; ++s) {
-                float *dst = p.y + (int64_t(s) * T + max(tok, 0)) * R;
-                for (int c = 0; c < RP; c += 16) {
-                    float v[16];
-                    tmem_ld16(tmem + (uint32_t(q * 32) << 16) + uint32_t(s * RP + c), v);
-#pragma unroll
-                    for (int jj = 0; jj < 16; jj += 4) {
-                        if (tok >= 0 && c + jj < R) {
-                            float4 *d4 = reinterpret_cast<float4 *>(dst + c + jj);
-                            const float4 a = make_float4(p.scale * v[jj], p.scale * v[jj + 1],
-                                                         p.scale * v[jj + 2], p.scale * v[jj + 3]);
-                            if (split) {
-                                atomicAdd(d4, a);
-                            } else {
-                                float4 o = *d4;
-                                o.x += a.x;
-                                o.y += a.y;
-                                o.z += a.z;
-                                o.w += a.w;
-                                *d4 = o;
-                            }
-                        }
-                    }
-                }
-            }
+            shrink_epilogue_row(tmem + (uint32_t(q * 32) << 16), p.y, tok, T, R, RP,
+                                p.num_slices, p.scale);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acce_leader);

@@ -27,8 +27,8 @@
 //               a tile, to hand the accumulators to the epilogue.
 //   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (one token row
 //               per thread), buf[s][t, :] += scale * acc with float4
-//               read-modify-writes, or float4 atomic adds when the tile's
-//               hidden dimension is split over several CTAs.
+//               reductions (red.global.add; see shrink_epilogue_row), also
+//               when the tile's hidden dimension is split over several CTAs.
 // x is read once per tile for all slices; the A block of a LoRA is shared in
 // L2 by the CTAs working on tiles of the same segment.
 //
@@ -142,7 +142,6 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     const int nk = (H + UM_BK - 1) / UM_BK;
     const int kchunks = shrink_kchunks(total_tiles, nk, int(gridDim.x), UM_MIN_BLOCKS);
     const int spc = (nk + kchunks - 1) / kchunks;
-    const bool split = kchunks > 1;
     const int total_items = total_tiles * kchunks;      // item = kc * total_tiles + tile
     if (int(blockIdx.x) >= total_items) return;
 
@@ -171,7 +170,6 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
             const int tile = item % total_tiles, kc = item / total_tiles;
             const int kb0 = kc * spc, kb1 = min(nk, kb0 + spc);
             const int seg = find_segment(tab.tile, p.nbins, tile);
-            const int id = tab.id[seg];
             const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * UM_BM;
             // rows of this tile that belong to the segment (all 128 but in
             // the last, partial tile of a segment); only they are loaded, and
@@ -335,31 +333,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
             bool got = mbar_wait_bounded(bar_acc_full, acc_phase, s_abort, deadline);
             if (__all_sync(0xffffffffu, got) == 0) break;       // warp-uniform exit
             tc_fence_after();
-            for (int s = 0; s < S; ++s) {
-                float *dst = p.y + (int64_t(s) * T + max(tok, 0)) * R;
-                for (int c = 0; c < RP; c += 16) {
-                    float v[16];
-                    tmem_ld16(tmem + (uint32_t(q * 32) << 16) + uint32_t(s * RP + c), v);
-#pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        if (tok >= 0 && c + j < R) {
-                            float4 *d4 = reinterpret_cast<float4 *>(dst + c + j);
-                            const float4 a = make_float4(p.scale * v[j], p.scale * v[j + 1],
-                                                         p.scale * v[j + 2], p.scale * v[j + 3]);
-                            if (split) {
-                                atomicAdd(d4, a);
-                            } else {
-                                float4 o = *d4;
-                                o.x += a.x;
-                                o.y += a.y;
-                                o.z += a.z;
-                                o.w += a.w;
-                                *d4 = o;
-                            }
-                        }
-                    }
-                }
-            }
+            shrink_epilogue_row(tmem + (uint32_t(q * 32) << 16), p.y, tok, T, R, RP,
+                                S, p.scale);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_acc_empty);

@@ -442,6 +442,62 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n)
          | (uint32_t(m >> 4) << 24);         // M / 16            [24, 29)
 }
 
+// ---------------------------------------------------------------- shrink epilogue
+
+// 16 consecutive fp32 columns of this thread's TMEM lane, without waiting.
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// buf[s][tok, :] += scale * acc for this thread's TMEM lane `tlane` (the
+// accumulator of slice s at columns s * RP ...), 64 columns at a time with
+// four TMEM loads in flight, added with float4 reductions (red.global.add):
+// nothing is read back into the SM, so no load latency is exposed, and an
+// element with one owner gets exactly old + scale * acc, as with a plain
+// read-modify-write.  tok < 0: nothing is written (the TMEM loads still
+// run: they are warp-wide).
+__device__ __forceinline__ void shrink_epilogue_row(uint32_t tlane, float *y, int tok, int T,
+                                                    int R, int RP, int S, float scale)
+{
+    const int per_slice = RP / 16;
+    const int nch = S * per_slice;
+    for (int k0 = 0; k0 < nch; k0 += 4) {
+        uint32_t v[4][16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = k0 + j;                  // warp-uniform
+            if (k < nch)
+                tmem_ld16_nowait(tlane + uint32_t((k / per_slice) * RP + (k % per_slice) * 16),
+                                 v[j]);
+        }
+        tmem_wait_ld();
+        if (tok < 0) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = k0 + j;
+            if (k >= nch) continue;
+            const int s = k / per_slice, c = (k % per_slice) * 16;
+            float *dst = y + (int64_t(s) * T + tok) * R + c;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (c + 4 * q >= R) continue;
+                atomicAdd(reinterpret_cast<float4 *>(dst + 4 * q),
+                          make_float4(scale * __uint_as_float(v[j][4 * q]),
+                                      scale * __uint_as_float(v[j][4 * q + 1]),
+                                      scale * __uint_as_float(v[j][4 * q + 2]),
+                                      scale * __uint_as_float(v[j][4 * q + 3])));
+            }
+        }
+    }
+}
+
 // Host: encodes a 2-D bf16 tensor map over `rows` rows of `cols` elements
 // (row stride in elements) with box {box_cols, box_rows} and the given
 // swizzle; false if the driver entry point is missing or rejects it.
