@@ -14,8 +14,8 @@
 //   2. shrink: (64-token tile, slice, hidden chunk) items spread over all
 //      CTAs; mma.sync with the r rows of A as M and the tile's tokens as N,
 //      through a 4-stage cp.async ring; the partial sums are added into the
-//      fp32 buffer with float4 atomics (a plain read-modify-write when the
-//      hidden dimension is not split);
+//      fp32 buffer with float4 reductions (red.global.add, also when the
+//      hidden dimension is not split: no load latency);
 //   3. each CTA announces its arrival at a grid-wide barrier, starts the
 //      copies of y, B and bias for its first expand chunks, then waits for
 //      every other arrival;
@@ -162,7 +162,7 @@ __device__ __forceinline__ void coop_shrink(const CoopArgs &p, SegTab tab, const
     const int pairs = total_tiles * S; int kchunks = 1;
     if (pairs < int(gridDim.x)) kchunks = max(1, min(int(gridDim.x) / pairs, max(1, nk / CO_MIN_STEPS)));
     const int spc = (nk + kchunks - 1) / kchunks; kchunks = (nk + spc - 1) / spc;
-    const bool split = kchunks > 1; const int total_items = pairs * kchunks;
+    const int total_items = pairs * kchunks;
     const uint32_t ring = smem_addr(smem); const int xc = tid & 7, xr = tid >> 3;
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
         const int s = item % S, rest = item / S, tile = rest % total_tiles, kc = rest / total_tiles;
@@ -215,7 +215,7 @@ __device__ __forceinline__ void coop_shrink(const CoopArgs &p, SegTab tab, const
             const int t = i / r4n, c4 = i - t * r4n; const int tok = s_tok[t]; if (tok < 0) continue;
             const float4 v = *reinterpret_cast<const float4 *>(&stage[t * Cfg::OUT_LD + 4 * c4]);
             float4 *dst = reinterpret_cast<float4 *>(p.buf + (int64_t(s) * T + tok) * R) + c4;
-            if (split) atomicAdd(dst, v); else { float4 o = __ldcg(dst); o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w; *dst = o; }
+            atomicAdd(dst, v);                // a reduction: no load latency
         }
     }
     __syncthreads();

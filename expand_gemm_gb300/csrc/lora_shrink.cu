@@ -12,9 +12,10 @@
 // The grid is persistent (SMs x resident CTAs); every CTA rebuilds the
 // segment -> tile table from the metadata and walks items with a grid
 // stride, so nothing is read back to the host.  When there are fewer
-// (tile, slice) pairs than CTAs the hidden dimension is split into chunks
-// and partial sums are added to y with float4 atomics; otherwise each
-// element has one owner and is updated with a plain read-modify-write.
+// (tile, slice) pairs than CTAs the hidden dimension is split into chunks.
+// Results are added to y with float4 reductions (red.global.add) in both
+// cases: without a split each element has one owner, and the reduction
+// adds exactly what a read-modify-write would.
 #include "lora_common.cuh"
 
 namespace lora {
@@ -160,7 +161,6 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
     }
     const int steps_per_chunk = (nk + kchunks - 1) / kchunks;
     kchunks = (nk + steps_per_chunk - 1) / steps_per_chunk;
-    const bool split = kchunks > 1;
     const int total_items = pairs * kchunks;
 
     const uint32_t ring = smem_addr(smem);
@@ -285,13 +285,10 @@ __global__ void __launch_bounds__(SH_THREADS) shrink_kernel(ShrinkArgs p)
             if (tok < 0) continue;
             const float4 v = *reinterpret_cast<const float4 *>(&stage[t * Cfg::OUT_LD + 4 * c4]);
             float4 *dst = reinterpret_cast<float4 *>(p.y + (int64_t(s) * T + tok) * R) + c4;
-            if (split) {
-                atomicAdd(dst, v);
-            } else {
-                float4 o = *dst;
-                o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
-                *dst = o;
-            }
+            // a reduction (red.global.add), nothing read back: with one
+            // owner per element (no split) it adds exactly what a
+            // read-modify-write would, without the load's latency
+            atomicAdd(dst, v);
         }
         __syncthreads();
     }
