@@ -51,10 +51,10 @@ E2E_GRAPH_STEPS = 8
 # hash of the kernel's sources the capture was taken on; a stale hash
 # reports null.
 NCU_TRAFFIC = {
-    # expand_kernel<8> and shrink_umma_kernel, one launch each at full size
+    # expand_tc_kernel<8> and shrink_umma_kernel, one launch each at full size
     # (profiles/traffic_large.md)
-    ("expand", "large"): ("5738bd39dcb618e0", 690987008),
-    ("shrink", "large"): ("2a03b371f531c0b1", 448630272),
+    ("expand", "large"): ("4b5468283bf9b3bf", 667451904),
+    ("shrink", "large"): ("3bd232621c2f634c", 448609280),
 }
 
 # The source files each reported kernel is built from.
