@@ -42,6 +42,7 @@ static Knobs read_knobs()
     k.umma_min_cols = env_int("LORA_PUNICA_UMMA_MIN_COLS", 256);
     k.umma_partial = env_int("LORA_PUNICA_UMMA_PARTIAL", 1);
     k.umma_pair = env_int("LORA_PUNICA_UMMA_PAIR", 0);
+    k.nvtx = env_int("LORA_PUNICA_NVTX", 1);
     k.early_shrink_ctas = env_int("LORA_PUNICA_EARLY_SHRINK_CTAS", 2);
     k.expand_tc = env_int("LORA_PUNICA_EXPAND_TC", -1);
     k.expand_tc_min_rank = env_int("LORA_PUNICA_EXPAND_TC_MIN_RANK", 64);

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "lora_punica.h"
@@ -429,6 +430,7 @@ struct Knobs {
     int umma_min_cols;        // LORA_PUNICA_UMMA_MIN_COLS (256)
     int umma_partial;         // LORA_PUNICA_UMMA_PARTIAL (1)
     int umma_pair;            // LORA_PUNICA_UMMA_PAIR: CTA-pair (M = 256) tensor-core shrink
+    int nvtx;                 // LORA_PUNICA_NVTX: NVTX ranges around the C-ABI calls (1)
     int early_shrink_ctas;    // LORA_PUNICA_EARLY_SHRINK_CTAS (2)
     int expand_tc;            // LORA_PUNICA_EXPAND_TC: tcgen05 expand (0 off, -1 ranks >= min, 1 where it fits, 2 required)
     int expand_tc_min_rank;   // LORA_PUNICA_EXPAND_TC_MIN_RANK (64)
@@ -440,6 +442,23 @@ struct Knobs {
 const Knobs &knobs();
 inline bool pdl_enabled() { return knobs().pdl != 0; }
 inline int knob_expand_tc() { return knobs().expand_tc; }
+
+// An NVTX range around one C-ABI call, so that a profiler's timeline shows
+// the library's calls (LORA_PUNICA_NVTX=0 turns them off; without a tool
+// attached a push and a pop cost a few nanoseconds).
+struct NvtxRange {
+    bool on;
+    explicit NvtxRange(const char *name) : on(knobs().nvtx != 0)
+    {
+        if (on) nvtxRangePushA(name);
+    }
+    ~NvtxRange()
+    {
+        if (on) nvtxRangePop();
+    }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 inline int knob_expand_tc_min_rank() { return knobs().expand_tc_min_rank; }
 
 // Host-side description of one lora_shrink call, shared by its two paths.

@@ -135,6 +135,7 @@ LORA_API int lora_expand(const float *x, const lora_bf16_t *const *lora_b,
                          int32_t offset_start, int32_t add_inputs,
                          const lora_meta_t *meta, void *stream)
 {
+    lora::NvtxRange nvtx_range("lora_expand");
     return lora::lora_expand_impl(x, 0, lora_b, lora_bias, slice_sizes, num_slices, rank, y,
                                   y_ld, num_tokens, offset_start, add_inputs, meta,
                                   static_cast<cudaStream_t>(stream), 0);
@@ -150,6 +151,7 @@ LORA_API int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lo
                               int32_t offset_start, int32_t add_inputs,
                               const lora_meta_t *meta, void *stream)
 {
+    lora::NvtxRange nvtx_range("lora_expand_bf16");
     return lora::lora_expand_impl(x, 1, lora_b, lora_bias, slice_sizes, num_slices, rank, y,
                                   y_ld, num_tokens, offset_start, add_inputs, meta,
                                   static_cast<cudaStream_t>(stream), 0);

@@ -666,6 +666,7 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
                          int32_t num_slices, int32_t rank, float scale, float *buf,
                          lora_bf16_t *y, int64_t y_ld, const lora_meta_t *meta, void *stream)
 {
+    lora::NvtxRange nvtx_range("lora_linear");
     if (meta == nullptr || lora_a == nullptr || lora_b == nullptr || slice_sizes == nullptr)
         return LORA_ERR_NULL;
     if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SLICES;

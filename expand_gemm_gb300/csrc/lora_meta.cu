@@ -8,9 +8,10 @@
 //   - meta_prepare_kernel: one CTA, the id map staged in shared memory;
 //     batches of up to META_MULTI_MIN tokens.
 //   - meta_multi_kernel: one CTA per run of META_MULTI_CHUNK tokens.  Every
-//     CTA counts the whole map itself (one coalesced load and one vote per
-//     32 tokens; the map is read from L2), keeping apart the tokens before
-//     its run, those of its run (per warp) and those after it.  That gives
+//     CTA counts the whole map itself (its run one 32-token group per warp,
+//     the rest 128 tokens per 16-byte warp load with one vote; the map is
+//     read from L2), keeping apart the tokens before its run, those of its
+//     run (per warp) and those after it.  That gives
 //     it the bin totals and its own start inside every bin without any
 //     exchange between CTAs, and it scatters the tokens of its run.
 //
@@ -245,7 +246,6 @@ __global__ void __launch_bounds__(NT) meta_multi_kernel(MetaArgs a)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.num_tokens, cta = int(blockIdx.x);
     const int g_run = cta * NW;                 // first 32-token group of the run
-    const int ngroups = (T + 31) / 32;
 
     pdl_wait();
     pdl_launch_dependents();
@@ -254,28 +254,65 @@ __global__ void __launch_bounds__(NT) meta_multi_kernel(MetaArgs a)
     if (tid == 0) s_invalid = 0;
     __syncthreads();
 
-    // Pass 1 over the whole map: the run's group of this warp into own[warp],
-    // every other group into bef or aft (groups dealt round-robin to warps).
-    // Sixteen groups' ids are loaded at once so their latencies overlap.
-    constexpr int U = 16;
+    // Pass 1.  The CTA's own run: warp w counts the run's 32-token group w
+    // into own[w] (pass 2 needs the per-warp offsets).  The rest of the map
+    // only needs its totals before and after the run: it is read in blocks
+    // of 128 tokens, four ids per lane from one 16-byte load, four blocks
+    // per warp at a time so that their latencies overlap, and a block whose
+    // ids all fall in one bin (runs of one sequence, the all -1 batch) takes
+    // a single add.
     int bad = 0;
-    for (int g0 = warp; g0 < ngroups; g0 += NW * U) {
-        int32_t idv[U];
+    {
+        const int gi = g_run + warp;
+        const int t = gi * 32 + lane;
+        const bool has = t < T;
+        const int b = has ? token_bin(a.map[t], a.max_loras, bad) : -1;
+        count_group(own + warp * nb, b, has, lane);
+    }
+    const bool vec = (reinterpret_cast<uintptr_t>(a.map) & 15u) == 0;
+    const int nblk = (T + 127) / 128, rb0 = cta * (NW / 4), rb1 = rb0 + NW / 4;
+    constexpr int UB = 4;
+    for (int k0 = warp; k0 < nblk; k0 += NW * UB) {
+        int4 v[UB];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int t = (g0 + u * NW) * 32 + lane;
-            idv[u] = (t < T) ? a.map[t] : -1;
+        for (int u = 0; u < UB; ++u) {
+            const int k = k0 + u * NW, t0 = k * 128 + lane * 4;
+            v[u] = make_int4(-1, -1, -1, -1);
+            if (k < nblk && (k < rb0 || k >= rb1)) {
+                if (vec && t0 + 3 < T) {
+                    v[u] = *reinterpret_cast<const int4 *>(a.map + t0);
+                } else {
+                    if (t0 < T) v[u].x = a.map[t0];
+                    if (t0 + 1 < T) v[u].y = a.map[t0 + 1];
+                    if (t0 + 2 < T) v[u].z = a.map[t0 + 2];
+                    if (t0 + 3 < T) v[u].w = a.map[t0 + 3];
+                }
+            }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int gi = g0 + u * NW;             // the same in every lane
-            if (gi >= ngroups) break;
-            const int t = gi * 32 + lane;
-            const bool has = t < T;
-            const int b = has ? token_bin(idv[u], a.max_loras, bad) : -1;
-            int32_t *dst = (gi < g_run) ? bef : (gi >= g_run + NW) ? aft
-                                                                   : own + (gi - g_run) * nb;
-            count_group(dst, b, has, lane);
+        for (int u = 0; u < UB; ++u) {
+            const int k = k0 + u * NW, t0 = k * 128 + lane * 4;     // k: the same in every lane
+            if (k >= nblk) break;
+            if (k >= rb0 && k < rb1) continue;                       // the run: counted above
+            int32_t *dst = k < rb0 ? bef : aft;
+            const int ids[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            int bs[4];
+            bool all_in = true;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool has = t0 + j < T;
+                bs[j] = has ? token_bin(ids[j], a.max_loras, bad) : -1;
+                all_in = all_in && has;
+            }
+            const int b0 = __shfl_sync(0xffffffffu, bs[0], 0);
+            const bool same = all_in && bs[0] == b0 && bs[1] == b0 && bs[2] == b0 && bs[3] == b0;
+            if (__all_sync(0xffffffffu, same)) {
+                if (lane == 0) atomicAdd(&dst[b0], 128);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (bs[j] >= 0) atomicAdd(&dst[bs[j]], 1);
+            }
         }
     }
 #pragma unroll
@@ -294,28 +331,29 @@ __global__ void __launch_bounds__(NT) meta_multi_kernel(MetaArgs a)
     }
     __syncthreads();
     // Exclusive scans over bins: first sorted slot, rank among the non-empty
-    // bins (torch.unique(sorted=True) order).
+    // bins (torch.unique(sorted=True) order).  Both run in one shuffle scan
+    // of a packed value: the token count in the low 21 bits (T < 2^21), the
+    // non-empty-bin count above it (at most 257 < 2^11).
     if (warp == 0) {
-        int carry_t = 0, carry_p = 0;
+        uint32_t carry = 0;
         for (int b0 = 0; b0 < nb; b0 += 32) {
             const int b = b0 + lane;
-            const int v = (b < nb) ? tot[b] : 0;
-            const int f = v > 0 ? 1 : 0;
-            int iv = v, jf = f;
+            const uint32_t v = (b < nb) ? uint32_t(tot[b]) : 0u;
+            const uint32_t pv = v | ((v > 0 ? 1u : 0u) << 21);
+            uint32_t incl = pv;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, iv, o);
-                const int w = __shfl_up_sync(0xffffffffu, jf, o);
-                if (lane >= o) { iv += u; jf += w; }
+                const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
             }
+            const uint32_t excl = carry + incl - pv;
             if (b < nb) {
-                base[b] = carry_t + iv - v;
-                pos[b] = carry_p + jf - f;
+                base[b] = int(excl & 0x1FFFFFu);
+                pos[b] = int(excl >> 21);
             }
-            carry_t += __shfl_sync(0xffffffffu, iv, 31);
-            carry_p += __shfl_sync(0xffffffffu, jf, 31);
+            carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (lane == 0) s_nactive = carry_p;
+        if (lane == 0) s_nactive = int(carry >> 21);
     }
     __syncthreads();
 
@@ -392,7 +430,8 @@ int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
     }
     // Batches above META_MULTI_MIN tokens on one CTA per 1024 tokens
     // (LORA_PUNICA_META_MULTI=0 turns it off).
-    if (a.num_tokens > META_MULTI_MIN && knobs().meta_multi) {
+    // (the multi-CTA kernel's bin scan packs token counts into 21 bits)
+    if (a.num_tokens > META_MULTI_MIN && a.num_tokens < (1 << 21) && knobs().meta_multi) {
         const int grid = (a.num_tokens + META_MULTI_CHUNK - 1) / META_MULTI_CHUNK;
         return int(launch_kernel(meta_multi_kernel<META_MULTI_THREADS>, dim3(grid),
                                  dim3(META_MULTI_THREADS), meta_multi_smem_bytes(a.max_loras),
@@ -415,6 +454,7 @@ int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
 LORA_API int lora_meta_prepare(const int32_t *token_lora_mapping, int32_t num_tokens,
                                const lora_meta_t *meta, void *stream)
 {
+    lora::NvtxRange nvtx_range("lora_meta_prepare");
     if (meta == nullptr) return LORA_ERR_NULL;
     if (!meta->token_lora_mapping || !meta->token_indices_sorted_by_lora_ids ||
         !meta->num_tokens_per_lora || !meta->lora_token_start_loc ||

@@ -42,6 +42,7 @@ LORA_API int lora_linear_noalloc(const int32_t *token_lora_mapping, int32_t num_
                                  float scale, lora_bf16_t *y, int64_t y_ld,
                                  const lora_meta_t *meta, void *stream)
 {
+    lora::NvtxRange nvtx_range("lora_linear_noalloc");
     if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SLICES;
     if (rank < 8 || rank > LORA_MAX_RANK || rank % 8 != 0) return LORA_ERR_RANK;
     if (num_tokens < 0) return LORA_ERR_SIZE;

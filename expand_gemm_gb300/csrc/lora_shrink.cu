@@ -336,6 +336,7 @@ LORA_API int lora_shrink(const lora_bf16_t *x, int32_t num_tokens, int32_t hidde
                          int32_t num_slices, int32_t rank, float *y,
                          const lora_meta_t *meta, float scale, void *stream)
 {
+    lora::NvtxRange nvtx_range("lora_shrink");
     if (meta == nullptr || lora_a == nullptr) return LORA_ERR_NULL;
     if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SLICES;
     if (rank < 8 || rank > LORA_MAX_RANK || rank % 8 != 0) return LORA_ERR_RANK;
