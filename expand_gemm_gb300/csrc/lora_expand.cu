@@ -255,10 +255,10 @@ int expand_dispatch(ExpandArgs &p, const lora_meta_t *meta, cudaStream_t st)
     // 32-byte-aligned outputs and slice widths that are multiples of 64.  By
     // default (LORA_PUNICA_EXPAND_TC=-1) it takes ranks of at least
     // LORA_PUNICA_EXPAND_TC_MIN_RANK (64): measured, large (rank 128, 16384
-    // tokens) 132 against 216 us for the mma.sync kernel, prefill (rank 64)
-    // 33.1 against 34.5 us; at lower ranks, with short segments, the
-    // mma.sync kernel's 64-token tiles win (MLP, rank 32: 39.8 against
-    // 49.5 us; decode, rank 16: 6.9 against 10.8 us).
+    // tokens) 131 against 216 us for the mma.sync kernel, prefill (rank 64)
+    // 30.7 against 34.5 us; at lower ranks, with short segments, the
+    // mma.sync kernel's 64-token tiles win (MLP, rank 32: 39.7 against
+    // 46.1 us; decode, rank 16: 6.9 against 11.3 us).
     // =1 takes it wherever it fits, =0 never, =2 requires it (a call it does
     // not fit fails with LORA_ERR_ALIGN or LORA_ERR_SIZE).
     const int tc_mode = lora::knob_expand_tc();

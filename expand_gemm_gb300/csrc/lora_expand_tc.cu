@@ -18,19 +18,20 @@
 // a large share of those bytes; from TMEM, each chunk reads only its B tile
 // from shared memory.
 //
-// Fourteen warps, one job each:
+// One job per warp (rank 128: fourteen warps; lower ranks: twelve, with two
+// y loader warps and more registers for the epilogue):
 //   warp 0       owns TMEM (two 128-column fp32 accumulators and the A
 //                operand); lane 0 issues tcgen05.mma (M = 128 tokens,
 //                N = 128 columns, K = 16 steps over the rank) and commits
 //                each chunk's accumulator and the release of its slot's B.
 //   warp 1       lane 0 loads each chunk's B tile with TMA through a 5-D
 //                tensor map that permutes its rows (below).
-//   warps 2..5   y loaders: the chunk's 128 old y rows, gathered through the
+//   warps 2..    y loaders: the chunk's 128 old y rows, gathered through the
 //                permutation with 16-byte cp.async (four whole 128-byte lines
 //                per instruction); each thread's copies arrive on the slot's
 //                y barrier when they land, so the loaders never wait for
 //                their own copies and run up to DEPTH chunks ahead.
-//   warps 6..13  epilogue.  Warp (q, h) = (warp % 4, (warp - 6) / 4) owns
+//   last 8 warps epilogue.  Warp (q, h) = (warp % 4, (warp - first) / 4) owns
 //                tile rows 32q + 16h .. 32q + 16h + 15 (TMEM lane quarter q,
 //                as tcgen05.ld requires).  It reads their accumulators one
 //                64-column half at a time in the 16x256b shape, in which
@@ -65,15 +66,11 @@ constexpr int TC_BM = 128;                    // tokens per tile (UMMA M, TMEM l
 constexpr int TC_BN = 128;                    // columns per chunk (UMMA N)
 constexpr int TC_HALVES = TC_BN / 64;         // 64-column blocks per chunk
 constexpr int TC_YL0 = 2;                     // first y loader warp
-constexpr int TC_YLOADERS = 4;
 constexpr int TC_EPI = 8;                     // epilogue warps
 constexpr int TC_NACC = 2;                    // TMEM accumulators (chunk g uses g % TC_NACC)
 constexpr int TC_A_COL = TC_NACC * TC_BN;    // TMEM column of the A operand
 constexpr int TC_TMEM_COLS = TC_A_COL + 64 <= 256 ? 256 : 512;   // accumulators + A
 static_assert(TC_BN == 64 || TC_BN == 128, "chunk width");
-constexpr int TC_EPI0 = TC_YL0 + TC_YLOADERS; // first epilogue warp
-constexpr int TC_THREADS = 32 * (TC_EPI0 + TC_EPI);
-constexpr int TC_LT = 32 * TC_YLOADERS;       // y loader threads
 constexpr long long TC_TIMEOUT_CYCLES = 2000000000ll;
 constexpr uint32_t TC_BACKOFF_NS = 200;       // loaders' sleep between polls of a full ring
 constexpr int TC_ERROR_BIT = 1 << 30;
@@ -119,10 +116,20 @@ struct TcCfg {
     static constexpr int BAR_OFF = RING_OFF + DEPTH * SLOT_BYTES;
     static constexpr int MISC_OFF = BAR_OFF + (3 * DEPTH + 2 * TC_NACC + 2) * 8;
     static constexpr int TAB_OFF = MISC_OFF + 16;
+    // Rank 128 keeps four y loader warps (its chunks carry the most bytes)
+    // and reads each accumulator half right before finishing it; lower ranks
+    // take two loader warps, which leaves the epilogue enough registers
+    // (twelve warps: up to 168 per thread) to request both halves'
+    // accumulators and old y before waiting for any of them.
+    static constexpr int YLOADERS = KT >= 8 ? 4 : 2;
+    static constexpr bool OVERLAP = KT < 8;
+    static constexpr int EPI0 = TC_YL0 + YLOADERS;         // first epilogue warp
+    static constexpr int THREADS = 32 * (EPI0 + TC_EPI);
+    static constexpr int LT = 32 * YLOADERS;               // y loader threads
     static constexpr int PPR = TC_BN / 8;                  // 16-byte y pieces per row
-    static constexpr int Y_PER_T = TC_BM * PPR / TC_LT;    // y pieces per loader thread
+    static constexpr int Y_PER_T = TC_BM * PPR / LT;       // y pieces per loader thread
     static_assert(SLOT_BYTES % 1024 == 0, "1024-byte aligned operands");
-    static_assert(TC_LT % PPR == 0, "whole y rows per loader pass");
+    static_assert(LT % PPR == 0, "whole y rows per loader pass");
 };
 
 // Byte offset of 16-byte piece `pc` (columns 8pc .. 8pc+7) of row `r` of a
@@ -194,7 +201,7 @@ struct TcCursor {
 };
 
 template <int KT>
-__global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_constant__ TcArgs p)
+__global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const __grid_constant__ TcArgs p)
 {
     using C = TcCfg<KT>;
     constexpr int RP = C::RP, CPR = C::CPR, DEPTH = C::DEPTH;
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
     if (tid == 0) {
         for (int i = 0; i < DEPTH; ++i) {
             mbar_init(bar_bfull + 8 * i, 1);
-            mbar_init(bar_yfull + 8 * i, TC_LT);
+            mbar_init(bar_yfull + 8 * i, C::LT);
             mbar_init(bar_empty + 8 * i, 1 + TC_EPI);
         }
         for (int i = 0; i < TC_NACC; ++i) {
@@ -343,12 +350,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                 }
         }
         __syncwarp();
-    } else if (warp < TC_EPI0) {
+    } else if (warp < C::EPI0) {
         // ------------------------------------------------------ y loaders
-        const int lt = tid - 32 * TC_YL0;                  // 0 .. TC_LT - 1
+        const int lt = tid - 32 * TC_YL0;                  // 0 .. C::LT - 1
         const uint16_t *const ydummy = p.y;
         int cur_tile = -1;
-        int ltok[C::Y_PER_T];                              // rows i * (TC_LT / PPR) + lt / PPR
+        int ltok[C::Y_PER_T];                              // rows i * (LT / PPR) + lt / PPR
         int g = 0;
         TcCursor k;
         k.start(p, w_begin, nchunks);
@@ -366,7 +373,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                     const int nrows = min(TC_BM, tab.start[seg] + tab.count[seg] - row0);
 #pragma unroll
                     for (int i = 0; i < C::Y_PER_T; ++i) {
-                        const int r = i * (TC_LT / C::PPR) + lt / C::PPR;
+                        const int r = i * (C::LT / C::PPR) + lt / C::PPR;
                         ltok[i] = (r < nrows) ? checked_token(p.sorted[row0 + r], T, p.error_word)
                                               : -1;
                     }
@@ -378,7 +385,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                 const uint32_t yt = base + C::RING_OFF + slot * C::SLOT_BYTES + C::B_BYTES;
 #pragma unroll
                 for (int i = 0; i < C::Y_PER_T; ++i) {
-                    const int r = i * (TC_LT / C::PPR) + lt / C::PPR;
+                    const int r = i * (C::LT / C::PPR) + lt / C::PPR;
                     const bool ld = cin && ltok[i] >= 0;
                     cp_async16(yt + tc_y_off(r, pc), ld ? ycol + int64_t(ltok[i]) * p.y_ld : ydummy,
                                ld);
@@ -389,7 +396,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
         cp_async_wait<0>();
     } else {
         // ------------------------------------------------------ epilogue
-        const int q = warp & 3, h = (warp - TC_EPI0) >> 2;
+        const int q = warp & 3, h = (warp - C::EPI0) >> 2;
         const int my_row = q * 32 + lane;                  // TMEM lane (A operand row)
         const int qg = lane >> 2, qt = lane & 3;           // 16x256b fragment coordinates
         const int qrow = q * 32 + h * 16 + qg;             // this thread's rows: qrow, qrow + 8
@@ -472,35 +479,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
             tc_fence_after();
             const int tok[2] = {qtok[0], qtok[1]};
             const uint8_t *yt = smem + C::RING_OFF + slot * C::SLOT_BYTES + C::B_BYTES;
-#pragma unroll
-            for (int hf = 0; hf < TC_HALVES; ++hf) {
-                uint32_t va[32];
-                tmem_ld16x256b_x8_nowait(tmem + (uint32_t(q * 32 + h * 16) << 16) +
-                                             uint32_t(ab * TC_BN + hf * 64),
-                                         va);
-                tmem_wait_ld();
-                if (hf == TC_HALVES - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
-                    // the next chunk opens a new tile or slice: its A operand
-                    // now (the MMAs up to chunk g are done; that of chunk g + 1
-                    // waits for it)
-                    k.next(p, nchunks);
-                    if (w + 1 < w_end && k.first) {
-                        tile_rows(k.tile);
-                        convert_x(k.s);
-                    }
-                }
-                // x B + old y + bias, rounded once, straight to y: output
-                // columns 64 hf + 16 qt + 2j + e of the chunk are accumulator
-                // columns 64 hf + 8j + 2 qt + e, registers va[4j + e] (row
-                // qrow) and va[4j + 2 + e] (row qrow + 8); one 32-byte store
-                // per row
+            const bool has_bias = bias_row != nullptr;
+            // x B + old y + bias, rounded once, straight to y: output columns
+            // 64 hf + 16 qt + 2j + e of the chunk are accumulator columns
+            // 64 hf + 8j + 2 qt + e, registers acc[4j + e] (row qrow) and
+            // acc[4j + 2 + e] (row qrow + 8); one 32-byte store per row.
+            auto finish_half = [&](int hf, const uint32_t (&acc)[32], const uint4 (&yh)[2][2]) {
                 const int cb = hf * 64 + qt * 16;
                 const bool cin = cb < ncols;
                 uint32_t bw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                const bool has_bias = bias_row != nullptr;
                 if (has_bias && cin) {
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
@@ -524,21 +511,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     if (cin && tok[u] >= 0) {
-                        uint32_t yw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                        if (p.add_inputs) {
-                            const int r = qrow + 8 * u;
-                            const uint4 y0 = *reinterpret_cast<const uint4 *>(
-                                yt + tc_y_off(r, hf * 8 + 2 * qt));
-                            const uint4 y1 = *reinterpret_cast<const uint4 *>(
-                                yt + tc_y_off(r, hf * 8 + 2 * qt + 1));
-                            yw[0] = y0.x; yw[1] = y0.y; yw[2] = y0.z; yw[3] = y0.w;
-                            yw[4] = y1.x; yw[5] = y1.y; yw[6] = y1.z; yw[7] = y1.w;
-                        }
+                        const uint32_t yw[8] = {yh[u][0].x, yh[u][0].y, yh[u][0].z, yh[u][0].w,
+                                                yh[u][1].x, yh[u][1].y, yh[u][1].z, yh[u][1].w};
                         uint32_t o[8];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            float a0 = __uint_as_float(va[4 * j + 2 * u]);
-                            float a1 = __uint_as_float(va[4 * j + 2 * u + 1]);
+                            float a0 = __uint_as_float(acc[4 * j + 2 * u]);
+                            float a1 = __uint_as_float(acc[4 * j + 2 * u + 1]);
                             a0 += bf16_lo(yw[j]);
                             a1 += bf16_hi(yw[j]);
                             if (has_bias) {
@@ -549,6 +528,59 @@ __global__ void __launch_bounds__(TC_THREADS, 1) expand_tc_kernel(const __grid_c
                         }
                         st_global_v8(ycol + int64_t(tok[u]) * p.y_ld, o);
                     }
+                }
+            };
+            // this thread's old y of half hf (both rows, 32 bytes each)
+            auto load_y = [&](int hf, uint4 (&yh)[2][2]) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        yh[u][e] = make_uint4(0u, 0u, 0u, 0u);
+                        if (p.add_inputs)
+                            yh[u][e] = *reinterpret_cast<const uint4 *>(
+                                yt + tc_y_off(qrow + 8 * u, hf * 8 + 2 * qt + e));
+                    }
+            };
+            // The accumulator goes back to the MMA once it is in registers;
+            // when the next chunk opens a new tile or slice, its A operand is
+            // written right then (the MMAs up to chunk g are done; that of
+            // chunk g + 1 waits for it).
+            auto release_acc = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
+                k.next(p, nchunks);
+                if (w + 1 < w_end && k.first) {
+                    tile_rows(k.tile);
+                    convert_x(k.s);
+                }
+            };
+            const uint32_t tl = tmem + (uint32_t(q * 32 + h * 16) << 16) + uint32_t(ab * TC_BN);
+            if constexpr (C::OVERLAP) {
+                // both halves' accumulators and old y requested before any
+                // is waited for: the chunk's latencies overlap
+                uint32_t va[TC_HALVES][32];
+                uint4 yv[TC_HALVES][2][2];
+#pragma unroll
+                for (int hf = 0; hf < TC_HALVES; ++hf)
+                    tmem_ld16x256b_x8_nowait(tl + uint32_t(hf * 64), va[hf]);
+#pragma unroll
+                for (int hf = 0; hf < TC_HALVES; ++hf) load_y(hf, yv[hf]);
+                tmem_wait_ld();
+                release_acc();
+#pragma unroll
+                for (int hf = 0; hf < TC_HALVES; ++hf) finish_half(hf, va[hf], yv[hf]);
+            } else {
+#pragma unroll
+                for (int hf = 0; hf < TC_HALVES; ++hf) {
+                    uint32_t va[32];
+                    uint4 yv[2][2];
+                    tmem_ld16x256b_x8_nowait(tl + uint32_t(hf * 64), va);
+                    tmem_wait_ld();
+                    if (hf == TC_HALVES - 1) release_acc();
+                    load_y(hf, yv);
+                    finish_half(hf, va, yv);
                 }
             }
             __syncwarp();
@@ -579,7 +611,7 @@ static int launch_tc_kt(const TcArgs &p, cudaStream_t stream)
         if (e != cudaSuccess) return int(e);
         configured[dev] = 1;
     }
-    e = launch_kernel(expand_tc_kernel<KT>, dim3(device_sm_count()), dim3(TC_THREADS), smem,
+    e = launch_kernel(expand_tc_kernel<KT>, dim3(device_sm_count()), dim3(TcCfg<KT>::THREADS), smem,
                       stream, p);
     return e == cudaSuccess ? int(TC_LAUNCHED) : int(e);
 }
