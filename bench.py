@@ -53,8 +53,8 @@ E2E_GRAPH_STEPS = 8
 NCU_TRAFFIC = {
     # expand_tc_kernel<8> and shrink_umma_kernel, one launch each at full size
     # (profiles/traffic_large.md)
-    ("expand", "large"): ("4b5468283bf9b3bf", 667451904),
-    ("shrink", "large"): ("3bd232621c2f634c", 448609280),
+    ("expand", "large"): ("07e80461fcf9af32", 667499264),
+    ("shrink", "large"): ("5c6eb0c54a708943", 445830656),
 }
 
 # The source files each reported kernel is built from.
