@@ -235,6 +235,88 @@ __device__ __forceinline__ int load_segments(const int32_t *no_lora, const int32
     return t.tile[nbins];
 }
 
+// Per bin b: the exclusive scan of cnt[w * nb + b] over the W warps (warp
+// order is token order), in place, and tot[b] = the bin's total (plus
+// bef[b] + aft[b] when given: tokens counted outside the warps' run).
+// With 32 warps, three threads share a bin, each summing 11 warps' counts
+// with independent loads and taking the others' sums by shuffle, instead
+// of one thread walking all 32 (a chain of dependent loads).  Banks: word
+// w * nb + b with nb = L + 1; with three threads per bin the lanes' words
+// differ mod 32 when nb = 257 (11 j + g for j < 3, g < 10).
+template <int NT, int W>
+__device__ __forceinline__ void scan_bins_over_warps(int32_t *cnt, int32_t *tot,
+                                                     const int32_t *bef, const int32_t *aft,
+                                                     int nb)
+{
+    constexpr int Q = W >= 24 ? 3 : 1;          // threads per bin
+    constexpr int SPAN = (W + Q - 1) / Q;       // warps per thread
+    constexpr int G = 32 / Q;                   // bins per warp and pass
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane / Q, j = lane - g * Q;
+    for (int b0 = warp * G; b0 < nb; b0 += (NT / 32) * G) {   // the same in every lane
+        const int b = b0 + g;
+        const bool act = g < G && b < nb;
+        int c[SPAN];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < SPAN; ++i) {
+            const int w = j * SPAN + i;
+            c[i] = (act && w < W) ? cnt[w * nb + b] : 0;
+            sum += c[i];
+        }
+        int run = 0;                            // sums of the bin's earlier threads
+#pragma unroll
+        for (int d = 1; d < Q; ++d) {
+            const int u = __shfl_up_sync(0xffffffffu, sum, d);
+            if (j >= d) run += u;
+        }
+#pragma unroll
+        for (int i = 0; i < SPAN; ++i) {
+            const int w = j * SPAN + i;
+            if (act && w < W) cnt[w * nb + b] = run;
+            run += c[i];
+        }
+        if (act && j == Q - 1) tot[b] = run + (bef != nullptr ? bef[b] + aft[b] : 0);
+    }
+}
+
+// Exclusive scans over the bins of tot: base[b] = tokens in bins before b,
+// pos[b] = non-empty bins before b (the torch.unique(sorted=True) order),
+// *nactive = non-empty bins.  One warp per 32 bins: each first sums every
+// earlier bin itself (up to eight independent loads a lane and one warp
+// reduction), then scans its own 32; no warp waits for another.  Token
+// counts and non-empty flags travel packed in one 64-bit value.
+template <int NT>
+__device__ __forceinline__ void scan_over_bins(const int32_t *tot, int32_t *base, int32_t *pos,
+                                               int32_t *nactive, int nb)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nchunk = (nb + 31) >> 5;
+    auto pack = [](int32_t v) {
+        return uint64_t(uint32_t(v)) | (uint64_t(v > 0 ? 1u : 0u) << 32);
+    };
+    for (int c = warp; c < nchunk; c += NT / 32) {
+        uint64_t before = 0;
+        for (int k = 0; k < c; ++k) before += pack(tot[k * 32 + lane]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+        const int b = c * 32 + lane;
+        const uint64_t pv = b < nb ? pack(tot[b]) : 0ull;
+        uint64_t incl = pv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        const uint64_t excl = before + incl - pv;
+        if (b < nb) {
+            base[b] = int32_t(uint32_t(excl));
+            pos[b] = int32_t(excl >> 32);
+        }
+        if (c == nchunk - 1 && lane == 31) *nactive = int32_t((before + incl) >> 32);
+    }
+}
+
 // Stable counting sort of a small batch's LoRA ids inside one CTA of NW
 // warps (the metadata step of LoRAKernelMeta.prepare_tensors, computed in
 // shared memory).  Bin 0 holds id -1 and invalid ids, bin b holds id b - 1.
@@ -276,35 +358,9 @@ __device__ __forceinline__ bool block_sort_ids(const int32_t *map_g, int T, int 
     for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
     if (lane == 0 && bad) atomicAdd(&misc[0], bad);
     __syncthreads();
-    for (int b = tid; b < nbins; b += NW * 32) {
-        int run = 0;
-        for (int w = 0; w < NW; ++w) {
-            const int c = cnt[w * nbins + b];
-            cnt[w * nbins + b] = run;
-            run += c;
-        }
-        tot[b] = run;
-    }
+    scan_bins_over_warps<NW * 32, NW>(cnt, tot, nullptr, nullptr, nbins);
     __syncthreads();
-    if (warp == 0) {
-        int ct = 0, cp = 0;
-        for (int b0 = 0; b0 < nbins; b0 += 32) {
-            const int b = b0 + lane;
-            const int v = (b < nbins) ? tot[b] : 0;
-            const int f = v > 0 ? 1 : 0;
-            int iv = v, jf = f;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, iv, o);
-                const int w = __shfl_up_sync(0xffffffffu, jf, o);
-                if (lane >= o) { iv += u; jf += w; }
-            }
-            if (b < nbins) { base[b] = ct + iv - v; pos[b] = cp + jf - f; }
-            ct += __shfl_sync(0xffffffffu, iv, 31);
-            cp += __shfl_sync(0xffffffffu, jf, 31);
-        }
-        if (lane == 0) misc[1] = cp;
-    }
+    scan_over_bins<NW * 32>(tot, base, pos, &misc[1], nbins);
     __syncthreads();
     const bool no_lora = (tot[0] == T);
     if (!no_lora) {

@@ -7,7 +7,8 @@
 // Two kernels compute it:
 //   - meta_prepare_kernel: one CTA, the id map staged in shared memory;
 //     batches of up to META_MULTI_MIN tokens.
-//   - meta_multi_kernel: one CTA per run of META_MULTI_CHUNK tokens.  Every
+//   - meta_multi_kernel<NT>: one CTA per run of NT tokens (256 up to
+//     META_MULTI_BIG tokens, 1024 above), one 32-token group per warp.  Every
 //     CTA counts the whole map itself (its run one 32-token group per warp,
 //     the rest 128 tokens per 16-byte warp load with one vote; the map is
 //     read from L2), keeping apart the tokens before its run, those of its
@@ -32,10 +33,13 @@ constexpr int META_SMALL_MAX = 512;
 // one block-wide load (all of it in flight at once); both passes then read
 // shared memory.  Larger batches read the map from global memory.
 constexpr int META_STAGE_MAX = 16384;
-// Batches above this many tokens take the multi-CTA kernel.
-constexpr int META_MULTI_MIN = 2048;
+// Batches above this many tokens take the multi-CTA kernel: runs of 256
+// tokens up to META_MULTI_BIG tokens (8 to 16 CTAs), runs of 1024 above.
+// One SM sorting 2048 tokens was issue-bound (4.4 us in the kernel).
+constexpr int META_MULTI_MIN = 512;
+constexpr int META_MULTI_BIG = 4096;
+constexpr int META_MULTI_SMALL_THREADS = 256;
 constexpr int META_MULTI_THREADS = 1024;
-constexpr int META_MULTI_CHUNK = 1024;   // tokens per CTA: one 32-token group per warp
 
 struct MetaArgs {
     const int32_t *map;
@@ -50,11 +54,27 @@ struct MetaArgs {
     int32_t *error_word;
 };
 
+// Batches up to this many tokens also build the permutation in shared
+// memory (written out in order at the end).  With 1025 bins and the map
+// staged, 4096 more ints is what still fits in one CTA's shared memory.
+constexpr int META_PERM_STAGE_MAX = 4096;
+
+// Ints of shared memory for the staged map and the staged permutation,
+// each rounded up to 16 bytes (0 when not staged).
+__host__ __device__ __forceinline__ int meta_staged_ints(int num_tokens)
+{
+    return num_tokens <= META_STAGE_MAX ? (num_tokens + 3) & ~3 : 0;
+}
+__host__ __device__ __forceinline__ int meta_perm_ints(int num_tokens)
+{
+    return num_tokens <= META_PERM_STAGE_MAX ? (num_tokens + 3) & ~3 : 0;
+}
+
 size_t meta_smem_bytes(int warps, int max_loras, int num_tokens)
 {
     const size_t nb = size_t(max_loras) + 1;
-    const size_t staged = num_tokens <= META_STAGE_MAX ? size_t(num_tokens) : 0;
-    return (size_t(warps) * nb + 3 * nb + staged) * sizeof(int32_t);
+    return (size_t(warps) * nb + 3 * nb + size_t(meta_staged_ints(num_tokens)) +
+            size_t(meta_perm_ints(num_tokens))) * sizeof(int32_t);
 }
 
 // Bin of one token; counts an invalid id into `bad`.
@@ -97,24 +117,34 @@ template <int NT>
 __global__ void __launch_bounds__(NT, 1) meta_prepare_kernel(MetaArgs a)
 {
     constexpr int META_WARPS = NT / 32;
-    extern __shared__ int32_t sm[];
+    extern __shared__ int4 sm4[];
     const int nb = a.max_loras + 1;
-    int32_t *cnt = sm;                          // [META_WARPS][nb]: count, then offset
+    const int T = a.num_tokens;
+    const int TS = meta_staged_ints(T);         // 0 when not staged
+    const int TP = meta_perm_ints(T);
+    int32_t *ids_s = reinterpret_cast<int32_t *>(sm4);  // [TS] the map, when staged
+    int32_t *perm_s = ids_s + TS;               // [TP] the permutation, when staged
+    int32_t *cnt = perm_s + TP;                 // [META_WARPS][nb]: count, then offset
     int32_t *tot = cnt + META_WARPS * nb;       // [nb] tokens per bin
     int32_t *base = tot + nb;                   // [nb] first sorted slot of the bin
     int32_t *pos = base + nb;                   // [nb] index among non-empty bins
-    int32_t *ids_s = pos + nb;                  // [T] the map, when staged
     __shared__ int32_t s_invalid, s_nactive;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int T = a.num_tokens;
 
     pdl_wait();
     pdl_launch_dependents();
 
-    const bool staged = T <= META_STAGE_MAX;
-    if (staged)
-        for (int t = tid; t < T; t += NT) ids_s[t] = a.map[t];
+    // Stage the map with one 16-byte load per thread and pass where it is
+    // aligned (all of it in flight at once).
+    const bool staged = TS > 0;
+    if (staged) {
+        const bool vec = (reinterpret_cast<uintptr_t>(a.map) & 15u) == 0;
+        const int nv = vec ? T >> 2 : 0;
+        for (int i = tid; i < nv; i += NT)
+            reinterpret_cast<int4 *>(ids_s)[i] = reinterpret_cast<const int4 *>(a.map)[i];
+        for (int t = nv * 4 + tid; t < T; t += NT) ids_s[t] = a.map[t];
+    }
     const int32_t *ids = staged ? ids_s : a.map;
     for (int i = tid; i < META_WARPS * nb; i += NT) cnt[i] = 0;
     if (tid == 0) s_invalid = 0;
@@ -128,8 +158,7 @@ __global__ void __launch_bounds__(NT, 1) meta_prepare_kernel(MetaArgs a)
     // Pass 1: per-warp histogram, one shared-memory atomic add per token,
     // or one per group of 32 tokens of one bin (counts only: pass 2 keeps
     // the order).  Per-token adds were measured faster than grouping lanes
-    // with __match_any_sync, whose cost grows with the number of distinct
-    // ids in a warp.
+    // (with __match_any_sync, or with one ballot per bit of the bin).
     int bad = 0;
     for (int g = t0; g < t1; g += 32) {
         const int t = g + lane;
@@ -142,42 +171,9 @@ __global__ void __launch_bounds__(NT, 1) meta_prepare_kernel(MetaArgs a)
     if (lane == 0 && bad) atomicAdd(&s_invalid, bad);
     __syncthreads();
 
-    // Per bin, exclusive scan over warps (warp order = token order).
-    for (int b = tid; b < nb; b += NT) {
-        int run = 0;
-        for (int w = 0; w < META_WARPS; ++w) {
-            const int c = cnt[w * nb + b];
-            cnt[w * nb + b] = run;
-            run += c;
-        }
-        tot[b] = run;
-    }
+    scan_bins_over_warps<NT, META_WARPS>(cnt, tot, nullptr, nullptr, nb);
     __syncthreads();
-
-    // Exclusive scans over bins: first sorted slot, and rank among the
-    // non-empty bins (torch.unique(sorted=True) order).
-    if (warp == 0) {
-        int carry_t = 0, carry_p = 0;
-        for (int b0 = 0; b0 < nb; b0 += 32) {
-            const int b = b0 + lane;
-            const int v = (b < nb) ? tot[b] : 0;
-            const int f = v > 0 ? 1 : 0;
-            int iv = v, jf = f;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, iv, o);
-                const int w = __shfl_up_sync(0xffffffffu, jf, o);
-                if (lane >= o) { iv += u; jf += w; }
-            }
-            if (b < nb) {
-                base[b] = carry_t + iv - v;
-                pos[b] = carry_p + jf - f;
-            }
-            carry_t += __shfl_sync(0xffffffffu, iv, 31);
-            carry_p += __shfl_sync(0xffffffffu, jf, 31);
-        }
-        if (lane == 0) s_nactive = carry_p;
-    }
+    scan_over_bins<NT>(tot, base, pos, &s_nactive, nb);
     __syncthreads();
 
     const bool no_lora = (tot[0] == T);         // also true for T == 0
@@ -209,7 +205,12 @@ __global__ void __launch_bounds__(NT, 1) meta_prepare_kernel(MetaArgs a)
         }
     }
 
-    // Pass 2: stable scatter + mapping copy.
+    // Pass 2: stable scatter + mapping copy.  A batch of up to
+    // META_PERM_STAGE_MAX tokens is scattered in shared memory and written
+    // out in order afterwards: scattered 4-byte stores from one SM (one L2
+    // request each) were the slowest phase with per-token ids.
+    const bool perm_staged = TP > 0;
+    int32_t *perm = perm_staged ? perm_s : a.sorted;
     int unused = 0;
     for (int g = t0; g < t1; g += 32) {
         const int t = g + lane;
@@ -219,20 +220,28 @@ __global__ void __launch_bounds__(NT, 1) meta_prepare_kernel(MetaArgs a)
         int n = 0;
         const int rank = rank_in_group(b, has, lane, n);
         if (has) {
-            a.sorted[base[b] + cnt[warp * nb + b] + rank] = t;
+            perm[base[b] + cnt[warp * nb + b] + rank] = t;
             a.mapping_copy[t] = id;
         }
         __syncwarp();
         if (has && rank == 0) cnt[warp * nb + b] += n;
         __syncwarp();
     }
+    if (perm_staged) {
+        __syncthreads();
+        const bool vec = (reinterpret_cast<uintptr_t>(a.sorted) & 15u) == 0;
+        const int nv = vec ? T >> 2 : 0;
+        for (int i = tid; i < nv; i += NT)
+            reinterpret_cast<int4 *>(a.sorted)[i] = reinterpret_cast<const int4 *>(perm_s)[i];
+        for (int t = nv * 4 + tid; t < T; t += NT) a.sorted[t] = perm_s[t];
+    }
 }
 
 template <int NT>
 __global__ void __launch_bounds__(NT) meta_multi_kernel(MetaArgs a)
 {
-    constexpr int NW = NT / 32;
-    static_assert(NW * 32 == META_MULTI_CHUNK, "one 32-token group per warp in the CTA's run");
+    constexpr int NW = NT / 32;                 // the run: one 32-token group per warp
+    static_assert(NT % 128 == 0, "the run is whole 128-token blocks");
     extern __shared__ int32_t sm[];
     const int nb = a.max_loras + 1;
     int32_t *own = sm;                          // [NW][nb]: run counts per warp, then offsets
@@ -262,13 +271,10 @@ __global__ void __launch_bounds__(NT) meta_multi_kernel(MetaArgs a)
     // ids all fall in one bin (runs of one sequence, the all -1 batch) takes
     // a single add.
     int bad = 0;
-    {
-        const int gi = g_run + warp;
-        const int t = gi * 32 + lane;
-        const bool has = t < T;
-        const int b = has ? token_bin(a.map[t], a.max_loras, bad) : -1;
-        count_group(own + warp * nb, b, has, lane);
-    }
+    // The run's id is loaded first and counted after the rest, so that all
+    // of this warp's loads are in flight together (one round trip, not two).
+    const int t_own = (g_run + warp) * 32 + lane;
+    const int32_t id_own = t_own < T ? a.map[t_own] : -1;
     const bool vec = (reinterpret_cast<uintptr_t>(a.map) & 15u) == 0;
     const int nblk = (T + 127) / 128, rb0 = cta * (NW / 4), rb1 = rb0 + NW / 4;
     constexpr int UB = 4;
@@ -315,46 +321,20 @@ __global__ void __launch_bounds__(NT) meta_multi_kernel(MetaArgs a)
             }
         }
     }
+    {
+        const bool has = t_own < T;
+        const int b = has ? token_bin(id_own, a.max_loras, bad) : -1;
+        count_group(own + warp * nb, b, has, lane);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
     if (lane == 0 && bad) atomicAdd(&s_invalid, bad);
     __syncthreads();
-    // Per bin: the run's warps scanned in token order, and the totals.
-    for (int b = tid; b < nb; b += NT) {
-        int run = 0;
-        for (int w = 0; w < NW; ++w) {
-            const int c = own[w * nb + b];
-            own[w * nb + b] = run;
-            run += c;
-        }
-        tot[b] = bef[b] + run + aft[b];
-    }
+    // Per bin: the run's warps scanned in token order, and the totals; then
+    // the scans over bins.
+    scan_bins_over_warps<NT, NW>(own, tot, bef, aft, nb);
     __syncthreads();
-    // Exclusive scans over bins: first sorted slot, rank among the non-empty
-    // bins (torch.unique(sorted=True) order).  Both run in one shuffle scan
-    // of a packed value: the token count in the low 21 bits (T < 2^21), the
-    // non-empty-bin count above it (at most 257 < 2^11).
-    if (warp == 0) {
-        uint32_t carry = 0;
-        for (int b0 = 0; b0 < nb; b0 += 32) {
-            const int b = b0 + lane;
-            const uint32_t v = (b < nb) ? uint32_t(tot[b]) : 0u;
-            const uint32_t pv = v | ((v > 0 ? 1u : 0u) << 21);
-            uint32_t incl = pv;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += u;
-            }
-            const uint32_t excl = carry + incl - pv;
-            if (b < nb) {
-                base[b] = int(excl & 0x1FFFFFu);
-                pos[b] = int(excl >> 21);
-            }
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) s_nactive = int(carry >> 21);
-    }
+    scan_over_bins<NT>(tot, base, pos, &s_nactive, nb);
     __syncthreads();
 
     const bool no_lora = (tot[0] == T);
@@ -386,23 +366,21 @@ __global__ void __launch_bounds__(NT) meta_multi_kernel(MetaArgs a)
     }
     if (no_lora) return;                        // early exit: nothing else written
     // Pass 2: stable scatter of this warp's group of the run + mapping copy.
-    const int t = (g_run + warp) * 32 + lane;
-    const bool has = t < T;
+    const bool has = t_own < T;
     int unused = 0;
-    const int32_t id = has ? a.map[t] : -1;
-    const int b = has ? token_bin(id, a.max_loras, unused) : -1;
+    const int b = has ? token_bin(id_own, a.max_loras, unused) : -1;
     int n = 0;
     const int rank = rank_in_group(b, has, lane, n);
     if (has) {
-        a.sorted[base[b] + bef[b] + own[warp * nb + b] + rank] = t;
-        a.mapping_copy[t] = id;
+        a.sorted[base[b] + bef[b] + own[warp * nb + b] + rank] = t_own;
+        a.mapping_copy[t_own] = id_own;
     }
 }
 
-size_t meta_multi_smem_bytes(int max_loras)
+size_t meta_multi_smem_bytes(int warps, int max_loras)
 {
     const size_t nb = size_t(max_loras) + 1;
-    return (size_t(META_MULTI_THREADS / 32) * nb + 5 * nb) * sizeof(int32_t);
+    return (size_t(warps) * nb + 5 * nb) * sizeof(int32_t);
 }
 
 int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
@@ -424,18 +402,29 @@ int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
         if (e != cudaSuccess) return int(e);
         e = cudaFuncSetAttribute(meta_multi_kernel<META_MULTI_THREADS>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(meta_multi_smem_bytes(LORA_MAX_LORAS)));
+                                 int(meta_multi_smem_bytes(META_MULTI_THREADS / 32,
+                                                           LORA_MAX_LORAS)));
+        if (e != cudaSuccess) return int(e);
+        e = cudaFuncSetAttribute(meta_multi_kernel<META_MULTI_SMALL_THREADS>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(meta_multi_smem_bytes(META_MULTI_SMALL_THREADS / 32,
+                                                           LORA_MAX_LORAS)));
         if (e != cudaSuccess) return int(e);
         configured[dev] = 1;
     }
-    // Batches above META_MULTI_MIN tokens on one CTA per 1024 tokens
-    // (LORA_PUNICA_META_MULTI=0 turns it off).
-    // (the multi-CTA kernel's bin scan packs token counts into 21 bits)
-    if (a.num_tokens > META_MULTI_MIN && a.num_tokens < (1 << 21) && knobs().meta_multi) {
-        const int grid = (a.num_tokens + META_MULTI_CHUNK - 1) / META_MULTI_CHUNK;
-        return int(launch_kernel(meta_multi_kernel<META_MULTI_THREADS>, dim3(grid),
-                                 dim3(META_MULTI_THREADS), meta_multi_smem_bytes(a.max_loras),
-                                 stream, a));
+    // Batches above META_MULTI_MIN tokens on one CTA per run of 256 or 1024
+    // tokens (LORA_PUNICA_META_MULTI=0 turns it off).
+    if (a.num_tokens > META_MULTI_MIN && knobs().meta_multi) {
+        if (a.num_tokens <= META_MULTI_BIG) {
+            constexpr int NT = META_MULTI_SMALL_THREADS;
+            return int(launch_kernel(meta_multi_kernel<NT>, dim3((a.num_tokens + NT - 1) / NT),
+                                     dim3(NT), meta_multi_smem_bytes(NT / 32, a.max_loras),
+                                     stream, a));
+        }
+        constexpr int NT = META_MULTI_THREADS;
+        return int(launch_kernel(meta_multi_kernel<NT>, dim3((a.num_tokens + NT - 1) / NT),
+                                 dim3(NT), meta_multi_smem_bytes(NT / 32, a.max_loras), stream,
+                                 a));
     }
     // Small batches on 8 warps (fewer warps to pass each barrier), the rest
     // on 32.  LORA_PUNICA_META_SMALL=0 always takes 32 warps.

@@ -141,13 +141,14 @@ def _maps(T, L, seed):
 
 
 @pytest.mark.parametrize("multi", ["0", "1"])
-@pytest.mark.parametrize("T,L", [(2048, 8), (2049, 8), (4096, 64), (16384, 64), (20000, 1024),
-                                 (70001, 300)])
+@pytest.mark.parametrize("T,L", [(513, 8), (1000, 1024), (2048, 8), (2049, 8), (4096, 64),
+                                 (4097, 33), (16384, 64), (20000, 1024), (70001, 300)])
 def test_meta_single_and_multi_cta(oracle_mod, knob, multi, T, L):
-    """The single-CTA kernel and the multi-CTA kernel (one CTA per 512
-    tokens, each counting the whole map itself; batches above 2048 tokens)
-    give the oracle's metadata bit for bit, on per-token maps with invalid
-    ids, run-ordered maps and the all -1 map."""
+    """The single-CTA kernel and the multi-CTA kernel (batches above 512
+    tokens: one CTA per 256 tokens up to 4096, per 1024 above, each
+    counting the whole map itself) give the oracle's metadata bit for bit,
+    on per-token maps with invalid ids, run-ordered maps and the all -1
+    map."""
     knob(LORA_PUNICA_META_MULTI=multi)
     for ids in _maps(T, L, seed=T + L):
         _check(ids, L, oracle_mod)
