@@ -65,11 +65,18 @@ namespace lora {
 constexpr int TC_BM = 128;                    // tokens per tile (UMMA M, TMEM lanes)
 constexpr int TC_BN = 128;                    // columns per chunk (UMMA N)
 constexpr int TC_HALVES = TC_BN / 64;         // 64-column blocks per chunk
-constexpr int TC_YL0 = 2;                     // first y loader warp
 constexpr int TC_EPI = 8;                     // epilogue warps
 constexpr int TC_NACC = 2;                    // TMEM accumulators (chunk g uses g % TC_NACC)
-constexpr int TC_A_COL = TC_NACC * TC_BN;    // TMEM column of the A operand
-constexpr int TC_TMEM_COLS = TC_A_COL + 64 <= 256 ? 256 : 512;   // accumulators + A
+constexpr int TC_A_COL = TC_NACC * TC_BN;    // TMEM column of the first A operand
+// A operands held at once: row item j (a tile and slice) uses buffer
+// j % TC_NXB.  The epilogue writes the first TC_NXB items' A operands when
+// the CTA starts, so that no item boundary waits for x (the shrink output)
+// while the y stream keeps HBM busy: there, x loads took 5-7 us a round
+// trip, and a boundary held the MMA and the epilogue for 4-10 us.  Items
+// past the first TC_NXB (CTAs with many short items) are written at their
+// boundary, into the buffer item - TC_NXB used.
+constexpr int TC_NXB = 4;
+constexpr int TC_TMEM_COLS = 512;             // accumulators + TC_NXB A operands
 static_assert(TC_BN == 64 || TC_BN == 128, "chunk width");
 constexpr long long TC_TIMEOUT_CYCLES = 2000000000ll;
 constexpr uint32_t TC_BACKOFF_NS = 200;       // loaders' sleep between polls of a full ring
@@ -114,7 +121,8 @@ struct TcCfg {
     static constexpr int DEPTH = 196608 / SLOT_BYTES < 8 ? 196608 / SLOT_BYTES : 8;
     static constexpr int RING_OFF = 0;
     static constexpr int BAR_OFF = RING_OFF + DEPTH * SLOT_BYTES;
-    static constexpr int MISC_OFF = BAR_OFF + (3 * DEPTH + 2 * TC_NACC + 2) * 8;
+    static constexpr int MISC_OFF = BAR_OFF + (3 * DEPTH + 2 * TC_NACC + TC_NXB + 1) * 8;
+    static_assert(TC_A_COL + TC_NXB * A_COLS <= TC_TMEM_COLS, "TMEM: accumulators + A buffers");
     static constexpr int TAB_OFF = MISC_OFF + 16;
     // Rank 128 keeps four y loader warps (its chunks carry the most bytes)
     // and reads each accumulator half right before finishing it; lower ranks
@@ -123,12 +131,19 @@ struct TcCfg {
     // accumulators and old y before waiting for any of them.
     static constexpr int YLOADERS = KT >= 8 ? 4 : 2;
     static constexpr bool OVERLAP = KT < 8;
-    static constexpr int EPI0 = TC_YL0 + YLOADERS;         // first epilogue warp
+    // B issuer warps (1 .. BISSUE), each with its share of the chunk's
+    // boxes: one thread streams about 15 bytes a clock by TMA, and the
+    // rank-128 chunk's 32 KB of B then set the chunk period (chunks of
+    // tiles with a handful of rows took nearly as long as full ones).
+    static constexpr int BISSUE = KT >= 8 ? 2 : 1;
+    static constexpr int YL0 = 1 + BISSUE;                 // first y loader warp
+    static constexpr int EPI0 = YL0 + YLOADERS;            // first epilogue warp
     static constexpr int THREADS = 32 * (EPI0 + TC_EPI);
     static constexpr int LT = 32 * YLOADERS;               // y loader threads
     static constexpr int PPR = TC_BN / 8;                  // 16-byte y pieces per row
     static constexpr int Y_PER_T = TC_BM * PPR / LT;       // y pieces per loader thread
     static_assert(SLOT_BYTES % 1024 == 0, "1024-byte aligned operands");
+    static_assert(NBOX % BISSUE == 0, "each B issuer takes the same number of boxes");
     static_assert(LT % PPR == 0, "whole y rows per loader pass");
 };
 
@@ -198,6 +213,21 @@ struct TcCursor {
         }
     }
     __device__ __forceinline__ int c0(const TcArgs &p) const { return (c - p.chunk0[s]) * TC_BN; }
+    // Moves to the first chunk of the next row item; returns the chunks passed.
+    __device__ __forceinline__ int skip_item(const TcArgs &p, int nchunks)
+    {
+        const int n = p.chunk0[s + 1] - c;
+        c += n;
+        if (c == nchunks) {
+            c = 0;
+            ++tile;
+            s = 0;
+        } else {
+            ++s;
+        }
+        first = true;
+        return n;
+    }
 };
 
 template <int KT>
@@ -214,8 +244,8 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
     const uint32_t bar_empty = bar_yfull + 8 * DEPTH;      // [DEPTH]: MMA + epilogue warps
     const uint32_t bar_accf = bar_empty + 8 * DEPTH;       // [TC_NACC]: MMA commit
     const uint32_t bar_acce = bar_accf + 8 * TC_NACC;      // [TC_NACC]: epilogue warps
-    const uint32_t bar_x = bar_acce + 8 * TC_NACC;         // A operand ready: epilogue warps
-    const uint32_t bar_drain = bar_x + 8;
+    const uint32_t bar_x = bar_acce + 8 * TC_NACC;         // [TC_NXB] A operand ready: epilogue
+    const uint32_t bar_drain = bar_x + 8 * TC_NXB;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -236,7 +266,7 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
 
     if (tid == 0) {
         for (int i = 0; i < DEPTH; ++i) {
-            mbar_init(bar_bfull + 8 * i, 1);
+            mbar_init(bar_bfull + 8 * i, C::BISSUE);
             mbar_init(bar_yfull + 8 * i, C::LT);
             mbar_init(bar_empty + 8 * i, 1 + TC_EPI);
         }
@@ -244,7 +274,7 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
             mbar_init(bar_accf + 8 * i, 1);
             mbar_init(bar_acce + 8 * i, TC_EPI);
         }
-        mbar_init(bar_x, TC_EPI);
+        for (int i = 0; i < TC_NXB; ++i) mbar_init(bar_x + 8 * i, TC_EPI);
         mbar_init(bar_drain, 1);
         mbar_fence_init();
         *s_abort = 0;
@@ -276,17 +306,20 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
         // ------------------------------------------------------ MMA issue
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_bf16(TC_BM, TC_BN);
-            int g = 0, items = 0;
+            int g = 0, item = -1;
+            uint32_t a_col = TC_A_COL;
             bool ok = true;
             TcCursor k;
             k.start(p, w_begin, nchunks);
             for (int64_t w = w_begin; w < w_end; ++w, ++g, k.next(p, nchunks)) {
                 if (k.first) {
-                    if (!mbar_wait_bounded(bar_x, uint32_t(items) & 1u, s_abort, deadline)) {
+                    ++item;
+                    if (!mbar_wait_bounded(bar_x + 8 * (item % TC_NXB),
+                                           uint32_t(item / TC_NXB) & 1u, s_abort, deadline)) {
                         ok = false;
                         break;
                     }
-                    ++items;
+                    a_col = TC_A_COL + uint32_t((item % TC_NXB) * C::A_COLS);
                 }
                 const int slot = g % DEPTH, ab = g % TC_NACC;
                 if (!mbar_wait_bounded(bar_bfull + 8 * slot, uint32_t(g / DEPTH) & 1u, s_abort,
@@ -300,7 +333,7 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
                 const uint32_t bt = base + C::RING_OFF + slot * C::SLOT_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < KT; ++kk)
-                    umma_bf16_tmem_a(tmem + ab * TC_BN, tmem + TC_A_COL + kk * 8,
+                    umma_bf16_tmem_a(tmem + ab * TC_BN, tmem + a_col + kk * 8,
                                      tc_kmajor_desc(RP, TC_BN, bt, kk), idesc, kk != 0);
                 umma_commit(bar_empty + 8 * slot);           // B read
                 umma_commit(bar_accf + 8 * ab);
@@ -315,7 +348,7 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp <= C::BISSUE) {
         // ------------------------------------------------------ B by TMA
         if (lane == 0) {
             int cur_tile = -1, l_id = 0, g = 0;
@@ -334,9 +367,9 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
                 // multiples of 64)
                 const int blk = (l_id * p.n[k.s] + k.c0(p)) >> 6;
                 const uint32_t bt = base + C::RING_OFF + slot * C::SLOT_BYTES;
-                mbar_arrive_expect_tx(bar_bfull + 8 * slot, C::B_BYTES);
+                mbar_arrive_expect_tx(bar_bfull + 8 * slot, C::B_BYTES / C::BISSUE);
 #pragma unroll
-                for (int b = 0; b < C::NBOX; ++b)
+                for (int b = warp - 1; b < C::NBOX; b += C::BISSUE)
                     tma_load_5d(bt + b * TC_BN * 128, &p.bmap[k.s], b * C::BOX_K, 0, 0, 0, blk,
                                 bar_bfull + 8 * slot);
             }
@@ -352,7 +385,7 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
         __syncwarp();
     } else if (warp < C::EPI0) {
         // ------------------------------------------------------ y loaders
-        const int lt = tid - 32 * TC_YL0;                  // 0 .. C::LT - 1
+        const int lt = tid - 32 * C::YL0;                  // 0 .. C::LT - 1
         const uint16_t *const ydummy = p.y;
         int cur_tile = -1;
         int ltok[C::Y_PER_T];                              // rows i * (LT / PPR) + lt / PPR
@@ -420,8 +453,8 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
             }
         };
         // this warp's row of x (slice s), half h of the rank, rounded to bf16
-        // into the A operand's TMEM columns
-        auto convert_x = [&](int s) {
+        // into A buffer buf's TMEM columns
+        auto convert_x = [&](int s, int buf) {
             wait_once();                                   // x is the shrink output
             const int64_t xrow = (int64_t(s) * T + (ctok >= 0 ? ctok : 0)) * R;
             uint32_t wv[RP / 4];
@@ -448,18 +481,28 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
                 wv[4 * j + 2] = v.z;
                 wv[4 * j + 3] = v.w;
             }
-            tmem_st<RP / 4>(tmem + (uint32_t(q * 32) << 16) + uint32_t(TC_A_COL + h * (RP / 4)),
+            tmem_st<RP / 4>(tmem + (uint32_t(q * 32) << 16) +
+                                uint32_t(TC_A_COL + buf * C::A_COLS + h * (RP / 4)),
                             wv);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_x);
+            if (lane == 0) mbar_arrive(bar_x + 8 * buf);
         };
 
         TcCursor k;
         k.start(p, w_begin, nchunks);
-        tile_rows(k.tile);
-        convert_x(k.s);
+        {
+            // the first TC_NXB row items' A operands, before the first chunk
+            TcCursor kc = k;
+            int64_t wc = w_begin;
+            for (int n = 0; n < TC_NXB && wc < w_end; ++n) {
+                tile_rows(kc.tile);
+                convert_x(kc.s, n);
+                wc += kc.skip_item(p, nchunks);
+            }
+        }
+        int item = 0;                                  // row item of the current chunk
 
         int g = 0;
 #pragma unroll 1
@@ -551,9 +594,9 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
                 k.next(p, nchunks);
-                if (w + 1 < w_end && k.first) {
+                if (w + 1 < w_end && k.first && ++item >= TC_NXB) {
                     tile_rows(k.tile);
-                    convert_x(k.s);
+                    convert_x(k.s, item % TC_NXB);
                 }
             };
             const uint32_t tl = tmem + (uint32_t(q * 32 + h * 16) << 16) + uint32_t(ab * TC_BN);
