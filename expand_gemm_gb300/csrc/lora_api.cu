@@ -48,6 +48,7 @@ static Knobs read_knobs()
     k.expand_tc_min_rank = env_int("LORA_PUNICA_EXPAND_TC_MIN_RANK", 64);
     k.meta_small = env_int("LORA_PUNICA_META_SMALL", 1);
     k.meta_multi = env_int("LORA_PUNICA_META_MULTI", 1);
+    k.meta_cluster = env_int("LORA_PUNICA_META_CLUSTER", 1);
     k.coop_test_extra = env_int("LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS", 0);
     k.coop_test_timeout = env_int("LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES", 0);
     return k;

@@ -492,6 +492,7 @@ struct Knobs {
     int expand_tc_min_rank;   // LORA_PUNICA_EXPAND_TC_MIN_RANK (64)
     int meta_small;           // LORA_PUNICA_META_SMALL (1)
     int meta_multi;           // LORA_PUNICA_META_MULTI: multi-CTA metadata kernel (1)
+    int meta_cluster;         // LORA_PUNICA_META_CLUSTER: its thread-block-cluster form (1)
     int coop_test_extra;      // LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS (0, tests only)
     int coop_test_timeout;    // LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES (0, tests only)
 };

@@ -377,6 +377,193 @@ __global__ void __launch_bounds__(NT) meta_multi_kernel(MetaArgs a)
     }
 }
 
+// ------------------------------------------------------------------------
+// Thread-block-cluster form (one cluster of C <= 8 CTAs is the whole grid,
+// batches of META_MULTI_BIG + 1 .. META_CLUSTER_MAX tokens): CTA c owns the
+// run of GW * NT tokens starting at c * GW * NT (GW 32-token groups per
+// warp) and counts only that run.  Its bin totals and its start inside
+// every bin come from the other CTAs' run counts, read from their shared
+// memory after a cluster barrier, instead of every CTA reading the whole
+// map (2.6 us of the 4 us kernel at 16384 tokens).  Every thread passes
+// both cluster barriers on one straight path (no early return), so neither
+// can be left waiting.
+constexpr int META_CLUSTER_MAX = 8 * 4 * 1024;
+
+__device__ __forceinline__ uint32_t meta_cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ int32_t meta_ld_cluster(const int32_t *local, uint32_t rank)
+{
+    uint32_t a, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(a) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(a) : "memory");
+    return int32_t(v);
+}
+// (.aligned: the warp reaches them converged)
+__device__ __forceinline__ void meta_cluster_arrive()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void meta_cluster_wait()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+template <int NT, int GW>
+__global__ void __launch_bounds__(NT) meta_cluster_kernel(MetaArgs a)
+{
+    constexpr int NW = NT / 32;
+    extern __shared__ int32_t sm[];
+    const int nb = a.max_loras + 1;
+    int32_t *own = sm;                          // [NW][nb]: run counts per warp, then offsets
+    int32_t *run = own + NW * nb;               // [nb] this CTA's run (read by the others)
+    int32_t *bef = run + nb;                    // [nb] tokens of the CTAs before this one
+    int32_t *tot = bef + nb;                    // [nb] all tokens
+    int32_t *base = tot + nb;                   // [nb] first sorted slot of the bin
+    int32_t *pos = base + nb;                   // [nb] index among non-empty bins
+    __shared__ int32_t s_invalid, s_nactive, s_bad_all;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = a.num_tokens;
+    const uint32_t crank = meta_cluster_rank();     // == blockIdx.x: one cluster per grid
+    const int nctas = int(gridDim.x);
+    const int tw0 = int(crank) * (NT * GW) + warp * (32 * GW);   // this warp's run
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    int32_t idv[GW];
+#pragma unroll
+    for (int j = 0; j < GW; ++j) {
+        const int t = tw0 + 32 * j + lane;
+        idv[j] = t < T ? a.map[t] : -1;
+    }
+    for (int i = tid; i < NW * nb; i += NT) own[i] = 0;
+    if (tid == 0) s_invalid = 0;
+    __syncthreads();
+    int bad = 0;
+#pragma unroll
+    for (int j = 0; j < GW; ++j) {
+        const int t = tw0 + 32 * j + lane;
+        const bool has = t < T;
+        const int b = has ? token_bin(idv[j], a.max_loras, bad) : -1;
+        count_group(own + warp * nb, b, has, lane);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if (lane == 0 && bad) atomicAdd(&s_invalid, bad);
+    __syncthreads();
+    scan_bins_over_warps<NT, NW>(own, run, nullptr, nullptr, nb);
+
+    meta_cluster_arrive();                      // every CTA's run counts are final
+    meta_cluster_wait();
+    // eight lanes per bin, one CTA's count each (one remote load a thread,
+    // all in flight together), summed by shuffles
+    for (int i0 = 0; i0 < nb * 8; i0 += NT) {      // the same in every thread
+        const int i = i0 + tid, b = i >> 3, c = i & 7;
+        const int v = (b < nb && c < nctas) ? meta_ld_cluster(run + b, uint32_t(c)) : 0;
+        int st = v, sb = c < int(crank) ? v : 0;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            st += __shfl_xor_sync(0xffffffffu, st, o);
+            sb += __shfl_xor_sync(0xffffffffu, sb, o);
+        }
+        if (b < nb && c == 0) {
+            bef[b] = sb;
+            tot[b] = st;
+        }
+    }
+    if (crank == 0 && tid == 0) {
+        int sbad = 0;
+        for (int c = 0; c < nctas; ++c) sbad += meta_ld_cluster(&s_invalid, uint32_t(c));
+        s_bad_all = sbad;
+    }
+    meta_cluster_arrive();                      // done reading the others' shared memory
+    __syncthreads();
+    scan_over_bins<NT>(tot, base, pos, &s_nactive, nb);
+    __syncthreads();
+
+    const bool no_lora = (tot[0] == T);
+    const int nact = no_lora ? 0 : s_nactive;
+    if (crank == 0) {
+        for (int k = tid; k < nb; k += NT) {
+            if (k >= nact) {
+                a.active[k] = -1;
+                a.counts[k] = 0;
+                a.start_loc[k + 1] = 0;
+            }
+        }
+        if (tid == 0) {
+            a.start_loc[0] = 0;
+            *a.no_lora = no_lora ? 1 : 0;
+            *a.error_word = s_bad_all;
+        }
+        if (!no_lora) {
+            for (int b = tid; b < nb; b += NT) {
+                const int c = tot[b];
+                if (c > 0) {
+                    const int k = pos[b];
+                    a.active[k] = b - 1;
+                    a.counts[k] = c;
+                    a.start_loc[k + 1] = base[b] + c;
+                }
+            }
+        }
+    }
+    if (!no_lora) {                             // stable scatter of this warp's run
+        int unused = 0;
+#pragma unroll
+        for (int j = 0; j < GW; ++j) {
+            const int t = tw0 + 32 * j + lane;
+            const bool has = t < T;
+            const int b = has ? token_bin(idv[j], a.max_loras, unused) : -1;
+            int n = 0;
+            const int rank = rank_in_group(b, has, lane, n);
+            if (has) {
+                a.sorted[base[b] + bef[b] + own[warp * nb + b] + rank] = t;
+                a.mapping_copy[t] = idv[j];
+            }
+            __syncwarp();
+            if (has && rank == 0) own[warp * nb + b] += n;
+            __syncwarp();
+        }
+    }
+    meta_cluster_wait();                        // no CTA leaves while another reads it
+}
+
+size_t meta_cluster_smem_bytes(int max_loras)
+{
+    const size_t nb = size_t(max_loras) + 1;
+    return (size_t(META_MULTI_THREADS / 32) * nb + 5 * nb) * sizeof(int32_t);
+}
+
+template <int GW>
+static cudaError_t launch_meta_cluster(const MetaArgs &a, cudaStream_t stream)
+{
+    constexpr int NT = META_MULTI_THREADS;
+    const int grid = (a.num_tokens + NT * GW - 1) / (NT * GW);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = meta_cluster_smem_bytes(a.max_loras);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(grid);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, meta_cluster_kernel<NT, GW>, a);
+}
+
 size_t meta_multi_smem_bytes(int warps, int max_loras)
 {
     const size_t nb = size_t(max_loras) + 1;
@@ -410,6 +597,16 @@ int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
                                  int(meta_multi_smem_bytes(META_MULTI_SMALL_THREADS / 32,
                                                            LORA_MAX_LORAS)));
         if (e != cudaSuccess) return int(e);
+        const int csm = int(meta_cluster_smem_bytes(LORA_MAX_LORAS));
+        e = cudaFuncSetAttribute(meta_cluster_kernel<META_MULTI_THREADS, 1>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, csm);
+        if (e != cudaSuccess) return int(e);
+        e = cudaFuncSetAttribute(meta_cluster_kernel<META_MULTI_THREADS, 2>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, csm);
+        if (e != cudaSuccess) return int(e);
+        e = cudaFuncSetAttribute(meta_cluster_kernel<META_MULTI_THREADS, 4>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, csm);
+        if (e != cudaSuccess) return int(e);
         configured[dev] = 1;
     }
     // Batches above META_MULTI_MIN tokens on one CTA per run of 256 or 1024
@@ -420,6 +617,16 @@ int launch_meta_prepare(const MetaArgs &a, cudaStream_t stream)
             return int(launch_kernel(meta_multi_kernel<NT>, dim3((a.num_tokens + NT - 1) / NT),
                                      dim3(NT), meta_multi_smem_bytes(NT / 32, a.max_loras),
                                      stream, a));
+        }
+        // up to META_CLUSTER_MAX tokens: one cluster of at most 8 CTAs
+        // (LORA_PUNICA_META_CLUSTER=0 keeps the plain multi-CTA kernel)
+        if (a.num_tokens <= META_CLUSTER_MAX && knobs().meta_cluster) {
+            const int t = a.num_tokens;
+            e = t <= 8 * 1024    ? launch_meta_cluster<1>(a, stream)
+                : t <= 16 * 1024 ? launch_meta_cluster<2>(a, stream)
+                                 : launch_meta_cluster<4>(a, stream);
+            if (e == cudaSuccess) return 0;
+            (void)cudaGetLastError();          // a cluster that cannot be placed: plain kernel
         }
         constexpr int NT = META_MULTI_THREADS;
         return int(launch_kernel(meta_multi_kernel<NT>, dim3((a.num_tokens + NT - 1) / NT),

@@ -140,15 +140,17 @@ def _maps(T, L, seed):
     return [per_token, runs, np.full(T, -1, np.int32)]
 
 
-@pytest.mark.parametrize("multi", ["0", "1"])
+@pytest.mark.parametrize("multi,cluster", [("0", "0"), ("1", "0"), ("1", "1")])
 @pytest.mark.parametrize("T,L", [(513, 8), (1000, 1024), (2048, 8), (2049, 8), (4096, 64),
-                                 (4097, 33), (16384, 64), (20000, 1024), (70001, 300)])
-def test_meta_single_and_multi_cta(oracle_mod, knob, multi, T, L):
-    """The single-CTA kernel and the multi-CTA kernel (batches above 512
+                                 (4097, 33), (8192, 16), (8193, 1024), (16384, 64),
+                                 (20000, 1024), (32768, 64), (32769, 8), (70001, 300)])
+def test_meta_single_and_multi_cta(oracle_mod, knob, multi, cluster, T, L):
+    """The single-CTA kernel, the multi-CTA kernel (batches above 512
     tokens: one CTA per 256 tokens up to 4096, per 1024 above, each
-    counting the whole map itself) give the oracle's metadata bit for bit,
-    on per-token maps with invalid ids, run-ordered maps and the all -1
-    map."""
-    knob(LORA_PUNICA_META_MULTI=multi)
+    counting the whole map itself) and its cluster form (4097 to 32768
+    tokens: up to 8 CTAs that read each other's run counts) give the
+    oracle's metadata bit for bit, on per-token maps with invalid ids,
+    run-ordered maps and the all -1 map."""
+    knob(LORA_PUNICA_META_MULTI=multi, LORA_PUNICA_META_CLUSTER=cluster)
     for ids in _maps(T, L, seed=T + L):
         _check(ids, L, oracle_mod)
