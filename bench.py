@@ -52,9 +52,9 @@ E2E_GRAPH_STEPS = 8
 # reports null.
 NCU_TRAFFIC = {
     # expand_tc_kernel<8> and shrink_umma_kernel, one launch each at full size
-    # (profiles/traffic_large.md)
-    ("expand", "large"): ("07e80461fcf9af32", 667499264),
-    ("shrink", "large"): ("5c6eb0c54a708943", 445830656),
+    # (dram__bytes_read.sum + dram__bytes_write.sum, one single-pass capture)
+    ("expand", "large"): ("eeb996531aa1f053", 659956736),
+    ("shrink", "large"): ("1c1a1a075fa46191", 445693184),
 }
 
 # The source files each reported kernel is built from.
