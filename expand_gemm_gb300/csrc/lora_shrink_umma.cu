@@ -142,7 +142,35 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     const int nk = (H + UM_BK - 1) / UM_BK;
     const int kchunks = shrink_kchunks(total_tiles, nk, int(gridDim.x), UM_MIN_BLOCKS);
     const int spc = (nk + kchunks - 1) / kchunks;
-    const int total_items = total_tiles * kchunks;      // item = kc * total_tiles + tile
+    // Items: item = kc * total_tiles + tile.  When every tile is one whole
+    // item and some CTAs would have none, the first `extra` tiles are halved
+    // along the hidden dimension instead (items 2j and 2j + 1 are the halves
+    // of tile j < extra, item extra + t the whole tile t >= extra): the
+    // idle SMs take half of those tiles, and the first tile (on a mixed
+    // batch, the one whose tokens break into the most short runs, whose CTA
+    // finished last) is one of them.
+    const int extra = (kchunks == 1 && total_tiles < int(gridDim.x) && nk >= 2 * UM_MIN_BLOCKS)
+                          ? min(int(gridDim.x) - total_tiles, total_tiles)
+                          : 0;
+    const int total_items = total_tiles * kchunks + extra;
+    auto item_range = [&](int item, int &tile, int &kb0, int &kb1) {
+        if (extra > 0) {
+            if (item < 2 * extra) {
+                tile = item >> 1;
+                kb0 = (item & 1) ? nk / 2 : 0;
+                kb1 = (item & 1) ? nk : nk / 2;
+            } else {
+                tile = item - extra;
+                kb0 = 0;
+                kb1 = nk;
+            }
+            return;
+        }
+        tile = item % total_tiles;
+        const int kc = item / total_tiles;
+        kb0 = kc * spc;
+        kb1 = min(nk, kb0 + spc);
+    };
     if (int(blockIdx.x) >= total_items) return;
 
     if (warp == UM_MMA_WARP) tmem_alloc(smem_addr(s_tmem), p.tmem_cols);
@@ -167,8 +195,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
         int issued = 0;
         bool ok = true;
         for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x) {
-            const int tile = item % total_tiles, kc = item / total_tiles;
-            const int kb0 = kc * spc, kb1 = min(nk, kb0 + spc);
+            int tile, kb0, kb1;
+            item_range(item, tile, kb0, kb1);
             const int seg = find_segment(tab.tile, p.nbins, tile);
             const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * UM_BM;
             // rows of this tile that belong to the segment (all 128 but in
@@ -235,8 +263,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
             int issued = 0;
             bool ok = true;
             for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x) {
-                const int tile = item % total_tiles, kc = item / total_tiles;
-                const int kb0 = kc * spc, kb1 = min(nk, kb0 + spc);
+                int tile, kb0, kb1;
+                item_range(item, tile, kb0, kb1);
                 const int id = tab.id[find_segment(tab.tile, p.nbins, tile)];
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, s_abort, deadline)) {
@@ -276,8 +304,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x) {
-                const int kc = item / total_tiles;
-                const int kb0 = kc * spc, kb1 = min(nk, kb0 + spc);
+                int tile, kb0, kb1;
+                item_range(item, tile, kb0, kb1);
                 if (!mbar_wait_bounded(bar_acc_empty, acc_phase ^ 1, s_abort, deadline)) {
                     ok = false;
                     break;
@@ -322,7 +350,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
         const int row = q * 32 + lane;          // token row inside the tile
         uint32_t acc_phase = 0;
         for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-            const int tile = item % total_tiles;
+            int tile, kb0, kb1;
+            item_range(item, tile, kb0, kb1);
             const int seg = find_segment(tab.tile, p.nbins, tile);
             const int row0 = tab.start[seg] + (tile - tab.tile[seg]) * UM_BM;
             // rows past the segment's end hold stale shared data: their
