@@ -23,7 +23,7 @@
 namespace lora {
 
 template <int KT>
-__global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(ExpandArgs p)
+__global__ void __launch_bounds__(EX_THREADS, (KT <= 2) ? 3 : 2) expand_kernel(ExpandArgs p)
 {
     using Cfg = ExpandTile<KT>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
     };
     if (!p.early) wait_once();
 
-    uint8_t *sA = smem + EX_STAGES * Cfg::STAGE_BYTES;
+    uint8_t *sA = smem + Cfg::NST * Cfg::STAGE_BYTES;
     const SegTab tab = seg_tab(reinterpret_cast<int *>(sA + Cfg::A_BYTES), p.nbins);
     const int32_t *tokens = p.sorted;
     int total_tiles;
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(EX_THREADS, (KT <= 1) ? 3 : 2) expand_kernel(E
     }
     // early mode: the grid-dependency wait sits right before the first read
     // of the shrink output
-    expand_items<KT>(p, tab, tokens, total_tiles, smem, s_tok, [&]() {
+    expand_items<KT, Cfg::NST>(p, tab, tokens, total_tiles, smem, s_tok, [&]() {
         wait_once();
         return true;
     });

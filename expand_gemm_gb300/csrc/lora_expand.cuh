@@ -74,7 +74,11 @@ struct ExpandTile {
     static constexpr int BIAS_BYTES = BN * 2;                // bf16 bias chunk
     static constexpr int STAGE_BYTES = Y_BYTES + B_BYTES + BIAS_BYTES;
     static constexpr int A_BYTES = EX_BM * RP * 2;
-    static constexpr int BYTES = EX_STAGES * STAGE_BYTES + A_BYTES;
+    // ring stages of the expand kernel: rank 32 takes two, which leaves room
+    // (shared memory and, at 80 registers, the register file) for three
+    // CTAs per SM instead of two
+    static constexpr int NST = (KT == 2) ? 2 : EX_STAGES;
+    static constexpr int BYTES = NST * STAGE_BYTES + A_BYTES;
     // Copy shapes: y pieces (16 bytes) of one row are taken by YCH
     // consecutive threads, so one pass covers Y_RPP rows and every thread
     // keeps the same Y_PASSES rows for a whole tile; B likewise with CPR
