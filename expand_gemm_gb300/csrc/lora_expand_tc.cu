@@ -230,10 +230,15 @@ struct TcCursor {
     }
 };
 
-template <int KT>
+// BIAS: some slice has a bias.  Without one the epilogue keeps fewer
+// registers live, which lets rank 128 request both accumulator halves
+// before finishing either (with the bias path compiled in, that spilled).
+template <int KT, bool BIAS>
 __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const __grid_constant__ TcArgs p)
 {
     using C = TcCfg<KT>;
+    constexpr bool OVERLAP = C::OVERLAP;
+    constexpr bool ACC_BOTH = !C::OVERLAP && !BIAS;     // both halves' accumulators, then y
     constexpr int RP = C::RP, CPR = C::CPR, DEPTH = C::DEPTH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -510,8 +515,8 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
             tile_rows(k.tile);
             const int kc0 = k.c0(p), ks = k.s;
             const int ncols = min(TC_BN, p.n[ks] - kc0);
-            const uint16_t *bias_row = p.bias[ks] ? p.bias[ks] + int64_t(c_id) * p.n[ks] + kc0
-                                                  : nullptr;
+            const uint16_t *bias_row = (BIAS && p.bias[ks]) ? p.bias[ks] + int64_t(c_id) * p.n[ks] + kc0
+                                                            : nullptr;
             const int ab = g % TC_NACC;
             const int slot = g % DEPTH;
             bool got = mbar_wait_bounded(bar_accf + 8 * ab, uint32_t(g / TC_NACC) & 1u, s_abort,
@@ -522,7 +527,7 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
             tc_fence_after();
             const int tok[2] = {qtok[0], qtok[1]};
             const uint8_t *yt = smem + C::RING_OFF + slot * C::SLOT_BYTES + C::B_BYTES;
-            const bool has_bias = bias_row != nullptr;
+            const bool has_bias = BIAS && bias_row != nullptr;
             // x B + old y + bias, rounded once, straight to y: output columns
             // 64 hf + 16 qt + 2j + e of the chunk are accumulator columns
             // 64 hf + 8j + 2 qt + e, registers acc[4j + e] (row qrow) and
@@ -600,7 +605,7 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
                 }
             };
             const uint32_t tl = tmem + (uint32_t(q * 32 + h * 16) << 16) + uint32_t(ab * TC_BN);
-            if constexpr (C::OVERLAP) {
+            if constexpr (OVERLAP) {
                 // both halves' accumulators and old y requested before any
                 // is waited for: the chunk's latencies overlap
                 uint32_t va[TC_HALVES][32];
@@ -614,6 +619,21 @@ __global__ void __launch_bounds__(TcCfg<KT>::THREADS, 1) expand_tc_kernel(const 
                 release_acc();
 #pragma unroll
                 for (int hf = 0; hf < TC_HALVES; ++hf) finish_half(hf, va[hf], yv[hf]);
+            } else if constexpr (ACC_BOTH) {
+                // both halves' accumulators requested together (one TMEM
+                // latency a chunk), old y read half by half
+                uint32_t va[TC_HALVES][32];
+#pragma unroll
+                for (int hf = 0; hf < TC_HALVES; ++hf)
+                    tmem_ld16x256b_x8_nowait(tl + uint32_t(hf * 64), va[hf]);
+                tmem_wait_ld();
+                release_acc();
+#pragma unroll
+                for (int hf = 0; hf < TC_HALVES; ++hf) {
+                    uint4 yv[2][2];
+                    load_y(hf, yv);
+                    finish_half(hf, va[hf], yv);
+                }
             } else {
 #pragma unroll
                 for (int hf = 0; hf < TC_HALVES; ++hf) {
@@ -649,13 +669,18 @@ static int launch_tc_kt(const TcArgs &p, cudaStream_t stream)
     const size_t smem = tc_smem_bytes<KT>(p.nbins);
     if (smem > 227 * 1024) return TC_NO_FIT;
     if (dev < 64 && configured[dev] == 0) {
-        e = cudaFuncSetAttribute(expand_tc_kernel<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 227 * 1024);
+        e = cudaFuncSetAttribute(expand_tc_kernel<KT, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return int(e);
+        e = cudaFuncSetAttribute(expand_tc_kernel<KT, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return int(e);
         configured[dev] = 1;
     }
-    e = launch_kernel(expand_tc_kernel<KT>, dim3(device_sm_count()), dim3(TcCfg<KT>::THREADS), smem,
-                      stream, p);
+    bool bias = false;
+    for (int s = 0; s < p.num_slices; ++s) bias = bias || p.bias[s] != nullptr;
+    e = launch_kernel(bias ? expand_tc_kernel<KT, true> : expand_tc_kernel<KT, false>,
+                      dim3(device_sm_count()), dim3(TcCfg<KT>::THREADS), smem, stream, p);
     return e == cudaSuccess ? int(TC_LAUNCHED) : int(e);
 }
 
