@@ -64,6 +64,7 @@ KERNEL_SOURCES = {
     "shrink": ("lora_shrink.cu", "lora_shrink_umma.cu", "lora_umma.cuh", "lora_common.cuh"),
     "linear_coop": ("lora_linear_coop.cu", "lora_expand.cuh", "lora_common.cuh"),
     "linear_fused": ("lora_fused.cu", "lora_common.cuh"),
+    "linear_tc": ("lora_linear_tc.cu", "lora_umma.cuh", "lora_common.cuh"),
 }
 
 
@@ -132,6 +133,18 @@ def fused_path(w) -> bool:
     limit = 512 if mode == "1" else int(os.environ.get("LORA_PUNICA_FUSED_MAX_TOKENS", "128"))
     return (w.num_tokens <= limit and w.max_loras <= 256 and _padded_rank(w.rank) <= 64
             and w.num_slices * _padded_rank(w.rank) <= 128 and mode != "0")
+
+
+def linear_tc_path(w) -> bool:
+    """lora_linear's rule for its rank-128 tensor-core kernel (metadata
+    kernel + one kernel for the shrink and expand of every tile)."""
+    if coop_path(w) or fused_path(w) or w.kind == "embedding":
+        return False
+    mode = os.environ.get("LORA_PUNICA_LINEAR_TC", "-1")
+    min_t = int(os.environ.get("LORA_PUNICA_UMMA_MIN_TOKENS", "1024"))
+    return (mode != "0" and (mode == "1" or w.num_tokens >= min_t) and w.rank == 128
+            and w.num_slices <= 3 and all(n % 64 == 0 for n in w.slices)
+            and w.hidden >= 64 and w.hidden % 8 == 0)
 
 
 def umma_shrink_path(w) -> bool:
@@ -389,7 +402,8 @@ class Measured:
         self.k = {"meta": k_meta, "shrink": k_shrink, "expand": k_expand, "step": k_step}
         self.coop = coop_path(w) and not emb
         self.fused = (fused_path(w) and not emb) or self.coop
-        self.launches_per_step = (2 if emb else 1 if self.fused else 3 + (
+        self.linear_tc = linear_tc_path(w) and not self.fused
+        self.launches_per_step = (2 if emb or self.linear_tc else 1 if self.fused else 3 + (
             1 if umma_shrink_path(w) and os.environ.get("LORA_PUNICA_UMMA_PARTIAL", "1") == "0"
             else 0))
         del sets, base
@@ -400,7 +414,9 @@ class Measured:
             return "metadata + expand of a bf16 input (add_lora_embedding): two kernels"
         return "lora_linear (metadata + shrink + expand): %s" % (
             "one cooperative kernel" if self.coop else
-            "one fused cluster kernel" if self.fused else "three kernels")
+            "one fused cluster kernel" if self.fused else
+            "metadata kernel + one tensor-core shrink/expand kernel" if self.linear_tc else
+            "three kernels")
 
     def summary(self, args, step_ms=None):
         """The workload's figures: the step and each kernel, with the
@@ -415,6 +431,13 @@ class Measured:
             dominant, dom_bytes, dom_ms = "linear_coop", step_bytes, k["step"]
         elif self.fused:
             dominant, dom_bytes, dom_ms = "linear_fused", step_bytes, k["step"]
+        elif self.linear_tc:
+            # the step is the metadata kernel + this one: its time is the
+            # step's less the metadata kernel's, both timed the same way; its
+            # bytes are the shrink's and the expand's without the expand's
+            # re-read of the buffer (the tile's rows stay on chip)
+            dominant, dom_bytes = "linear_tc", ub["linear"]
+            dom_ms = k["step"] - k["meta"]
         else:
             dominant = "expand" if k["expand"] >= k["shrink"] else "shrink"
             dom_bytes, dom_ms = ub[dominant], k[dominant]
@@ -455,7 +478,10 @@ class Measured:
             "roofline": {
                 "bound": "hbm", "kernel": "lora_" + dominant,
                 "note": ("single kernel: algorithmic bytes of shrink + expand per launch"
-                         if self.fused else "the step's longest kernel"),
+                         if self.fused else
+                         "shrink + expand kernel (the buffer read once, written once); "
+                         "launch time = step - metadata kernel" if self.linear_tc else
+                         "the step's longest kernel"),
                 "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic,
                 "algorithmic_bytes_per_launch": dom_bytes,

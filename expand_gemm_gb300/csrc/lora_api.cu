@@ -49,6 +49,7 @@ static Knobs read_knobs()
     k.meta_small = env_int("LORA_PUNICA_META_SMALL", 1);
     k.meta_multi = env_int("LORA_PUNICA_META_MULTI", 1);
     k.meta_cluster = env_int("LORA_PUNICA_META_CLUSTER", 1);
+    k.linear_tc = env_int("LORA_PUNICA_LINEAR_TC", -1);
     k.coop_test_extra = env_int("LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS", 0);
     k.coop_test_timeout = env_int("LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES", 0);
     return k;
@@ -85,6 +86,21 @@ bool encode_tile_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t co
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tile_map_f32(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols,
+                         uint64_t row_stride, uint32_t box_cols, uint32_t box_rows,
+                         CUtensorMapSwizzle swizzle)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_stride * 4};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

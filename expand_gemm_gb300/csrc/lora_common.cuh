@@ -493,6 +493,7 @@ struct Knobs {
     int meta_small;           // LORA_PUNICA_META_SMALL (1)
     int meta_multi;           // LORA_PUNICA_META_MULTI: multi-CTA metadata kernel (1)
     int meta_cluster;         // LORA_PUNICA_META_CLUSTER: its thread-block-cluster form (1)
+    int linear_tc;            // LORA_PUNICA_LINEAR_TC: lora_linear's one-kernel tensor-core path (-1)
     int coop_test_extra;      // LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS (0, tests only)
     int coop_test_timeout;    // LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES (0, tests only)
 };
@@ -582,6 +583,36 @@ struct ExpandLaunch {
     const int32_t *no_lora;
     int32_t *error_word;
 };
+// The shrink and expand of one lora_linear call in one tensor-core kernel
+// (lora_linear_tc.cu): rank 128, up to three slices.  linear_tc_fits says
+// whether a call fits it; launch_linear_tc returns 0 when launched or a
+// cudaError_t.
+struct LinearTcLaunch {
+    const uint16_t *x;
+    int64_t x_ld;
+    int32_t hidden;
+    int32_t num_tokens;
+    const uint16_t *a[LORA_MAX_SLICES];
+    const uint16_t *b[LORA_MAX_SLICES];
+    const uint16_t *bias[LORA_MAX_SLICES];
+    int32_t n[LORA_MAX_SLICES];
+    int32_t num_slices;
+    int32_t rank;
+    int32_t max_loras;
+    float scale;
+    float *buf;
+    uint16_t *y;
+    int64_t y_ld;
+    const int32_t *sorted;
+    const int32_t *counts;
+    const int32_t *start_loc;
+    const int32_t *active;
+    const int32_t *no_lora;
+    int32_t *error_word;
+};
+bool linear_tc_fits(const LinearTcLaunch &a);
+int launch_linear_tc(const LinearTcLaunch &a, cudaStream_t stream);
+
 // launch_expand_tc's results besides a cudaError_t (positive).
 enum : int { TC_LAUNCHED = 0, TC_NO_FIT = -1, TC_MISALIGNED = -2 };
 int launch_expand_tc(const ExpandLaunch &a, cudaStream_t stream);

@@ -765,6 +765,51 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
             if (r != 0) return r;
         }
     }
+    // Rank 128, up to three slices, batches of at least
+    // LORA_PUNICA_UMMA_MIN_TOKENS tokens: the metadata kernel, then the
+    // shrink and the expand of every 128-token tile in one tensor-core
+    // kernel (lora_linear_tc.cu).  Measured on the large workload (16384
+    // tokens, three slices): 223 us against 241 for the metadata kernel and
+    // the separate tcgen05 shrink and expand.  LORA_PUNICA_LINEAR_TC=0 keeps
+    // the separate kernels; =1 takes it for every call it fits.
+    if (kn.linear_tc != 0 && token_lora_mapping != nullptr && meta->error_word != nullptr &&
+        (kn.linear_tc == 1 || num_tokens >= kn.umma_min_tokens) && rank == 128 &&
+        num_slices <= 3) {
+        lora::LinearTcLaunch u;
+        int64_t width = 0;
+        for (int s = 0; s < LORA_MAX_SLICES; ++s) u.a[s] = u.b[s] = u.bias[s] = nullptr;
+        for (int s = 0; s < num_slices; ++s) {
+            u.a[s] = lora_a[s];
+            u.b[s] = lora_b[s];
+            u.bias[s] = lora_bias ? lora_bias[s] : nullptr;
+            u.n[s] = slice_sizes[s];
+            width += slice_sizes[s];
+        }
+        u.x = x;
+        u.x_ld = x_ld;
+        u.hidden = hidden;
+        u.num_tokens = num_tokens;
+        u.num_slices = num_slices;
+        u.rank = rank;
+        u.max_loras = meta->max_loras;
+        u.scale = scale;
+        u.buf = buf;
+        u.y = y;
+        u.y_ld = y_ld;
+        u.sorted = meta->token_indices_sorted_by_lora_ids;
+        u.counts = meta->num_tokens_per_lora;
+        u.start_loc = meta->lora_token_start_loc;
+        u.active = meta->active_lora_ids;
+        u.no_lora = meta->no_lora_flag;
+        u.error_word = meta->error_word;
+        if (width <= y_ld && lora::linear_tc_fits(u)) {
+            int r = lora_meta_prepare(token_lora_mapping, num_tokens, meta, stream);
+            if (r != 0) return r;
+            r = lora::launch_linear_tc(u, st);
+            return r == 0 ? LORA_OK : r;
+        }
+    }
+
     // The metadata kernel, then the shrink in early mode (for batches of up
     // to 512 tokens it sorts the ids itself and starts its loads while the
     // metadata kernel runs), then the expand in early mode (it fetches the

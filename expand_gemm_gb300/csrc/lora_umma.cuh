@@ -243,11 +243,35 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 2-D tile store shared -> global (bulk group; coordinates not negative).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int c1, uint32_t src)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n"
+        :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(src) : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+// Waits until the shared memory read by this thread's bulk stores is free.
+__device__ __forceinline__ void bulk_wait_group_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's count includes this arrival: no pending-count increment).
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
 {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" :: "r"(bar) : "memory");
+}
+
+// The same with the pending count incremented first: a net-zero arrival
+// (the barrier waits for this thread's copies without counting the thread).
+__device__ __forceinline__ void cp_async_mbar_arrive_track(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" :: "r"(bar) : "memory");
 }
 
 // 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
@@ -262,6 +286,12 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// Brings the 128-byte line holding p into L2 (no register written, no wait).
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];\n" :: "l"(reinterpret_cast<uint64_t>(p)));
 }
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
@@ -504,6 +534,11 @@ __device__ __forceinline__ void shrink_epilogue_row(uint32_t tlane, float *y, in
 bool encode_tile_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols,
                      uint64_t row_stride, uint32_t box_cols, uint32_t box_rows,
                      CUtensorMapSwizzle swizzle);
+
+// The same over a 2-D fp32 tensor (row stride in elements).
+bool encode_tile_map_f32(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols,
+                         uint64_t row_stride, uint32_t box_cols, uint32_t box_rows,
+                         CUtensorMapSwizzle swizzle);
 
 // Host: encodes the B map of the tensor-core expand over a bf16 matrix of
 // `rows` rows (a multiple of 64) of `rank` elements, whose boxes of

@@ -257,6 +257,13 @@ int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lora_b,
  *     bit 30 of the error word on expiry) separates it from the expand;
  *   - one thread-block-cluster kernel for other batches of at most 128
  *     tokens (max_loras <= 256, num_slices * padded rank <= 128);
+ *   - rank 128, at most three slices, slice widths multiples of 64, y
+ *     32-byte aligned with y_ld a multiple of 16, x and buf 16-byte
+ *     aligned, batches of at least LORA_PUNICA_UMMA_MIN_TOKENS tokens
+ *     (1024): the metadata kernel, then one tensor-core kernel that runs
+ *     the shrink of a 128-token tile, adds its result into that tile's
+ *     buffer rows and runs the tile's expand (one CTA per SM, tiles of one
+ *     LoRA in turn);
  *   - otherwise three kernels with programmatic dependent launch: the
  *     metadata kernel, the shrink (sorting the ids itself and loading
  *     before its dependency wait, for <= 512 tokens) and the expand
@@ -264,8 +271,9 @@ int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lora_b,
  * Environment (read once, see lora_reload_options): LORA_PUNICA_COOP=0/1
  * never / always (when the batch fits) the cooperative kernel;
  * LORA_PUNICA_FUSED=0/1 and LORA_PUNICA_FUSED_MAX_TOKENS the cluster
- * kernel; LORA_PUNICA_SELF_META=1 two kernels (the shrink writes the
- * metadata), =0 the plain three calls.
+ * kernel; LORA_PUNICA_LINEAR_TC=0/1 never / for every call that fits (any
+ * batch size) the rank-128 tensor-core kernel; LORA_PUNICA_SELF_META=1 two
+ * kernels (the shrink writes the metadata), =0 the plain three calls.
  */
 int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
                 const lora_bf16_t *x, int32_t hidden, int64_t x_ld,

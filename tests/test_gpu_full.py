@@ -1,8 +1,10 @@
 """Full-size parity: every workload at its stated size, every token.
 
-Two routes are checked against the oracle: ``lora_linear`` (the metadata
+Three routes are checked against the oracle: ``lora_linear`` (the metadata
 kernel, the shrink and the expand of one layer in one call: the step the
-benchmark times, in the same launch configuration) and the separate
+benchmark times, in the same launch configuration; on rank 128 one
+tensor-core kernel after the metadata kernel), the same call with the shrink
+and expand kernels apart (LORA_PUNICA_LINEAR_TC=0), and the separate
 ``lora_meta_prepare`` / ``lora_shrink`` / ``lora_expand`` calls.  For each:
 
 * the metadata, bit-exact, in full;
@@ -16,7 +18,7 @@ benchmark times, in the same launch configuration) and the separate
 
 The oracle computes the large workload (16384 tokens, hidden 8192, rank 128,
 three slices) in seconds on the host cores, so nothing is sampled.  Inputs
-and oracle results are computed once per workload and shared by both routes.
+and oracle results are computed once per workload and shared by the routes.
 """
 import numpy as np
 import pytest
@@ -88,6 +90,26 @@ def _run_lora_linear(eg, inp, x, A, B, bias, y, buf, meta):
     eg.lora_linear(dev_i32(inp.ids), x, A, B, bias, w.scale, buf, y, meta)
 
 
+def _run_lora_linear_three_kernels(eg, inp, x, A, B, bias, y, buf, meta):
+    """lora_linear with its one-kernel tensor-core path turned off
+    (LORA_PUNICA_LINEAR_TC=0): the rank-128 workloads, which take that path
+    by default, run the metadata, shrink and expand kernels instead."""
+    import os
+    w = inp.workload
+    old = os.environ.get("LORA_PUNICA_LINEAR_TC")
+    os.environ["LORA_PUNICA_LINEAR_TC"] = "0"
+    eg.reload_options()
+    try:
+        eg.lora_linear(dev_i32(inp.ids), x, A, B, bias, w.scale, buf, y, meta)
+        torch.cuda.synchronize()
+    finally:
+        if old is None:
+            del os.environ["LORA_PUNICA_LINEAR_TC"]
+        else:
+            os.environ["LORA_PUNICA_LINEAR_TC"] = old
+        eg.reload_options()
+
+
 def _run_separate(eg, inp, x, A, B, bias, y, buf, meta):
     w = inp.workload
     meta.prepare_tensors(dev_i32(inp.ids))
@@ -95,9 +117,11 @@ def _run_separate(eg, inp, x, A, B, bias, y, buf, meta):
     eg.lora_expand(buf, B, y, meta, w.offset_start, w.add_inputs, bias)
 
 
-# lora_linear is the benchmark's step; the separate calls are the three
-# entry points one by one.
+# lora_linear is the benchmark's step (on rank 128 the one tensor-core
+# kernel after the metadata kernel); the same call with the separate kernels;
+# the separate calls are the three entry points one by one.
 ROUTES = [pytest.param(_run_lora_linear, id="lora_linear"),
+          pytest.param(_run_lora_linear_three_kernels, id="lora_linear_three_kernels"),
           pytest.param(_run_separate, id="separate_calls")]
 
 

@@ -95,6 +95,51 @@ def test_linear_shapes(oracle_mod, knob, path, T, H, r, L, slices, bias, ids):
     _check_linear(oracle_mod, inp, buf0=b0)
 
 
+@pytest.mark.parametrize("T,H,slices,L,bias,ids", [
+    (300, 512, (128,), 4, False, "zipf_seq"),          # one slice
+    (700, 200, (256, 64), 6, True, "uniform_p"),       # ragged hidden, per-token ids, bias
+    (1100, 1024, (1024, 128, 192), 3, False, "zipf_seq"),   # three slices, a 64-column chunk
+    (129, 128, (64, 64, 64), 2, True, "uniform"),      # a one-row tile, 64-column slices
+    (2000, 2048, (512, 128, 128), 64, True, "mixed"),  # the large workload's id mix
+])
+def test_linear_one_kernel_tensor_core(oracle_mod, knob, T, H, slices, L, bias, ids):
+    """lora_linear's one-kernel tensor-core path (rank 128, up to three
+    slices: every tile's shrink, buffer update and expand on one SM) gives
+    the oracle's metadata, buffer and y, with a non-zero starting buffer."""
+    knob(LORA_PUNICA_LINEAR_TC="1", LORA_PUNICA_COOP="0", LORA_PUNICA_FUSED="0")
+    w = W.Workload("lintc", T + H, T, H, 128, L, slices, ids, p_none=0.15, seq_len=(40, 400),
+                   bias=bias, scale=0.7)
+    inp = W.generate(w)
+    b0 = np.random.default_rng(T + 1).standard_normal(inp.buf.shape).astype(np.float32)
+    _check_linear(oracle_mod, inp, buf0=b0)
+
+
+@pytest.mark.parametrize("T,slices", [
+    (1500, (200, 64)),       # a slice width that is not a multiple of 64: separate kernels
+    (600, (128, 128)),       # below the default's 1024 tokens: separate kernels
+    (1024, (256, 64, 128)),  # at the threshold: the one kernel
+])
+def test_linear_rank128_default_rule(oracle_mod, knob, T, slices):
+    """With the default rule (LORA_PUNICA_LINEAR_TC unset) rank-128 calls
+    take the one kernel or the separate ones; both give the oracle's
+    results."""
+    knob(LORA_PUNICA_LINEAR_TC=None)
+    w = W.Workload("lintc_default", T, T, 512, 128, 5, slices, "zipf_seq", p_none=0.1,
+                   seq_len=(40, 300), bias=True, scale=0.5)
+    _check_linear(oracle_mod, W.generate(w))
+
+
+def test_linear_one_kernel_tensor_core_no_lora(oracle_mod, knob):
+    """The one-kernel path on the all -1 batch and on invalid ids."""
+    knob(LORA_PUNICA_LINEAR_TC="1", LORA_PUNICA_COOP="0", LORA_PUNICA_FUSED="0")
+    inp = W.generate("large", num_tokens=640)
+    _check_linear(oracle_mod, inp, ids=np.full(640, -1, np.int32))
+    ids = inp.ids.copy()
+    ids[::7] = 64
+    ids[::11] = -5
+    _check_linear(oracle_mod, inp, ids=ids)
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_linear_no_lora_and_invalid_ids(oracle_mod, knob, path):
     _set_path(knob, path)

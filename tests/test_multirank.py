@@ -60,6 +60,25 @@ def test_single_process_helpers():
     assert bench.job_tokens_per_s(1, 256, 100, 10.0) == pytest.approx(256 * 100 / 0.010)
 
 
+def test_bench_path_rules_follow_the_library(monkeypatch):
+    """bench.py names the kernels lora_linear takes (and counts its launches
+    from them): the cooperative kernel on the tiny batch, the rank-128
+    tensor-core kernel on the large one unless LORA_PUNICA_LINEAR_TC=0,
+    three kernels on the rank-64 prefill."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    for k in ("LORA_PUNICA_COOP", "LORA_PUNICA_FUSED", "LORA_PUNICA_LINEAR_TC",
+              "LORA_PUNICA_UMMA_MIN_TOKENS"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.coop_path(W.WORKLOADS["tiny"]) and not bench.linear_tc_path(W.WORKLOADS["tiny"])
+    assert bench.linear_tc_path(W.WORKLOADS["large"])
+    assert not bench.linear_tc_path(W.WORKLOADS["prefill"])          # rank 64
+    assert not bench.linear_tc_path(W.WORKLOADS["embedding"])
+    monkeypatch.setenv("LORA_PUNICA_LINEAR_TC", "0")
+    assert not bench.linear_tc_path(W.WORKLOADS["large"])
+
+
 def test_reference_line_matches_the_contract():
     """The reference arm times the oracle on the host on the same workload
     config as the GPU arm, with zero host-device bytes in its e2e."""

@@ -69,6 +69,8 @@ def test_unique_bytes_counts_active_rows_and_loras():
     assert ub["t_active"] == 3 and ub["distinct"] == 2
     assert ub["shrink"] == 3 * 4096 * 2 + 2 * 3 * 16 * 4096 * 2 + 2 * 3 * 3 * 16 * 4
     assert ub["expand"] == 3 * 3 * 16 * 4 + 2 * 12288 * 16 * 2 + 3 * 12288 * 2 * 2
+    # shrink and expand in one kernel: the expand's read of the buffer goes
+    assert ub["linear"] == ub["shrink"] + ub["expand"] - 3 * 3 * 16 * 4
 
 
 def test_embedding_workload_has_a_bf16_rank_wide_input_and_no_a():

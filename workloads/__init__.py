@@ -201,7 +201,8 @@ def unique_bytes(w: Workload, ids: np.ndarray) -> dict:
     Counted from the id map: x rows of tokens with an id (once, not per
     slice); A, B and bias of the LoRAs that occur; the fp32 buffer read and
     written by shrink (+=) and read by expand; y read and written for rows
-    with an id (write only when add_inputs is false).
+    with an id (write only when add_inputs is false).  "linear" is both
+    calls in one kernel, the buffer read and written once.
     """
     L = w.max_loras
     act = (ids >= 0) & (ids < L)
@@ -219,5 +220,8 @@ def unique_bytes(w: Workload, ids: np.ndarray) -> dict:
               + t_act * n_tot * 2 * (2 if w.add_inputs else 1))
     flops_shrink = 0 if w.kind == "embedding" else 2 * t_act * S * r * H
     flops_expand = 2 * t_act * n_tot * r
+    # shrink and expand in one kernel: the buffer is read and written once
+    linear = shrink + expand - (0 if w.kind == "embedding" else x_bytes)
     return {"t_active": t_act, "distinct": d, "shrink": shrink, "expand": expand,
+            "linear": linear,
             "flops_shrink": flops_shrink, "flops_expand": flops_expand}
