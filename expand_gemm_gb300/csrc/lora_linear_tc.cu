@@ -11,9 +11,10 @@
 //            into a TMEM accumulator of S x 128 fp32 columns, as in
 //            lora_shrink_umma.cu;
 //   phase 2  buf[s][t, :] = old + scale * acc for the tile's tokens (the
-//            old rows by TMA into the freed ring, the new ones by plain
-//            stores: the tile's CTA is their only writer), and the same
-//            values rounded to bf16 into TMEM as the expand's A operands;
+//            old rows by TMA into the freed ring, the new ones written over
+//            them there and stored by TMA: the tile's CTA is their only
+//            writer), and the same values rounded to bf16 into TMEM as the
+//            expand's A operands;
 //   phase 3  the expand of the tile over every 128-column chunk of every
 //            slice: B by TMA, old y by cp.async, UMMAs with A from TMEM,
 //            32-byte stores, as in lora_expand_tc.cu.
@@ -62,15 +63,12 @@ constexpr int LT_ACC3 = 128;          // phase-3 accumulators at 128 and 256
 constexpr long long LT_TIMEOUT_CYCLES = 2000000000ll;
 constexpr uint32_t LT_BACKOFF_NS = 200;
 constexpr int LT_ERROR_BIT = 1 << 30;
-constexpr int LT_GATHER_PIECES = 128;  // runs above which a tile's x is gathered by cp.async
 
 struct LinearTcArgs {
     CUtensorMap map_x[LT_XMAPS];              // x: [T, H] bf16, box {64, 2^i}, 128B swizzle
     CUtensorMap map_a[LT_MAXS];               // A[s]: [L * 128, H] bf16, box {64, 128}
     CUtensorMap map_buf[LT_XMAPS];            // buf: [S * T, 128] fp32, box {32, 2^i}
     CUtensorMap map_b[LT_MAXS];               // B[s] rows, permuted (encode_perm_rows_map)
-    const uint16_t *x;                        // [T, x_ld] bf16 (the gathered tiles)
-    int64_t x_ld;
     const uint16_t *bias[LT_MAXS];            // [L, n_s] or null
     int32_t n[LT_MAXS];                       // slice widths (multiples of 64)
     int32_t col0[LT_MAXS];                    // first y column of each slice
@@ -244,17 +242,6 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
             if (lane == 0) npieces = lt_pieces(p.sorted + row0, nrows, pieces);
             const int np = __shfl_sync(0xffffffffu, npieces, 0);
             __syncwarp();
-            // A tile whose tokens break into more than LT_GATHER_PIECES runs
-            // is gathered by the warp's 32 lanes with cp.async (four rows a
-            // lane, the same swizzled layout) instead of one TMA box per run:
-            // small boxes made that tile's shrink 15% slower than the others.
-            const bool gather = np > LT_GATHER_PIECES;
-            int gtok[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int rr = lane + 32 * i;
-                gtok[i] = (gather && rr < nrows) ? p.sorted[row0 + rr] : -1;
-            }
             int issued = 0;
             for (int kb = 0; kb < nk; ++kb) {
                 const int n = n1 + kb, stage = n % LT_SLOTS;
@@ -263,37 +250,15 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
                                                    deadline);
                 if (__all_sync(0xffffffffu, got) == 0) break;
                 const uint32_t sx = base + stage * LT_SLOT;
-                if (gather) {
-                    const int k0 = kb * LT_BK;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int rr = lane + 32 * i;
-                        if (gtok[i] < 0) continue;
-                        const uint16_t *src = p.x + int64_t(gtok[i]) * p.x_ld + k0;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const bool in = k0 + 8 * c < H;
-                            cp_async16(sx + uint32_t(rr * 128 + ((c ^ (rr & 7)) << 4)),
-                                       in ? src + 8 * c : p.x, in);
-                        }
-                    }
-                    // the barrier waits for every lane's copies; lane 0's plain
-                    // arrival (the x producer's one) comes after all of them
-                    cp_async_mbar_arrive_track(full1 + 8 * stage);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(full1 + 8 * stage);
-                } else {
-                    if (lane == 0) mbar_arrive_expect_tx(full1 + 8 * stage, uint32_t(nrows * 128));
-                    __syncwarp();
-                    for (int i = lane; i < np; i += 32) {
-                        const uint32_t pc = pieces[i];
-                        const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
-                        tma_load_2d(sx + r * 128, &p.map_x[lg], kb * LT_BK, t0, full1 + 8 * stage);
-                    }
+                if (lane == 0) mbar_arrive_expect_tx(full1 + 8 * stage, uint32_t(nrows * 128));
+                __syncwarp();
+                for (int i = lane; i < np; i += 32) {
+                    const uint32_t pc = pieces[i];
+                    const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
+                    tma_load_2d(sx + r * 128, &p.map_x[lg], kb * LT_BK, t0, full1 + 8 * stage);
                 }
                 ++issued;
             }
-            if (gather) cp_async_wait<0>();
             if (lane == 0) {                 // every issued fill lands before the ring is reused
                 const long long dd = clock64() + LT_TIMEOUT_CYCLES;
                 for (int i = max(0, issued - LT_SLOTS); i < issued; ++i) {
@@ -344,7 +309,6 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
                         break;
                     }
                     tc_fence_after();
-                    fence_proxy_async_smem();    // x may have come by cp.async (generic proxy)
                     const uint32_t sx = base + stage * LT_SLOT;
 #pragma unroll
                     for (int kk = 0; kk < LT_BK / 16; ++kk) {
@@ -658,23 +622,17 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
                     __syncwarp();
                     if (lane == 0) mbar_arrive(acce + 8 * ab);
                 };
-                if constexpr (!BIAS) {
-                    uint32_t va[2][32];
-                    tmem_ld16x256b_x8_nowait(tl, va[0]);
-                    tmem_ld16x256b_x8_nowait(tl + 64u, va[1]);
-                    tmem_wait_ld();
-                    release_acc();
-                    finish_half(0, va[0]);
-                    finish_half(1, va[1]);
-                } else {
+                // the two 64-column halves one after the other (requesting
+                // both before finishing either, as the expand kernel does
+                // without a bias, measured 4.9 us slower here on the large
+                // workload, 223.3 against 218.4 us)
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        uint32_t va[32];
-                        tmem_ld16x256b_x8_nowait(tl + uint32_t(hf * 64), va);
-                        tmem_wait_ld();
-                        if (hf == 1) release_acc();
-                        finish_half(hf, va);
-                    }
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t va[32];
+                    tmem_ld16x256b_x8_nowait(tl + uint32_t(hf * 64), va);
+                    tmem_wait_ld();
+                    if (hf == 1) release_acc();
+                    finish_half(hf, va);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty3 + 8 * slot);   // done with the slot's y
@@ -768,8 +726,6 @@ int launch_linear_tc(const LinearTcLaunch &a, cudaStream_t stream)
     }
     p.chunk0[S] = chunks;
     for (int s = S + 1; s <= LT_MAXS; ++s) p.chunk0[s] = chunks;
-    p.x = a.x;
-    p.x_ld = a.x_ld;
     p.num_slices = S;
     p.hidden = a.hidden;
     p.num_tokens = T;

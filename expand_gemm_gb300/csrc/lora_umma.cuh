@@ -267,13 +267,6 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" :: "r"(bar) : "memory");
 }
 
-// The same with the pending count incremented first: a net-zero arrival
-// (the barrier waits for this thread's copies without counting the thread).
-__device__ __forceinline__ void cp_async_mbar_arrive_track(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" :: "r"(bar) : "memory");
-}
-
 // 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint32_t bytes,
                                              uint32_t bar)
