@@ -51,6 +51,7 @@ constexpr int LT_SLOTS = 3;           // ring slots, both phases
 constexpr int LT_SLOT = 65536;        // bytes per slot
 constexpr int LT_XMAPS = 8;           // box heights 1, 2, 4, ..., 128
 constexpr int LT_EPI = 8;             // conversion / epilogue warps
+constexpr int LT_ST_ISSUERS = 6;      // warps issuing the new buffer rows' TMA stores
 constexpr int LT_W_X = 0;             // x producer; old-buffer loads; B issuer 0
 constexpr int LT_W_MMA = 1;           // TMEM owner, UMMA issue
 constexpr int LT_W_B1 = 2;            // A producer of slice 0; B issuer 1
@@ -58,6 +59,7 @@ constexpr int LT_W_YL0 = 3;           // A producers of slices 1, 2; y loaders 3
 constexpr int LT_YL = 4;              // y loader warps
 constexpr int LT_W_EPI0 = LT_W_YL0 + LT_YL;
 constexpr int LT_THREADS = 32 * (LT_W_EPI0 + LT_EPI);
+static_assert(LT_ST_ISSUERS == 2 + LT_YL, "store issuers: the x producer, B issuer 1, the y loaders");
 constexpr int LT_ACC_A01 = 384;       // TMEM columns of the A operands of slices 0, 1 (+64)
 constexpr int LT_ACC3 = 128;          // phase-3 accumulators at 128 and 256
 constexpr long long LT_TIMEOUT_CYCLES = 2000000000ll;
@@ -163,6 +165,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
     const uint32_t drain = acce + 16;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + LtLayout::MISC);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + LtLayout::MISC + 4);
+    volatile int *s_np = reinterpret_cast<volatile int *>(smem + LtLayout::MISC + 8);
     uint32_t *pieces = reinterpret_cast<uint32_t *>(smem + LtLayout::PIECES);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = p.num_slices, T = p.num_tokens, H = p.hidden;
@@ -239,7 +242,10 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
 
         // ============================================================ phase 1: shrink
         if (warp == LT_W_X) {
-            if (lane == 0) npieces = lt_pieces(p.sorted + row0, nrows, pieces);
+            if (lane == 0) {
+                npieces = lt_pieces(p.sorted + row0, nrows, pieces);
+                *s_np = npieces;             // for the store issuers of phase 2
+            }
             const int np = __shfl_sync(0xffffffffu, npieces, 0);
             __syncwarp();
             int issued = 0;
@@ -371,11 +377,13 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
             __syncwarp();
             // the conversion warps have written the new rows over the old ones
             // in shared memory: they leave with the same boxes, by TMA stores
-            // (a thread's 16-byte stores of its own row touched 32 lines a
-            // warp store: 9 us for the phase)
-            asm volatile("bar.sync 1, %0;\n" :: "n"(32 * (LT_EPI + 1)) : "memory");
+            // from LT_ST_ISSUERS warps (this one and the expand's producers,
+            // idle here).  Issued by this warp alone, the wait for their reads
+            // of the ring took 6 us; a thread's 16-byte stores of its own row
+            // (32 lines a warp store) 9 us; 512-byte rows by warp stores 8 us.
+            asm volatile("bar.sync 1, %0;\n" :: "n"(32 * (LT_EPI + LT_ST_ISSUERS)) : "memory");
             if (__shfl_sync(0xffffffffu, *s_abort == 0 ? 1 : 0, 0) != 0) {
-                for (int i = lane; i < S * np * 4; i += 32) {
+                for (int i = lane; i < S * np * 4; i += 32 * LT_ST_ISSUERS) {
                     const int sb = i / (np * 4), rem = i - sb * np * 4, pi = rem >> 2, j = rem & 3;
                     const uint32_t pc = pieces[pi];
                     const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
@@ -384,6 +392,23 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
                 }
                 bulk_commit_group();
                 bulk_wait_group_read0();             // the ring is read before it changes hands
+            }
+            __syncwarp();
+        } else if (warp == LT_W_B1 || (warp >= LT_W_YL0 && warp < LT_W_EPI0)) {
+            // store issuers 1 .. LT_ST_ISSUERS - 1 (see the x producer above)
+            const int k = warp == LT_W_B1 ? 1 : 2 + warp - LT_W_YL0;
+            const int np = *s_np;
+            asm volatile("bar.sync 1, %0;\n" :: "n"(32 * (LT_EPI + LT_ST_ISSUERS)) : "memory");
+            if (__shfl_sync(0xffffffffu, *s_abort == 0 ? 1 : 0, 0) != 0) {
+                for (int i = 32 * k + lane; i < S * np * 4; i += 32 * LT_ST_ISSUERS) {
+                    const int sb = i / (np * 4), rem = i - sb * np * 4, pi = rem >> 2, j = rem & 3;
+                    const uint32_t pc = pieces[pi];
+                    const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
+                    tma_store_2d(&p.map_buf[lg], 32 * j, sb * T + t0,
+                                 base + sb * LT_SLOT + j * (LT_BM * 128) + r * 128);
+                }
+                bulk_commit_group();
+                bulk_wait_group_read0();
             }
             __syncwarp();
         } else if (warp >= LT_W_EPI0) {
@@ -435,7 +460,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
             // once all are in shared memory (taken by the eight warps and
             // the x producer, whatever happened above)
             fence_proxy_async_smem();
-            asm volatile("bar.sync 1, %0;\n" :: "n"(32 * (LT_EPI + 1)) : "memory");
+            asm volatile("bar.sync 1, %0;\n" :: "n"(32 * (LT_EPI + LT_ST_ISSUERS)) : "memory");
             if (ok && S == 3) {
 #pragma unroll
                 for (int u = 0; u < 2; ++u)
