@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
             mbar_init(empty3 + 8 * i, 1 + LT_EPI);
         }
         mbar_init(accf1, 1);
-        mbar_init(bufb, 1);
+        mbar_init(bufb, LT_ST_ISSUERS);
         for (int i = 0; i < 2; ++i) {
             mbar_init(accf + 8 * i, 1);
             mbar_init(acce + 8 * i, LT_EPI);
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
         if (warp == LT_W_X) {
             if (lane == 0) {
                 npieces = lt_pieces(p.sorted + row0, nrows, pieces);
-                *s_np = npieces;             // for the store issuers of phase 2
+                *s_np = npieces;             // for the buffer-row issuers of phase 2
             }
             const int np = __shfl_sync(0xffffffffu, npieces, 0);
             __syncwarp();
@@ -350,19 +350,32 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
         if (__syncthreads_or(*s_abort != 0)) break;      // (one answer for the whole CTA)
 
         // ============================================================ phase 2: buffer, A operands
-        if (warp == LT_W_X) {
+        if (warp == LT_W_X || warp == LT_W_B1 || (warp >= LT_W_YL0 && warp < LT_W_EPI0)) {
+            // LT_ST_ISSUERS warps (the x producer, B issuer 1 and the y
+            // loaders; idle here) move the tile's buffer rows, one box per
+            // (slice, run, 32-column block), box i by warp i / 32 mod
+            // LT_ST_ISSUERS.  Slot s receives slice s's old rows: four
+            // 32-column blocks of 128 rows x 128 bytes, 128-byte swizzled.
+            // Issued by one warp, the stores' reads of the ring took 6 us
+            // (every CTA storing at once); a thread's 16-byte stores of its
+            // own row (32 lines a warp store) 9 us; 512-byte rows by warp
+            // stores 8 us.
+            const int k = warp == LT_W_X ? 0 : warp == LT_W_B1 ? 1 : 2 + warp - LT_W_YL0;
+            const int np = *s_np;
+            const int nbox = S * np * 4;
+            bool go = true;
             if (lane == 0) {
-                // the ring is free once the shrink's last UMMAs have completed;
-                // slot s receives slice s's old rows: four 32-column blocks of
-                // 128 rows x 128 bytes, 128-byte swizzled, one box per piece
-                if (mbar_wait_bounded(accf1, uint32_t(it) & 1u, s_abort, deadline))
-                    mbar_arrive_expect_tx(bufb, uint32_t(S * nrows * LT_R * 4));
+                // the ring is free once the shrink's last UMMAs have completed
+                go = mbar_wait_bounded(accf1, uint32_t(it) & 1u, s_abort, deadline);
+                uint32_t bytes = 0;
+                for (int i = 32 * k; i < nbox; i += 32 * LT_ST_ISSUERS)
+                    for (int l = i; l < min(i + 32, nbox); ++l)
+                        bytes += (128u << ((pieces[(l % (np * 4)) >> 2] >> 8) & 7u));
+                if (go) mbar_arrive_expect_tx(bufb, bytes);
             }
-            const int np = __shfl_sync(0xffffffffu, npieces, 0);
-            const bool go = __shfl_sync(0xffffffffu, *s_abort == 0 ? 1 : 0, 0) != 0;
-            // one box per (slice, run, 32-column block), spread over the lanes
+            go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
             if (go)
-                for (int i = lane; i < S * np * 4; i += 32) {
+                for (int i = 32 * k + lane; i < nbox; i += 32 * LT_ST_ISSUERS) {
                     const int sb = i / (np * 4), rem = i - sb * np * 4, pi = rem >> 2, j = rem & 3;
                     const uint32_t pc = pieces[pi];
                     const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
@@ -375,15 +388,11 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
                 }
             }
             __syncwarp();
-            // the conversion warps have written the new rows over the old ones
-            // in shared memory: they leave with the same boxes, by TMA stores
-            // from LT_ST_ISSUERS warps (this one and the expand's producers,
-            // idle here).  Issued by this warp alone, the wait for their reads
-            // of the ring took 6 us; a thread's 16-byte stores of its own row
-            // (32 lines a warp store) 9 us; 512-byte rows by warp stores 8 us.
+            // the conversion warps have written the new rows over the old
+            // ones in shared memory: they leave with the same boxes
             asm volatile("bar.sync 1, %0;\n" :: "n"(32 * (LT_EPI + LT_ST_ISSUERS)) : "memory");
             if (__shfl_sync(0xffffffffu, *s_abort == 0 ? 1 : 0, 0) != 0) {
-                for (int i = lane; i < S * np * 4; i += 32 * LT_ST_ISSUERS) {
+                for (int i = 32 * k + lane; i < nbox; i += 32 * LT_ST_ISSUERS) {
                     const int sb = i / (np * 4), rem = i - sb * np * 4, pi = rem >> 2, j = rem & 3;
                     const uint32_t pc = pieces[pi];
                     const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
@@ -392,23 +401,6 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
                 }
                 bulk_commit_group();
                 bulk_wait_group_read0();             // the ring is read before it changes hands
-            }
-            __syncwarp();
-        } else if (warp == LT_W_B1 || (warp >= LT_W_YL0 && warp < LT_W_EPI0)) {
-            // store issuers 1 .. LT_ST_ISSUERS - 1 (see the x producer above)
-            const int k = warp == LT_W_B1 ? 1 : 2 + warp - LT_W_YL0;
-            const int np = *s_np;
-            asm volatile("bar.sync 1, %0;\n" :: "n"(32 * (LT_EPI + LT_ST_ISSUERS)) : "memory");
-            if (__shfl_sync(0xffffffffu, *s_abort == 0 ? 1 : 0, 0) != 0) {
-                for (int i = 32 * k + lane; i < S * np * 4; i += 32 * LT_ST_ISSUERS) {
-                    const int sb = i / (np * 4), rem = i - sb * np * 4, pi = rem >> 2, j = rem & 3;
-                    const uint32_t pc = pieces[pi];
-                    const int r = int(pc & 0xFFu), lg = int((pc >> 8) & 7u), t0 = int(pc >> 11);
-                    tma_store_2d(&p.map_buf[lg], 32 * j, sb * T + t0,
-                                 base + sb * LT_SLOT + j * (LT_BM * 128) + r * 128);
-                }
-                bulk_commit_group();
-                bulk_wait_group_read0();
             }
             __syncwarp();
         } else if (warp >= LT_W_EPI0) {
