@@ -137,13 +137,14 @@ def fused_path(w) -> bool:
             and w.num_slices * _padded_rank(w.rank) <= 128 and mode != "0")
 
 
-def linear_tc_path(w) -> bool:
+def linear_tc_path(w, sms: int = 152) -> bool:
     """lora_linear's rule for its rank-128 tensor-core kernel (metadata
-    kernel + one kernel for the shrink and expand of every tile)."""
+    kernel + one kernel for the shrink and expand of every tile) on a GPU of
+    `sms` SMs."""
     if coop_path(w) or fused_path(w) or w.kind == "embedding":
         return False
     mode = os.environ.get("LORA_PUNICA_LINEAR_TC", "-1")
-    min_t = int(os.environ.get("LORA_PUNICA_UMMA_MIN_TOKENS", "1024"))
+    min_t = int(os.environ.get("LORA_PUNICA_LINEAR_TC_MIN_TOKENS", "0")) or 72 * sms
     return (mode != "0" and (mode == "1" or w.num_tokens >= min_t) and w.rank == 128
             and w.num_slices <= 3 and all(n % 64 == 0 for n in w.slices)
             and w.hidden >= 64 and w.hidden % 8 == 0)
@@ -404,7 +405,7 @@ class Measured:
         self.k = {"meta": k_meta, "shrink": k_shrink, "expand": k_expand, "step": k_step}
         self.coop = coop_path(w) and not emb
         self.fused = (fused_path(w) and not emb) or self.coop
-        self.linear_tc = linear_tc_path(w) and not self.fused
+        self.linear_tc = linear_tc_path(w, props.multi_processor_count) and not self.fused
         self.launches_per_step = (2 if emb or self.linear_tc else 1 if self.fused else 3 + (
             1 if umma_shrink_path(w) and os.environ.get("LORA_PUNICA_UMMA_PARTIAL", "1") == "0"
             else 0))

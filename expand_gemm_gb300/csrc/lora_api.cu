@@ -50,6 +50,7 @@ static Knobs read_knobs()
     k.meta_multi = env_int("LORA_PUNICA_META_MULTI", 1);
     k.meta_cluster = env_int("LORA_PUNICA_META_CLUSTER", 1);
     k.linear_tc = env_int("LORA_PUNICA_LINEAR_TC", -1);
+    k.linear_tc_min_tokens = env_int("LORA_PUNICA_LINEAR_TC_MIN_TOKENS", 0);
     k.coop_test_extra = env_int("LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS", 0);
     k.coop_test_timeout = env_int("LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES", 0);
     return k;

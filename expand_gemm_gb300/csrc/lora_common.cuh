@@ -494,6 +494,7 @@ struct Knobs {
     int meta_multi;           // LORA_PUNICA_META_MULTI: multi-CTA metadata kernel (1)
     int meta_cluster;         // LORA_PUNICA_META_CLUSTER: its thread-block-cluster form (1)
     int linear_tc;            // LORA_PUNICA_LINEAR_TC: lora_linear's one-kernel tensor-core path (-1)
+    int linear_tc_min_tokens; // LORA_PUNICA_LINEAR_TC_MIN_TOKENS: its batch threshold (0: 72 x SMs)
     int coop_test_extra;      // LORA_PUNICA_COOP_TEST_EXTRA_ARRIVALS (0, tests only)
     int coop_test_timeout;    // LORA_PUNICA_COOP_TEST_TIMEOUT_CYCLES (0, tests only)
 };

@@ -765,16 +765,22 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
             if (r != 0) return r;
         }
     }
-    // Rank 128, up to three slices, batches of at least
-    // LORA_PUNICA_UMMA_MIN_TOKENS tokens: the metadata kernel, then the
+    // Rank 128, up to three slices, batches of at least 72 tokens per SM
+    // (LORA_PUNICA_LINEAR_TC_MIN_TOKENS): the metadata kernel, then the
     // shrink and the expand of every 128-token tile in one tensor-core
-    // kernel (lora_linear_tc.cu).  Measured on the large workload (16384
-    // tokens, three slices): 223 us against 241 for the metadata kernel and
-    // the separate tcgen05 shrink and expand.  LORA_PUNICA_LINEAR_TC=0 keeps
-    // the separate kernels; =1 takes it for every call it fits.
+    // kernel (lora_linear_tc.cu).  A CTA takes a whole tile through both,
+    // about 180 us at hidden 8192 and 10240 output columns whatever its
+    // rows, so the kernel pays when the tiles fill the SMs.  Measured on the
+    // large workload's shapes (hidden 8192, slices 8192/1024/1024), step
+    // time, separate kernels against this one: 140 / 181 us at 8192 tokens,
+    // 211 / 195 at 11264, 239 / 214.5 at 16384, 339 / 351 at 17408 (past one
+    // tile per SM both take two rounds of tiles), 415 / 398 at 24576, 461 /
+    // 409 at 32768.  LORA_PUNICA_LINEAR_TC=0 keeps the separate kernels; =1
+    // takes it for every call it fits.
+    const int64_t tc_min = kn.linear_tc_min_tokens > 0 ? int64_t(kn.linear_tc_min_tokens)
+                                                       : int64_t(72) * lora::device_sm_count();
     if (kn.linear_tc != 0 && token_lora_mapping != nullptr && meta->error_word != nullptr &&
-        (kn.linear_tc == 1 || num_tokens >= kn.umma_min_tokens) && rank == 128 &&
-        num_slices <= 3) {
+        (kn.linear_tc == 1 || num_tokens >= tc_min) && rank == 128 && num_slices <= 3) {
         lora::LinearTcLaunch u;
         int64_t width = 0;
         for (int s = 0; s < LORA_MAX_SLICES; ++s) u.a[s] = u.b[s] = u.bias[s] = nullptr;

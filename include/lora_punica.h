@@ -259,8 +259,9 @@ int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lora_b,
  *     tokens (max_loras <= 256, num_slices * padded rank <= 128);
  *   - rank 128, at most three slices, slice widths multiples of 64, y
  *     32-byte aligned with y_ld a multiple of 16, x and buf 16-byte
- *     aligned, batches of at least LORA_PUNICA_UMMA_MIN_TOKENS tokens
- *     (1024): the metadata kernel, then one tensor-core kernel that runs
+ *     aligned, batches of at least 72 tokens per SM of the device
+ *     (LORA_PUNICA_LINEAR_TC_MIN_TOKENS sets another threshold): the
+ *     metadata kernel, then one tensor-core kernel that runs
  *     the shrink of a 128-token tile, adds its result into that tile's
  *     buffer rows and runs the tile's expand (one CTA per SM, tiles of one
  *     LoRA in turn);
@@ -272,7 +273,8 @@ int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lora_b,
  * never / always (when the batch fits) the cooperative kernel;
  * LORA_PUNICA_FUSED=0/1 and LORA_PUNICA_FUSED_MAX_TOKENS the cluster
  * kernel; LORA_PUNICA_LINEAR_TC=0/1 never / for every call that fits (any
- * batch size) the rank-128 tensor-core kernel; LORA_PUNICA_SELF_META=1 two
+ * batch size) the rank-128 tensor-core kernel, and
+ * LORA_PUNICA_LINEAR_TC_MIN_TOKENS its threshold; LORA_PUNICA_SELF_META=1 two
  * kernels (the shrink writes the metadata), =0 the plain three calls.
  */
 int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,

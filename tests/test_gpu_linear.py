@@ -114,16 +114,17 @@ def test_linear_one_kernel_tensor_core(oracle_mod, knob, T, H, slices, L, bias, 
     _check_linear(oracle_mod, inp, buf0=b0)
 
 
-@pytest.mark.parametrize("T,slices", [
-    (1500, (200, 64)),       # a slice width that is not a multiple of 64: separate kernels
-    (600, (128, 128)),       # below the default's 1024 tokens: separate kernels
-    (1024, (256, 64, 128)),  # at the threshold: the one kernel
+@pytest.mark.parametrize("T,slices,min_tokens", [
+    (1500, (200, 64), 1000),       # a slice width that is not a multiple of 64: separate kernels
+    (600, (128, 128), None),       # below the default threshold (72 tokens per SM): separate
+    (1024, (256, 64, 128), 1024),  # at a set threshold: the one kernel
+    (12000, (128, 64), None),      # above the default threshold: the one kernel
 ])
-def test_linear_rank128_default_rule(oracle_mod, knob, T, slices):
+def test_linear_rank128_default_rule(oracle_mod, knob, T, slices, min_tokens):
     """With the default rule (LORA_PUNICA_LINEAR_TC unset) rank-128 calls
     take the one kernel or the separate ones; both give the oracle's
     results."""
-    knob(LORA_PUNICA_LINEAR_TC=None)
+    knob(LORA_PUNICA_LINEAR_TC=None, LORA_PUNICA_LINEAR_TC_MIN_TOKENS=min_tokens)
     w = W.Workload("lintc_default", T, T, 512, 128, 5, slices, "zipf_seq", p_none=0.1,
                    seq_len=(40, 300), bias=True, scale=0.5)
     _check_linear(oracle_mod, W.generate(w))

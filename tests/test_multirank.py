@@ -63,16 +63,20 @@ def test_single_process_helpers():
 def test_bench_path_rules_follow_the_library(monkeypatch):
     """bench.py names the kernels lora_linear takes (and counts its launches
     from them): the cooperative kernel on the tiny batch, the rank-128
-    tensor-core kernel on the large one unless LORA_PUNICA_LINEAR_TC=0,
-    three kernels on the rank-64 prefill."""
+    tensor-core kernel on the large one (72 or more tokens per SM) unless
+    LORA_PUNICA_LINEAR_TC=0, three kernels on the rank-64 prefill."""
     sys.path.insert(0, ROOT)
     import bench
     import workloads as W
+    from dataclasses import replace
     for k in ("LORA_PUNICA_COOP", "LORA_PUNICA_FUSED", "LORA_PUNICA_LINEAR_TC",
-              "LORA_PUNICA_UMMA_MIN_TOKENS"):
+              "LORA_PUNICA_LINEAR_TC_MIN_TOKENS"):
         monkeypatch.delenv(k, raising=False)
     assert bench.coop_path(W.WORKLOADS["tiny"]) and not bench.linear_tc_path(W.WORKLOADS["tiny"])
-    assert bench.linear_tc_path(W.WORKLOADS["large"])
+    assert bench.linear_tc_path(W.WORKLOADS["large"], 152)
+    # below 72 tokens per SM: the separate kernels
+    assert not bench.linear_tc_path(replace(W.WORKLOADS["large"], num_tokens=8192), 152)
+    assert bench.linear_tc_path(replace(W.WORKLOADS["large"], num_tokens=8192), 100)
     assert not bench.linear_tc_path(W.WORKLOADS["prefill"])          # rank 64
     assert not bench.linear_tc_path(W.WORKLOADS["embedding"])
     monkeypatch.setenv("LORA_PUNICA_LINEAR_TC", "0")
