@@ -170,9 +170,6 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = p.num_slices, T = p.num_tokens, H = p.hidden;
 
-    pdl_wait();
-    pdl_launch_dependents();
-
     if (tid == 0) {
         for (int i = 0; i < LT_SLOTS; ++i) {
             mbar_init(full1 + 8 * i, 1 + S);
@@ -201,6 +198,10 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
             tma_prefetch_map(&p.map_b[s]);
         }
     }
+    // (barriers and tensor maps above need nothing from the metadata kernel:
+    // they are set up while it runs)
+    pdl_wait();
+    pdl_launch_dependents();
     const SegTab tab = seg_tab(reinterpret_cast<int *>(smem + LtLayout::TAB), p.nbins);
     const int total_tiles = load_segments(p.no_lora, p.active, p.counts, p.start_loc, p.nbins,
                                           LT_BM, tab, false, 0, T, p.error_word);

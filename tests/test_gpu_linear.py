@@ -114,6 +114,21 @@ def test_linear_one_kernel_tensor_core(oracle_mod, knob, T, H, slices, L, bias, 
     _check_linear(oracle_mod, inp, buf0=b0)
 
 
+@pytest.mark.parametrize("T,H,slices,L,bias,ids", [
+    (24000, 128, (64, 128, 192), 40, False, "uniform"),   # ~200 tiles of 128 runs each
+    (30000, 256, (128,), 8, True, "zipf_seq"),             # ~235 tiles, bias
+])
+def test_linear_one_kernel_several_tiles_per_cta(oracle_mod, knob, T, H, slices, L, bias, ids):
+    """More tiles than SMs: CTAs take a second tile, whose barrier phases,
+    ring slots and TMEM buffers follow on from the first's."""
+    knob(LORA_PUNICA_LINEAR_TC="1", LORA_PUNICA_COOP="0", LORA_PUNICA_FUSED="0")
+    w = W.Workload("lintc_multi", T + H, T, H, 128, L, slices, ids, p_none=0.1,
+                   seq_len=(100, 900), bias=bias, scale=0.25)
+    inp = W.generate(w)
+    b0 = np.random.default_rng(T).standard_normal(inp.buf.shape).astype(np.float32)
+    _check_linear(oracle_mod, inp, buf0=b0)
+
+
 @pytest.mark.parametrize("T,slices,min_tokens", [
     (1500, (200, 64), 1000),       # a slice width that is not a multiple of 64: separate kernels
     (600, (128, 128), None),       # below the default threshold (72 tokens per SM): separate
