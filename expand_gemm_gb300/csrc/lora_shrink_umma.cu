@@ -184,11 +184,11 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
     if (warp == 0) {
         // ------------------------------------------------------ producer
         // Tokens of a tile are increasing (the sort is stable), so they
-        // split into runs of consecutive tokens.  Lane 0 cuts the tile into
-        // pieces whose heights are powers of two and whose tokens are
-        // consecutive; each piece is one 2-D TMA box of the x map with that
-        // height, written at its row of the 128-byte-swizzled tile.  Long
-        // prefill sequences make most tiles a single 128-row box.
+        // split into runs of consecutive tokens, cut into pieces whose
+        // heights are powers of two (tile_pieces_warp); each piece is one 2-D
+        // TMA box of the x map with that height, written at its row of the
+        // 128-byte-swizzled tile.  Long prefill sequences make most tiles a
+        // single 128-row box.
         uint32_t *pieces = reinterpret_cast<uint32_t *>(smem + L.piece_off);
         int stage = 0;
         uint32_t phase = 0;
@@ -204,21 +204,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) shrink_umma_kernel(const __grid
             // the stage's barrier expects exactly their bytes
             const int nrows = min(UM_BM, tab.start[seg] + tab.count[seg] - row0);
             const uint32_t tx = uint32_t(nrows * 128);
-            int npieces = 0;
-            if (lane == 0) {
-                const int32_t *tk = p.sorted + row0;
-                int j = 0;
-                while (j < nrows) {
-                    int lg = 7;
-                    while ((1 << lg) > nrows - j || (j & ((1 << lg) - 1)) != 0 ||
-                           tk[j + (1 << lg) - 1] - tk[j] != (1 << lg) - 1)
-                        --lg;
-                    pieces[npieces++] = uint32_t(j) | (uint32_t(lg) << 8) |
-                                        (uint32_t(tk[j]) << 11);
-                    j += 1 << lg;
-                }
-            }
-            npieces = __shfl_sync(0xffffffffu, npieces, 0);
+            const int npieces = tile_pieces_warp(p.sorted + row0, nrows, pieces);
             __syncwarp();
             for (int kb = kb0; kb < kb1; ++kb) {
                 bool got = mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, s_abort, deadline);

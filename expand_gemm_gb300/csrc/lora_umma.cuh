@@ -156,6 +156,76 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar)
 
 // ---------------------------------------------------------------- shrink work split
 
+// One of four warp-uniform values, by a warp-uniform index (no local-memory
+// array).
+__device__ __forceinline__ uint32_t pick4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          int i)
+{
+    return i == 0 ? a0 : i == 1 ? a1 : i == 2 ? a2 : a3;
+}
+
+// The TMA boxes of a tile's x rows.  The tile's nrows (<= 128) sorted tokens
+// tk[0 .. nrows) are increasing, so they split into runs of consecutive
+// tokens; each run is cut greedily into pieces whose heights are powers of
+// two and whose first rows are multiples of their heights (at row j of a run
+// ending at e: the largest 2^lg with j a multiple of 2^lg and j + 2^lg <= e).
+// Piece word: row | lg << 8 | first token << 11 (tokens below 2^21).  Called
+// by a whole warp: the lanes load the tokens (rows lane + 32 i), find the
+// run starts by ballots, and walk the runs together; lane 0 writes the
+// pieces.  Returns the piece count in every lane.  (Lane 0 alone testing
+// each candidate height against the tokens in global memory cost about
+// 190 us for a tile of 128 single-token runs: a lora_linear step of the
+// large workload's shapes with per-token ids took 1204 us that way, 1017
+// this way.)
+__device__ __forceinline__ int tile_pieces_warp(const int32_t *tk, int nrows, uint32_t *pieces)
+{
+    const int lane = threadIdx.x & 31;
+    int v[4];
+    uint32_t st[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+        v[i] = r < nrows ? tk[r] : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+        int prev = __shfl_up_sync(0xffffffffu, v[i], 1);
+        if (i > 0) {
+            const int last = __shfl_sync(0xffffffffu, v[i > 0 ? i - 1 : 0], 31);
+            if (lane == 0) prev = last;
+        }
+        st[i] = __ballot_sync(0xffffffffu, r < nrows && (r == 0 || v[i] != prev + 1));
+    }
+    int n = 0;
+    for (int s = 0; s < nrows;) {
+        // the run's end: the next run start after s, else nrows
+        int e = nrows;
+        for (int w = (s + 1) >> 5; w < 4; ++w) {
+            uint32_t b = pick4(st[0], st[1], st[2], st[3], w);
+            if (w == ((s + 1) >> 5)) b &= ~0u << ((s + 1) & 31);
+            if (b != 0u) {
+                e = min(nrows, 32 * w + __ffs(int(b)) - 1);
+                break;
+            }
+        }
+        const int ts = __shfl_sync(0xffffffffu,
+                                   int(pick4(uint32_t(v[0]), uint32_t(v[1]), uint32_t(v[2]),
+                                             uint32_t(v[3]), s >> 5)),
+                                   s & 31);
+        for (int j = s; j < e;) {
+            int lg = j == 0 ? 7 : __ffs(j) - 1;
+            lg = min(lg, 31 - __clz(e - j));
+            if (lane == 0)
+                pieces[n] = uint32_t(j) | (uint32_t(lg) << 8) | (uint32_t(ts + (j - s)) << 11);
+            ++n;
+            j += 1 << lg;
+        }
+        s = e;
+    }
+    return n;
+}
+
 // Split of the hidden dimension of the tensor-core shrinks: the number of
 // chunks (items per tile) that minimises rounds x chunk length (+ a fixed
 // cost of about two blocks per item for the pipeline fill and the
