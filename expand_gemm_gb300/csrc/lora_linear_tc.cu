@@ -51,7 +51,7 @@ constexpr int LT_SLOTS = 3;           // ring slots, both phases
 constexpr int LT_SLOT = 65536;        // bytes per slot
 constexpr int LT_XMAPS = 8;           // box heights 1, 2, 4, ..., 128
 constexpr int LT_EPI = 8;             // conversion / epilogue warps
-constexpr int LT_ST_ISSUERS = 6;      // warps issuing the new buffer rows' TMA stores
+constexpr int LT_ST_ISSUERS = 6;      // warps moving a tile's buffer rows by TMA (phase 2)
 constexpr int LT_W_X = 0;             // x producer; old-buffer loads; B issuer 0
 constexpr int LT_W_MMA = 1;           // TMEM owner, UMMA issue
 constexpr int LT_W_B1 = 2;            // A producer of slice 0; B issuer 1
