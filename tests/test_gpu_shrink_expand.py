@@ -113,6 +113,21 @@ def test_shrink_long_segments(oracle_mod, knob, umma, partial, pair, T, H, r, L,
     _shrink_case(oracle_mod, inp, buf0=b0)
 
 
+@pytest.mark.parametrize("ids", ["uniform", "uniform_p", "mixed"])
+def test_shrink_tensor_core_fragmented_tiles(oracle_mod, knob, ids):
+    """The tensor-core shrink on tiles whose tokens break into many runs
+    (per-token ids: up to 128 one-row TMA boxes a stage; the decode-token
+    prefix of a mixed batch): the pieces the producer warp builds cover
+    every row of every tile exactly once."""
+    knob(LORA_PUNICA_UMMA="1", LORA_PUNICA_UMMA_PARTIAL="1", LORA_PUNICA_UMMA_MIN_COLS=0,
+         LORA_PUNICA_UMMA_MIN_TOKENS=0, LORA_PUNICA_UMMA_PAIR="0")
+    w = W.Workload("frag", 1777, 1777, 256, 128, 3, (128, 128, 128), ids, p_none=0.1,
+                   seq_len=(30, 300), n_decode=40, scale=0.5)
+    inp = W.generate(w)
+    b0 = np.random.default_rng(5).standard_normal(inp.buf.shape).astype(np.float32)
+    _shrink_case(oracle_mod, inp, buf0=b0)
+
+
 def test_shrink_accumulates_and_scales(oracle_mod):
     inp = _custom(300, 512, 32, 4, [8, 8], seed=9)
     rng = np.random.default_rng(0)
