@@ -685,8 +685,8 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
     // (up to 512 tokens), LORA_PUNICA_COOP=0 never.
     const lora::Knobs &kn = lora::knobs();
     const int coop_mode = kn.coop;
-    if (coop_mode == 1 ||
-        (coop_mode != 0 && int64_t(num_tokens) * num_slices <= 256)) {
+    if (kn.linear_tc != 2 && (coop_mode == 1 ||
+                              (coop_mode != 0 && int64_t(num_tokens) * num_slices <= 256))) {
         const int r = lora::linear_coop(token_lora_mapping, num_tokens, x, hidden, x_ld, lora_a,
                                         lora_b, lora_bias, slice_sizes, num_slices, rank, scale,
                                         buf, y, y_ld, meta, st);
@@ -703,7 +703,7 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
     // LORA_PUNICA_FUSED=0 never.
     const int fused_mode = kn.fused;
     const int fused_max = fused_mode == 1 ? lora::FU_TMAX : kn.fused_max_tokens;
-    bool fused = fused_mode != 0 && num_tokens > 0 && num_tokens <= fused_max &&
+    bool fused = fused_mode != 0 && kn.linear_tc != 2 && num_tokens > 0 && num_tokens <= fused_max &&
                  token_lora_mapping != nullptr && x != nullptr && buf != nullptr && y != nullptr &&
                  hidden > 0 && hidden % 8 == 0 && x_ld % 8 == 0 && y_ld % 8 == 0 &&
                  meta->max_loras >= 1 && meta->max_loras <= lora::FU_MAX_LORAS &&
@@ -776,11 +776,17 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
     // 211 / 195 at 11264, 239 / 214.5 at 16384, 339 / 351 at 17408 (past one
     // tile per SM both take two rounds of tiles), 415 / 398 at 24576, 461 /
     // 409 at 32768.  LORA_PUNICA_LINEAR_TC=0 keeps the separate kernels; =1
-    // takes it for every call it fits.
+    // takes it for every call it fits; =2 requires it (a call it does not
+    // fit fails with LORA_ERR_SIZE: for tests that must not pass on the
+    // separate kernels).
     const int64_t tc_min = kn.linear_tc_min_tokens > 0 ? int64_t(kn.linear_tc_min_tokens)
                                                        : int64_t(72) * lora::device_sm_count();
+    const bool tc_req = kn.linear_tc == 2;
+    if (tc_req && (token_lora_mapping == nullptr || meta->error_word == nullptr || rank != 128 ||
+                   num_slices > 3))
+        return LORA_ERR_SIZE;
     if (kn.linear_tc != 0 && token_lora_mapping != nullptr && meta->error_word != nullptr &&
-        (kn.linear_tc == 1 || num_tokens >= tc_min) && rank == 128 && num_slices <= 3) {
+        (kn.linear_tc >= 1 || num_tokens >= tc_min) && rank == 128 && num_slices <= 3) {
         lora::LinearTcLaunch u;
         int64_t width = 0;
         for (int s = 0; s < LORA_MAX_SLICES; ++s) u.a[s] = u.b[s] = u.bias[s] = nullptr;
@@ -814,6 +820,7 @@ LORA_API int lora_linear(const int32_t *token_lora_mapping, int32_t num_tokens,
             r = lora::launch_linear_tc(u, st);
             return r == 0 ? LORA_OK : r;
         }
+        if (tc_req) return LORA_ERR_SIZE;
     }
 
     // The metadata kernel, then the shrink in early mode (for batches of up

@@ -273,7 +273,8 @@ int lora_expand_bf16(const lora_bf16_t *x, const lora_bf16_t *const *lora_b,
  * never / always (when the batch fits) the cooperative kernel;
  * LORA_PUNICA_FUSED=0/1 and LORA_PUNICA_FUSED_MAX_TOKENS the cluster
  * kernel; LORA_PUNICA_LINEAR_TC=0/1 never / for every call that fits (any
- * batch size) the rank-128 tensor-core kernel, and
+ * batch size) the rank-128 tensor-core kernel (=2 requires it: a call it
+ * does not fit fails with LORA_ERR_SIZE), and
  * LORA_PUNICA_LINEAR_TC_MIN_TOKENS its threshold; LORA_PUNICA_SELF_META=1 two
  * kernels (the shrink writes the metadata), =0 the plain three calls.
  */

@@ -122,6 +122,35 @@ def test_guard_bands_on_every_path(oracle_mod, knob, path, name, T):
     np.testing.assert_array_equal(got_y[none], inp.y[none])
 
 
+def test_guard_bands_one_kernel_tensor_core(oracle_mod, knob):
+    """lora_linear's rank-128 tensor-core kernel with x, y and the buffer
+    inside guard bands (the large workload's shapes and id mix at 1536
+    tokens: partial and fragmented tiles, halves on idle SMs)."""
+    import expand_gemm_gb300 as eg
+    knob(LORA_PUNICA_LINEAR_TC=2)                   # required: no fallback
+    inp = W.generate("large", num_tokens=1536)
+    w = inp.workload
+    T = w.num_tokens
+    x_full, x = _guarded_bf16(inp.x)
+    y_full, y = _guarded_bf16(inp.y)
+    buf_full, buf, g = _guarded_buf(inp.buf.shape, w.rank)
+    A = _weights_with_spare(inp.lora_a)
+    B = _weights_with_spare(inp.lora_b)
+    meta = eg.LoRAKernelMeta.make(w.max_loras, T, "cuda")
+    eg.lora_linear(dev_i32(inp.ids), x, A, B, None, w.scale, buf, y, meta)
+    torch.cuda.synchronize()
+    _check_guards(x_full, y_full, buf_full, g, T, "lora_linear (one tensor-core kernel)")
+    assert int(meta.error_word.item()) == 0
+    ref_buf = oracle_mod.shrink(inp.x, inp.lora_a, inp.ids, w.scale, inp.buf)
+    assert_close(buf.cpu().numpy(), ref_buf, SHRINK_ATOL, SHRINK_RTOL, "buffer")
+    ref_y = oracle_mod.expand(ref_buf.astype(np.float32), inp.lora_b, inp.ids, inp.y, w.slices,
+                              0, True, None)
+    got_y = host_bits(y)
+    assert_close(bits_to_f64(got_y), ref_y, EXPAND_ATOL, EXPAND_RTOL, "y")
+    none = inp.ids < 0
+    np.testing.assert_array_equal(got_y[none], inp.y[none])
+
+
 @pytest.mark.parametrize("tc", ["0", "2"])
 def test_guard_bands_separate_calls_with_offset(oracle_mod, knob, tc):
     """lora_shrink and lora_expand (offset_start, add_inputs=False) with

@@ -106,7 +106,7 @@ def test_linear_one_kernel_tensor_core(oracle_mod, knob, T, H, slices, L, bias, 
     """lora_linear's one-kernel tensor-core path (rank 128, up to three
     slices: every tile's shrink, buffer update and expand on one SM) gives
     the oracle's metadata, buffer and y, with a non-zero starting buffer."""
-    knob(LORA_PUNICA_LINEAR_TC="1", LORA_PUNICA_COOP="0", LORA_PUNICA_FUSED="0")
+    knob(LORA_PUNICA_LINEAR_TC="2")                 # required: no fallback
     w = W.Workload("lintc", T + H, T, H, 128, L, slices, ids, p_none=0.15, seq_len=(40, 400),
                    bias=bias, scale=0.7)
     inp = W.generate(w)
@@ -121,7 +121,7 @@ def test_linear_one_kernel_tensor_core(oracle_mod, knob, T, H, slices, L, bias, 
 def test_linear_one_kernel_several_tiles_per_cta(oracle_mod, knob, T, H, slices, L, bias, ids):
     """More tiles than SMs: CTAs take a second tile, whose barrier phases,
     ring slots and TMEM buffers follow on from the first's."""
-    knob(LORA_PUNICA_LINEAR_TC="1", LORA_PUNICA_COOP="0", LORA_PUNICA_FUSED="0")
+    knob(LORA_PUNICA_LINEAR_TC="2")                 # required: no fallback
     w = W.Workload("lintc_multi", T + H, T, H, 128, L, slices, ids, p_none=0.1,
                    seq_len=(100, 900), bias=bias, scale=0.25)
     inp = W.generate(w)
@@ -145,9 +145,30 @@ def test_linear_rank128_default_rule(oracle_mod, knob, T, slices, min_tokens):
     _check_linear(oracle_mod, W.generate(w))
 
 
+def test_linear_one_kernel_required_refuses_what_it_does_not_take(knob):
+    """LORA_PUNICA_LINEAR_TC=2 makes a call the kernel does not take fail
+    (rank 64; a slice width that is not a multiple of 64) instead of
+    running the separate kernels; y is left untouched."""
+    import expand_gemm_gb300 as eg
+    from expand_gemm_gb300._lib import LoraError
+    knob(LORA_PUNICA_LINEAR_TC="2")
+    for r, slices in ((64, (128,)), (128, (96,))):
+        w = W.Workload("lintc_refuse", 5, 300, 256, r, 2, slices, "zipf_seq", p_none=0.1,
+                       seq_len=(40, 200))
+        inp = W.generate(w)
+        y = dev_bf16(inp.y)
+        meta = eg.LoRAKernelMeta.make(w.max_loras, w.num_tokens, "cuda")
+        with pytest.raises(LoraError):
+            eg.lora_linear(dev_i32(inp.ids), dev_bf16(inp.x), [dev_bf16(a) for a in inp.lora_a],
+                           [dev_bf16(b) for b in inp.lora_b], None, w.scale,
+                           dev_f32(inp.buf), y, meta)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host_bits(y), inp.y)
+
+
 def test_linear_one_kernel_tensor_core_no_lora(oracle_mod, knob):
     """The one-kernel path on the all -1 batch and on invalid ids."""
-    knob(LORA_PUNICA_LINEAR_TC="1", LORA_PUNICA_COOP="0", LORA_PUNICA_FUSED="0")
+    knob(LORA_PUNICA_LINEAR_TC="2")                 # required: no fallback
     inp = W.generate("large", num_tokens=640)
     _check_linear(oracle_mod, inp, ids=np.full(640, -1, np.int32))
     ids = inp.ids.copy()
