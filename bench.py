@@ -56,7 +56,7 @@ NCU_TRAFFIC = {
     ("expand", "large"): ("efc2bfc911fdb557", 664651776),
     ("shrink", "large"): ("960e6f1709e55feb", 450486272),
     # linear_tc_kernel<0>, the step's kernel after the metadata kernel
-    ("linear_tc", "large"): ("519ffc0cfc82ab42", 1116556288),
+    ("linear_tc", "large"): ("530c5a60b03f1ca4", 1117510400),
 }
 
 # The source files each reported kernel is built from.

@@ -59,7 +59,7 @@ constexpr int LT_W_YL0 = 3;           // A producers of slices 1, 2; y loaders 3
 constexpr int LT_YL = 4;              // y loader warps
 constexpr int LT_W_EPI0 = LT_W_YL0 + LT_YL;
 constexpr int LT_THREADS = 32 * (LT_W_EPI0 + LT_EPI);
-static_assert(LT_ST_ISSUERS == 2 + LT_YL, "store issuers: the x producer, B issuer 1, the y loaders");
+static_assert(LT_ST_ISSUERS == 2 + LT_YL, "buffer-row issuers: the x producer, B issuer 1, the y loaders");
 constexpr int LT_ACC_A01 = 384;       // TMEM columns of the A operands of slices 0, 1 (+64)
 constexpr int LT_ACC3 = 128;          // phase-3 accumulators at 128 and 256
 constexpr long long LT_TIMEOUT_CYCLES = 2000000000ll;
@@ -450,8 +450,9 @@ __global__ void __launch_bounds__(LT_THREADS, 1) linear_tc_kernel(const __grid_c
             }
             // slice 2's A operand goes over the accumulator of slice 0: only
             // once every conversion warp has read it; the new rows go out
-            // once all are in shared memory (taken by the eight warps and
-            // the x producer, whatever happened above)
+            // once all are in shared memory (the barrier is taken by the
+            // eight conversion warps and the LT_ST_ISSUERS issuers, whatever
+            // happened above)
             fence_proxy_async_smem();
             asm volatile("bar.sync 1, %0;\n" :: "n"(32 * (LT_EPI + LT_ST_ISSUERS)) : "memory");
             if (ok && S == 3) {
